@@ -1,0 +1,69 @@
+"""NumPy float64 oracle for row-wise normalization (test infrastructure only).
+
+Each function restates one definition in the order the pages give it; no
+blocking, fusion or reordering is added beyond what NumPy does inside a
+single ``sum``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _eps64(eps) -> float:
+    # The GPU receives eps as an FP32 value; the oracle widens that exact value.
+    return float(np.float32(eps))
+
+
+def layer_norm(x, gamma, beta, eps=1e-5):
+    """LayerNorm forward of every row of ``x`` in float64.
+
+    Statistics, from "Rewriting the layer norm and matmul kernels", section
+    "A reduction has to meet somewhere" (the displayed equation)::
+
+        mu_i      = (1/d) * sum_j x_ij
+        sigma_i^2 = (1/d) * sum_j (x_ij - mu_i)^2        (biased, centred)
+
+    The pages print only these two statistics. The output step is the
+    standard layer-normalization affine map, with eps inside the root as in
+    the RMSNorm equation of "RMSNorm on an RTX 5070 ..." (section "The
+    operator and the change")::
+
+        rstd_i = (sigma_i^2 + eps)^(-1/2)
+        y_ij   = (x_ij - mu_i) * rstd_i * gamma_j + beta_j
+
+    Returns float64 (y [rows, d], mean [rows], rstd [rows]).
+    """
+    x64 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    g64 = np.asarray(gamma, dtype=np.float32).astype(np.float64)
+    b64 = np.asarray(beta, dtype=np.float32).astype(np.float64)
+    rows, d = x64.shape
+    if d == 0:
+        raise ValueError("d must be positive")
+    mu = x64.sum(axis=1) / d
+    dev = x64 - mu[:, None]
+    var = (dev * dev).sum(axis=1) / d
+    rstd = 1.0 / np.sqrt(var + _eps64(eps))
+    y = dev * rstd[:, None] * g64[None, :] + b64[None, :]
+    return y, mu, rstd
+
+
+def rms_norm(x, w, eps=1e-5):
+    """RMSNorm forward of every row of ``x`` in float64.
+
+    From "RMSNorm on an RTX 5070 ...", section "The operator and the change"
+    (the displayed equation)::
+
+        y_rc = x_rc * w_c * ( (1/D) * sum_j x_rj^2 + eps )^(-1/2)
+
+    Returns float64 (y [rows, d], r [rows]) where r is the per-row scale
+    ``(mean(x^2) + eps)^(-1/2)``.
+    """
+    x64 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    w64 = np.asarray(w, dtype=np.float32).astype(np.float64)
+    rows, d = x64.shape
+    if d == 0:
+        raise ValueError("d must be positive")
+    ms = (x64 * x64).sum(axis=1) / d
+    r = 1.0 / np.sqrt(ms + _eps64(eps))
+    y = x64 * w64[None, :] * r[:, None]
+    return y, r

@@ -1,0 +1,97 @@
+"""Element-by-element comparison of a device result with the float64 oracle.
+
+Tolerances:
+
+* y: ``|y - y_ref| <= 1e-5 + 1e-4 * |y_ref|`` for every element, the rule of
+  "RMSNorm on an RTX 5070 ..." (section "Correctness before timing"); a NaN
+  or Inf where the reference is finite fails.
+* mean: ``|mean - mu_ref| <= 1e-6 * max(|mu_ref|, mean_j |x_ij|)``. A bare
+  1e-6 relative bound is ill-posed for rows whose mean is near zero (an
+  N(0,1) row of width 768 has |mu| ~ 1e-5 while FP32 summation error is
+  ~1e-9 absolute), so the bound is taken relative to the row's magnitude.
+* rstd: ``|rstd - rstd_ref| <= 1e-6 * rstd_ref``.
+
+Guard regions (the same page) are stretches of sentinel values before and
+after each output; they must be bit-for-bit unchanged after the call, and a
+sentinel left inside the output region fails the y check.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+Y_ATOL = 1e-5
+Y_RTOL = 1e-4
+STAT_RTOL = 1e-6
+GUARD = 1024                     # elements of guard before and after an output
+SENTINEL_BITS = 0x7FC0DEAD       # a quiet NaN with a payload
+
+
+def sentinel_f32():
+    return np.array([SENTINEL_BITS], np.uint32).view(np.float32)[0]
+
+
+class ParityError(AssertionError):
+    pass
+
+
+def _first_bad(bad):
+    idx = np.argwhere(bad)
+    return tuple(int(i) for i in idx[0]) if len(idx) else None
+
+
+def check_y(y, y_ref, what="y"):
+    y = np.asarray(y, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    if y.shape != y_ref.shape:
+        raise ParityError(f"{what}: shape {y.shape} != {y_ref.shape}")
+    err = np.abs(y - y_ref)
+    lim = Y_ATOL + Y_RTOL * np.abs(y_ref)
+    bad = ~(err <= lim)           # NaN in y fails
+    if bad.any():
+        i = _first_bad(bad)
+        raise ParityError(f"{what}: {int(bad.sum())} elements out of tolerance; first at {i}: "
+                          f"got {y[i]!r}, want {y_ref[i]!r}")
+    return float(err.max()) if err.size else 0.0
+
+
+def check_mean(mean, mu_ref, x, what="mean"):
+    mean = np.asarray(mean, np.float64)
+    mu_ref = np.asarray(mu_ref, np.float64)
+    scale = np.maximum(np.abs(mu_ref), np.abs(np.asarray(x, np.float64)).mean(axis=1))
+    err = np.abs(mean - mu_ref)
+    bad = ~(err <= STAT_RTOL * scale)
+    if bad.any():
+        i = _first_bad(bad)
+        raise ParityError(f"{what}: {int(bad.sum())} rows out of tolerance; first row {i}: "
+                          f"got {mean[i]!r}, want {mu_ref[i]!r}")
+    with np.errstate(invalid="ignore", divide="ignore"):
+        rel = np.where(scale > 0, err / scale, err)
+    return float(rel.max()) if rel.size else 0.0
+
+
+def check_rstd(rstd, rstd_ref, what="rstd"):
+    rstd = np.asarray(rstd, np.float64)
+    rstd_ref = np.asarray(rstd_ref, np.float64)
+    err = np.abs(rstd - rstd_ref)
+    bad = ~(err <= STAT_RTOL * np.abs(rstd_ref))
+    if bad.any():
+        i = _first_bad(bad)
+        raise ParityError(f"{what}: {int(bad.sum())} rows out of tolerance; first row {i}: "
+                          f"got {rstd[i]!r}, want {rstd_ref[i]!r}")
+    rel = err / np.abs(rstd_ref)
+    return float(rel.max()) if rel.size else 0.0
+
+
+def check_guards(buf, n, what="guard"):
+    """``buf`` holds GUARD sentinels, n outputs, GUARD sentinels (as FP32)."""
+    bits = np.asarray(buf, np.float32).view(np.uint32)
+    if bits.shape[0] != n + 2 * GUARD:
+        raise ParityError(f"{what}: buffer length {bits.shape[0]} != {n + 2 * GUARD}")
+    head, tail = bits[:GUARD], bits[GUARD + n:]
+    if not (np.all(head == SENTINEL_BITS) and np.all(tail == SENTINEL_BITS)):
+        raise ParityError(f"{what}: guard region overwritten")
+
+
+def guarded(n):
+    """A host buffer of n outputs framed by guards, every element a sentinel."""
+    return np.full(n + 2 * GUARD, SENTINEL_BITS, np.uint32).view(np.float32)
