@@ -1,0 +1,572 @@
+#!/usr/bin/env python3
+"""Benchmark of the row-wise normalization forward pass on GB300.
+
+Headline workload: LayerNorm FP32 forward, rows = 4096, d = 768 (the pages'
+harness shape), x ~ N(0,1), gamma ~ N(1,0.1), beta ~ N(0,0.1), seed 1,
+eps = 1e-5. One step = one ln_fwd call (one kernel) over that batch, with
+the L2 flushed before every step (a buffer of twice the L2 size written
+outside the timed events). Metric: algorithmic GB/s
+(4*rows*d read + 4*rows*d written + 8*d parameters + 8*rows statistics)
+over the CUDA-event duration of the launch, and its fraction of the
+measured HBM copy bandwidth.
+
+Also reported in the same JSON line: the e2e number (pinned host x in,
+device result back to pinned host, through the public API), the oracle on
+the host cores (``cpu_baseline``), the warm-L2 and CUDA-graph numbers of the
+headline shape, the empty-kernel launch floor, a same-session
+device-to-device copy, and the large / sweep shapes (cold L2) for both
+LayerNorm and RMSNorm.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank normalises its own batch of the same shape
+(rows are independent, so there is no collective on the data path); the
+step time is the max over ranks and ``value`` counts the bytes of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "LayerNorm/RMSNorm FP32 GB/s and % of HBM roofline (cold L2) at 1 GB300"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+# ---------------------------------------------------------------------------
+# bytes and peaks
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(op: str, rows: int, d: int) -> int:
+    """Bytes the operation must move at least once: x in, y out, the
+    parameter vectors, and (LayerNorm) the per-row mean and rstd."""
+    if op == "ln":
+        return 8 * rows * d + 8 * d + 8 * rows
+    return 8 * rows * d + 4 * d
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "row_wise_normalization_gb300", "csrc", "*"))):
+        if p.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(p).encode())
+            h.update(open(p, "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "rownorm.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_tag: str, current_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(PROFILES, f"{kernel_tag}.traffic.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if "=" in line and not line.lstrip().startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_hash") != current_hash:
+        return None
+    try:
+        return int(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.proc = None
+        self.out = None
+        self.windows = []
+
+    def start(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, name, t0, t1):
+        self.windows.append((name, t0, t1))
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.flush()
+
+    def _samples(self):
+        rows = []
+        try:
+            with open(self.out.name) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = time.mktime(time.strptime(parts[0].split(".")[0],
+                                                       "%Y/%m/%d %H:%M:%S"))
+                        frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                        rows.append(dict(t=ts + frac, sm=float(parts[2]), smax=float(parts[3]),
+                                         active=parts[5], hw=parts[6], hwt=parts[7],
+                                         swt=parts[8], swp=parts[9]))
+                    except (ValueError, IndexError):
+                        continue
+        finally:
+            try:
+                os.unlink(self.out.name)
+            except OSError:
+                pass
+        return rows
+
+    def summary(self, window: str):
+        rows = self._samples()
+        sel = []
+        for name, t0, t1 in self.windows:
+            if name == window:
+                sel = [r for r in rows if t0 - 0.01 <= r["t"] <= t1 + 0.01]
+        label = window
+        if len(sel) < 3:
+            # the timed region is shorter than a few sampling intervals: use
+            # every sample taken while the benchmark kept the GPU busy
+            sel = [r for r in rows
+                   if any(t0 <= r["t"] <= t1 for _, t0, t1 in self.windows)]
+            label = "all measured regions"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "none (nvidia-smi unavailable)"}
+        reasons = set()
+        for r in sel:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in sel),
+                "sm_max_mhz": max(r["smax"] for r in sel),
+                "reasons": sorted(reasons), "samples": len(sel), "window": label}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class Flusher:
+    """Writes a buffer of twice the L2 size, leaving no input in L2."""
+
+    def __init__(self, torch, device):
+        props = torch.cuda.get_device_properties(device)
+        l2 = getattr(props, "L2_cache_size", 0) or (128 << 20)
+        self.nbytes = 2 * l2
+        self.buf = torch.empty(self.nbytes // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_launches(torch, launch, steps, flush=None):
+    """Per-launch device time (ms) of `launch`, CUDA events on the current
+    stream; `flush` (if any) runs before each launch, outside the events."""
+    s = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        if flush is not None:
+            flush()
+        a.record(s)
+        launch()
+        b.record(s)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+class LnCase:
+    """Device-resident inputs/outputs of one workload and its C-ABI launch."""
+
+    def __init__(self, torch, wl, device):
+        from row_wise_normalization_gb300 import capi
+
+        self.capi = capi
+        self.wl = wl
+        self.torch = torch
+        x = wl.x()
+        self.x = torch.from_numpy(x).to(device)
+        self.params = [torch.from_numpy(p).to(device) for p in wl.params()]
+        self.y = torch.empty_like(self.x)
+        self.mean = torch.empty(wl.rows, dtype=torch.float32, device=device)
+        self.rstd = torch.empty(wl.rows, dtype=torch.float32, device=device)
+        self.bytes = algorithmic_bytes(wl.op, wl.rows, wl.d)
+        self.x_host = x
+
+    def launch(self):
+        s = self.torch.cuda.current_stream().cuda_stream
+        c = self.capi
+        if self.wl.op == "ln":
+            st = c.ln_fwd(self.x.data_ptr(), self.params[0].data_ptr(), self.params[1].data_ptr(),
+                          self.y.data_ptr(), self.mean.data_ptr(), self.rstd.data_ptr(),
+                          self.wl.rows, self.wl.d, self.wl.eps, s)
+        else:
+            st = c.rms_fwd(self.x.data_ptr(), self.params[0].data_ptr(), self.y.data_ptr(),
+                           self.wl.rows, self.wl.d, self.wl.eps, s)
+        if st != c.RN_OK:
+            c.check(st)
+
+    def plan(self):
+        c = self.capi
+        op = c.RN_OP_LN if self.wl.op == "ln" else c.RN_OP_RMS
+        p = c.plan(op, c.RN_VARIANT_AUTO, self.wl.d, self.x.data_ptr(), self.y.data_ptr())
+        return {"variant": c.variant_name(p.variant), "vec": p.vec, "slots": p.slots,
+                "threads_per_row": p.threads_per_row, "threads_per_cta": p.threads_per_cta}
+
+
+def gbs(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9
+
+
+def cpu_baseline_leg(case_wl, gpu_result=None, seconds=10.0):
+    """Time the C oracle (as it stands) on the host: whole passes over the
+    headline batch until `seconds` have elapsed. Also the parity gate: the
+    oracle's output for that batch is compared with the GPU's."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import c_oracle
+
+    x = case_wl.x()
+    params = case_wl.params()
+    fn = c_oracle.layer_norm if case_wl.op == "ln" else c_oracle.rms_norm
+    out = fn(x, *params, case_wl.eps)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        fn(x, *params, case_wl.eps)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    nbytes = algorithmic_bytes(case_wl.op, case_wl.rows, case_wl.d)
+    parity = None
+    if gpu_result is not None:
+        import parity as P
+
+        try:
+            P.check_y(gpu_result[0], out[0])
+            if case_wl.op == "ln":
+                P.check_mean(gpu_result[1], out[1], x)
+                P.check_rstd(gpu_result[2], out[2])
+            parity = "pass"
+        except AssertionError as e:
+            parity = f"FAIL: {e}"
+    return {"value": nbytes * n / el / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole passes of the C float64 oracle over {case_wl.rows}x{case_wl.d} "
+                      f"({case_wl.op}), single thread, {el:.1f} s",
+            "cpu": platform.processor() or platform.machine(),
+            "host_cores_available": len(os.sched_getaffinity(0))}, parity
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from row_wise_normalization_gb300 import capi
+
+    capi.load()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    peak, peak_src = hbm_peak()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    seed_shift = 1000 * rank
+    base = workloads.ln_4096x768()
+    wl = workloads.Workload(base.op, base.rows, base.d, base.seed + seed_shift, tag=base.tag)
+    case = LnCase(torch, wl, device)
+    flush = Flusher(torch, device)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+
+    # warm-up
+    for _ in range(args.warmup):
+        flush()
+        case.launch()
+    barrier()
+
+    # ---- timed region: exactly K steps, L2 flushed before each ---------------
+    t0 = time.time()
+    times = time_launches(torch, case.launch, args.steps, flush)
+    barrier()
+    t1 = time.time()
+    if sampler:
+        sampler.mark("timed", t0, t1)
+    step_ms = statistics.fmean(times)
+    if dist is not None:
+        tt = torch.tensor([step_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms = float(tt.item())
+    value = gbs(case.bytes * world, step_ms)
+
+    # ---- e2e through the public API with pinned host buffers ----------------
+    import row_wise_normalization_gb300 as rn
+
+    xh = torch.from_numpy(case.x_host).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    mh = torch.empty(wl.rows, dtype=torch.float32).pin_memory()
+    rh = torch.empty(wl.rows, dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(case.x)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        y, m, r = rn.ln_fwd(xd, case.params[0], case.params[1], wl.eps,
+                            y=case.y, mean=case.mean, rstd=case.rstd)
+        yh.copy_(y, non_blocking=True)
+        mh.copy_(m, non_blocking=True)
+        rh.copy_(r, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    t2 = time.time()
+    e2e_times = time_launches(torch, e2e_step, args.steps, flush)
+    barrier()
+    if sampler:
+        sampler.mark("e2e", t2, time.time())
+    e2e_ms = statistics.fmean(e2e_times)
+    if dist is not None:
+        tt = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = 4 * wl.rows * wl.d
+    d2h = 4 * wl.rows * wl.d + 8 * wl.rows
+
+    if rank != 0:
+        return None
+
+    # ---- context measurements (rank 0 only) ---------------------------------
+    extra = {}
+    warm = time_launches(torch, case.launch, args.steps)
+    extra["headline_warm_l2"] = {"ms_median": statistics.median(warm),
+                                 "GBps": gbs(case.bytes, statistics.median(warm))}
+    # CUDA graph of 64 back-to-back launches (warm), per-launch average
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        case.launch()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(64):
+                case.launch()
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    gt = time_launches(torch, g.replay, 15)
+    extra["headline_graph64_warm"] = {"us_per_launch_median": 1e3 * statistics.median(gt) / 64}
+    pl = case.plan()
+    n_sm = torch.cuda.get_device_properties(device).multi_processor_count
+    empty = time_launches(torch, lambda: capi.check(capi.launch_empty(
+        n_sm, pl["threads_per_cta"], torch.cuda.current_stream().cuda_stream)), args.steps)
+    extra["empty_kernel_us_median"] = 1e3 * statistics.median(empty)
+
+    sweep = []
+    if not args.no_sweep:
+        cases = [workloads.large_32768x8192("ln"), workloads.large_32768x8192("rms")]
+        cases += [w for w in workloads.sweep_offset()]
+        t3 = time.time()
+        for w in cases:
+            c = LnCase(torch, w, device)
+            for _ in range(3):
+                flush()
+                c.launch()
+            ts = time_launches(torch, c.launch, args.sweep_steps, flush)
+            med = statistics.median(ts)
+            sweep.append({"workload": w.tag, "op": w.op, "rows": w.rows, "d": w.d,
+                          "plan": c.plan(), "ms_median": med, "GBps": gbs(c.bytes, med),
+                          "frac_of_measured_hbm": gbs(c.bytes, med) / peak})
+            del c
+        # same-session roofline control: a device-to-device copy of 1 GiB
+        src = torch.empty(1 << 28, dtype=torch.float32, device=device)
+        dst = torch.empty_like(src)
+        ts = time_launches(torch, lambda: dst.copy_(src), args.sweep_steps, flush)
+        med = statistics.median(ts)
+        extra["d2d_copy_1GiB"] = {"ms_median": med, "GBps": gbs(2 * src.numel() * 4, med)}
+        del src, dst
+        if sampler:
+            sampler.mark("sweep", t3, time.time())
+    extra["sweep_cold_l2"] = sweep
+
+    clocks = None
+    if sampler:
+        sampler.stop()
+        clocks = sampler.summary("timed")
+
+    # ---- CPU baseline + parity gate (oracle on the host cores) --------------
+    gpu_out = (case.y.cpu().numpy(), case.mean.cpu().numpy(), case.rstd.cpu().numpy())
+    cpu, parity = cpu_baseline_leg(wl, gpu_out, seconds=args.cpu_seconds)
+    if parity != "pass":
+        print(f"parity gate failed: {parity}", file=sys.stderr)
+
+    h = source_hash()
+    traffic = recorded_traffic("ln_4096x768", h)
+    achieved = gbs(case.bytes, statistics.fmean(times))
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded NumPy: x ~ N(0,1), gamma ~ N(1,0.1), beta ~ N(0,0.1))",
+        "config": {"workload": "layernorm_fwd_fp32_4096x768", "rows": wl.rows, "d": wl.d,
+                   "eps": wl.eps, "seed": wl.seed, "op": "ln_fwd",
+                   "l2": f"flushed before every step ({flush.nbytes >> 20} MiB written, "
+                         "outside the timed events)",
+                   "rows_per_rank": wl.rows, "parallelism": f"rows sharded, {world} rank(s)",
+                   "plan": pl},
+        "e2e": {"value": gbs(case.bytes * world, e2e_ms), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms,
+                "path": "pinned host x -> device, ln_fwd via the Python binding, "
+                        "y/mean/rstd -> pinned host, per step"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6800 GB/s",
+                     "kernel": f"reg_kernel ({pl['variant']}), one launch per step"},
+        "cpu_baseline": cpu,
+        "parity": parity,
+        "clocks": clocks,
+        "extra": extra,
+        "source_hash": h,
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle as it stands, on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from oracle import c_oracle
+
+    wl = workloads.ln_4096x768()
+    x = wl.x()
+    g, b = wl.params()
+    nbytes = algorithmic_bytes("ln", wl.rows, wl.d)
+    for _ in range(args.warmup):
+        c_oracle.layer_norm(x, g, b, wl.eps)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        c_oracle.layer_norm(x, g, b, wl.eps)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.fmean(times)
+    value = gbs(nbytes, ms)
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded NumPy)",
+        "config": {"workload": "layernorm_fwd_fp32_4096x768", "rows": wl.rows, "d": wl.d,
+                   "eps": wl.eps, "seed": wl.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step one whole pass of the C float64 oracle over "
+                                   f"{wl.rows}x{wl.d}, single thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--sweep-steps", type=int, default=20)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,159 @@
+/*
+ * rownorm.h -- C ABI of the GB300 (sm_103a) row-wise normalization library.
+ *
+ * Two operations over a contiguous, row-major FP32 matrix x[rows][d]:
+ *
+ *   LayerNorm:  mu_i      = (1/d) sum_j x_ij
+ *               sigma_i^2 = (1/d) sum_j (x_ij - mu_i)^2
+ *     (the statistics equation of "Rewriting the layer norm and matmul
+ *     kernels", section "A reduction has to meet somewhere"), then
+ *               rstd_i = (sigma_i^2 + eps)^(-1/2)
+ *               y_ij   = (x_ij - mu_i) * rstd_i * gamma_j + beta_j
+ *     (the standard affine output; eps inside the root as in the RMSNorm
+ *     equation below).
+ *
+ *   RMSNorm:    y_rc = x_rc * w_c * ((1/D) sum_j x_rj^2 + eps)^(-1/2)
+ *     ("RMSNorm on an RTX 5070: why more reduction threads did not win every
+ *     shape", section "The operator and the change", displayed equation).
+ *
+ * Conventions shared by every entry point:
+ *
+ *   Memory      All array pointers are DEVICE pointers (cudaMalloc'd or any
+ *               memory the GPU can address). The caller owns every buffer;
+ *               the library allocates nothing and never synchronizes. Rows
+ *               are contiguous with row stride d (in elements). Every pointer
+ *               must be 4-byte aligned; no other alignment is required
+ *               (16-byte aligned rows take the vector path, others a scalar
+ *               head/tail or the scalar path).
+ *   Stream      `stream` is a cudaStream_t passed as void*; NULL means the
+ *               legacy default stream. Work is enqueued asynchronously; the
+ *               results are valid once the stream has reached that point.
+ *   Sizes       rows == 0 is a no-op returning RN_OK (pointers may then be
+ *               NULL). rows < 0, d <= 0, or rows*d beyond 2^61 elements
+ *               returns RN_ERR_SIZE.
+ *   eps         Must be finite and >= 0, else RN_ERR_EPS. eps == 0 is
+ *               allowed (an all-zero row then gives Inf/NaN, as it should).
+ *   Aliasing    No output may overlap any input or another output
+ *               (RN_ERR_ALIAS); x, gamma, beta and w are read through the
+ *               read-only data path, which assumes they do not change while
+ *               the kernel runs. In-place normalization is not supported.
+ *   Errors      Validation happens on the host before anything is enqueued;
+ *               on any non-RN_OK status nothing was launched, except
+ *               RN_ERR_CUDA, which reports a launch error from the CUDA
+ *               runtime (the cudaError_t is kept per thread and returned by
+ *               rn_last_cuda_error()).
+ *   Threads     Every entry point may be called from several host threads.
+ */
+#ifndef ROWNORM_H
+#define ROWNORM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rn_status {
+    RN_OK = 0,
+    RN_ERR_NULL = 1,    /* a required pointer is NULL while rows > 0          */
+    RN_ERR_SIZE = 2,    /* rows < 0, d <= 0, or rows * d too large             */
+    RN_ERR_EPS = 3,     /* eps < 0, NaN or infinite                            */
+    RN_ERR_ALIAS = 4,   /* an output overlaps an input or another output      */
+    RN_ERR_CUDA = 5,    /* the CUDA runtime reported an error on launch       */
+    RN_ERR_ALIGN = 6,   /* a pointer is not 4-byte aligned                     */
+    RN_ERR_VARIANT = 7  /* a forced variant cannot run this shape / alignment  */
+} rn_status;
+
+/*
+ * LayerNorm forward.
+ *   x        [rows][d]  input, read once from HBM
+ *   gamma    [d]        scale
+ *   beta     [d]        shift
+ *   y        [rows][d]  output
+ *   mean_out [rows]     per-row mean mu_i (FP32); may be NULL (not written)
+ *   rstd_out [rows]     per-row (sigma_i^2 + eps)^(-1/2), the factor that
+ *                       scaled the row (FP32); may be NULL (not written)
+ * Statistics are accumulated in FP32 from the values held on chip: the row
+ * mean first, then the centred sum of squares about it (no E[x^2] - mu^2
+ * cancellation). One kernel launch per call.
+ */
+int ln_fwd(const float *x, const float *gamma, const float *beta,
+           float *y, float *mean_out, float *rstd_out,
+           int64_t rows, int64_t d, float eps, void *stream);
+
+/*
+ * RMSNorm forward.
+ *   x [rows][d] input, w [d] weight, y [rows][d] output.
+ * One kernel launch per call.
+ */
+int rms_fwd(const float *x, const float *w, float *y,
+            int64_t rows, int64_t d, float eps, void *stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char *rn_status_str(int status);
+
+/* The cudaError_t behind the last RN_ERR_CUDA returned on this thread
+ * (0 if none). */
+int rn_last_cuda_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Kernel variants. ln_fwd / rms_fwd pick one from d and pointer alignment;
+ * the *_variant entry points force one (testing and tuning) and return
+ * RN_ERR_VARIANT if it cannot run the request.
+ *
+ *   RN_VARIANT_WARP     one warp per row, row held in registers (narrow d)
+ *   RN_VARIANT_BLOCK    a multi-warp CTA per row, row held in registers
+ *   RN_VARIANT_STAGED   row copied to shared memory by the bulk-copy (TMA)
+ *                       engine, then reduced and written from there
+ *   RN_VARIANT_STREAM   any width: statistics in one streaming read, the
+ *                       output in a second (x is read twice)
+ * ------------------------------------------------------------------------ */
+enum {
+    RN_VARIANT_AUTO = 0,
+    RN_VARIANT_WARP = 1,
+    RN_VARIANT_BLOCK = 2,
+    RN_VARIANT_STAGED = 3,
+    RN_VARIANT_STREAM = 4,
+    RN_VARIANT_COUNT = 5
+};
+
+/* Which kernel configuration a call would launch (host-only; no CUDA call). */
+typedef struct rn_plan {
+    int variant;          /* RN_VARIANT_* actually chosen                      */
+    int vec;              /* elements per vector access: 4 or 1                */
+    int slots;            /* vectors held per thread (register variants)      */
+    int threads_per_row;  /* threads cooperating on one row                    */
+    int rows_per_cta;     /* rows a CTA works on at once                       */
+    int threads_per_cta;
+    int smem_bytes;       /* dynamic shared memory per CTA                     */
+} rn_plan;
+
+enum { RN_OP_LN = 0, RN_OP_RMS = 1 };
+
+/* Fill *plan for op RN_OP_LN / RN_OP_RMS, the requested variant (or AUTO),
+ * width d and the pointers' alignment (x, y, and the parameter vectors p0 =
+ * gamma or w, p1 = beta or NULL). Returns RN_OK, RN_ERR_SIZE or
+ * RN_ERR_VARIANT. Performs no CUDA call. */
+int rn_plan_for(int op, int variant, int64_t d, const void *x, const void *y,
+                const void *p0, const void *p1, rn_plan *plan);
+
+/* Short static name of a variant ("warp", "block", ...). */
+const char *rn_variant_name(int variant);
+
+int ln_fwd_variant(int variant, const float *x, const float *gamma, const float *beta,
+                   float *y, float *mean_out, float *rstd_out,
+                   int64_t rows, int64_t d, float eps, void *stream);
+
+int rms_fwd_variant(int variant, const float *x, const float *w, float *y,
+                    int64_t rows, int64_t d, float eps, void *stream);
+
+/* Measurement aid: launch an empty kernel with `grid` CTAs of `threads`
+ * threads on `stream` (the launch-latency floor small shapes are compared
+ * against). grid in [1, 2^31), threads in [1, 1024], else RN_ERR_SIZE. */
+int rn_launch_empty(int64_t grid, int threads, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROWNORM_H */

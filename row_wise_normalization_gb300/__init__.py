@@ -1,0 +1,90 @@
+"""Row-wise LayerNorm / RMSNorm forward on GB300 (sm_103a).
+
+A thin torch-facing binding over the C ABI of ``librownorm.so``
+(include/rownorm.h): it checks tensor shapes and dtypes, allocates outputs
+with torch when the caller does not pass them, and hands raw device pointers
+and the current CUDA stream to the library. Every arithmetic step runs in the
+library's CUDA kernels; if the library is missing, calls raise.
+"""
+from __future__ import annotations
+
+from . import capi
+from .capi import RowNormError, load  # noqa: F401
+
+__all__ = ["ln_fwd", "rms_fwd", "capi", "RowNormError", "load"]
+
+
+def _stream_handle(t, stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_f32_cuda(name, t):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, stream=None,
+           variant: int = capi.RN_VARIANT_AUTO):
+    """LayerNorm forward over the last dimension of ``x``.
+
+    Returns ``(y, mean, rstd)``: y like x; mean and rstd of shape x.shape[:-1]
+    (FP32). Output tensors may be passed in (contiguous FP32 CUDA).
+    """
+    import torch
+
+    _check_f32_cuda("x", x)
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    for n, t in (("gamma", gamma), ("beta", beta)):
+        _check_f32_cuda(n, t)
+        if t.numel() != d:
+            raise ValueError(f"{n} must have {d} elements")
+    if y is None:
+        y = torch.empty_like(x)
+    if mean is None:
+        mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    for n, t, k in (("y", y, x.numel()), ("mean", mean, rows), ("rstd", rstd, rows)):
+        _check_f32_cuda(n, t)
+        if t.numel() != k:
+            raise ValueError(f"{n} must have {k} elements")
+    st = capi.ln_fwd_variant(variant, x.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
+                             y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), rows, d,
+                             float(eps), _stream_handle(x, stream))
+    capi.check(st)
+    return y, mean, rstd
+
+
+def rms_fwd(x, w, eps: float = 1e-5, *, y=None, stream=None,
+            variant: int = capi.RN_VARIANT_AUTO):
+    """RMSNorm forward over the last dimension of ``x``; returns y."""
+    import torch
+
+    _check_f32_cuda("x", x)
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    _check_f32_cuda("w", w)
+    if w.numel() != d:
+        raise ValueError(f"w must have {d} elements")
+    if y is None:
+        y = torch.empty_like(x)
+    _check_f32_cuda("y", y)
+    if y.numel() != x.numel():
+        raise ValueError("y must be shaped like x")
+    st = capi.rms_fwd_variant(variant, x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, d,
+                              float(eps), _stream_handle(x, stream))
+    capi.check(st)
+    return y

@@ -1,0 +1,130 @@
+"""ctypes declarations of the C ABI in include/rownorm.h.
+
+Argument marshalling only: every function here is the C entry point of
+``librownorm.so`` with its argument and return types set. Pointers are plain
+integers (device addresses), sizes are int64, eps is float32 and the stream
+is a ``cudaStream_t`` passed as an integer (0 = legacy default stream).
+
+Importing this module does not load the library; ``load()`` does, and fails
+loudly if the library has not been built: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librownorm.so")
+
+RN_OK = 0
+RN_ERR_NULL = 1
+RN_ERR_SIZE = 2
+RN_ERR_EPS = 3
+RN_ERR_ALIAS = 4
+RN_ERR_CUDA = 5
+RN_ERR_ALIGN = 6
+RN_ERR_VARIANT = 7
+
+RN_VARIANT_AUTO = 0
+RN_VARIANT_WARP = 1
+RN_VARIANT_BLOCK = 2
+RN_VARIANT_STAGED = 3
+RN_VARIANT_STREAM = 4
+RN_VARIANT_COUNT = 5
+
+RN_OP_LN = 0
+RN_OP_RMS = 1
+
+# Every function include/rownorm.h declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_INT = ctypes.c_int
+
+
+class rn_plan(ctypes.Structure):
+    _fields_ = [("variant", _INT), ("vec", _INT), ("slots", _INT), ("threads_per_row", _INT),
+                ("rows_per_cta", _INT), ("threads_per_cta", _INT), ("smem_bytes", _INT)]
+
+
+SIGNATURES = {
+    "ln_fwd": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+    "rms_fwd": (_INT, [_P, _P, _P, _I64, _I64, _F, _P]),
+    "rn_status_str": (ctypes.c_char_p, [_INT]),
+    "rn_last_cuda_error": (_INT, []),
+    "rn_plan_for": (_INT, [_INT, _INT, _I64, _P, _P, _P, _P, ctypes.POINTER(rn_plan)]),
+    "rn_variant_name": (ctypes.c_char_p, [_INT]),
+    "ln_fwd_variant": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+    "rms_fwd_variant": (_INT, [_INT, _P, _P, _P, _I64, _I64, _F, _P]),
+    "rn_launch_empty": (_INT, [_I64, _INT, _P]),
+}
+
+_lib = None
+
+
+class RowNormError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def load() -> ctypes.CDLL:
+    """Load librownorm.so (once) and declare every entry point."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run `python -m row_wise_normalization_gb300.build` "
+                "(or __graft_entry__.build()). There is no CPU fallback.")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return load().rn_status_str(status).decode()
+
+
+def check(status: int) -> None:
+    """Raise RowNormError for a non-RN_OK status."""
+    if status != RN_OK:
+        msg = status_str(status)
+        if status == RN_ERR_CUDA:
+            msg += f" (cudaError {load().rn_last_cuda_error()})"
+        raise RowNormError(status, msg)
+
+
+def plan(op: int, variant: int, d: int, x: int, y: int, p0: int = 0, p1: int = 0) -> rn_plan:
+    """The kernel configuration a call would launch (host only)."""
+    out = rn_plan()
+    check(load().rn_plan_for(op, variant, d, x, y, p0, p1, ctypes.byref(out)))
+    return out
+
+
+def variant_name(v: int) -> str:
+    return load().rn_variant_name(v).decode()
+
+
+# Raw entry points (device pointers as ints), same names as the C ABI.
+def ln_fwd(x, gamma, beta, y, mean_out, rstd_out, rows, d, eps, stream=0) -> int:
+    return load().ln_fwd(x, gamma, beta, y, mean_out, rstd_out, rows, d, eps, stream)
+
+
+def rms_fwd(x, w, y, rows, d, eps, stream=0) -> int:
+    return load().rms_fwd(x, w, y, rows, d, eps, stream)
+
+
+def ln_fwd_variant(variant, x, gamma, beta, y, mean_out, rstd_out, rows, d, eps, stream=0) -> int:
+    return load().ln_fwd_variant(variant, x, gamma, beta, y, mean_out, rstd_out, rows, d, eps,
+                                 stream)
+
+
+def rms_fwd_variant(variant, x, w, y, rows, d, eps, stream=0) -> int:
+    return load().rms_fwd_variant(variant, x, w, y, rows, d, eps, stream)
+
+
+def launch_empty(grid, threads, stream=0) -> int:
+    return load().rn_launch_empty(grid, threads, stream)

@@ -1,0 +1,163 @@
+// rn_device.cuh -- device helpers shared by the row-normalization kernels:
+// cache-hinted global loads and stores, warp and named-barrier primitives.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "rn_params.h"
+
+namespace rn {
+
+// ---------------------------------------------------------------------------
+// Global memory access.
+//
+// x is streamed: read exactly once, so it bypasses L1 (no_allocate) and asks
+// L2 to fetch whole 256-byte blocks. gamma/beta/w are re-read by every row, so
+// they go through the read-only path with L1 allocation. y is written once and
+// never re-read by the kernel, so it is stored with the streaming (.cs) hint.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 ld_x4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_x1(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_p4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_p1(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_y4(float* p, float a, float b, float c, float d) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_y1(float* p, float a) {
+    asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(a) : "memory");
+}
+
+// Vector of VEC consecutive floats (VEC = 4: one 128-bit access; VEC = 1: scalar).
+template <int VEC>
+struct Vec {
+    float v[VEC];
+};
+
+template <int VEC>
+__device__ __forceinline__ void ld_x(Vec<VEC>& r, const float* p) {
+    if constexpr (VEC == 4) {
+        float4 t = ld_x4(p);
+        r.v[0] = t.x; r.v[1] = t.y; r.v[2] = t.z; r.v[3] = t.w;
+    } else {
+        r.v[0] = ld_x1(p);
+    }
+}
+
+// Parameter vector at column j. `aligned` says whether p + j is 16-byte aligned.
+template <int VEC>
+__device__ __forceinline__ void ld_p(Vec<VEC>& r, const float* p, bool aligned) {
+    if constexpr (VEC == 4) {
+        if (aligned) {
+            float4 t = ld_p4(p);
+            r.v[0] = t.x; r.v[1] = t.y; r.v[2] = t.z; r.v[3] = t.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) r.v[k] = ld_p1(p + k);
+        }
+    } else {
+        r.v[0] = ld_p1(p);
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void st_y(float* p, const Vec<VEC>& r) {
+    if constexpr (VEC == 4) {
+        st_y4(p, r.v[0], r.v[1], r.v[2], r.v[3]);
+    } else {
+        st_y1(p, r.v[0]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Reductions.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Barrier over `nthreads` threads (a multiple of 32) using hardware barrier
+// `id` (1..15; 0 is __syncthreads). Every thread of the named group arrives.
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Cross-warp merge of per-warp LayerNorm partials published as float4
+// (count, sum, mean, M2) in slot[0..NW): returns the row mean
+// mu = sum_w sum_w / fd and M2 = sum_w [M2_w + n_w (mean_w - mu)^2] (the
+// parallel-axis rule). Few warps: every thread walks the slots; many warps:
+// lane k takes slot k and the warp reduces with shuffles.
+template <int NW>
+__device__ __forceinline__ void merge_ln_warps(const float (*slot)[4], int lane, float fd,
+                                               float& mu, float& M2) {
+    if constexpr (NW <= 8) {
+        float tot = 0.f;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) tot += slot[k][1];
+        mu = tot / fd;
+        float m2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            const float4 q4 = *reinterpret_cast<const float4*>(slot[k]);
+            const float dm = q4.z - mu;
+            m2 += fmaf(q4.x * dm, dm, q4.w);
+        }
+        M2 = m2;
+    } else {
+        float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < NW) q4 = *reinterpret_cast<const float4*>(slot[lane]);
+        mu = warp_sum(q4.y) / fd;
+        const float dm = q4.z - mu;
+        M2 = warp_sum(lane < NW ? fmaf(q4.x * dm, dm, q4.w) : 0.f);
+    }
+}
+
+// Sum of one float per warp published in slot[0..NW)[0].
+template <int NW, int STRIDE>
+__device__ __forceinline__ float merge_sum_warps(const float (*slot)[STRIDE], int lane) {
+    if constexpr (NW <= 8) {
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) s += slot[k][0];
+        return s;
+    } else {
+        return warp_sum(lane < NW ? slot[lane][0] : 0.f);
+    }
+}
+
+// Elements to the next 16-byte boundary of p (0..3), clamped to d.
+__device__ __forceinline__ int head_peel(const float* p, int64_t d) {
+    int h = (int)((0u - (unsigned)((uintptr_t)p >> 2)) & 3u);
+    return h > d ? (int)d : h;
+}
+
+}  // namespace rn

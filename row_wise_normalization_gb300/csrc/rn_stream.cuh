@@ -1,0 +1,159 @@
+// rn_stream.cuh -- streaming row kernel for any width (x read twice).
+//
+// One CTA per row (persistent over rows). The first read accumulates the row
+// statistics without holding the row: for LayerNorm each thread keeps a
+// running (count, mean, M2) and folds in one vector at a time with Chan's
+// pairwise update (the vector's own mean and centred square sum merged into
+// the running triple), warps merge lane triples through shuffles, and the
+// warps meet once in shared memory. The second read writes y. No width limit
+// and no shared memory beyond the exchange slots; it is the fallback for rows
+// the register-held and staged kernels cannot hold.
+#pragma once
+
+#include "rn_device.cuh"
+
+namespace rn {
+
+// (n, mean, M2) <- (n, mean, M2) merged with (nb, mb, Mb).
+__device__ __forceinline__ void chan_merge(float& n, float& m, float& M, float nb, float mb,
+                                           float Mb) {
+    const float nn = n + nb;
+    if (nn == 0.f) return;
+    const float f = nb * __frcp_rn(nn);
+    const float dl = mb - m;
+    m = fmaf(dl, f, m);
+    M = M + Mb + dl * dl * n * f;
+    n = nn;
+}
+
+template <int OP, int VEC, int TPB>
+__global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p) {
+    constexpr int W = TPB / 32;
+    __shared__ __align__(16) float xch[2][W][4];
+    const int t = threadIdx.x;
+    const int w = t >> 5, lane = t & 31;
+    const int64_t d = p.d;
+    const float fd = (float)d;
+
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
+        const float* xr = p.x + row * d;
+        float* yr = p.y + row * d;
+        int h = 0, tl = 0;
+        int64_t nv;
+        if constexpr (VEC == 4) {
+            h = head_peel(xr, d);
+            nv = (d - h) >> 2;
+            tl = (int)(d - h - 4 * nv);
+        } else {
+            nv = d;
+        }
+        const bool has_e = (VEC == 4) && (t < h + tl);
+        const int64_t ei = (t < h) ? (int64_t)t : (int64_t)h + 4 * nv + (t - h);
+        float(*slot)[4] = xch[it & 1];
+
+        float mu = 0.f, rs;
+        if constexpr (OP == OP_LN) {
+            float n = 0.f, m = 0.f, M = 0.f;
+            for (int64_t q = t; q < nv; q += TPB) {
+                Vec<VEC> v;
+                ld_x(v, xr + h + q * VEC);
+                float s = 0.f;
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) s += v.v[k];
+                const float mc = s * (1.0f / VEC);
+                float Mc = 0.f;
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) {
+                    const float c = v.v[k] - mc;
+                    Mc = fmaf(c, c, Mc);
+                }
+                chan_merge(n, m, M, (float)VEC, mc, Mc);
+            }
+            if (has_e) chan_merge(n, m, M, 1.f, ld_x1(xr + ei), 0.f);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float nb = __shfl_xor_sync(0xffffffffu, n, o);
+                const float mb = __shfl_xor_sync(0xffffffffu, m, o);
+                const float Mb = __shfl_xor_sync(0xffffffffu, M, o);
+                chan_merge(n, m, M, nb, mb, Mb);
+            }
+            if (lane == 0) *reinterpret_cast<float4*>(slot[w]) = make_float4(n, n * m, m, M);
+            __syncthreads();
+            float M2;
+            merge_ln_warps<W>(slot, lane, fd, mu, M2);
+            rs = rsqrtf(M2 / fd + p.eps);
+        } else {
+            float ss = 0.f;
+            for (int64_t q = t; q < nv; q += TPB) {
+                Vec<VEC> v;
+                ld_x(v, xr + h + q * VEC);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) ss = fmaf(v.v[k], v.v[k], ss);
+            }
+            if (has_e) {
+                const float e = ld_x1(xr + ei);
+                ss = fmaf(e, e, ss);
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) slot[w][0] = ss;
+            __syncthreads();
+            ss = merge_sum_warps<W, 4>(slot, lane);
+            rs = rsqrtf(ss / fd + p.eps);
+        }
+
+        bool pa = true;
+        if constexpr (VEC == 4) {
+            pa = ((((uintptr_t)p.p0 >> 2) + h) & 3) == 0;
+            if constexpr (OP == OP_LN) pa = pa && ((((uintptr_t)p.p1 >> 2) + h) & 3) == 0;
+        }
+        for (int64_t q = t; q < nv; q += TPB) {
+            const int64_t j = h + q * VEC;
+            Vec<VEC> v, a, o;
+            ld_x(v, xr + j);
+            ld_p(a, p.p0 + j, pa);
+            if constexpr (OP == OP_LN) {
+                Vec<VEC> b;
+                ld_p(b, p.p1 + j, pa);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) o.v[k] = fmaf((v.v[k] - mu) * rs, a.v[k], b.v[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) o.v[k] = v.v[k] * rs * a.v[k];
+            }
+            st_y(yr + j, o);
+        }
+        if (has_e) {
+            const float e = ld_x1(xr + ei);
+            const float a = ld_p1(p.p0 + ei);
+            float o;
+            if constexpr (OP == OP_LN)
+                o = fmaf((e - mu) * rs, a, ld_p1(p.p1 + ei));
+            else
+                o = e * rs * a;
+            st_y1(yr + ei, o);
+        }
+        if constexpr (OP == OP_LN) {
+            if (t == 0) {
+                if (p.mean) p.mean[row] = mu;
+                if (p.rstd) p.rstd[row] = rs;
+            }
+        }
+    }
+}
+
+template <int OP, int VEC>
+struct StreamInst {
+    static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
+        stream_kernel<OP, VEC, kStreamThreads><<<grid, kStreamThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    static const KernelEntry entry;
+};
+
+template <int OP, int VEC>
+const KernelEntry StreamInst<OP, VEC>::entry = {
+    (const void*)&stream_kernel<OP, VEC, kStreamThreads>, kStreamThreads, 1, 0,
+    &StreamInst<OP, VEC>::launch};
+
+}  // namespace rn

@@ -1,0 +1,282 @@
+// rownorm_api.cu -- the C ABI declared in include/rownorm.h: argument
+// validation, width/alignment dispatch and the launch of one kernel per call.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "rownorm.h"
+#include "rn_params.h"
+
+namespace rn {
+const KernelEntry* reg_entry_ln_v4(int slots, int tpr);
+const KernelEntry* reg_entry_ln_v1(int slots, int tpr);
+const KernelEntry* reg_entry_rms_v4(int slots, int tpr);
+const KernelEntry* reg_entry_rms_v1(int slots, int tpr);
+
+const KernelEntry* reg_entry(int op, int vec, int slots, int tpr) {
+    if (op == OP_LN) return vec == 4 ? reg_entry_ln_v4(slots, tpr) : reg_entry_ln_v1(slots, tpr);
+    return vec == 4 ? reg_entry_rms_v4(slots, tpr) : reg_entry_rms_v1(slots, tpr);
+}
+}  // namespace rn
+
+namespace {
+
+using namespace rn;
+
+__global__ void empty_kernel() {}
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int64_t kMaxElems = (int64_t)1 << 61;
+constexpr int kMaxDevices = 64;
+
+// Vectors (of `vec` floats) a row of width d needs held, excluding the <= 6
+// scalars of an unaligned head and tail.
+int64_t row_units(int64_t d, int vec) { return vec == 4 ? d / 4 : d; }
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Register-held CTA-per-row configuration: the fewest threads (>= 64, a power
+// of two) that hold the row in at most kMaxSlots vectors each.
+bool block_shape(int64_t units, int* tpr, int* slots) {
+    for (int t = 64; t <= 1024; t *= 2) {
+        if (units <= (int64_t)t * kMaxSlots) {
+            *tpr = t;
+            *slots = units == 0 ? 1 : ceil_div(units, t);
+            return true;
+        }
+    }
+    return false;
+}
+
+int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, rn_plan* pl) {
+    if (d <= 0) return RN_ERR_SIZE;
+    std::memset(pl, 0, sizeof(*pl));
+    // 16-byte vectors need x and y in the same 16-byte phase (a row's head
+    // peel then aligns both); otherwise every access is scalar.
+    const int vec = ((((uintptr_t)x ^ (uintptr_t)y) & 15u) == 0) ? 4 : 1;
+    const int64_t units = row_units(d, vec);
+    pl->vec = vec;
+
+    int v = variant;
+    if (v == RN_VARIANT_AUTO) {
+        if (units <= 32 * kMaxSlots)
+            v = RN_VARIANT_WARP;
+        else if (units <= 1024 * kMaxSlots)
+            v = RN_VARIANT_BLOCK;
+        else
+            v = RN_VARIANT_STREAM;
+    }
+    switch (v) {
+        case RN_VARIANT_WARP:
+            if (units > 32 * kMaxSlots) return RN_ERR_VARIANT;
+            pl->slots = units == 0 ? 1 : ceil_div(units, 32);
+            pl->threads_per_row = 32;
+            pl->rows_per_cta = kWarpRowsPerCta;
+            pl->threads_per_cta = 32 * kWarpRowsPerCta;
+            break;
+        case RN_VARIANT_BLOCK: {
+            int tpr, slots;
+            if (!block_shape(units, &tpr, &slots)) return RN_ERR_VARIANT;
+            pl->slots = slots;
+            pl->threads_per_row = tpr;
+            pl->rows_per_cta = 1;
+            pl->threads_per_cta = tpr;
+            break;
+        }
+        case RN_VARIANT_STREAM:
+            pl->slots = 0;
+            pl->threads_per_row = kStreamThreads;
+            pl->rows_per_cta = 1;
+            pl->threads_per_cta = kStreamThreads;
+            break;
+        default:
+            return RN_ERR_VARIANT;
+    }
+    pl->variant = v;
+    pl->smem_bytes = 0;
+    (void)op;
+    return RN_OK;
+}
+
+bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+    if (!a || !b || na <= 0 || nb <= 0) return false;
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    return pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
+}
+
+bool misaligned(const void* p) { return p && ((uintptr_t)p & 3u); }
+
+int validate(int op, const float* x, const float* p0, const float* p1, const float* y,
+             const float* mean, const float* rstd, int64_t rows, int64_t d, float eps) {
+    if (rows < 0 || d <= 0) return RN_ERR_SIZE;
+    if (rows > 0 && d > kMaxElems / rows) return RN_ERR_SIZE;
+    if (!std::isfinite(eps) || eps < 0.f) return RN_ERR_EPS;
+    if (rows == 0) return RN_OK;
+    if (!x || !y || !p0 || (op == OP_LN && !p1)) return RN_ERR_NULL;
+    if (misaligned(x) || misaligned(y) || misaligned(p0) || misaligned(p1) || misaligned(mean) ||
+        misaligned(rstd))
+        return RN_ERR_ALIGN;
+    const int64_t nx = rows * d * 4, np = d * 4, ns = rows * 4;
+    // outputs against inputs
+    const void* outs[3] = {y, mean, rstd};
+    const int64_t nouts[3] = {nx, ns, ns};
+    const void* ins[3] = {x, p0, p1};
+    const int64_t nins[3] = {nx, np, np};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j)
+            if (overlaps(outs[i], nouts[i], ins[j], nins[j])) return RN_ERR_ALIAS;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], nouts[i], outs[j], nouts[j])) return RN_ERR_ALIAS;
+    }
+    return RN_OK;
+}
+
+// CTAs of `e` that fit on the current device at once (0 on error).
+int resident_ctas(const KernelEntry* e, cudaError_t* err) {
+    struct Cache {
+        const void* fn;
+        int dev;
+        int n;
+    };
+    static thread_local Cache cache[16];
+    static thread_local int cache_next = 0;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return 0;
+    for (auto& c : cache)
+        if (c.fn == e->fn && c.dev == dev && c.n > 0) return c.n;
+    int sms = 0, per_sm = 0;
+    *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (*err != cudaSuccess) return 0;
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, e->fn, e->threads, e->smem_bytes);
+    if (*err != cudaSuccess) return 0;
+    const int n = (per_sm > 0 ? per_sm : 1) * sms;
+    cache[cache_next] = {e->fn, dev, n};
+    cache_next = (cache_next + 1) % 16;
+    return n;
+}
+
+int run(int op, int variant, const float* x, const float* p0, const float* p1, float* y,
+        float* mean, float* rstd, int64_t rows, int64_t d, float eps, void* stream) {
+    int st = validate(op, x, p0, p1, y, mean, rstd, rows, d, eps);
+    if (st != RN_OK) return st;
+    if (rows == 0) return RN_OK;
+    rn_plan pl;
+    st = plan_impl(op, variant, d, x, y, &pl);
+    if (st != RN_OK) return st;
+
+    const KernelEntry* e = nullptr;
+    if (pl.variant == RN_VARIANT_STREAM)
+        e = stream_entry(op, pl.vec);
+    else
+        e = reg_entry(op, pl.vec, pl.slots, pl.threads_per_row);
+    if (!e) return RN_ERR_VARIANT;
+
+    cudaError_t err = cudaSuccess;
+    const int resident = resident_ctas(e, &err);
+    if (err != cudaSuccess) {
+        g_last_cuda_error = (int)err;
+        return RN_ERR_CUDA;
+    }
+    const int64_t want = (rows + e->rows_per_cta - 1) / e->rows_per_cta;
+    const int grid = (int)(want < resident ? want : resident);
+
+    Params prm;
+    prm.x = x;
+    prm.y = y;
+    prm.p0 = p0;
+    prm.p1 = p1;
+    prm.mean = mean;
+    prm.rstd = rstd;
+    prm.rows = rows;
+    prm.d = d;
+    prm.eps = eps;
+    err = e->launch(prm, grid, (cudaStream_t)stream);
+    if (err != cudaSuccess) {
+        g_last_cuda_error = (int)err;
+        return RN_ERR_CUDA;
+    }
+    return RN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ln_fwd(const float* x, const float* gamma, const float* beta, float* y, float* mean_out,
+           float* rstd_out, int64_t rows, int64_t d, float eps, void* stream) {
+    return run(OP_LN, RN_VARIANT_AUTO, x, gamma, beta, y, mean_out, rstd_out, rows, d, eps, stream);
+}
+
+int rms_fwd(const float* x, const float* w, float* y, int64_t rows, int64_t d, float eps,
+            void* stream) {
+    return run(OP_RMS, RN_VARIANT_AUTO, x, w, nullptr, y, nullptr, nullptr, rows, d, eps, stream);
+}
+
+int ln_fwd_variant(int variant, const float* x, const float* gamma, const float* beta, float* y,
+                   float* mean_out, float* rstd_out, int64_t rows, int64_t d, float eps,
+                   void* stream) {
+    if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
+    return run(OP_LN, variant, x, gamma, beta, y, mean_out, rstd_out, rows, d, eps, stream);
+}
+
+int rms_fwd_variant(int variant, const float* x, const float* w, float* y, int64_t rows,
+                    int64_t d, float eps, void* stream) {
+    if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
+    return run(OP_RMS, variant, x, w, nullptr, y, nullptr, nullptr, rows, d, eps, stream);
+}
+
+int rn_plan_for(int op, int variant, int64_t d, const void* x, const void* y, const void* p0,
+                const void* p1, rn_plan* plan) {
+    (void)p0;
+    (void)p1;
+    if (!plan) return RN_ERR_NULL;
+    if (op != RN_OP_LN && op != RN_OP_RMS) return RN_ERR_VARIANT;
+    if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
+    return plan_impl(op, variant, d, x, y, plan);
+}
+
+const char* rn_status_str(int status) {
+    switch (status) {
+        case RN_OK: return "ok";
+        case RN_ERR_NULL: return "a required pointer is NULL";
+        case RN_ERR_SIZE: return "invalid size (rows < 0, d <= 0 or rows*d too large)";
+        case RN_ERR_EPS: return "eps must be finite and >= 0";
+        case RN_ERR_ALIAS: return "an output overlaps an input or another output";
+        case RN_ERR_CUDA: return "CUDA runtime error (see rn_last_cuda_error)";
+        case RN_ERR_ALIGN: return "a pointer is not 4-byte aligned";
+        case RN_ERR_VARIANT: return "the requested kernel variant cannot run this request";
+        default: return "unknown status";
+    }
+}
+
+int rn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int rn_launch_empty(int64_t grid, int threads, void* stream) {
+    if (grid < 1 || grid >= ((int64_t)1 << 31) || threads < 1 || threads > 1024)
+        return RN_ERR_SIZE;
+    empty_kernel<<<(unsigned)grid, threads, 0, (cudaStream_t)stream>>>();
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) {
+        g_last_cuda_error = (int)err;
+        return RN_ERR_CUDA;
+    }
+    return RN_OK;
+}
+
+const char* rn_variant_name(int variant) {
+    switch (variant) {
+        case RN_VARIANT_AUTO: return "auto";
+        case RN_VARIANT_WARP: return "warp";
+        case RN_VARIANT_BLOCK: return "block";
+        case RN_VARIANT_STAGED: return "staged";
+        case RN_VARIANT_STREAM: return "stream";
+        default: return "unknown";
+    }
+}
+
+}  // extern "C"

@@ -82,16 +82,16 @@ def check_rstd(rstd, rstd_ref, what="rstd"):
     return float(rel.max()) if rel.size else 0.0
 
 
-def check_guards(buf, n, what="guard"):
-    """``buf`` holds GUARD sentinels, n outputs, GUARD sentinels (as FP32)."""
+def check_guards(buf, n, what="guard", head=GUARD):
+    """``buf`` holds ``head`` sentinels, n outputs, GUARD sentinels (as FP32)."""
     bits = np.asarray(buf, np.float32).view(np.uint32)
-    if bits.shape[0] != n + 2 * GUARD:
-        raise ParityError(f"{what}: buffer length {bits.shape[0]} != {n + 2 * GUARD}")
-    head, tail = bits[:GUARD], bits[GUARD + n:]
+    if bits.shape[0] != n + head + GUARD:
+        raise ParityError(f"{what}: buffer length {bits.shape[0]} != {n + head + GUARD}")
+    head, tail = bits[:head], bits[head + n:]
     if not (np.all(head == SENTINEL_BITS) and np.all(tail == SENTINEL_BITS)):
         raise ParityError(f"{what}: guard region overwritten")
 
 
-def guarded(n):
+def guarded(n, head=GUARD):
     """A host buffer of n outputs framed by guards, every element a sentinel."""
-    return np.full(n + 2 * GUARD, SENTINEL_BITS, np.uint32).view(np.float32)
+    return np.full(n + head + GUARD, SENTINEL_BITS, np.uint32).view(np.float32)

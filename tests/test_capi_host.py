@@ -1,0 +1,131 @@
+"""The C-ABI library on the host: it loads, exports every symbol the header
+declares, and validates arguments before touching CUDA (no GPU needed)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from row_wise_normalization_gb300 import capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rownorm.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b([A-Za-z_]\w*)\s*\([^;{)]*(?:\([^)]*\)[^;{)]*)*\)\s*;", src)
+    return sorted(set(n for n in names if n not in ("if", "return", "sizeof")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return capi.load()
+
+
+def test_header_functions_parsed():
+    names = _declared_functions()
+    assert {"ln_fwd", "rms_fwd", "rn_status_str"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"librownorm.so does not export {name}"
+        assert name in capi.SIGNATURES, f"capi.py does not declare {name}"
+
+
+def test_status_strings(lib):
+    for s in range(0, 8):
+        assert capi.status_str(s)
+    assert capi.status_str(99) == "unknown status"
+    assert capi.variant_name(capi.RN_VARIANT_WARP) == "warp"
+
+
+A = 1 << 20   # fake, 16-byte aligned "device" addresses; never dereferenced
+
+
+def _ln(**kw):
+    args = dict(x=A, gamma=A + 0x100000, beta=A + 0x200000, y=A + 0x300000,
+                mean_out=0, rstd_out=0, rows=4, d=8, eps=1e-5, stream=0)
+    args.update(kw)
+    return capi.ln_fwd(**args)
+
+
+def test_validation_errors_without_launch(lib):
+    assert _ln(rows=-1) == capi.RN_ERR_SIZE
+    assert _ln(d=0) == capi.RN_ERR_SIZE
+    assert _ln(d=-3) == capi.RN_ERR_SIZE
+    assert _ln(rows=1 << 40, d=1 << 30) == capi.RN_ERR_SIZE
+    assert _ln(eps=-1e-5) == capi.RN_ERR_EPS
+    assert _ln(eps=math.nan) == capi.RN_ERR_EPS
+    assert _ln(eps=math.inf) == capi.RN_ERR_EPS
+    assert _ln(x=0) == capi.RN_ERR_NULL
+    assert _ln(y=0) == capi.RN_ERR_NULL
+    assert _ln(gamma=0) == capi.RN_ERR_NULL
+    assert _ln(beta=0) == capi.RN_ERR_NULL
+    assert _ln(x=A + 2) == capi.RN_ERR_ALIGN
+    assert _ln(mean_out=A + 0x400001) == capi.RN_ERR_ALIGN
+    # outputs overlapping inputs or each other
+    assert _ln(y=A + 4) == capi.RN_ERR_ALIAS
+    assert _ln(y=A + 0x100000 - 8) == capi.RN_ERR_ALIAS          # y's tail over gamma
+    assert _ln(mean_out=A + 0x200000 + 4) == capi.RN_ERR_ALIAS    # mean inside beta
+    assert _ln(mean_out=A + 0x400000, rstd_out=A + 0x400008) == capi.RN_ERR_ALIAS
+    assert capi.rms_fwd(A, A + 0x1000, A + 16, 4, 8, 1e-5, 0) == capi.RN_ERR_ALIAS
+    assert capi.rms_fwd(A, 0, A + 0x1000, 4, 8, 1e-5, 0) == capi.RN_ERR_NULL
+
+
+def test_empty_is_a_noop(lib):
+    assert _ln(rows=0, x=0, y=0, gamma=0, beta=0) == capi.RN_OK
+    assert capi.rms_fwd(0, 0, 0, 0, 5, 1e-5, 0) == capi.RN_OK
+    # eps zero is allowed
+    assert _ln(rows=0, eps=0.0) == capi.RN_OK
+
+
+def test_bad_variant(lib):
+    assert capi.ln_fwd_variant(99, A, A + 0x100000, A + 0x200000, A + 0x300000, 0, 0, 4, 8,
+                               1e-5, 0) == capi.RN_ERR_VARIANT
+    assert capi.rms_fwd_variant(-1, A, A + 0x1000, A + 0x2000, 4, 8, 1e-5, 0) == capi.RN_ERR_VARIANT
+
+
+@pytest.mark.parametrize("d,variant,tpr,slots", [
+    (1, capi.RN_VARIANT_WARP, 32, 1),
+    (128, capi.RN_VARIANT_WARP, 32, 1),
+    (768, capi.RN_VARIANT_WARP, 32, 6),
+    (1027, capi.RN_VARIANT_WARP, 32, 8),
+    (1028, capi.RN_VARIANT_BLOCK, 64, 5),
+    (4096, capi.RN_VARIANT_BLOCK, 128, 8),
+    (8193, capi.RN_VARIANT_BLOCK, 256, 8),
+    (32771, capi.RN_VARIANT_BLOCK, 1024, 8),
+    (32772, capi.RN_VARIANT_STREAM, 512, 0),
+])
+def test_plan_by_width(lib, d, variant, tpr, slots):
+    p = capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_AUTO, d, A, A + 0x1000000)
+    assert (p.variant, p.vec, p.threads_per_row, p.slots) == (variant, 4, tpr, slots)
+
+
+def test_plan_phase_mismatch_goes_scalar(lib):
+    p = capi.plan(capi.RN_OP_RMS, capi.RN_VARIANT_AUTO, 768, A, A + 4)
+    assert p.vec == 1 and p.variant == capi.RN_VARIANT_BLOCK
+    p = capi.plan(capi.RN_OP_RMS, capi.RN_VARIANT_AUTO, 200, A + 4, A + 0x1004)
+    assert p.vec == 4 and p.variant == capi.RN_VARIANT_WARP
+
+
+def test_forced_variant_limits(lib):
+    with pytest.raises(capi.RowNormError):
+        capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_WARP, 1028, A, A + 0x100000)
+    with pytest.raises(capi.RowNormError):
+        capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_BLOCK, 32772, A, A + 0x100000)
+    p = capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_STREAM, 5, A, A + 0x100000)
+    assert p.variant == capi.RN_VARIANT_STREAM
+
+
+def test_torch_binding_rejects_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    import row_wise_normalization_gb300 as rn
+    x = torch.zeros(2, 4)
+    with pytest.raises(ValueError):
+        rn.ln_fwd(x, torch.ones(4), torch.zeros(4))
+    with pytest.raises(ValueError):
+        rn.rms_fwd(x, torch.ones(4))

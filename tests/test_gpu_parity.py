@@ -1,0 +1,216 @@
+"""CUDA path against the float64 oracle, element by element (GPU required).
+
+Every call goes through the C ABI (ln_fwd_variant / rms_fwd_variant, AUTO and
+each forced kernel variant that accepts the width). Outputs are framed by
+sentinel guards that must survive, and the output region starts as
+sentinels, so a dropped element fails. Tolerances are those of
+``tests/parity.py``.
+"""
+import numpy as np
+import pytest
+
+import gpu_util as G
+import parity
+import workloads
+from oracle import reference
+from row_wise_normalization_gb300 import capi
+
+pytestmark = pytest.mark.gpu
+
+LN, RMS = capi.RN_OP_LN, capi.RN_OP_RMS
+
+
+def _check_ln(x, g, b, out, eps=1e-5):
+    y, mean, rstd = out
+    yr, mr, rr = reference.layer_norm(x, g, b, eps)
+    parity.check_y(y, yr)
+    if mean is not None:
+        parity.check_mean(mean, mr, x)
+        parity.check_rstd(rstd, rr)
+
+
+def _check_rms(x, w, y, eps=1e-5):
+    yr, _ = reference.rms_norm(x, w, eps)
+    parity.check_y(y, yr)
+
+
+# ---------------------------------------------------------------------------
+# the LayerNorm shapes: 512 x 128 (seed 0) and the harness shape 4096 x 768
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("wl", [workloads.ln_512x128(), workloads.ln_4096x768()],
+                         ids=lambda w: w.tag)
+def test_ln_configs_every_variant(wl):
+    x = wl.x()
+    g, b = wl.params()
+    for v in G.variants_for(LN, wl.d):
+        _check_ln(x, g, b, G.run_ln(x, g, b, wl.eps, variant=v))
+
+
+# ---------------------------------------------------------------------------
+# the RMSNorm case matrix: 512 rows x 7 widths x 4 patterns x every variant
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("wl", workloads.rms_512_matrix(), ids=lambda w: w.tag)
+def test_rms_case_matrix(wl):
+    x = wl.x()
+    (w,) = wl.params()
+    for v in G.variants_for(RMS, wl.d):
+        _check_rms(x, w, G.run_rms(x, w, wl.eps, variant=v))
+
+
+@pytest.mark.parametrize("d", workloads.RMS_WIDTHS)
+@pytest.mark.parametrize("pattern", workloads.PATTERNS)
+def test_ln_on_the_rms_case_matrix(d, pattern):
+    """LayerNorm over the same widths and patterns (zeros give y = beta)."""
+    wl = workloads.Workload("ln", 512, d, seed=2, x_dist=pattern)
+    x = wl.x()
+    g, b = wl.params()
+    for v in G.variants_for(LN, d):
+        _check_ln(x, g, b, G.run_ln(x, g, b, wl.eps, variant=v))
+
+
+# ---------------------------------------------------------------------------
+# the offset-row sweep (centred variance under a large per-row mean)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("wl", workloads.sweep_offset(), ids=lambda w: w.tag)
+def test_sweep_offset_rows(wl):
+    x = wl.x()
+    if wl.op == "ln":
+        g, b = wl.params()
+        for v in G.variants_for(LN, wl.d):
+            _check_ln(x, g, b, G.run_ln(x, g, b, wl.eps, variant=v))
+    else:
+        (w,) = wl.params()
+        for v in G.variants_for(RMS, wl.d):
+            _check_rms(x, w, G.run_rms(x, w, wl.eps, variant=v))
+
+
+# ---------------------------------------------------------------------------
+# ragged widths and every 16-byte phase of x, y and the parameters
+# ---------------------------------------------------------------------------
+PHASE_WIDTHS = [1, 2, 3, 5, 7, 31, 33, 127, 130, 769, 1027, 1029, 4099, 8193, 9000, 32771,
+                33001]
+
+
+@pytest.mark.parametrize("d", PHASE_WIDTHS)
+def test_phases_and_ragged_widths(d):
+    rows = 37
+    wl = workloads.Workload("ln", rows, d, seed=17, x_dist="offset", x_std=2.0)
+    x = wl.x()
+    g, b = wl.params()
+    for x_off, y_off, p_off in ((0, 0, 0), (1, 1, 0), (2, 2, 3), (3, 3, 1), (0, 1, 2), (3, 0, 0)):
+        for v in G.variants_for(LN, d, x_off, y_off):
+            _check_ln(x, g, b, G.run_ln(x, g, b, variant=v, x_off=x_off, y_off=y_off,
+                                        p_off=p_off))
+        for v in G.variants_for(RMS, d, x_off, y_off):
+            _check_rms(x, g, G.run_rms(x, g, variant=v, x_off=x_off, y_off=y_off, p_off=p_off))
+
+
+# ---------------------------------------------------------------------------
+# rows far beyond the resident grid: every CTA walks many rows
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("rows,d", [(200003, 64), (60001, 200), (20011, 1500), (3001, 40000)])
+def test_many_rows_per_cta(rows, d):
+    wl = workloads.Workload("ln", rows, d, seed=23)
+    x = wl.x()
+    g, b = wl.params()
+    _check_ln(x, g, b, G.run_ln(x, g, b))
+    _check_rms(x, g, G.run_rms(x, g))
+
+
+# ---------------------------------------------------------------------------
+# optional statistics, empty input, eps = 0
+# ---------------------------------------------------------------------------
+def test_statistics_optional():
+    wl = workloads.Workload("ln", 300, 768, seed=5)
+    x = wl.x()
+    g, b = wl.params()
+    for v in G.variants_for(LN, 768):
+        _check_ln(x, g, b, G.run_ln(x, g, b, variant=v, stats=False))
+
+
+def test_empty_rows_is_noop_on_device():
+    torch = G.torch_cuda()
+    y = G.Guarded(16)
+    xb, xp = G.dev_copy(np.ones(16, np.float32))
+    assert capi.ln_fwd(xp, xp, xp, y.ptr, 0, 0, 0, 16, 1e-5, G.stream_handle()) == capi.RN_OK
+    assert capi.rms_fwd(xp, xp, y.ptr, 0, 16, 1e-5, G.stream_handle()) == capi.RN_OK
+    torch.cuda.synchronize()
+    out = y.fetch("guard")
+    assert np.all(out.view(np.uint32) == parity.SENTINEL_BITS)
+
+
+def test_eps_zero_matches_oracle_including_nan():
+    """eps = 0 is accepted: zero rows then give NaN exactly where the oracle does."""
+    x = np.zeros((4, 33), np.float32)
+    x[1] = np.arange(33, dtype=np.float32) - 16
+    g = np.ones(33, np.float32)
+    b = np.zeros(33, np.float32)
+    y, mean, rstd = G.run_ln(x, g, b, eps=0.0)
+    with np.errstate(all="ignore"):
+        yr, mr, rr = reference.layer_norm(x, g, b, 0.0)
+    assert np.array_equal(np.isnan(y), np.isnan(yr))
+    parity.check_y(y[1], yr[1])
+    assert np.all(np.isinf(rstd[[0, 2, 3]]))
+    yq = G.run_rms(x, g, eps=0.0)
+    with np.errstate(all="ignore"):
+        yqr, _ = reference.rms_norm(x, g, 0.0)
+    assert np.array_equal(np.isnan(yq), np.isnan(yqr))
+
+
+def test_torch_binding_and_side_stream():
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn
+
+    wl = workloads.Workload("ln", 1000, 1000, seed=8)
+    x = wl.x()
+    g, b = wl.params()
+    s = torch.cuda.Stream()
+    xt = torch.from_numpy(x).cuda()
+    gt = torch.from_numpy(g).cuda()
+    bt = torch.from_numpy(b).cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        y, mean, rstd = rn.ln_fwd(xt, gt, bt)
+        yq = rn.rms_fwd(xt, gt)
+    s.synchronize()
+    _check_ln(x, g, b, (y.cpu().numpy(), mean.cpu().numpy(), rstd.cpu().numpy()))
+    _check_rms(x, g, yq.cpu().numpy())
+    # a 3-D input normalises its last dimension
+    y3, m3, r3 = rn.ln_fwd(xt.view(10, 100, 1000), gt, bt)
+    assert y3.shape == (10, 100, 1000) and m3.shape == (10, 100)
+    torch.testing.assert_close(y3.view(1000, 1000), y, rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# full size, in the launch configuration the benchmark times
+# ---------------------------------------------------------------------------
+@pytest.mark.slow
+@pytest.mark.parametrize("op", ["ln", "rms"])
+def test_full_size_32768x8192(op):
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn
+
+    wl = workloads.large_32768x8192(op)
+    x = wl.x()
+    xt = torch.from_numpy(x).cuda()
+    params = [torch.from_numpy(p).cuda() for p in wl.params()]
+    if op == "ln":
+        y, mean, rstd = rn.ln_fwd(xt, *params)
+        mean, rstd = mean.cpu().numpy(), rstd.cpu().numpy()
+    else:
+        y = rn.rms_fwd(xt, *params)
+    torch.cuda.synchronize()
+    yh = y.cpu().numpy()
+    del xt, y
+    p = [t.cpu().numpy() for t in params]
+    step = 2048
+    for r0 in range(0, wl.rows, step):
+        xs = x[r0:r0 + step]
+        if op == "ln":
+            yr, mr, rr = reference.layer_norm(xs, p[0], p[1], wl.eps)
+            parity.check_y(yh[r0:r0 + step], yr, what=f"y rows {r0}+")
+            parity.check_mean(mean[r0:r0 + step], mr, xs)
+            parity.check_rstd(rstd[r0:r0 + step], rr)
+        else:
+            yr, _ = reference.rms_norm(xs, p[0], wl.eps)
+            parity.check_y(yh[r0:r0 + step], yr, what=f"y rows {r0}+")
