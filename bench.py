@@ -194,16 +194,28 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 class Flusher:
-    """Writes a buffer of twice the L2 size, leaving no input in L2."""
+    """Writes a buffer of twice the L2 size, leaving no input in L2.
 
-    def __init__(self, torch, device):
+    mode "write": L2 is left full of dirty lines of that buffer, which the
+    timed kernel's own traffic must write back (the conservative cold case).
+    mode "clean": a second buffer of twice the L2 size is then read, so the
+    timed kernel starts with clean, unrelated lines in L2.
+    """
+
+    def __init__(self, torch, device, mode="write"):
         props = torch.cuda.get_device_properties(device)
         l2 = getattr(props, "L2_cache_size", 0) or (128 << 20)
         self.nbytes = 2 * l2
+        self.mode = mode
         self.buf = torch.empty(self.nbytes // 4, dtype=torch.float32, device=device)
+        self.rbuf = (torch.ones(self.nbytes // 4, dtype=torch.float32, device=device)
+                     if mode == "clean" else None)
+        self.sink = torch.empty(1, dtype=torch.float32, device=device)
 
     def __call__(self):
         self.buf.fill_(1.0)
+        if self.rbuf is not None:
+            self.sink.copy_(self.rbuf.amax().view(1))
 
 
 def time_launches(torch, launch, steps, flush=None):
@@ -259,6 +271,26 @@ class LnCase:
         p = c.plan(op, c.RN_VARIANT_AUTO, self.wl.d, self.x.data_ptr(), self.y.data_ptr())
         return {"variant": c.variant_name(p.variant), "vec": p.vec, "slots": p.slots,
                 "threads_per_row": p.threads_per_row, "threads_per_cta": p.threads_per_cta}
+
+
+NAMED = {
+    "ln_512x128": workloads.ln_512x128,
+    "ln_4096x768": workloads.ln_4096x768,
+    "ln_32768x8192": lambda: workloads.large_32768x8192("ln"),
+    "rms_32768x8192": lambda: workloads.large_32768x8192("rms"),
+}
+
+
+def pick_workload(name: str) -> workloads.Workload:
+    """A named workload, or op:rows:d (seed 1, x ~ N(0,1))."""
+    if name in NAMED:
+        return NAMED[name]()
+    try:
+        op, rows, d = name.split(":")
+        assert op in ("ln", "rms")
+        return workloads.Workload(op, int(rows), int(d), seed=1, tag=f"{op}_{rows}x{d}")
+    except (ValueError, AssertionError):
+        raise SystemExit(f"unknown workload {name!r}: one of {sorted(NAMED)} or op:rows:d")
 
 
 def gbs(nbytes, ms):
@@ -323,8 +355,9 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     seed_shift = 1000 * rank
-    base = workloads.ln_4096x768()
-    wl = workloads.Workload(base.op, base.rows, base.d, base.seed + seed_shift, tag=base.tag)
+    base = pick_workload(args.workload)
+    wl = workloads.Workload(base.op, base.rows, base.d, base.seed + seed_shift,
+                            base.x_dist, base.x_std, base.eps, tag=base.tag)
     case = LnCase(torch, wl, device)
     flush = Flusher(torch, device)
     sampler = ClockSampler(local_rank) if rank == 0 else None
@@ -362,11 +395,14 @@ def run_ours(args, rank, world, local_rank):
 
     def e2e_step():
         xd.copy_(xh, non_blocking=True)
-        y, m, r = rn.ln_fwd(xd, case.params[0], case.params[1], wl.eps,
-                            y=case.y, mean=case.mean, rstd=case.rstd)
+        if wl.op == "ln":
+            y, m, r = rn.ln_fwd(xd, case.params[0], case.params[1], wl.eps,
+                                y=case.y, mean=case.mean, rstd=case.rstd)
+            mh.copy_(m, non_blocking=True)
+            rh.copy_(r, non_blocking=True)
+        else:
+            y = rn.rms_fwd(xd, case.params[0], wl.eps, y=case.y)
         yh.copy_(y, non_blocking=True)
-        mh.copy_(m, non_blocking=True)
-        rh.copy_(r, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -382,13 +418,18 @@ def run_ours(args, rank, world, local_rank):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     h2d = 4 * wl.rows * wl.d
-    d2h = 4 * wl.rows * wl.d + 8 * wl.rows
+    d2h = 4 * wl.rows * wl.d + (8 * wl.rows if wl.op == "ln" else 0)
 
     if rank != 0:
         return None
 
     # ---- context measurements (rank 0 only) ---------------------------------
     extra = {}
+    clean = Flusher(torch, device, "clean")
+    ct = time_launches(torch, case.launch, args.steps, clean)
+    extra["headline_cold_clean_l2"] = {"ms_median": statistics.median(ct),
+                                       "GBps": gbs(case.bytes, statistics.median(ct))}
+    del clean
     warm = time_launches(torch, case.launch, args.steps)
     extra["headline_warm_l2"] = {"ms_median": statistics.median(warm),
                                  "GBps": gbs(case.bytes, statistics.median(warm))}
@@ -452,7 +493,7 @@ def run_ours(args, rank, world, local_rank):
         print(f"parity gate failed: {parity}", file=sys.stderr)
 
     h = source_hash()
-    traffic = recorded_traffic("ln_4096x768", h)
+    traffic = recorded_traffic(wl.tag, h)
     achieved = gbs(case.bytes, statistics.fmean(times))
     line = {
         "metric": METRIC,
@@ -467,8 +508,9 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded NumPy: x ~ N(0,1), gamma ~ N(1,0.1), beta ~ N(0,0.1))",
-        "config": {"workload": "layernorm_fwd_fp32_4096x768", "rows": wl.rows, "d": wl.d,
-                   "eps": wl.eps, "seed": wl.seed, "op": "ln_fwd",
+        "config": {"workload": f"{'layernorm' if wl.op == 'ln' else 'rmsnorm'}_fwd_fp32_"
+                               f"{wl.rows}x{wl.d}", "rows": wl.rows, "d": wl.d,
+                   "eps": wl.eps, "seed": wl.seed, "op": f"{wl.op}_fwd",
                    "l2": f"flushed before every step ({flush.nbytes >> 20} MiB written, "
                          "outside the timed events)",
                    "rows_per_rank": wl.rows, "parallelism": f"rows sharded, {world} rank(s)",
@@ -476,8 +518,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": gbs(case.bytes * world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms,
-                "path": "pinned host x -> device, ln_fwd via the Python binding, "
-                        "y/mean/rstd -> pinned host, per step"},
+                "path": f"pinned host x -> device, {wl.op}_fwd via the Python binding, "
+                        "outputs -> pinned host, per step"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": traffic,
@@ -502,16 +544,17 @@ def run_reference(args, rank, world):
         return None
     from oracle import c_oracle
 
-    wl = workloads.ln_4096x768()
+    wl = pick_workload(args.workload)
     x = wl.x()
-    g, b = wl.params()
-    nbytes = algorithmic_bytes("ln", wl.rows, wl.d)
+    params = wl.params()
+    fn = c_oracle.layer_norm if wl.op == "ln" else c_oracle.rms_norm
+    nbytes = algorithmic_bytes(wl.op, wl.rows, wl.d)
     for _ in range(args.warmup):
-        c_oracle.layer_norm(x, g, b, wl.eps)
+        fn(x, *params, wl.eps)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        c_oracle.layer_norm(x, g, b, wl.eps)
+        fn(x, *params, wl.eps)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.fmean(times)
     value = gbs(nbytes, ms)
@@ -521,7 +564,8 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded NumPy)",
-        "config": {"workload": "layernorm_fwd_fp32_4096x768", "rows": wl.rows, "d": wl.d,
+        "config": {"workload": f"{'layernorm' if wl.op == 'ln' else 'rmsnorm'}_fwd_fp32_"
+                               f"{wl.rows}x{wl.d}", "rows": wl.rows, "d": wl.d,
                    "eps": wl.eps, "seed": wl.seed},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"each step one whole pass of the C float64 oracle over "
@@ -541,6 +585,8 @@ def main(argv=None):
     ap.add_argument("--sweep-steps", type=int, default=20)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default="ln_4096x768",
+                    help="named workload or op:rows:d (default: the 4096x768 LayerNorm)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

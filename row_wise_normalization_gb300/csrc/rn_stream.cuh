@@ -5,7 +5,11 @@
 // running (count, mean, M2) and folds in one vector at a time with Chan's
 // pairwise update (the vector's own mean and centred square sum merged into
 // the running triple), warps merge lane triples through shuffles, and the
-// warps meet once in shared memory. The second read writes y. No width limit
+// warps meet once in shared memory. Every element is first shifted by the
+// row's first element K: a merge adds the product of the partial means'
+// rounding error (~u |mean|) and their spread to M2, so working on x - K
+// (mean ~ mu - K, of the order of sigma for typical rows) keeps that error
+// ~u instead of ~u |mu| / sigma. The second read writes y. No width limit
 // and no shared memory beyond the exchange slots; it is the fallback for rows
 // the register-held and staged kernels cannot hold.
 #pragma once
@@ -54,10 +58,13 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
 
         float mu = 0.f, rs;
         if constexpr (OP == OP_LN) {
+            const float K = ld_x1(xr);   // shift (the same address for every thread)
             float n = 0.f, m = 0.f, M = 0.f;
             for (int64_t q = t; q < nv; q += TPB) {
                 Vec<VEC> v;
                 ld_x(v, xr + h + q * VEC);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) v.v[k] -= K;
                 float s = 0.f;
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) s += v.v[k];
@@ -70,7 +77,7 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
                 }
                 chan_merge(n, m, M, (float)VEC, mc, Mc);
             }
-            if (has_e) chan_merge(n, m, M, 1.f, ld_x1(xr + ei), 0.f);
+            if (has_e) chan_merge(n, m, M, 1.f, ld_x1(xr + ei) - K, 0.f);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const float nb = __shfl_xor_sync(0xffffffffu, n, o);
@@ -80,8 +87,9 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
             }
             if (lane == 0) *reinterpret_cast<float4*>(slot[w]) = make_float4(n, n * m, m, M);
             __syncthreads();
-            float M2;
-            merge_ln_warps<W>(slot, lane, fd, mu, M2);
+            float M2, mus;
+            merge_ln_warps<W>(slot, lane, fd, mus, M2);
+            mu = K + mus;
             rs = rsqrtf(M2 / fd + p.eps);
         } else {
             float ss = 0.f;
