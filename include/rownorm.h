@@ -121,11 +121,15 @@ enum {
 typedef struct rn_plan {
     int variant;          /* RN_VARIANT_* actually chosen                      */
     int vec;              /* elements per vector access: 4 or 1                */
-    int slots;            /* vectors held per thread (register variants)      */
+    int slots;            /* vectors held per thread (register variants);
+                             row buffers in the ring (staged variant)          */
     int threads_per_row;  /* threads cooperating on one row                    */
     int rows_per_cta;     /* rows a CTA works on at once                       */
     int threads_per_cta;
     int smem_bytes;       /* dynamic shared memory per CTA                     */
+    int prefetch;         /* 1: the next row's loads overlap this row's work   */
+    int params_held;      /* 1: gamma/beta (w) held in registers across rows   */
+    int aligned;          /* 1: x, y, params 16-byte aligned and d % 4 == 0    */
 } rn_plan;
 
 enum { RN_OP_LN = 0, RN_OP_RMS = 1 };
@@ -146,6 +150,15 @@ int ln_fwd_variant(int variant, const float *x, const float *gamma, const float 
 
 int rms_fwd_variant(int variant, const float *x, const float *w, float *y,
                     int64_t rows, int64_t d, float eps, void *stream);
+
+/* Device error word of the current device: bit 0 (RN_DEVERR_STAGED_TIMEOUT)
+ * is set if a staged kernel's wait for a bulk copy ran out (about one
+ * second; the kernel then stops early and its outputs are incomplete). The
+ * word is sticky until cleared: `clear` != 0 resets it after reading.
+ * Synchronous (a device-to-host copy). Returns RN_OK, RN_ERR_NULL or
+ * RN_ERR_CUDA. */
+enum { RN_DEVERR_STAGED_TIMEOUT = 1 };
+int rn_device_error(unsigned int *flags, int clear);
 
 /* Measurement aid: launch an empty kernel with `grid` CTAs of `threads`
  * threads on `stream` (the launch-latency floor small shapes are compared

@@ -43,7 +43,8 @@ _INT = ctypes.c_int
 
 class rn_plan(ctypes.Structure):
     _fields_ = [("variant", _INT), ("vec", _INT), ("slots", _INT), ("threads_per_row", _INT),
-                ("rows_per_cta", _INT), ("threads_per_cta", _INT), ("smem_bytes", _INT)]
+                ("rows_per_cta", _INT), ("threads_per_cta", _INT), ("smem_bytes", _INT),
+                ("prefetch", _INT), ("params_held", _INT), ("aligned", _INT)]
 
 
 SIGNATURES = {
@@ -56,6 +57,7 @@ SIGNATURES = {
     "ln_fwd_variant": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
     "rms_fwd_variant": (_INT, [_INT, _P, _P, _P, _I64, _I64, _F, _P]),
     "rn_launch_empty": (_INT, [_I64, _INT, _P]),
+    "rn_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
 }
 
 _lib = None
@@ -128,3 +130,10 @@ def rms_fwd_variant(variant, x, w, y, rows, d, eps, stream=0) -> int:
 
 def launch_empty(grid, threads, stream=0) -> int:
     return load().rn_launch_empty(grid, threads, stream)
+
+
+def device_error(clear: bool = False) -> int:
+    """The device error word (0 when no kernel reported a problem)."""
+    out = ctypes.c_uint(0)
+    check(load().rn_device_error(ctypes.byref(out), 1 if clear else 0))
+    return out.value

@@ -1,6 +1,6 @@
-// Register-held kernels: LN, VEC = 1, every (slots, threads-per-row) pair.
+// Register-held kernels: LN, scalar accesses (x and y in different 16-byte phases).
 #include "rn_reg.cuh"
 
 namespace rn {
-const KernelEntry* reg_entry_ln_v1(int slots, int tpr) { return reg_pick<OP_LN, 1>(slots, tpr); }
+const KernelEntry* reg_entry_ln_v1(int slots, int tpr) { return reg_pick<OP_LN, 1, false, false>(slots, tpr); }
 }  // namespace rn

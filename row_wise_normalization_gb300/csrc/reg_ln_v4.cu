@@ -1,6 +1,6 @@
-// Register-held kernels: LN, VEC = 4, every (slots, threads-per-row) pair.
+// Register-held kernels: LN, 128-bit vectors, any row phase (head peel, scalar tail).
 #include "rn_reg.cuh"
 
 namespace rn {
-const KernelEntry* reg_entry_ln_v4(int slots, int tpr) { return reg_pick<OP_LN, 4>(slots, tpr); }
+const KernelEntry* reg_entry_ln_v4(int slots, int tpr) { return reg_pick<OP_LN, 4, false, false>(slots, tpr); }
 }  // namespace rn

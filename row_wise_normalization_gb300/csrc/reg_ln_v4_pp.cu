@@ -1,0 +1,6 @@
+// Register-held kernels: LN, every row 16-byte aligned whole vectors, parameters held across rows.
+#include "rn_reg.cuh"
+
+namespace rn {
+const KernelEntry* reg_entry_ln_v4_pp(int slots, int tpr) { return reg_pick<OP_LN, 4, true, true>(slots, tpr); }
+}  // namespace rn

@@ -1,0 +1,6 @@
+// Register-held kernels: RMS, every row 16-byte aligned whole vectors, parameters per row.
+#include "rn_reg.cuh"
+
+namespace rn {
+const KernelEntry* reg_entry_rms_v4_al(int slots, int tpr) { return reg_pick<OP_RMS, 4, false, true>(slots, tpr); }
+}  // namespace rn

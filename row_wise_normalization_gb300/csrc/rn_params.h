@@ -28,20 +28,56 @@ struct KernelEntry {
     const void* fn;        // the __global__ function (for occupancy queries)
     int threads;           // threads per CTA
     int rows_per_cta;      // rows a CTA handles per iteration of its row loop
-    int smem_bytes;        // dynamic shared memory per CTA
+    int smem_bytes;        // dynamic shared memory per CTA (0: set per launch)
     cudaError_t (*launch)(const Params&, int grid, cudaStream_t);
+    // Raises the kernel's dynamic shared memory limit (NULL if not needed).
+    cudaError_t (*prepare)(int smem_bytes);
 };
 
 // Register-held kernels (warp per row when tpr == 32, a CTA per row above).
-// Returns NULL if the configuration was not compiled.
-const KernelEntry* reg_entry(int op, int vec, int slots, int tpr);
+// al: x, y and the parameters are 16-byte aligned and d % 4 == 0 (no head or
+// tail scalars); pp: the parameter vectors are held in registers across rows
+// (requires al, tpr <= 128 and slots <= 6). Returns NULL if the
+// configuration was not compiled.
+const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool al);
+
+// Register-held configurations, measured on GB300 (cold L2, same-session
+// device-to-device copy as the reference):
+//  * warp per row: 4 rows (128 threads) per CTA, prefetching the next row;
+//  * CTA per row: the fewest threads (a power of two >= 64) that hold the row
+//    in at most kMaxSlots vectors each, prefetching except for the widest
+//    slices on 256+ threads, where doubling the held registers costs more
+//    resident warps than the overlap wins (a thread then holds 32 floats and
+//    3 CTAs of 256 per SM keep enough bytes in flight), and where two rows
+//    would not fit the 64 registers a thread of a 1024-thread CTA can have;
+//  * parameters held across rows for rows of up to 128 threads holding at
+//    most 6 vectors each, when every row starts at the same 16-byte phase
+//    (with 8 vectors the held parameters cost a resident CTA per SM).
+constexpr bool reg_prefetch(int vec, int slots, int tpr) {
+    return vec == 4 && !(slots >= 8 && tpr >= 256) &&
+           (52 + 8 * slots) * tpr <= 65536;   // both rows fit the registers of one CTA
+}
+constexpr bool reg_may_hold_params(int vec, int slots, int tpr) {
+    return vec == 4 && tpr <= 128 && slots <= 6;
+}
 
 // Streaming two-read kernels (any width).
 const KernelEntry* stream_entry(int op, int vec);
+
+// Shared-memory-staged kernels with `stages` row buffers (1..kMaxStages).
+const KernelEntry* staged_entry(int op, int stages);
+
+// Reads (and optionally clears) the device error word of the current device.
+cudaError_t device_error_word(unsigned int* out, bool clear);
 
 // Compiled configuration space of the register-held kernels.
 constexpr int kMaxSlots = 8;
 constexpr int kWarpRowsPerCta = 4;  // rows (warps) per CTA in the warp variant
 constexpr int kStreamThreads = 512;
+constexpr int kStagedThreads = 512;
+constexpr int kMaxStages = 4;
+// Dynamic shared memory the staged kernel may use for its row buffers: the
+// 227 KiB per-CTA limit of sm_100-class GPUs less room for static shared data.
+constexpr int kStagedSmemBudget = 232448 - 1024;
 
 }  // namespace rn

@@ -19,6 +19,15 @@
 //   3. rstd = rsqrtf(var + eps) and the row is written from the registers
 //      with streaming 128-bit stores.
 //
+// The grid is persistent (at most the resident CTA count); a row group walks
+// rows g, g + step, ... With PF the loads of the next row are issued before
+// the current row is reduced and stored, so every thread keeps a row's worth
+// of loads in flight while it computes (software pipelining across rows, the
+// grid-stride hypothesis of issue #54 taken one step further). With PP the
+// parameter vectors are loaded into registers once per thread and reused for
+// every row, which requires every row to start at the same 16-byte phase
+// (d % 4 == 0; the host checks).
+//
 // Vector layout of a row: h scalars up to the first 16-byte boundary of the
 // row (the "head peel", 0..3), nv aligned vectors, tl scalars of tail (0..3).
 // Vector q goes to thread q % TPR, slot q / TPR; the h + tl <= 6 scalars go to
@@ -29,17 +38,76 @@
 
 namespace rn {
 
-// Resident CTAs each kernel is compiled for, which sets its register cap:
-// 64 registers per thread when a thread holds at most 16 floats of the row
-// (4 on the scalar path, whose per-element addressing costs more), 80 above
-// that (the largest slice, 8 vectors of 4, is 32 floats).
-constexpr int reg_min_ctas(int threads, int held, int vec) {
-    return threads >= 1024 ? 1 : 65536 / ((held > 16 || (vec == 1 && held > 4) ? 80 : 64) * threads);
+// Registers a thread of reg_kernel is budgeted: the held row (twice with
+// prefetch), the parameters held across rows, and a fixed allowance for
+// indices, statistics and addresses.
+constexpr int reg_budget(int op, int vec, int slots, bool pf, bool pp) {
+    return 48 + slots * vec * (pf ? 2 : 1) + (pp ? 8 + slots * vec * (op == 0 ? 2 : 1) : 0) +
+           (vec == 1 ? 3 * slots : 0);
 }
 
-template <int OP, int VEC, int SLOTS, int TPR, int RPC>
-__global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, SLOTS * VEC, VEC)) reg_kernel(const Params p) {
+// Resident CTAs each kernel is compiled for, which sets its register cap
+// (65536 registers per SM, allocated in units of 8 per thread). For the wide
+// slices (6+ vectors per thread) the counts are the measured optima on
+// GB300 (cold L2, against a same-session device-to-device copy): with
+// prefetch about 384 resident threads per SM (the two held rows keep enough
+// bytes in flight, and the spare registers let loads issue early), without
+// it about 768-1024. Narrower slices fill the SM as far as the budget allows.
+constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, bool pp) {
+    if (vec == 4 && slots >= 6) {
+        if (pf) return threads == 64 ? 5 : (threads >= 384 ? 1 : 384 / threads);
+        return threads >= 1024 ? 1 : (threads == 512 ? 2 : (768 / threads > 0 ? 768 / threads : 1));
+    }
+    const int per = ((reg_budget(op, vec, slots, pf, pp) + 7) / 8) * 8;
+    const int n = 65536 / (per * threads);
+    return n < 1 ? 1 : (n > 32 ? 32 : n);
+}
+
+// One row as a thread holds it.
+template <int VEC, int SLOTS>
+struct HeldRow {
+    Vec<VEC> v[SLOTS];
+    float e;          // the thread's head/tail scalar (0 if none)
+    int h, nv, tl;    // head peel, aligned vectors, tail of this row
+};
+
+template <int VEC, int SLOTS, int TPR, bool AL>
+__device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS>& r, const float* xr, int d, int t) {
+    if constexpr (AL) {
+        r.h = 0;
+        r.nv = d >> 2;
+        r.tl = 0;
+    } else if constexpr (VEC == 4) {
+        r.h = head_peel(xr, d);
+        r.nv = (d - r.h) >> 2;
+        r.tl = d - r.h - 4 * r.nv;
+    } else {
+        r.h = 0;
+        r.nv = d;
+        r.tl = 0;
+    }
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        const int q = t + s * TPR;
+        if (q < r.nv) {
+            ld_x(r.v[s], xr + r.h + q * VEC);
+        } else {
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) r.v[s].v[k] = 0.f;
+        }
+    }
+    r.e = 0.f;
+    if constexpr (VEC == 4 && !AL) {
+        if (t < r.h + r.tl) r.e = ld_x1(xr + ((t < r.h) ? t : r.h + 4 * r.nv + (t - r.h)));
+    }
+}
+
+template <int OP, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL>
+__global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP))
+    reg_kernel(const Params p) {
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
+    static_assert(!PP || VEC == 4, "parameters are held only on the vector path");
+    static_assert(!AL || VEC == 4, "the aligned layout is a vector layout");
     constexpr int WPR = TPR / 32;                    // warps per row
     constexpr int NST = (OP == OP_LN) ? 4 : 1;       // floats a warp publishes
     constexpr int NBUF = (WPR > 1) ? 2 : 1;
@@ -51,65 +119,63 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, SLOTS * VEC
     const int lane = t & 31;
     const int d = (int)p.d;                          // register-held rows are < 2^31 wide
     const float fd = (float)d;
+    const int64_t step = (int64_t)gridDim.x * RPC;
+    int64_t row = (int64_t)blockIdx.x * RPC + g;
+    if (row >= p.rows) return;                       // the whole group leaves together
 
-    int it = 0;
-    for (int64_t row = (int64_t)blockIdx.x * RPC + g; row < p.rows;
-         row += (int64_t)gridDim.x * RPC, ++it) {
-        const float* xr = p.x + row * p.d;
-        float* yr = p.y + row * p.d;
+    HeldRow<VEC, SLOTS> cur;
+    load_row<VEC, SLOTS, TPR, AL>(cur, p.x + row * p.d, d, t);
 
-        int h = 0, tl = 0;
-        int nv;
-        if constexpr (VEC == 4) {
-            h = head_peel(xr, d);
-            nv = (d - h) >> 2;
-            tl = (int)(d - h - 4 * nv);
-        } else {
-            nv = d;
-        }
-
-        // ---- 1. load the row slice --------------------------------------
-        Vec<VEC> v[SLOTS];
+    // Parameters held across rows (PP): every row has the phase of row 0.
+    Vec<VEC> pg[PP ? SLOTS : 1], pb[(PP && OP == OP_LN) ? SLOTS : 1];
+    float pge = 0.f, pbe = 0.f;
+    if constexpr (PP) {
+        const bool pa0 = AL || ((((uintptr_t)p.p0 >> 2) + cur.h) & 3) == 0;
+        const bool pa1 = AL || OP != OP_LN || ((((uintptr_t)p.p1 >> 2) + cur.h) & 3) == 0;
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             const int q = t + s * TPR;
-            if (q < nv) {
-                ld_x(v[s], xr + h + q * VEC);
-            } else {
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) v[s].v[k] = 0.f;
+            if (q < cur.nv) {
+                ld_p(pg[s], p.p0 + cur.h + q * VEC, pa0);
+                if constexpr (OP == OP_LN) ld_p(pb[s], p.p1 + cur.h + q * VEC, pa1);
             }
         }
-        float e = 0.f;
-        int ei = 0;
-        bool has_e = false;
-        if constexpr (VEC == 4) {
-            has_e = t < h + tl;
-            if (has_e) {
-                ei = (t < h) ? t : h + 4 * nv + (t - h);
-                e = ld_x1(xr + ei);
-            }
+        if (!AL && t < cur.h + cur.tl) {
+            const int ei = (t < cur.h) ? t : cur.h + 4 * cur.nv + (t - cur.h);
+            pge = ld_p1(p.p0 + ei);
+            if constexpr (OP == OP_LN) pbe = ld_p1(p.p1 + ei);
         }
+    }
 
-        // ---- 2. statistics ---------------------------------------------
+    int it = 0;
+    for (;; ++it) {
+        const int64_t nrow = row + step;
+        HeldRow<VEC, SLOTS> nxt;
+        if constexpr (PF) {
+            if (nrow < p.rows) load_row<VEC, SLOTS, TPR, AL>(nxt, p.x + nrow * p.d, d, t);
+        }
+        const int h = cur.h, nv = cur.nv, tl = cur.tl;
+        const bool has_e = (VEC == 4) && !AL && (t < h + tl);
+        const int ei = (t < h) ? t : h + 4 * nv + (t - h);
+
+        // ---- statistics ------------------------------------------------
         float mu = 0.f, rs;
         if constexpr (OP == OP_LN) {
-            float sum = e;
+            float sum = cur.e;
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s)
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) sum += v[s].v[k];   // unused slots hold 0
+                for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
 
             if constexpr (WPR == 1) {
                 mu = warp_sum(sum) / fd;
-                float m2 = 0.f;
-                if (has_e) m2 = (e - mu) * (e - mu);
+                float m2 = has_e ? (cur.e - mu) * (cur.e - mu) : 0.f;
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
                     if (t + s * TPR < nv) {
 #pragma unroll
                         for (int k = 0; k < VEC; ++k) {
-                            const float c = v[s].v[k] - mu;
+                            const float c = cur.v[s].v[k] - mu;
                             m2 = fmaf(c, c, m2);
                         }
                     }
@@ -124,14 +190,13 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, SLOTS * VEC
                     nw += VEC * (rem <= 0 ? 0 : (rem >= 32 ? 32 : rem));
                 }
                 const float wmean = nw > 0 ? wsum / (float)nw : 0.f;
-                float m2 = 0.f;
-                if (has_e) m2 = (e - wmean) * (e - wmean);
+                float m2 = has_e ? (cur.e - wmean) * (cur.e - wmean) : 0.f;
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
                     if (t + s * TPR < nv) {
 #pragma unroll
                         for (int k = 0; k < VEC; ++k) {
-                            const float c = v[s].v[k] - wmean;
+                            const float c = cur.v[s].v[k] - wmean;
                             m2 = fmaf(c, c, m2);
                         }
                     }
@@ -146,11 +211,11 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, SLOTS * VEC
                 rs = rsqrtf(M2 / fd + p.eps);
             }
         } else {
-            float ss = e * e;
+            float ss = cur.e * cur.e;
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s)
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) ss = fmaf(v[s].v[k], v[s].v[k], ss);
+                for (int k = 0; k < VEC; ++k) ss = fmaf(cur.v[s].v[k], cur.v[s].v[k], ss);
             if constexpr (WPR == 1) {
                 ss = warp_sum(ss);
             } else {
@@ -163,9 +228,10 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, SLOTS * VEC
             rs = rsqrtf(ss / fd + p.eps);
         }
 
-        // ---- 3. normalize and store from the held registers --------------
+        // ---- normalize and store from the held registers ----------------
+        float* yr = p.y + row * p.d;
         bool pa = true;   // parameter vectors 16-byte aligned at this row's phase
-        if constexpr (VEC == 4) {
+        if constexpr (VEC == 4 && !PP && !AL) {
             pa = ((((uintptr_t)p.p0 >> 2) + h) & 3) == 0;
             if constexpr (OP == OP_LN) pa = pa && ((((uintptr_t)p.p1 >> 2) + h) & 3) == 0;
         }
@@ -174,28 +240,32 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, SLOTS * VEC
             const int q = t + s * TPR;
             if (q < nv) {
                 const int j = h + q * VEC;
-                Vec<VEC> a, o;
-                ld_p(a, p.p0 + j, pa);
+                Vec<VEC> a, b, o;
+                if constexpr (PP) {
+                    a = pg[s];
+                    if constexpr (OP == OP_LN) b = pb[s];
+                } else {
+                    ld_p(a, p.p0 + j, pa);
+                    if constexpr (OP == OP_LN) ld_p(b, p.p1 + j, pa);
+                }
                 if constexpr (OP == OP_LN) {
-                    Vec<VEC> b;
-                    ld_p(b, p.p1 + j, pa);
 #pragma unroll
                     for (int k = 0; k < VEC; ++k)
-                        o.v[k] = fmaf((v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
+                        o.v[k] = fmaf((cur.v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
                 } else {
 #pragma unroll
-                    for (int k = 0; k < VEC; ++k) o.v[k] = v[s].v[k] * rs * a.v[k];
+                    for (int k = 0; k < VEC; ++k) o.v[k] = cur.v[s].v[k] * rs * a.v[k];
                 }
                 st_y(yr + j, o);
             }
         }
         if (has_e) {
-            const float a = ld_p1(p.p0 + ei);
+            const float a = PP ? pge : ld_p1(p.p0 + ei);
             float o;
             if constexpr (OP == OP_LN)
-                o = fmaf((e - mu) * rs, a, ld_p1(p.p1 + ei));
+                o = fmaf((cur.e - mu) * rs, a, PP ? pbe : ld_p1(p.p1 + ei));
             else
-                o = e * rs * a;
+                o = cur.e * rs * a;
             st_y1(yr + ei, o);
         }
         if constexpr (OP == OP_LN) {
@@ -204,50 +274,68 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, SLOTS * VEC
                 if (p.rstd) p.rstd[row] = rs;
             }
         }
+
+        if (nrow >= p.rows) break;
+        row = nrow;
+        if constexpr (PF)
+            cur = nxt;
+        else
+            load_row<VEC, SLOTS, TPR, AL>(cur, p.x + row * p.d, d, t);
     }
 }
 
-// Launcher and registry entry of one configuration.
-template <int OP, int VEC, int SLOTS, int TPR>
+// ---------------------------------------------------------------------------
+// Configurations and their registry entries (the choice of PF and PP per
+// configuration is in rn_params.h, shared with the host-side planner).
+// ---------------------------------------------------------------------------
+// AL (all aligned): x, y and the parameter vectors are 16-byte aligned and
+// d % 4 == 0, so every row is whole 128-bit vectors -- no head/tail scalars
+// and no per-row alignment tests (the common case: allocators align to 256
+// bytes). PP is only compiled with AL.
+template <int OP, int VEC, int SLOTS, int TPR, bool PP, bool AL = PP>
 struct RegInst {
     static constexpr int RPC = (TPR == 32) ? kWarpRowsPerCta : 1;
+    static constexpr bool PF = reg_prefetch(VEC, SLOTS, TPR);
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
-        reg_kernel<OP, VEC, SLOTS, TPR, RPC><<<grid, TPR * RPC, 0, s>>>(p);
+        reg_kernel<OP, VEC, SLOTS, TPR, RPC, PF, PP, AL><<<grid, TPR * RPC, 0, s>>>(p);
         return cudaGetLastError();
     }
     static const KernelEntry entry;
 };
 
-template <int OP, int VEC, int SLOTS, int TPR>
-const KernelEntry RegInst<OP, VEC, SLOTS, TPR>::entry = {
-    (const void*)&reg_kernel<OP, VEC, SLOTS, TPR, RegInst<OP, VEC, SLOTS, TPR>::RPC>,
-    TPR * RegInst<OP, VEC, SLOTS, TPR>::RPC, RegInst<OP, VEC, SLOTS, TPR>::RPC, 0,
-    &RegInst<OP, VEC, SLOTS, TPR>::launch};
+template <int OP, int VEC, int SLOTS, int TPR, bool PP, bool AL>
+const KernelEntry RegInst<OP, VEC, SLOTS, TPR, PP, AL>::entry = {
+    (const void*)&reg_kernel<OP, VEC, SLOTS, TPR, RegInst<OP, VEC, SLOTS, TPR, PP, AL>::RPC,
+                             RegInst<OP, VEC, SLOTS, TPR, PP, AL>::PF, PP, AL>,
+    TPR * RegInst<OP, VEC, SLOTS, TPR, PP, AL>::RPC, RegInst<OP, VEC, SLOTS, TPR, PP, AL>::RPC,
+    0, &RegInst<OP, VEC, SLOTS, TPR, PP, AL>::launch, nullptr};
 
-template <int OP, int VEC, int TPR>
+template <int OP, int VEC, int TPR, bool PP, bool AL>
 const KernelEntry* reg_pick_slots(int slots) {
     switch (slots) {
-        case 1: return &RegInst<OP, VEC, 1, TPR>::entry;
-        case 2: return &RegInst<OP, VEC, 2, TPR>::entry;
-        case 3: return &RegInst<OP, VEC, 3, TPR>::entry;
-        case 4: return &RegInst<OP, VEC, 4, TPR>::entry;
-        case 5: return &RegInst<OP, VEC, 5, TPR>::entry;
-        case 6: return &RegInst<OP, VEC, 6, TPR>::entry;
-        case 7: return &RegInst<OP, VEC, 7, TPR>::entry;
-        case 8: return &RegInst<OP, VEC, 8, TPR>::entry;
+        case 1: return &RegInst<OP, VEC, 1, TPR, PP, AL>::entry;
+        case 2: return &RegInst<OP, VEC, 2, TPR, PP, AL>::entry;
+        case 3: return &RegInst<OP, VEC, 3, TPR, PP, AL>::entry;
+        case 4: return &RegInst<OP, VEC, 4, TPR, PP, AL>::entry;
+        case 5: return &RegInst<OP, VEC, 5, TPR, PP, AL>::entry;
+        case 6: return &RegInst<OP, VEC, 6, TPR, PP, AL>::entry;
+        case 7: if constexpr (!PP) return &RegInst<OP, VEC, 7, TPR, PP, AL>::entry; else return nullptr;
+        case 8: if constexpr (!PP) return &RegInst<OP, VEC, 8, TPR, PP, AL>::entry; else return nullptr;
         default: return nullptr;
     }
 }
 
-template <int OP, int VEC>
+// (slots, tpr) -> entry for one (VEC, PP, AL) family; PP families exist for
+// rows of at most 128 threads and 6 vectors per thread.
+template <int OP, int VEC, bool PP, bool AL>
 const KernelEntry* reg_pick(int slots, int tpr) {
     switch (tpr) {
-        case 32: return reg_pick_slots<OP, VEC, 32>(slots);
-        case 64: return reg_pick_slots<OP, VEC, 64>(slots);
-        case 128: return reg_pick_slots<OP, VEC, 128>(slots);
-        case 256: return reg_pick_slots<OP, VEC, 256>(slots);
-        case 512: return reg_pick_slots<OP, VEC, 512>(slots);
-        case 1024: return reg_pick_slots<OP, VEC, 1024>(slots);
+        case 32: return reg_pick_slots<OP, VEC, 32, PP, AL>(slots);
+        case 64: return reg_pick_slots<OP, VEC, 64, PP, AL>(slots);
+        case 128: return reg_pick_slots<OP, VEC, 128, PP, AL>(slots);
+        case 256: if constexpr (!PP) return reg_pick_slots<OP, VEC, 256, PP, AL>(slots); else return nullptr;
+        case 512: if constexpr (!PP) return reg_pick_slots<OP, VEC, 512, PP, AL>(slots); else return nullptr;
+        case 1024: if constexpr (!PP) return reg_pick_slots<OP, VEC, 1024, PP, AL>(slots); else return nullptr;
         default: return nullptr;
     }
 }

@@ -162,6 +162,6 @@ struct StreamInst {
 template <int OP, int VEC>
 const KernelEntry StreamInst<OP, VEC>::entry = {
     (const void*)&stream_kernel<OP, VEC, kStreamThreads>, kStreamThreads, 1, 0,
-    &StreamInst<OP, VEC>::launch};
+    &StreamInst<OP, VEC>::launch, nullptr};
 
 }  // namespace rn

@@ -12,13 +12,20 @@
 
 namespace rn {
 const KernelEntry* reg_entry_ln_v4(int slots, int tpr);
+const KernelEntry* reg_entry_ln_v4_al(int slots, int tpr);
+const KernelEntry* reg_entry_ln_v4_pp(int slots, int tpr);
 const KernelEntry* reg_entry_ln_v1(int slots, int tpr);
 const KernelEntry* reg_entry_rms_v4(int slots, int tpr);
+const KernelEntry* reg_entry_rms_v4_al(int slots, int tpr);
+const KernelEntry* reg_entry_rms_v4_pp(int slots, int tpr);
 const KernelEntry* reg_entry_rms_v1(int slots, int tpr);
 
-const KernelEntry* reg_entry(int op, int vec, int slots, int tpr) {
-    if (op == OP_LN) return vec == 4 ? reg_entry_ln_v4(slots, tpr) : reg_entry_ln_v1(slots, tpr);
-    return vec == 4 ? reg_entry_rms_v4(slots, tpr) : reg_entry_rms_v1(slots, tpr);
+const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool al) {
+    const bool ln = op == OP_LN;
+    if (vec != 4) return ln ? reg_entry_ln_v1(slots, tpr) : reg_entry_rms_v1(slots, tpr);
+    if (pp) return ln ? reg_entry_ln_v4_pp(slots, tpr) : reg_entry_rms_v4_pp(slots, tpr);
+    if (al) return ln ? reg_entry_ln_v4_al(slots, tpr) : reg_entry_rms_v4_al(slots, tpr);
+    return ln ? reg_entry_ln_v4(slots, tpr) : reg_entry_rms_v4(slots, tpr);
 }
 }  // namespace rn
 
@@ -52,7 +59,20 @@ bool block_shape(int64_t units, int* tpr, int* slots) {
     return false;
 }
 
-int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, rn_plan* pl) {
+// Shared-memory staging: row buffers of the aligned body, as many as fit (at
+// most kMaxStages). Returns false if one row does not fit.
+bool staged_shape(int64_t d, int* stages, int* smem) {
+    const int64_t sb = ((d / 4) * 16 + 127) / 128 * 128;
+    if (sb > kStagedSmemBudget) return false;
+    int n = sb == 0 ? kMaxStages : (int)(kStagedSmemBudget / sb);
+    if (n > kMaxStages) n = kMaxStages;
+    *stages = n;
+    *smem = (int)(n * sb);
+    return true;
+}
+
+int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, const void* p0,
+              const void* p1, rn_plan* pl) {
     if (d <= 0) return RN_ERR_SIZE;
     std::memset(pl, 0, sizeof(*pl));
     // 16-byte vectors need x and y in the same 16-byte phase (a row's head
@@ -60,13 +80,19 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, rn_p
     const int vec = ((((uintptr_t)x ^ (uintptr_t)y) & 15u) == 0) ? 4 : 1;
     const int64_t units = row_units(d, vec);
     pl->vec = vec;
+    // Every row whole aligned vectors, parameters included.
+    const bool al = vec == 4 && d % 4 == 0 && (((uintptr_t)x | (uintptr_t)p0 |
+                                                 (op == OP_LN ? (uintptr_t)p1 : 0)) & 15u) == 0;
 
     int v = variant;
     if (v == RN_VARIANT_AUTO) {
+        int st, sm;
         if (units <= 32 * kMaxSlots)
             v = RN_VARIANT_WARP;
         else if (units <= 1024 * kMaxSlots)
             v = RN_VARIANT_BLOCK;
+        else if (vec == 4 && staged_shape(d, &st, &sm))
+            v = RN_VARIANT_STAGED;
         else
             v = RN_VARIANT_STREAM;
     }
@@ -77,6 +103,9 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, rn_p
             pl->threads_per_row = 32;
             pl->rows_per_cta = kWarpRowsPerCta;
             pl->threads_per_cta = 32 * kWarpRowsPerCta;
+            pl->prefetch = reg_prefetch(vec, pl->slots, 32);
+            pl->aligned = al;
+            pl->params_held = al && reg_may_hold_params(vec, pl->slots, 32);
             break;
         case RN_VARIANT_BLOCK: {
             int tpr, slots;
@@ -85,6 +114,19 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, rn_p
             pl->threads_per_row = tpr;
             pl->rows_per_cta = 1;
             pl->threads_per_cta = tpr;
+            pl->prefetch = reg_prefetch(vec, slots, tpr);
+            pl->aligned = al;
+            pl->params_held = al && reg_may_hold_params(vec, slots, tpr);
+            break;
+        }
+        case RN_VARIANT_STAGED: {
+            int st, sm;
+            if (vec != 4 || !staged_shape(d, &st, &sm)) return RN_ERR_VARIANT;
+            pl->slots = st;            // row buffers in the ring
+            pl->threads_per_row = kStagedThreads;
+            pl->rows_per_cta = 1;
+            pl->threads_per_cta = kStagedThreads;
+            pl->smem_bytes = sm;
             break;
         }
         case RN_VARIANT_STREAM:
@@ -97,7 +139,6 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, rn_p
             return RN_ERR_VARIANT;
     }
     pl->variant = v;
-    pl->smem_bytes = 0;
     (void)op;
     return RN_OK;
 }
@@ -135,28 +176,39 @@ int validate(int op, const float* x, const float* p0, const float* p1, const flo
     return RN_OK;
 }
 
-// CTAs of `e` that fit on the current device at once (0 on error).
-int resident_ctas(const KernelEntry* e, cudaError_t* err) {
+// CTAs of `e` with `smem` bytes of dynamic shared memory that fit on the
+// current device at once (0 on error). Raises the kernel's dynamic shared
+// memory limit first when it needs more than the default.
+int resident_ctas(const KernelEntry* e, int smem, cudaError_t* err) {
     struct Cache {
         const void* fn;
         int dev;
+        int smem;
         int n;
     };
-    static thread_local Cache cache[16];
+    static thread_local Cache cache[32];
     static thread_local int cache_next = 0;
     int dev = 0;
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return 0;
     for (auto& c : cache)
-        if (c.fn == e->fn && c.dev == dev && c.n > 0) return c.n;
+        if (c.fn == e->fn && c.dev == dev && c.smem == smem && c.n > 0) return c.n;
+    if (e->prepare) {
+        *err = e->prepare(smem);
+        if (*err != cudaSuccess) return 0;
+    }
     int sms = 0, per_sm = 0;
     *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (*err != cudaSuccess) return 0;
-    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, e->fn, e->threads, e->smem_bytes);
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, e->fn, e->threads, smem);
     if (*err != cudaSuccess) return 0;
-    const int n = (per_sm > 0 ? per_sm : 1) * sms;
-    cache[cache_next] = {e->fn, dev, n};
-    cache_next = (cache_next + 1) % 16;
+    if (per_sm < 1) {
+        *err = cudaErrorInvalidConfiguration;
+        return 0;
+    }
+    const int n = per_sm * sms;
+    cache[cache_next] = {e->fn, dev, smem, n};
+    cache_next = (cache_next + 1) % 32;
     return n;
 }
 
@@ -166,18 +218,21 @@ int run(int op, int variant, const float* x, const float* p0, const float* p1, f
     if (st != RN_OK) return st;
     if (rows == 0) return RN_OK;
     rn_plan pl;
-    st = plan_impl(op, variant, d, x, y, &pl);
+    st = plan_impl(op, variant, d, x, y, p0, p1, &pl);
     if (st != RN_OK) return st;
 
     const KernelEntry* e = nullptr;
     if (pl.variant == RN_VARIANT_STREAM)
         e = stream_entry(op, pl.vec);
+    else if (pl.variant == RN_VARIANT_STAGED)
+        e = staged_entry(op, pl.slots);
     else
-        e = reg_entry(op, pl.vec, pl.slots, pl.threads_per_row);
+        e = reg_entry(op, pl.vec, pl.slots, pl.threads_per_row, pl.params_held != 0,
+                      pl.aligned != 0);
     if (!e) return RN_ERR_VARIANT;
 
     cudaError_t err = cudaSuccess;
-    const int resident = resident_ctas(e, &err);
+    const int resident = resident_ctas(e, pl.smem_bytes, &err);
     if (err != cudaSuccess) {
         g_last_cuda_error = (int)err;
         return RN_ERR_CUDA;
@@ -232,12 +287,10 @@ int rms_fwd_variant(int variant, const float* x, const float* w, float* y, int64
 
 int rn_plan_for(int op, int variant, int64_t d, const void* x, const void* y, const void* p0,
                 const void* p1, rn_plan* plan) {
-    (void)p0;
-    (void)p1;
     if (!plan) return RN_ERR_NULL;
     if (op != RN_OP_LN && op != RN_OP_RMS) return RN_ERR_VARIANT;
     if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
-    return plan_impl(op, variant, d, x, y, plan);
+    return plan_impl(op, variant, d, x, y, p0, p1, plan);
 }
 
 const char* rn_status_str(int status) {
@@ -255,6 +308,16 @@ const char* rn_status_str(int status) {
 }
 
 int rn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int rn_device_error(unsigned int* flags, int clear) {
+    if (!flags) return RN_ERR_NULL;
+    const cudaError_t err = device_error_word(flags, clear != 0);
+    if (err != cudaSuccess) {
+        g_last_cuda_error = (int)err;
+        return RN_ERR_CUDA;
+    }
+    return RN_OK;
+}
 
 int rn_launch_empty(int64_t grid, int threads, void* stream) {
     if (grid < 1 || grid >= ((int64_t)1 << 31) || threads < 1 || threads > 1024)

@@ -98,11 +98,31 @@ def test_bad_variant(lib):
     (4096, capi.RN_VARIANT_BLOCK, 128, 8),
     (8193, capi.RN_VARIANT_BLOCK, 256, 8),
     (32771, capi.RN_VARIANT_BLOCK, 1024, 8),
-    (32772, capi.RN_VARIANT_STREAM, 512, 0),
+    (32772, capi.RN_VARIANT_STAGED, 512, 1),
+    (57000, capi.RN_VARIANT_STAGED, 512, 1),
+    (57860, capi.RN_VARIANT_STREAM, 512, 0),
 ])
 def test_plan_by_width(lib, d, variant, tpr, slots):
     p = capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_AUTO, d, A, A + 0x1000000)
     assert (p.variant, p.vec, p.threads_per_row, p.slots) == (variant, 4, tpr, slots)
+
+
+@pytest.mark.parametrize("d,stages", [(1, 4), (3, 4), (4, 4), (8192, 4), (14464, 4),
+                                      (14468, 3), (19264, 3), (19268, 2), (28928, 2),
+                                      (28932, 1), (57856, 1)])
+def test_staged_ring_depth(lib, d, stages):
+    """Row buffers of 16*(d/4) bytes (rounded to 128) fill at most 226 KiB, up to 4 of them."""
+    p = capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_STAGED, d, A, A + 0x1000000)
+    assert p.variant == capi.RN_VARIANT_STAGED and p.slots == stages
+    sb = ((d // 4) * 16 + 127) // 128 * 128
+    assert p.smem_bytes == stages * sb and p.smem_bytes <= 232448 - 1024
+
+
+def test_staged_needs_matching_phases(lib):
+    with pytest.raises(capi.RowNormError):
+        capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_STAGED, 40000, A, A + 4)
+    p = capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_AUTO, 40000, A, A + 4)
+    assert p.variant == capi.RN_VARIANT_STREAM and p.vec == 1
 
 
 def test_plan_phase_mismatch_goes_scalar(lib):

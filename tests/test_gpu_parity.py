@@ -106,6 +106,23 @@ def test_phases_and_ragged_widths(d):
 
 
 # ---------------------------------------------------------------------------
+# rows too wide for registers: staged (bulk copy into shared memory) and
+# streaming kernels, up to the largest row one CTA can stage
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [24577, 40000, 57856, 57860, 100003])
+def test_wide_rows(d):
+    wl = workloads.Workload("ln", 67, d, seed=29, x_dist="offset", x_std=2.0)
+    x = wl.x()
+    g, b = wl.params()
+    for x_off, y_off in ((0, 0), (3, 3), (1, 2)):
+        for v in G.variants_for(LN, d, x_off, y_off):
+            _check_ln(x, g, b, G.run_ln(x, g, b, variant=v, x_off=x_off, y_off=y_off, p_off=1))
+        for v in G.variants_for(RMS, d, x_off, y_off):
+            _check_rms(x, g, G.run_rms(x, g, variant=v, x_off=x_off, y_off=y_off))
+    assert capi.device_error() == 0
+
+
+# ---------------------------------------------------------------------------
 # rows far beyond the resident grid: every CTA walks many rows
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("rows,d", [(200003, 64), (60001, 200), (20011, 1500), (3001, 40000)])
@@ -120,6 +137,11 @@ def test_many_rows_per_cta(rows, d):
 # ---------------------------------------------------------------------------
 # optional statistics, empty input, eps = 0
 # ---------------------------------------------------------------------------
+def test_no_device_error_reported():
+    """No staged kernel of the runs above hit its bounded wait."""
+    assert capi.device_error() == 0
+
+
 def test_statistics_optional():
     wl = workloads.Workload("ln", 300, 768, seed=5)
     x = wl.x()
