@@ -18,10 +18,17 @@
  *
  * Conventions shared by every entry point:
  *
- *   Memory      All array pointers are DEVICE pointers (cudaMalloc'd or any
- *               memory the GPU can address). The caller owns every buffer;
- *               the library allocates nothing and never synchronizes. Rows
- *               are contiguous with row stride d (in elements). Every pointer
+ *   Memory      Every array pointer is an address the current GPU can
+ *               dereference: device memory (cudaMalloc), or host memory the
+ *               GPU can address -- pinned host memory (cudaHostAlloc /
+ *               cudaHostRegister; with unified addressing its host pointer
+ *               is valid on the device) and, on systems whose GPU reads host
+ *               page tables (GB300 over NVLink-C2C), ordinary pageable host
+ *               memory. Host-resident x is then read and host-resident y
+ *               written by the kernel itself over the host link, with no
+ *               staging copies. The caller owns every buffer; the library
+ *               allocates nothing and never synchronizes. Rows are
+ *               contiguous with row stride d (in elements). Every pointer
  *               must be 4-byte aligned; no other alignment is required
  *               (16-byte aligned rows take the vector path, others a scalar
  *               head/tail or the scalar path).

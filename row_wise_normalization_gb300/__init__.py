@@ -18,17 +18,27 @@ def _stream_handle(t, stream):
     import torch
 
     if stream is None:
-        stream = torch.cuda.current_stream(t.device)
+        stream = torch.cuda.current_stream(t.device if t.is_cuda else None)
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _empty_like_home(x, shape):
+    import torch
+
+    if x.is_cuda:
+        return torch.empty(shape, dtype=torch.float32, device=x.device)
+    return torch.empty(shape, dtype=torch.float32, pin_memory=True)
+
+
 def _check_f32_cuda(name, t):
+    """FP32, contiguous, and addressable by the GPU: a CUDA tensor or a pinned
+    CPU tensor (which the kernel reads or writes over the host link)."""
     import torch
 
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
     if t.dtype != torch.float32:
         raise TypeError(f"{name} must be float32, got {t.dtype}")
     if not t.is_contiguous():
@@ -40,7 +50,9 @@ def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, s
     """LayerNorm forward over the last dimension of ``x``.
 
     Returns ``(y, mean, rstd)``: y like x; mean and rstd of shape x.shape[:-1]
-    (FP32). Output tensors may be passed in (contiguous FP32 CUDA).
+    (FP32). Tensors are CUDA tensors or pinned CPU tensors (read or written by
+    the kernel over the host link); outputs not passed in are allocated where
+    x lives.
     """
     import torch
 
@@ -52,11 +64,11 @@ def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, s
         if t.numel() != d:
             raise ValueError(f"{n} must have {d} elements")
     if y is None:
-        y = torch.empty_like(x)
+        y = _empty_like_home(x, x.shape)
     if mean is None:
-        mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+        mean = _empty_like_home(x, x.shape[:-1])
     if rstd is None:
-        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+        rstd = _empty_like_home(x, x.shape[:-1])
     for n, t, k in (("y", y, x.numel()), ("mean", mean, rows), ("rstd", rstd, rows)):
         _check_f32_cuda(n, t)
         if t.numel() != k:
@@ -80,7 +92,7 @@ def rms_fwd(x, w, eps: float = 1e-5, *, y=None, stream=None,
     if w.numel() != d:
         raise ValueError(f"w must have {d} elements")
     if y is None:
-        y = torch.empty_like(x)
+        y = _empty_like_home(x, x.shape)
     _check_f32_cuda("y", y)
     if y.numel() != x.numel():
         raise ValueError("y must be shaped like x")

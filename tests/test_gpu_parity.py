@@ -204,6 +204,42 @@ def test_torch_binding_and_side_stream():
 
 
 # ---------------------------------------------------------------------------
+# host-resident buffers: pinned host memory read and written by the kernel
+# over the host link (no staging copies)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("where", ["host_in", "host_out", "host_both"])
+@pytest.mark.parametrize("rows,d", [(4096, 768), (333, 1029), (64, 40000)])
+def test_host_resident_buffers(where, rows, d):
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn
+
+    wl = workloads.Workload("ln", rows, d, seed=31, x_dist="offset", x_std=2.0)
+    x = wl.x()
+    g, b = wl.params()
+    dev = torch.device("cuda", 0)
+    xin = torch.from_numpy(x).pin_memory() if where != "host_out" else torch.from_numpy(x).to(dev)
+    gt, bt = torch.from_numpy(g).to(dev), torch.from_numpy(b).to(dev)
+
+    def out(shape):
+        if where == "host_in":
+            return torch.full(shape, float("nan"), device=dev)
+        return torch.full(shape, float("nan")).pin_memory()
+
+    y, m, r = out((rows, d)), out((rows,)), out((rows,))
+    rn.ln_fwd(xin, gt, bt, y=y, mean=m, rstd=r)
+    yq = rn.rms_fwd(xin, gt, y=out((rows, d)))
+    torch.cuda.synchronize()
+    _check_ln(x, g, b, (y.cpu().numpy(), m.cpu().numpy(), r.cpu().numpy()))
+    _check_rms(x, g, yq.cpu().numpy())
+    if where == "host_both":
+        # outputs allocated by the binding live where x lives
+        y2, m2, _ = rn.ln_fwd(xin, gt, bt)
+        torch.cuda.synchronize()
+        assert not y2.is_cuda and y2.is_pinned() and m2.is_pinned()
+        parity.check_y(y2.numpy(), reference.layer_norm(x, g, b)[0])
+
+
+# ---------------------------------------------------------------------------
 # full size, in the launch configuration the benchmark times
 # ---------------------------------------------------------------------------
 @pytest.mark.slow
