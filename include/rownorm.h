@@ -114,6 +114,10 @@ int rn_last_cuda_error(void);
  *                       engine, then reduced and written from there
  *   RN_VARIANT_STREAM   any width: statistics in one streaming read, the
  *                       output in a second (x is read twice)
+ *   RN_VARIANT_CLUSTER  a row split over a thread-block cluster of 2..16
+ *                       CTAs (one per SM), each holding its slice in
+ *                       registers; the statistics meet through distributed
+ *                       shared memory (rows up to 524288 elements)
  * ------------------------------------------------------------------------ */
 enum {
     RN_VARIANT_AUTO = 0,
@@ -121,15 +125,16 @@ enum {
     RN_VARIANT_BLOCK = 2,
     RN_VARIANT_STAGED = 3,
     RN_VARIANT_STREAM = 4,
-    RN_VARIANT_COUNT = 5
+    RN_VARIANT_CLUSTER = 5,
+    RN_VARIANT_COUNT = 6
 };
 
 /* Which kernel configuration a call would launch (host-only; no CUDA call). */
 typedef struct rn_plan {
     int variant;          /* RN_VARIANT_* actually chosen                      */
     int vec;              /* elements per vector access: 4 or 1                */
-    int slots;            /* vectors held per thread (register variants);
-                             row buffers in the ring (staged variant)          */
+    int slots;            /* vectors held per thread (register and cluster
+                             variants); row buffers in the ring (staged)       */
     int threads_per_row;  /* threads cooperating on one row                    */
     int rows_per_cta;     /* rows a CTA works on at once                       */
     int threads_per_cta;
@@ -137,6 +142,7 @@ typedef struct rn_plan {
     int prefetch;         /* 1: the next row's loads overlap this row's work   */
     int params_held;      /* 1: gamma/beta (w) held in registers across rows   */
     int aligned;          /* 1: x, y, params 16-byte aligned and d % 4 == 0    */
+    int cluster;          /* CTAs per cluster (cluster variant), else 1        */
 } rn_plan;
 
 enum { RN_OP_LN = 0, RN_OP_RMS = 1 };

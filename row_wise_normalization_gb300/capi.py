@@ -29,7 +29,8 @@ RN_VARIANT_WARP = 1
 RN_VARIANT_BLOCK = 2
 RN_VARIANT_STAGED = 3
 RN_VARIANT_STREAM = 4
-RN_VARIANT_COUNT = 5
+RN_VARIANT_CLUSTER = 5
+RN_VARIANT_COUNT = 6
 
 RN_OP_LN = 0
 RN_OP_RMS = 1
@@ -44,7 +45,8 @@ _INT = ctypes.c_int
 class rn_plan(ctypes.Structure):
     _fields_ = [("variant", _INT), ("vec", _INT), ("slots", _INT), ("threads_per_row", _INT),
                 ("rows_per_cta", _INT), ("threads_per_cta", _INT), ("smem_bytes", _INT),
-                ("prefetch", _INT), ("params_held", _INT), ("aligned", _INT)]
+                ("prefetch", _INT), ("params_held", _INT), ("aligned", _INT),
+                ("cluster", _INT)]
 
 
 SIGNATURES = {

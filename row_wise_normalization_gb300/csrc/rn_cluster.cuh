@@ -1,0 +1,293 @@
+// rn_cluster.cuh -- rows split across a thread-block cluster.
+//
+// A row too wide for one CTA's registers is spread over the CL CTAs of a
+// cluster (CL = 2..16, each on its own SM): CTA c holds quads
+// [c*Q, (c+1)*Q) of the row's aligned body in registers (Q = ceil(nv/CL);
+// SLOTS quads per thread), CTA 0 also takes the <= 6 head/tail scalars. The
+// row is read from HBM once and written from the registers, exactly as in the
+// CTA-per-row kernel; only the statistics cross SMs. Each warp reduces its
+// share to (count, sum, mean, centred M2) about its own mean, and lanes
+// 0..CL-1 store that float4 straight into slot (c, warp) of every CTA of the
+// cluster through distributed shared memory (mapa + st.shared::cluster). One
+// cluster barrier (release/acquire) later every thread merges the CL*WPR
+// partials with the parallel-axis rule. Slots are double-buffered by row
+// parity, so one cluster barrier per row is the only synchronisation.
+//
+// The partials are formed on x - K, K the row's first element: a merge adds
+// the product of a partial mean's rounding error (~u |mean|) and the spread
+// of the partial means to M2, which matters when a row is split into partials
+// of few elements and |mu| >> sigma; after the shift the partial means are
+// of the order of sigma.
+//
+// Clusters are persistent: cluster k walks rows k, k + nclusters, ... with
+// all its CTAs in step (the same trip count), prefetching the next row's
+// slice when PF is set.
+#pragma once
+
+#include "rn_device.cuh"
+
+namespace rn {
+
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store a float4 into CTA `rank`'s shared memory at the address that `local`
+// has in this CTA.
+__device__ __forceinline__ void dsmem_store4(const void* local, unsigned rank, float4 v) {
+    unsigned la = (unsigned)__cvta_generic_to_shared(local), ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+template <int OP, int SLOTS, int TPB, int CL, bool PF, bool AL>
+struct ClusterCfg {
+    static constexpr int WPR = TPB / 32;
+    static constexpr int NE = CL * WPR;          // partials merged per row
+    static constexpr int MINB = PF ? (TPB <= 256 ? 2 : 1) : (TPB >= 1024 ? 1 : (TPB == 512 ? 2 : 768 / TPB));
+};
+
+template <int OP, int SLOTS, int TPB, int CL, bool PF, bool AL>
+__global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::MINB))
+    cluster_kernel(const Params p) {
+    using C = ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>;
+    constexpr int WPR = C::WPR;
+    constexpr int NE = C::NE;
+    __shared__ __align__(16) float4 slots[2][NE];
+
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    const unsigned c = cluster_ctarank();
+    const int64_t cluster_id = blockIdx.x / CL;
+    const int64_t nclusters = gridDim.x / CL;
+    const int d = (int)p.d;
+    const float fd = (float)d;
+
+    // every CTA of the cluster is running before anyone writes into a peer
+    cluster_sync_all();
+
+    struct Slice {
+        Vec<4> v[SLOTS];
+        float e, K;              // head/tail scalar, the row's first element
+        int h, nv, tl, q0, nq;   // row layout and this CTA's quads [q0, q0 + nq)
+    };
+    auto load = [&](Slice& s, int64_t row) {
+        const float* xr = p.x + row * p.d;
+        if constexpr (AL) {
+            s.h = 0;
+            s.nv = d >> 2;
+            s.tl = 0;
+        } else {
+            s.h = head_peel(xr, d);
+            s.nv = (d - s.h) >> 2;
+            s.tl = d - s.h - 4 * s.nv;
+        }
+        const int Q = (s.nv + CL - 1) / CL;
+        s.q0 = (int)c * Q;
+        s.nq = s.nv - s.q0 < Q ? s.nv - s.q0 : Q;
+        if (s.nq < 0) s.nq = 0;
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+            const int q = t + k * TPB;
+            if (q < s.nq) {
+                ld_x(s.v[k], xr + s.h + 4 * (s.q0 + q));
+            } else {
+                s.v[k].v[0] = s.v[k].v[1] = s.v[k].v[2] = s.v[k].v[3] = 0.f;
+            }
+        }
+        s.e = 0.f;
+        if (!AL && c == 0 && t < s.h + s.tl)
+            s.e = ld_x1(xr + ((t < s.h) ? t : s.h + 4 * s.nv + (t - s.h)));
+        s.K = OP == OP_LN ? ld_x1(xr) : 0.f;   // the same address for every thread
+    };
+
+    int64_t row = cluster_id;
+    Slice cur;
+    if (row < p.rows) load(cur, row);
+    int it = 0;
+    for (; row < p.rows; row += nclusters, ++it) {
+        const int64_t nrow = row + nclusters;
+        Slice nxt;
+        if constexpr (PF) {
+            if (nrow < p.rows) load(nxt, nrow);
+        }
+        const int h = cur.h, nv = cur.nv, tl = cur.tl, q0 = cur.q0, nq = cur.nq;
+        const bool has_e = !AL && c == 0 && t < h + tl;
+        const int ei = (t < h) ? t : h + 4 * nv + (t - h);
+
+        // ---- per-warp partial statistics --------------------------------
+        float4 part;   // (count, sum, mean, M2) or (-, sum of squares, -, -)
+        {
+            int nw = (!AL && c == 0 && w == 0) ? (h + tl) : 0;
+#pragma unroll
+            for (int k = 0; k < SLOTS; ++k) {
+                const int rem = nq - k * TPB - 32 * w;
+                nw += 4 * (rem <= 0 ? 0 : (rem >= 32 ? 32 : rem));
+            }
+            if constexpr (OP == OP_LN) {
+                const float K = cur.K;
+                float sum = has_e ? cur.e - K : 0.f;
+#pragma unroll
+                for (int k = 0; k < SLOTS; ++k) {
+                    if (t + k * TPB < nq) {
+                        sum += ((cur.v[k].v[0] - K) + (cur.v[k].v[1] - K)) +
+                               ((cur.v[k].v[2] - K) + (cur.v[k].v[3] - K));
+                    }
+                }
+                const float wsum = warp_sum(sum);
+                const float wmean = nw > 0 ? wsum / (float)nw : 0.f;   // of x - K
+                const float de = (cur.e - K) - wmean;
+                float m2 = has_e ? de * de : 0.f;
+#pragma unroll
+                for (int k = 0; k < SLOTS; ++k) {
+                    if (t + k * TPB < nq) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float dd = (cur.v[k].v[j] - K) - wmean;
+                            m2 = fmaf(dd, dd, m2);
+                        }
+                    }
+                }
+                part = make_float4((float)nw, wsum, wmean, warp_sum(m2));
+            } else {
+                float ss = cur.e * cur.e;
+#pragma unroll
+                for (int k = 0; k < SLOTS; ++k)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) ss = fmaf(cur.v[k].v[j], cur.v[k].v[j], ss);
+                part = make_float4(0.f, warp_sum(ss), 0.f, 0.f);
+            }
+        }
+        // lane r publishes this warp's partial into CTA r's slot (c, w)
+        float4* buf = slots[it & 1];
+        if (lane < CL) dsmem_store4(&buf[c * WPR + w], (unsigned)lane, part);
+        cluster_sync_all();
+
+        // ---- merge the CL * WPR partials (every thread) -----------------
+        float mu = 0.f, rs;
+        {
+            float s1 = 0.f;
+#pragma unroll
+            for (int k = lane; k < NE; k += 32) s1 += buf[k].y;
+            s1 = warp_sum(s1);
+            if constexpr (OP == OP_LN) {
+                const float mus = s1 / fd;            // mean of x - K
+                float m2 = 0.f;
+#pragma unroll
+                for (int k = lane; k < NE; k += 32) {
+                    const float4 e4 = buf[k];
+                    const float dm = e4.z - mus;
+                    m2 += fmaf(e4.x * dm, dm, e4.w);
+                }
+                mu = cur.K + mus;
+                rs = rsqrtf(warp_sum(m2) / fd + p.eps);
+            } else {
+                rs = rsqrtf(s1 / fd + p.eps);
+            }
+        }
+
+        // ---- normalize and store from the held registers ----------------
+        float* yr = p.y + row * p.d;
+        bool pa = true;
+        if constexpr (!AL) {
+            pa = ((((uintptr_t)p.p0 >> 2) + h) & 3) == 0;
+            if constexpr (OP == OP_LN) pa = pa && ((((uintptr_t)p.p1 >> 2) + h) & 3) == 0;
+        }
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+            const int q = t + k * TPB;
+            if (q < nq) {
+                const int j = h + 4 * (q0 + q);
+                Vec<4> a, b, o;
+                ld_p(a, p.p0 + j, pa);
+                if constexpr (OP == OP_LN) {
+                    ld_p(b, p.p1 + j, pa);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) o.v[u] = fmaf((cur.v[k].v[u] - mu) * rs, a.v[u], b.v[u]);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) o.v[u] = cur.v[k].v[u] * rs * a.v[u];
+                }
+                st_y(yr + j, o);
+            }
+        }
+        if (has_e) {
+            const float a = ld_p1(p.p0 + ei);
+            float o;
+            if constexpr (OP == OP_LN)
+                o = fmaf((cur.e - mu) * rs, a, ld_p1(p.p1 + ei));
+            else
+                o = cur.e * rs * a;
+            st_y1(yr + ei, o);
+        }
+        if constexpr (OP == OP_LN) {
+            if (c == 0 && t == 0) {
+                if (p.mean) p.mean[row] = mu;
+                if (p.rstd) p.rstd[row] = rs;
+            }
+        }
+        if constexpr (PF) {
+            cur = nxt;
+        } else {
+            if (nrow < p.rows) load(cur, nrow);
+        }
+    }
+    // no CTA leaves while a peer could still address its shared memory
+    cluster_sync_all();
+}
+
+template <int OP, int SLOTS, int TPB, int CL, bool AL>
+struct ClusterInst {
+    static constexpr bool PF = TPB <= 256;
+    static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.blockDim = dim3(TPB, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, cluster_kernel<OP, SLOTS, TPB, CL, PF, AL>, p);
+    }
+    static cudaError_t prepare(int) {
+        if (CL > 8)
+            return cudaFuncSetAttribute(cluster_kernel<OP, SLOTS, TPB, CL, PF, AL>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return cudaSuccess;
+    }
+    // Clusters that can be resident at once.
+    static cudaError_t max_clusters(int* n) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(CL, 1, 1);
+        cfg.blockDim = dim3(TPB, 1, 1);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaOccupancyMaxActiveClusters(n, cluster_kernel<OP, SLOTS, TPB, CL, PF, AL>, &cfg);
+    }
+    static const ClusterEntry entry;
+};
+
+template <int OP, int SLOTS, int TPB, int CL, bool AL>
+const ClusterEntry ClusterInst<OP, SLOTS, TPB, CL, AL>::entry = {
+    CL, TPB, SLOTS, &ClusterInst<OP, SLOTS, TPB, CL, AL>::launch,
+    &ClusterInst<OP, SLOTS, TPB, CL, AL>::prepare, &ClusterInst<OP, SLOTS, TPB, CL, AL>::max_clusters};
+
+}  // namespace rn

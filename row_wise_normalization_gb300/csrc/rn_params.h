@@ -67,6 +67,20 @@ const KernelEntry* stream_entry(int op, int vec);
 // Shared-memory-staged kernels with `stages` row buffers (1..kMaxStages).
 const KernelEntry* staged_entry(int op, int stages);
 
+// Rows split across a thread-block cluster of `cl` CTAs of `threads` threads,
+// each holding `slots` quads of the row per thread.
+struct ClusterEntry {
+    int cl;
+    int threads;
+    int slots;
+    cudaError_t (*launch)(const Params&, int grid, cudaStream_t);
+    cudaError_t (*prepare)(int);
+    cudaError_t (*max_clusters)(int* n);
+};
+const ClusterEntry* cluster_entry(int op, int slots, int threads, int cl, bool al);
+constexpr int kMaxCluster = 16;
+constexpr int kClusterMaxQuads = 1024 * 8 * kMaxCluster;   // 524288 floats per row
+
 // Reads (and optionally clears) the device error word of the current device.
 cudaError_t device_error_word(unsigned int* out, bool clear);
 

@@ -59,6 +59,27 @@ bool block_shape(int64_t units, int* tpr, int* slots) {
     return false;
 }
 
+// Cluster split: 256 threads per CTA and 4/6/8 quads per thread over the
+// fewest CTAs (2..16); then 512 and 1024 threads with 16 CTAs of 8 quads.
+bool cluster_shape(int64_t units, int* threads, int* cl, int* slots) {
+    for (int c = 2; c <= kMaxCluster; c *= 2)
+        for (int s : {4, 6, 8})
+            if (units <= (int64_t)c * 256 * s) {
+                *threads = 256;
+                *cl = c;
+                *slots = s;
+                return true;
+            }
+    for (int t : {512, 1024})
+        if (units <= (int64_t)kMaxCluster * t * 8) {
+            *threads = t;
+            *cl = kMaxCluster;
+            *slots = 8;
+            return true;
+        }
+    return false;
+}
+
 // Shared-memory staging: row buffers of the aligned body, as many as fit (at
 // most kMaxStages). Returns false if one row does not fit.
 bool staged_shape(int64_t d, int* stages, int* smem) {
@@ -86,16 +107,23 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, cons
 
     int v = variant;
     if (v == RN_VARIANT_AUTO) {
-        int st, sm;
+        int st, sm, ct, cc, cs;
+        // Measured on GB300: one CTA per row holds up to 32768 floats and
+        // beats splitting the row over a cluster there; beyond, the cluster
+        // keeps the single HBM read that the staged and streaming kernels
+        // give up or pay for in shared-memory passes.
         if (units <= 32 * kMaxSlots)
             v = RN_VARIANT_WARP;
         else if (units <= 1024 * kMaxSlots)
             v = RN_VARIANT_BLOCK;
+        else if (vec == 4 && cluster_shape(units, &ct, &cc, &cs))
+            v = RN_VARIANT_CLUSTER;
         else if (vec == 4 && staged_shape(d, &st, &sm))
             v = RN_VARIANT_STAGED;
         else
             v = RN_VARIANT_STREAM;
     }
+    pl->cluster = 1;
     switch (v) {
         case RN_VARIANT_WARP:
             if (units > 32 * kMaxSlots) return RN_ERR_VARIANT;
@@ -127,6 +155,17 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, cons
             pl->rows_per_cta = 1;
             pl->threads_per_cta = kStagedThreads;
             pl->smem_bytes = sm;
+            break;
+        }
+        case RN_VARIANT_CLUSTER: {
+            int ct, cc, cs;
+            if (vec != 4 || !cluster_shape(units, &ct, &cc, &cs)) return RN_ERR_VARIANT;
+            pl->slots = cs;
+            pl->threads_per_row = ct * cc;
+            pl->rows_per_cta = 1;
+            pl->threads_per_cta = ct;
+            pl->cluster = cc;
+            pl->aligned = al;
             break;
         }
         case RN_VARIANT_STREAM:
@@ -212,6 +251,34 @@ int resident_ctas(const KernelEntry* e, int smem, cudaError_t* err) {
     return n;
 }
 
+// Clusters of `ce` that fit on the current device at once (0 on error).
+int resident_clusters(const ClusterEntry* ce, cudaError_t* err) {
+    struct Cache {
+        const ClusterEntry* e;
+        int dev;
+        int n;
+    };
+    static thread_local Cache cache[16];
+    static thread_local int cache_next = 0;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return 0;
+    for (auto& c : cache)
+        if (c.e == ce && c.dev == dev && c.n > 0) return c.n;
+    *err = ce->prepare(0);
+    if (*err != cudaSuccess) return 0;
+    int n = 0;
+    *err = ce->max_clusters(&n);
+    if (*err != cudaSuccess) return 0;
+    if (n < 1) {
+        *err = cudaErrorInvalidConfiguration;
+        return 0;
+    }
+    cache[cache_next] = {ce, dev, n};
+    cache_next = (cache_next + 1) % 16;
+    return n;
+}
+
 int run(int op, int variant, const float* x, const float* p0, const float* p1, float* y,
         float* mean, float* rstd, int64_t rows, int64_t d, float eps, void* stream) {
     int st = validate(op, x, p0, p1, y, mean, rstd, rows, d, eps);
@@ -220,6 +287,34 @@ int run(int op, int variant, const float* x, const float* p0, const float* p1, f
     rn_plan pl;
     st = plan_impl(op, variant, d, x, y, p0, p1, &pl);
     if (st != RN_OK) return st;
+
+    Params prm;
+    prm.x = x;
+    prm.y = y;
+    prm.p0 = p0;
+    prm.p1 = p1;
+    prm.mean = mean;
+    prm.rstd = rstd;
+    prm.rows = rows;
+    prm.d = d;
+    prm.eps = eps;
+
+    if (pl.variant == RN_VARIANT_CLUSTER) {
+        const ClusterEntry* ce =
+            cluster_entry(op, pl.slots, pl.threads_per_cta, pl.cluster, pl.aligned != 0);
+        if (!ce) return RN_ERR_VARIANT;
+        cudaError_t err = cudaSuccess;
+        const int nclusters = resident_clusters(ce, &err);
+        if (err == cudaSuccess) {
+            const int64_t want = rows < nclusters ? rows : nclusters;
+            err = ce->launch(prm, (int)want * ce->cl, (cudaStream_t)stream);
+        }
+        if (err != cudaSuccess) {
+            g_last_cuda_error = (int)err;
+            return RN_ERR_CUDA;
+        }
+        return RN_OK;
+    }
 
     const KernelEntry* e = nullptr;
     if (pl.variant == RN_VARIANT_STREAM)
@@ -239,17 +334,6 @@ int run(int op, int variant, const float* x, const float* p0, const float* p1, f
     }
     const int64_t want = (rows + e->rows_per_cta - 1) / e->rows_per_cta;
     const int grid = (int)(want < resident ? want : resident);
-
-    Params prm;
-    prm.x = x;
-    prm.y = y;
-    prm.p0 = p0;
-    prm.p1 = p1;
-    prm.mean = mean;
-    prm.rstd = rstd;
-    prm.rows = rows;
-    prm.d = d;
-    prm.eps = eps;
     err = e->launch(prm, grid, (cudaStream_t)stream);
     if (err != cudaSuccess) {
         g_last_cuda_error = (int)err;
@@ -338,6 +422,7 @@ const char* rn_variant_name(int variant) {
         case RN_VARIANT_BLOCK: return "block";
         case RN_VARIANT_STAGED: return "staged";
         case RN_VARIANT_STREAM: return "stream";
+        case RN_VARIANT_CLUSTER: return "cluster";
         default: return "unknown";
     }
 }

@@ -39,6 +39,8 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     for s in range(0, 8):
         assert capi.status_str(s)
+    for v in range(capi.RN_VARIANT_COUNT):
+        assert capi.variant_name(v) != "unknown"
     assert capi.status_str(99) == "unknown status"
     assert capi.variant_name(capi.RN_VARIANT_WARP) == "warp"
 
@@ -97,10 +99,15 @@ def test_bad_variant(lib):
     (1028, capi.RN_VARIANT_BLOCK, 64, 5),
     (4096, capi.RN_VARIANT_BLOCK, 128, 8),
     (8193, capi.RN_VARIANT_BLOCK, 256, 8),
+    (8196, capi.RN_VARIANT_BLOCK, 512, 5),
+    (16384, capi.RN_VARIANT_BLOCK, 512, 8),
     (32771, capi.RN_VARIANT_BLOCK, 1024, 8),
-    (32772, capi.RN_VARIANT_STAGED, 512, 1),
-    (57000, capi.RN_VARIANT_STAGED, 512, 1),
-    (57860, capi.RN_VARIANT_STREAM, 512, 0),
+    (32772, capi.RN_VARIANT_CLUSTER, 8 * 256, 6),
+    (65536, capi.RN_VARIANT_CLUSTER, 8 * 256, 8),
+    (131072, capi.RN_VARIANT_CLUSTER, 16 * 256, 8),
+    (262144, capi.RN_VARIANT_CLUSTER, 16 * 512, 8),
+    (524288, capi.RN_VARIANT_CLUSTER, 16 * 1024, 8),
+    (524292, capi.RN_VARIANT_STREAM, 512, 0),
 ])
 def test_plan_by_width(lib, d, variant, tpr, slots):
     p = capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_AUTO, d, A, A + 0x1000000)
@@ -118,11 +125,30 @@ def test_staged_ring_depth(lib, d, stages):
     assert p.smem_bytes == stages * sb and p.smem_bytes <= 232448 - 1024
 
 
+@pytest.mark.parametrize("d,cl,threads,slots", [(8196, 2, 256, 6), (12288, 2, 256, 6),
+                                               (12292, 2, 256, 8), (20000, 4, 256, 6),
+                                               (100000, 16, 256, 8), (400000, 16, 1024, 8)])
+def test_cluster_shape(lib, d, cl, threads, slots):
+    """The fewest CTAs of 256 threads (then 512, 1024) whose slices hold the row."""
+    p = capi.plan(capi.RN_OP_RMS, capi.RN_VARIANT_CLUSTER, d, A, A + 0x10000000)
+    assert (p.cluster, p.threads_per_cta, p.slots) == (cl, threads, slots)
+    assert p.cluster * p.threads_per_cta * p.slots * 4 >= d
+
+
+def test_cluster_needs_matching_phases(lib):
+    with pytest.raises(capi.RowNormError):
+        capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_CLUSTER, 40000, A, A + 4)
+    with pytest.raises(capi.RowNormError):
+        capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_CLUSTER, 524292, A, A + 0x1000000)
+
+
 def test_staged_needs_matching_phases(lib):
     with pytest.raises(capi.RowNormError):
         capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_STAGED, 40000, A, A + 4)
     p = capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_AUTO, 40000, A, A + 4)
     assert p.variant == capi.RN_VARIANT_STREAM and p.vec == 1
+    p = capi.plan(capi.RN_OP_LN, capi.RN_VARIANT_STAGED, 40000, A, A + 0x1000000)
+    assert p.variant == capi.RN_VARIANT_STAGED
 
 
 def test_plan_phase_mismatch_goes_scalar(lib):

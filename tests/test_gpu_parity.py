@@ -122,6 +122,29 @@ def test_wide_rows(d):
     assert capi.device_error() == 0
 
 
+@pytest.mark.parametrize("rows,d", [(9, 65539), (5, 131072), (3, 200003), (3, 524288),
+                                    (7, 524291)])
+def test_very_wide_rows(rows, d):
+    """Rows split over 8-16 CTA clusters (and the streaming kernel beyond)."""
+    wl = workloads.Workload("ln", rows, d, seed=37, x_dist="offset", x_std=2.0)
+    x = wl.x()
+    g, b = wl.params()
+    for x_off, y_off in ((0, 0), (1, 1)):
+        for v in G.variants_for(LN, d, x_off, y_off):
+            _check_ln(x, g, b, G.run_ln(x, g, b, variant=v, x_off=x_off, y_off=y_off, p_off=2))
+        for v in G.variants_for(RMS, d, x_off, y_off):
+            _check_rms(x, g, G.run_rms(x, g, variant=v, x_off=x_off, y_off=y_off))
+
+
+@pytest.mark.parametrize("rows,d", [(40000, 16384), (5000, 65536)])
+def test_cluster_rows_beyond_resident_clusters(rows, d):
+    """More rows than resident clusters: every cluster walks many rows."""
+    wl = workloads.Workload("rms", rows, d, seed=41)
+    x = wl.x()
+    (w,) = wl.params()
+    _check_rms(x, w, G.run_rms(x, w, variant=capi.RN_VARIANT_CLUSTER))
+
+
 # ---------------------------------------------------------------------------
 # rows far beyond the resident grid: every CTA walks many rows
 # ---------------------------------------------------------------------------
