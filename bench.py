@@ -499,6 +499,41 @@ def run_ours(args, rank, world, local_rank):
             sampler.mark("sweep", t3, time.time())
     extra["sweep_cold_l2"] = sweep
 
+    # residual add fused with the normalization, against the same work done
+    # as a separate add followed by the normalization (cold L2)
+    if not args.no_sweep:
+        import row_wise_normalization_gb300 as rn
+
+        fused = []
+        for op, rows_, d_ in (("ln", 4096, 768), ("ln", 16384, 4096), ("rms", 16384, 4096)):
+            xw = workloads.Workload(op, rows_, d_, seed=61)
+            xt = torch.from_numpy(xw.x()).to(device)
+            rt = torch.from_numpy(workloads.Workload(op, rows_, d_, seed=62).x()).to(device)
+            pt = [torch.from_numpy(p_).to(device) for p_ in xw.params()]
+            ht, yt = torch.empty_like(xt), torch.empty_like(xt)
+            mt = torch.empty(rows_, device=device)
+            st_ = torch.empty(rows_, device=device)
+            if op == "ln":
+                f_fused = lambda: rn.ln_fwd_residual(xt, rt, *pt, h=ht, y=yt, mean=mt, rstd=st_)
+                f_split = lambda: (torch.add(xt, rt, out=ht),
+                                   rn.ln_fwd(ht, *pt, y=yt, mean=mt, rstd=st_))
+            else:
+                f_fused = lambda: rn.rms_fwd_residual(xt, rt, *pt, h=ht, y=yt)
+                f_split = lambda: (torch.add(xt, rt, out=ht), rn.rms_fwd(ht, *pt, y=yt))
+            res_ = {}
+            for name, f in (("fused", f_fused), ("add_then_norm", f_split)):
+                for _ in range(3):
+                    flush()
+                    f()
+                res_[name] = statistics.median(time_launches(torch, f, args.sweep_steps, flush))
+            nb = 16 * rows_ * d_ + (8 if op == "ln" else 4) * d_ + (8 * rows_ if op == "ln" else 0)
+            fused.append({"workload": f"{op}_residual_{rows_}x{d_}",
+                          "fused_ms": res_["fused"], "add_then_norm_ms": res_["add_then_norm"],
+                          "fused_GBps": gbs(nb, res_["fused"]),
+                          "speedup": res_["add_then_norm"] / res_["fused"]})
+            del xt, rt, ht, yt
+        extra["residual_fused_cold_l2"] = fused
+
     clocks = None
     if sampler:
         sampler.stop()

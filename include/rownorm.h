@@ -96,6 +96,26 @@ int ln_fwd(const float *x, const float *gamma, const float *beta,
 int rms_fwd(const float *x, const float *w, float *y,
             int64_t rows, int64_t d, float eps, void *stream);
 
+/*
+ * Residual add fused with the normalization: h = x + res (an FP32 add, the
+ * updated residual stream of a pre-norm transformer block), then LayerNorm
+ * or RMSNorm of h, in one pass over the row.
+ *   x, res   [rows][d]  inputs (res must not alias any output)
+ *   h_out    [rows][d]  h = x + res; may be NULL (not written)
+ *   y, mean_out, rstd_out, gamma, beta, w: as in ln_fwd / rms_fwd, of h.
+ * The pages name this fusion as absent from their kernels ("RMSNorm on an
+ * RTX 5070 ...", section "The operator and the change"). One kernel launch;
+ * AUTO uses the register-held kernels up to d = 32768 floats and the
+ * streaming kernel beyond (the staged and cluster variants have no residual
+ * form: RN_ERR_VARIANT).
+ */
+int ln_fwd_residual(const float *x, const float *res, const float *gamma, const float *beta,
+                    float *h_out, float *y, float *mean_out, float *rstd_out,
+                    int64_t rows, int64_t d, float eps, void *stream);
+
+int rms_fwd_residual(const float *x, const float *res, const float *w, float *h_out,
+                     float *y, int64_t rows, int64_t d, float eps, void *stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *rn_status_str(int status);
 
@@ -163,6 +183,21 @@ int ln_fwd_variant(int variant, const float *x, const float *gamma, const float 
 
 int rms_fwd_variant(int variant, const float *x, const float *w, float *y,
                     int64_t rows, int64_t d, float eps, void *stream);
+
+int ln_fwd_residual_variant(int variant, const float *x, const float *res,
+                            const float *gamma, const float *beta, float *h_out, float *y,
+                            float *mean_out, float *rstd_out, int64_t rows, int64_t d,
+                            float eps, void *stream);
+
+int rms_fwd_residual_variant(int variant, const float *x, const float *res, const float *w,
+                             float *h_out, float *y, int64_t rows, int64_t d, float eps,
+                             void *stream);
+
+/* rn_plan_for for the residual entry points (res and h as they will be
+ * passed; h may be NULL). Host-only. */
+int rn_plan_for_residual(int op, int variant, int64_t d, const void *x, const void *res,
+                         const void *h, const void *y, const void *p0, const void *p1,
+                         rn_plan *plan);
 
 /* Device error word of the current device: bit 0 (RN_DEVERR_STAGED_TIMEOUT)
  * is set if a staged kernel's wait for a bulk copy ran out (about one

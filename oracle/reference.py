@@ -67,3 +67,32 @@ def rms_norm(x, w, eps=1e-5):
     r = 1.0 / np.sqrt(ms + _eps64(eps))
     y = x64 * w64[None, :] * r[:, None]
     return y, r
+
+
+def residual_sum(x, res):
+    """h = x + res, rounded to FP32 (the stored residual stream).
+
+    The sum of two FP32 values rounded to nearest FP32 is what an FP32 add
+    produces; computing it in float64 first and rounding once gives the same
+    bits (the exact sum of two FP32 values fits in float64).
+    """
+    x64 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    r64 = np.asarray(res, dtype=np.float32).astype(np.float64)
+    return (x64 + r64).astype(np.float32)
+
+
+def layer_norm_residual(x, res, gamma, beta, eps=1e-5):
+    """Residual add followed by LayerNorm: h = x + res (FP32), then
+    ``layer_norm(h)``. Returns (h FP32, y, mean, rstd) with y/mean/rstd in
+    float64."""
+    h = residual_sum(x, res)
+    y, mean, rstd = layer_norm(h, gamma, beta, eps)
+    return h, y, mean, rstd
+
+
+def rms_norm_residual(x, res, w, eps=1e-5):
+    """Residual add followed by RMSNorm: h = x + res (FP32), then
+    ``rms_norm(h)``. Returns (h FP32, y, r)."""
+    h = residual_sum(x, res)
+    y, r = rms_norm(h, w, eps)
+    return h, y, r

@@ -11,7 +11,8 @@ from __future__ import annotations
 from . import capi
 from .capi import RowNormError, load  # noqa: F401
 
-__all__ = ["ln_fwd", "rms_fwd", "capi", "RowNormError", "load"]
+__all__ = ["ln_fwd", "rms_fwd", "ln_fwd_residual", "rms_fwd_residual", "capi",
+           "RowNormError", "load"]
 
 
 def _stream_handle(t, stream):
@@ -100,3 +101,65 @@ def rms_fwd(x, w, eps: float = 1e-5, *, y=None, stream=None,
                               float(eps), _stream_handle(x, stream))
     capi.check(st)
     return y
+
+
+def _check_like(name, t, numel):
+    _check_f32_cuda(name, t)
+    if t.numel() != numel:
+        raise ValueError(f"{name} must have {numel} elements")
+
+
+def ln_fwd_residual(x, res, gamma, beta, eps: float = 1e-5, *, h=None, y=None, mean=None,
+                    rstd=None, write_h: bool = True, stream=None,
+                    variant: int = capi.RN_VARIANT_AUTO):
+    """h = x + res, then LayerNorm of h over the last dimension, in one kernel.
+
+    Returns ``(h, y, mean, rstd)``; h is None when ``write_h`` is False and no
+    h tensor is passed. Tensors are CUDA tensors or pinned CPU tensors.
+    """
+    _check_f32_cuda("x", x)
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    _check_like("res", res, x.numel())
+    _check_like("gamma", gamma, d)
+    _check_like("beta", beta, d)
+    if h is None and write_h:
+        h = _empty_like_home(x, x.shape)
+    y = _empty_like_home(x, x.shape) if y is None else y
+    mean = _empty_like_home(x, x.shape[:-1]) if mean is None else mean
+    rstd = _empty_like_home(x, x.shape[:-1]) if rstd is None else rstd
+    if h is not None:
+        _check_like("h", h, x.numel())
+    _check_like("y", y, x.numel())
+    _check_like("mean", mean, rows)
+    _check_like("rstd", rstd, rows)
+    st = capi.ln_fwd_residual_variant(variant, x.data_ptr(), res.data_ptr(), gamma.data_ptr(),
+                                      beta.data_ptr(), h.data_ptr() if h is not None else 0,
+                                      y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), rows, d,
+                                      float(eps), _stream_handle(x, stream))
+    capi.check(st)
+    return h, y, mean, rstd
+
+
+def rms_fwd_residual(x, res, w, eps: float = 1e-5, *, h=None, y=None, write_h: bool = True,
+                     stream=None, variant: int = capi.RN_VARIANT_AUTO):
+    """h = x + res, then RMSNorm of h over the last dimension, in one kernel.
+
+    Returns ``(h, y)``; h is None when ``write_h`` is False and none is passed.
+    """
+    _check_f32_cuda("x", x)
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    _check_like("res", res, x.numel())
+    _check_like("w", w, d)
+    if h is None and write_h:
+        h = _empty_like_home(x, x.shape)
+    y = _empty_like_home(x, x.shape) if y is None else y
+    if h is not None:
+        _check_like("h", h, x.numel())
+    _check_like("y", y, x.numel())
+    st = capi.rms_fwd_residual_variant(variant, x.data_ptr(), res.data_ptr(), w.data_ptr(),
+                                       h.data_ptr() if h is not None else 0, y.data_ptr(), rows,
+                                       d, float(eps), _stream_handle(x, stream))
+    capi.check(st)
+    return h, y

@@ -59,6 +59,12 @@ SIGNATURES = {
     "ln_fwd_variant": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
     "rms_fwd_variant": (_INT, [_INT, _P, _P, _P, _I64, _I64, _F, _P]),
     "rn_launch_empty": (_INT, [_I64, _INT, _P]),
+    "ln_fwd_residual": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+    "rms_fwd_residual": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+    "ln_fwd_residual_variant": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+    "rms_fwd_residual_variant": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+    "rn_plan_for_residual": (_INT, [_INT, _INT, _I64, _P, _P, _P, _P, _P, _P,
+                                    ctypes.POINTER(rn_plan)]),
     "rn_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
 }
 
@@ -108,6 +114,14 @@ def plan(op: int, variant: int, d: int, x: int, y: int, p0: int = 0, p1: int = 0
     return out
 
 
+def plan_residual(op: int, variant: int, d: int, x: int, res: int, h: int, y: int, p0: int = 0,
+                  p1: int = 0) -> rn_plan:
+    """The kernel configuration a residual call would launch (host only)."""
+    out = rn_plan()
+    check(load().rn_plan_for_residual(op, variant, d, x, res, h, y, p0, p1, ctypes.byref(out)))
+    return out
+
+
 def variant_name(v: int) -> str:
     return load().rn_variant_name(v).decode()
 
@@ -139,3 +153,23 @@ def device_error(clear: bool = False) -> int:
     out = ctypes.c_uint(0)
     check(load().rn_device_error(ctypes.byref(out), 1 if clear else 0))
     return out.value
+
+
+def ln_fwd_residual(x, res, gamma, beta, h_out, y, mean_out, rstd_out, rows, d, eps,
+                    stream=0) -> int:
+    return load().ln_fwd_residual(x, res, gamma, beta, h_out, y, mean_out, rstd_out, rows, d,
+                                  eps, stream)
+
+
+def rms_fwd_residual(x, res, w, h_out, y, rows, d, eps, stream=0) -> int:
+    return load().rms_fwd_residual(x, res, w, h_out, y, rows, d, eps, stream)
+
+
+def ln_fwd_residual_variant(variant, x, res, gamma, beta, h_out, y, mean_out, rstd_out, rows, d,
+                            eps, stream=0) -> int:
+    return load().ln_fwd_residual_variant(variant, x, res, gamma, beta, h_out, y, mean_out,
+                                          rstd_out, rows, d, eps, stream)
+
+
+def rms_fwd_residual_variant(variant, x, res, w, h_out, y, rows, d, eps, stream=0) -> int:
+    return load().rms_fwd_residual_variant(variant, x, res, w, h_out, y, rows, d, eps, stream)

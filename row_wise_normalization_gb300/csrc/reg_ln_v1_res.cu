@@ -1,0 +1,6 @@
+// Register-held kernels with a residual add: LN, family v1.
+#include "rn_reg.cuh"
+
+namespace rn {
+const KernelEntry* reg_entry_ln_v1_res(int slots, int tpr) { return reg_pick<OP_LN, 1,false,false, true>(slots, tpr); }
+}  // namespace rn

@@ -1,0 +1,6 @@
+// Register-held kernels with a residual add: LN, family v4_al.
+#include "rn_reg.cuh"
+
+namespace rn {
+const KernelEntry* reg_entry_ln_v4_al_res(int slots, int tpr) { return reg_pick<OP_LN, 4,false,true, true>(slots, tpr); }
+}  // namespace rn

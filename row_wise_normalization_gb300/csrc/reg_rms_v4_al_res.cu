@@ -1,0 +1,6 @@
+// Register-held kernels with a residual add: RMS, family v4_al.
+#include "rn_reg.cuh"
+
+namespace rn {
+const KernelEntry* reg_entry_rms_v4_al_res(int slots, int tpr) { return reg_pick<OP_RMS, 4,false,true, true>(slots, tpr); }
+}  // namespace rn

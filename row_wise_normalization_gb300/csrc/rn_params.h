@@ -10,10 +10,13 @@ namespace rn {
 enum Op : int { OP_LN = 0, OP_RMS = 1 };
 
 // Arguments of every row-normalization kernel. For RMSNorm p0 = w, p1 = NULL,
-// mean = rstd = NULL.
+// mean = rstd = NULL. With a residual (r != NULL) the kernels normalise
+// h = x + r and write h to `h` when it is not NULL.
 struct Params {
     const float* x;
     float* y;
+    const float* r;    // residual added to x (residual variants only)
+    float* h;          // x + r written back (may be NULL)
     const float* p0;   // gamma or w
     const float* p1;   // beta (LN only)
     float* mean;       // may be NULL
@@ -39,7 +42,7 @@ struct KernelEntry {
 // tail scalars); pp: the parameter vectors are held in registers across rows
 // (requires al, tpr <= 128 and slots <= 6). Returns NULL if the
 // configuration was not compiled.
-const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool al);
+const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool al, bool res);
 
 // Register-held configurations, measured on GB300 (cold L2, same-session
 // device-to-device copy as the reference):
@@ -50,19 +53,22 @@ const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool 
 //    resident warps than the overlap wins (a thread then holds 32 floats and
 //    3 CTAs of 256 per SM keep enough bytes in flight), and where two rows
 //    would not fit the 64 registers a thread of a 1024-thread CTA can have;
+//  * with a residual the prefetched row holds x and the residual apart until
+//    it is processed (three slices live), so only slices of <= 4 vectors
+//    prefetch;
 //  * parameters held across rows for rows of up to 128 threads holding at
 //    most 6 vectors each, when every row starts at the same 16-byte phase
 //    (with 8 vectors the held parameters cost a resident CTA per SM).
-constexpr bool reg_prefetch(int vec, int slots, int tpr) {
-    return vec == 4 && !(slots >= 8 && tpr >= 256) &&
+constexpr bool reg_prefetch(int vec, int slots, int tpr, bool res = false) {
+    return vec == 4 && !(slots >= 8 && tpr >= 256) && (!res || slots <= 4) &&
            (52 + 8 * slots) * tpr <= 65536;   // both rows fit the registers of one CTA
 }
 constexpr bool reg_may_hold_params(int vec, int slots, int tpr) {
     return vec == 4 && tpr <= 128 && slots <= 6;
 }
 
-// Streaming two-read kernels (any width).
-const KernelEntry* stream_entry(int op, int vec);
+// Streaming two-read kernels (any width); res: with a residual add.
+const KernelEntry* stream_entry(int op, int vec, bool res);
 
 // Shared-memory-staged kernels with `stages` row buffers (1..kMaxStages).
 const KernelEntry* staged_entry(int op, int stages);

@@ -41,9 +41,9 @@ namespace rn {
 // Registers a thread of reg_kernel is budgeted: the held row (twice with
 // prefetch), the parameters held across rows, and a fixed allowance for
 // indices, statistics and addresses.
-constexpr int reg_budget(int op, int vec, int slots, bool pf, bool pp) {
-    return 48 + slots * vec * (pf ? 2 : 1) + (pp ? 8 + slots * vec * (op == 0 ? 2 : 1) : 0) +
-           (vec == 1 ? 3 * slots : 0);
+constexpr int reg_budget(int op, int vec, int slots, bool pf, bool pp, bool res = false) {
+    return 48 + slots * vec * (pf ? 2 : 1) * (res ? 2 : 1) + (res && !pf ? slots * vec : 0) +
+           (pp ? 8 + slots * vec * (op == 0 ? 2 : 1) : 0) + (vec == 1 ? 3 * slots : 0);
 }
 
 // Resident CTAs each kernel is compiled for, which sets its register cap
@@ -53,26 +53,44 @@ constexpr int reg_budget(int op, int vec, int slots, bool pf, bool pp) {
 // prefetch about 384 resident threads per SM (the two held rows keep enough
 // bytes in flight, and the spare registers let loads issue early), without
 // it about 768-1024. Narrower slices fill the SM as far as the budget allows.
-constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, bool pp) {
-    if (vec == 4 && slots >= 6) {
+constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, bool pp,
+                           bool res = false) {
+    if (vec == 4 && slots >= 6 && !res) {
         if (pf) return threads == 64 ? 5 : (threads >= 384 ? 1 : 384 / threads);
         return threads >= 1024 ? 1 : (threads == 512 ? 2 : (768 / threads > 0 ? 768 / threads : 1));
     }
-    const int per = ((reg_budget(op, vec, slots, pf, pp) + 7) / 8) * 8;
+    const int per = ((reg_budget(op, vec, slots, pf, pp, res) + 7) / 8) * 8;
     const int n = 65536 / (per * threads);
     return n < 1 ? 1 : (n > 32 ? 32 : n);
 }
 
-// One row as a thread holds it.
-template <int VEC, int SLOTS>
+// One row as a thread holds it. With a residual (RES) the residual slice is
+// held apart (vr, er) until the row is processed, so that a prefetched row's
+// loads stay in flight; add_residual() then folds it into v and e.
+template <int VEC, int SLOTS, bool RES = false>
 struct HeldRow {
     Vec<VEC> v[SLOTS];
-    float e;          // the thread's head/tail scalar (0 if none)
+    Vec<VEC> vr[RES ? SLOTS : 1];
+    float e, er;      // the thread's head/tail scalar (0 if none), its residual
     int h, nv, tl;    // head peel, aligned vectors, tail of this row
 };
 
-template <int VEC, int SLOTS, int TPR, bool AL>
-__device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS>& r, const float* xr, int d, int t) {
+template <int VEC, int SLOTS, bool RES>
+__device__ __forceinline__ void add_residual(HeldRow<VEC, SLOTS, RES>& r) {
+    if constexpr (RES) {
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) r.v[s].v[k] = r.v[s].v[k] + r.vr[s].v[k];
+        r.e = r.e + r.er;
+    }
+}
+
+// Loads one row of x (and of the residual rr when RES) at the phase of xr; the
+// residual must share x's 16-byte phase (the host checks).
+template <int VEC, int SLOTS, int TPR, bool AL, bool RES = false>
+__device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const float* xr,
+                                         const float* rr, int d, int t) {
     if constexpr (AL) {
         r.h = 0;
         r.nv = d >> 2;
@@ -91,19 +109,29 @@ __device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS>& r, const float* xr
         const int q = t + s * TPR;
         if (q < r.nv) {
             ld_x(r.v[s], xr + r.h + q * VEC);
+            if constexpr (RES) ld_x(r.vr[s], rr + r.h + q * VEC);
         } else {
 #pragma unroll
             for (int k = 0; k < VEC; ++k) r.v[s].v[k] = 0.f;
+            if constexpr (RES) {
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) r.vr[s].v[k] = 0.f;
+            }
         }
     }
     r.e = 0.f;
+    r.er = 0.f;
     if constexpr (VEC == 4 && !AL) {
-        if (t < r.h + r.tl) r.e = ld_x1(xr + ((t < r.h) ? t : r.h + 4 * r.nv + (t - r.h)));
+        if (t < r.h + r.tl) {
+            const int ei = (t < r.h) ? t : r.h + 4 * r.nv + (t - r.h);
+            r.e = ld_x1(xr + ei);
+            if constexpr (RES) r.er = ld_x1(rr + ei);
+        }
     }
 }
 
-template <int OP, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL>
-__global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP))
+template <int OP, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL, bool RES>
+__global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES))
     reg_kernel(const Params p) {
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
     static_assert(!PP || VEC == 4, "parameters are held only on the vector path");
@@ -123,8 +151,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     int64_t row = (int64_t)blockIdx.x * RPC + g;
     if (row >= p.rows) return;                       // the whole group leaves together
 
-    HeldRow<VEC, SLOTS> cur;
-    load_row<VEC, SLOTS, TPR, AL>(cur, p.x + row * p.d, d, t);
+    HeldRow<VEC, SLOTS, RES> cur;
+    load_row<VEC, SLOTS, TPR, AL, RES>(cur, p.x + row * p.d, RES ? p.r + row * p.d : nullptr, d, t);
 
     // Parameters held across rows (PP): every row has the phase of row 0.
     Vec<VEC> pg[PP ? SLOTS : 1], pb[(PP && OP == OP_LN) ? SLOTS : 1];
@@ -150,10 +178,13 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     int it = 0;
     for (;; ++it) {
         const int64_t nrow = row + step;
-        HeldRow<VEC, SLOTS> nxt;
+        HeldRow<VEC, SLOTS, RES> nxt;
         if constexpr (PF) {
-            if (nrow < p.rows) load_row<VEC, SLOTS, TPR, AL>(nxt, p.x + nrow * p.d, d, t);
+            if (nrow < p.rows)
+                load_row<VEC, SLOTS, TPR, AL, RES>(nxt, p.x + nrow * p.d,
+                                                   RES ? p.r + nrow * p.d : nullptr, d, t);
         }
+        add_residual(cur);
         const int h = cur.h, nv = cur.nv, tl = cur.tl;
         const bool has_e = (VEC == 4) && !AL && (t < h + tl);
         const int ei = (t < h) ? t : h + 4 * nv + (t - h);
@@ -230,6 +261,7 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
 
         // ---- normalize and store from the held registers ----------------
         float* yr = p.y + row * p.d;
+        float* hr = RES && p.h ? p.h + row * p.d : nullptr;
         bool pa = true;   // parameter vectors 16-byte aligned at this row's phase
         if constexpr (VEC == 4 && !PP && !AL) {
             pa = ((((uintptr_t)p.p0 >> 2) + h) & 3) == 0;
@@ -257,8 +289,12 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                     for (int k = 0; k < VEC; ++k) o.v[k] = cur.v[s].v[k] * rs * a.v[k];
                 }
                 st_y(yr + j, o);
+                if constexpr (RES) {
+                    if (hr) st_y(hr + j, cur.v[s]);
+                }
             }
         }
+        if (RES && has_e && hr) st_y1(hr + ei, cur.e);
         if (has_e) {
             const float a = PP ? pge : ld_p1(p.p0 + ei);
             float o;
@@ -280,7 +316,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         if constexpr (PF)
             cur = nxt;
         else
-            load_row<VEC, SLOTS, TPR, AL>(cur, p.x + row * p.d, d, t);
+            load_row<VEC, SLOTS, TPR, AL, RES>(cur, p.x + row * p.d, RES ? p.r + row * p.d : nullptr,
+                                               d, t);
     }
 }
 
@@ -292,50 +329,51 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
 // d % 4 == 0, so every row is whole 128-bit vectors -- no head/tail scalars
 // and no per-row alignment tests (the common case: allocators align to 256
 // bytes). PP is only compiled with AL.
-template <int OP, int VEC, int SLOTS, int TPR, bool PP, bool AL = PP>
+template <int OP, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES>
 struct RegInst {
     static constexpr int RPC = (TPR == 32) ? kWarpRowsPerCta : 1;
-    static constexpr bool PF = reg_prefetch(VEC, SLOTS, TPR);
+    static constexpr bool PF = reg_prefetch(VEC, SLOTS, TPR, RES);
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
-        reg_kernel<OP, VEC, SLOTS, TPR, RPC, PF, PP, AL><<<grid, TPR * RPC, 0, s>>>(p);
+        reg_kernel<OP, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES><<<grid, TPR * RPC, 0, s>>>(p);
         return cudaGetLastError();
     }
     static const KernelEntry entry;
 };
 
-template <int OP, int VEC, int SLOTS, int TPR, bool PP, bool AL>
-const KernelEntry RegInst<OP, VEC, SLOTS, TPR, PP, AL>::entry = {
-    (const void*)&reg_kernel<OP, VEC, SLOTS, TPR, RegInst<OP, VEC, SLOTS, TPR, PP, AL>::RPC,
-                             RegInst<OP, VEC, SLOTS, TPR, PP, AL>::PF, PP, AL>,
-    TPR * RegInst<OP, VEC, SLOTS, TPR, PP, AL>::RPC, RegInst<OP, VEC, SLOTS, TPR, PP, AL>::RPC,
-    0, &RegInst<OP, VEC, SLOTS, TPR, PP, AL>::launch, nullptr};
+template <int OP, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES>
+const KernelEntry RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::entry = {
+    (const void*)&reg_kernel<OP, VEC, SLOTS, TPR, RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::RPC,
+                             RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::PF, PP, AL, RES>,
+    TPR * RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::RPC,
+    RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::RPC, 0,
+    &RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::launch, nullptr};
 
-template <int OP, int VEC, int TPR, bool PP, bool AL>
+template <int OP, int VEC, int TPR, bool PP, bool AL, bool RES>
 const KernelEntry* reg_pick_slots(int slots) {
     switch (slots) {
-        case 1: return &RegInst<OP, VEC, 1, TPR, PP, AL>::entry;
-        case 2: return &RegInst<OP, VEC, 2, TPR, PP, AL>::entry;
-        case 3: return &RegInst<OP, VEC, 3, TPR, PP, AL>::entry;
-        case 4: return &RegInst<OP, VEC, 4, TPR, PP, AL>::entry;
-        case 5: return &RegInst<OP, VEC, 5, TPR, PP, AL>::entry;
-        case 6: return &RegInst<OP, VEC, 6, TPR, PP, AL>::entry;
-        case 7: if constexpr (!PP) return &RegInst<OP, VEC, 7, TPR, PP, AL>::entry; else return nullptr;
-        case 8: if constexpr (!PP) return &RegInst<OP, VEC, 8, TPR, PP, AL>::entry; else return nullptr;
+        case 1: return &RegInst<OP, VEC, 1, TPR, PP, AL, RES>::entry;
+        case 2: return &RegInst<OP, VEC, 2, TPR, PP, AL, RES>::entry;
+        case 3: return &RegInst<OP, VEC, 3, TPR, PP, AL, RES>::entry;
+        case 4: return &RegInst<OP, VEC, 4, TPR, PP, AL, RES>::entry;
+        case 5: return &RegInst<OP, VEC, 5, TPR, PP, AL, RES>::entry;
+        case 6: return &RegInst<OP, VEC, 6, TPR, PP, AL, RES>::entry;
+        case 7: if constexpr (!PP) return &RegInst<OP, VEC, 7, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 8: if constexpr (!PP) return &RegInst<OP, VEC, 8, TPR, PP, AL, RES>::entry; else return nullptr;
         default: return nullptr;
     }
 }
 
 // (slots, tpr) -> entry for one (VEC, PP, AL) family; PP families exist for
 // rows of at most 128 threads and 6 vectors per thread.
-template <int OP, int VEC, bool PP, bool AL>
+template <int OP, int VEC, bool PP, bool AL, bool RES = false>
 const KernelEntry* reg_pick(int slots, int tpr) {
     switch (tpr) {
-        case 32: return reg_pick_slots<OP, VEC, 32, PP, AL>(slots);
-        case 64: return reg_pick_slots<OP, VEC, 64, PP, AL>(slots);
-        case 128: return reg_pick_slots<OP, VEC, 128, PP, AL>(slots);
-        case 256: if constexpr (!PP) return reg_pick_slots<OP, VEC, 256, PP, AL>(slots); else return nullptr;
-        case 512: if constexpr (!PP) return reg_pick_slots<OP, VEC, 512, PP, AL>(slots); else return nullptr;
-        case 1024: if constexpr (!PP) return reg_pick_slots<OP, VEC, 1024, PP, AL>(slots); else return nullptr;
+        case 32: return reg_pick_slots<OP, VEC, 32, PP, AL, RES>(slots);
+        case 64: return reg_pick_slots<OP, VEC, 64, PP, AL, RES>(slots);
+        case 128: return reg_pick_slots<OP, VEC, 128, PP, AL, RES>(slots);
+        case 256: if constexpr (!PP) return reg_pick_slots<OP, VEC, 256, PP, AL, RES>(slots); else return nullptr;
+        case 512: if constexpr (!PP) return reg_pick_slots<OP, VEC, 512, PP, AL, RES>(slots); else return nullptr;
+        case 1024: if constexpr (!PP) return reg_pick_slots<OP, VEC, 1024, PP, AL, RES>(slots); else return nullptr;
         default: return nullptr;
     }
 }

@@ -30,8 +30,25 @@ __device__ __forceinline__ void chan_merge(float& n, float& m, float& M, float n
     n = nn;
 }
 
-template <int OP, int VEC, int TPB>
-__global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p) {
+// Loads VEC floats of x (plus the residual when RES) at element offset j.
+template <int VEC, bool RES>
+__device__ __forceinline__ void ld_xr(Vec<VEC>& v, const float* xr, const float* rr, int64_t j) {
+    ld_x(v, xr + j);
+    if constexpr (RES) {
+        Vec<VEC> r;
+        ld_x(r, rr + j);
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) v.v[k] = v.v[k] + r.v[k];
+    }
+}
+
+template <bool RES>
+__device__ __forceinline__ float ld_xr1(const float* xr, const float* rr, int64_t j) {
+    return RES ? ld_x1(xr + j) + ld_x1(rr + j) : ld_x1(xr + j);
+}
+
+template <int OP, int VEC, int TPB, bool RES>
+__global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p) {
     constexpr int W = TPB / 32;
     __shared__ __align__(16) float xch[2][W][4];
     const int t = threadIdx.x;
@@ -42,7 +59,9 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
     int it = 0;
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
         const float* xr = p.x + row * d;
+        const float* rr = RES ? p.r + row * d : nullptr;
         float* yr = p.y + row * d;
+        float* hr = RES && p.h ? p.h + row * d : nullptr;
         int h = 0, tl = 0;
         int64_t nv;
         if constexpr (VEC == 4) {
@@ -58,11 +77,11 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
 
         float mu = 0.f, rs;
         if constexpr (OP == OP_LN) {
-            const float K = ld_x1(xr);   // shift (the same address for every thread)
+            const float K = ld_xr1<RES>(xr, rr, 0);   // shift (the same address for every thread)
             float n = 0.f, m = 0.f, M = 0.f;
             for (int64_t q = t; q < nv; q += TPB) {
                 Vec<VEC> v;
-                ld_x(v, xr + h + q * VEC);
+                ld_xr<VEC, RES>(v, xr, rr, h + q * VEC);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) v.v[k] -= K;
                 float s = 0.f;
@@ -77,7 +96,7 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
                 }
                 chan_merge(n, m, M, (float)VEC, mc, Mc);
             }
-            if (has_e) chan_merge(n, m, M, 1.f, ld_x1(xr + ei) - K, 0.f);
+            if (has_e) chan_merge(n, m, M, 1.f, ld_xr1<RES>(xr, rr, ei) - K, 0.f);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const float nb = __shfl_xor_sync(0xffffffffu, n, o);
@@ -95,12 +114,12 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
             float ss = 0.f;
             for (int64_t q = t; q < nv; q += TPB) {
                 Vec<VEC> v;
-                ld_x(v, xr + h + q * VEC);
+                ld_xr<VEC, RES>(v, xr, rr, h + q * VEC);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) ss = fmaf(v.v[k], v.v[k], ss);
             }
             if (has_e) {
-                const float e = ld_x1(xr + ei);
+                const float e = ld_xr1<RES>(xr, rr, ei);
                 ss = fmaf(e, e, ss);
             }
             ss = warp_sum(ss);
@@ -118,7 +137,8 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
         for (int64_t q = t; q < nv; q += TPB) {
             const int64_t j = h + q * VEC;
             Vec<VEC> v, a, o;
-            ld_x(v, xr + j);
+            ld_xr<VEC, RES>(v, xr, rr, j);
+            if (RES && hr) st_y(hr + j, v);
             ld_p(a, p.p0 + j, pa);
             if constexpr (OP == OP_LN) {
                 Vec<VEC> b;
@@ -132,7 +152,8 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
             st_y(yr + j, o);
         }
         if (has_e) {
-            const float e = ld_x1(xr + ei);
+            const float e = ld_xr1<RES>(xr, rr, ei);
+            if (RES && hr) st_y1(hr + ei, e);
             const float a = ld_p1(p.p0 + ei);
             float o;
             if constexpr (OP == OP_LN)
@@ -150,18 +171,18 @@ __global__ void __launch_bounds__(TPB, 2048 / TPB) stream_kernel(const Params p)
     }
 }
 
-template <int OP, int VEC>
+template <int OP, int VEC, bool RES>
 struct StreamInst {
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
-        stream_kernel<OP, VEC, kStreamThreads><<<grid, kStreamThreads, 0, s>>>(p);
+        stream_kernel<OP, VEC, kStreamThreads, RES><<<grid, kStreamThreads, 0, s>>>(p);
         return cudaGetLastError();
     }
     static const KernelEntry entry;
 };
 
-template <int OP, int VEC>
-const KernelEntry StreamInst<OP, VEC>::entry = {
-    (const void*)&stream_kernel<OP, VEC, kStreamThreads>, kStreamThreads, 1, 0,
-    &StreamInst<OP, VEC>::launch, nullptr};
+template <int OP, int VEC, bool RES>
+const KernelEntry StreamInst<OP, VEC, RES>::entry = {
+    (const void*)&stream_kernel<OP, VEC, kStreamThreads, RES>, kStreamThreads, 1, 0,
+    &StreamInst<OP, VEC, RES>::launch, nullptr};
 
 }  // namespace rn

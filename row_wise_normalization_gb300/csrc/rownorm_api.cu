@@ -11,17 +11,27 @@
 #include "rn_params.h"
 
 namespace rn {
-const KernelEntry* reg_entry_ln_v4(int slots, int tpr);
-const KernelEntry* reg_entry_ln_v4_al(int slots, int tpr);
-const KernelEntry* reg_entry_ln_v4_pp(int slots, int tpr);
-const KernelEntry* reg_entry_ln_v1(int slots, int tpr);
-const KernelEntry* reg_entry_rms_v4(int slots, int tpr);
-const KernelEntry* reg_entry_rms_v4_al(int slots, int tpr);
-const KernelEntry* reg_entry_rms_v4_pp(int slots, int tpr);
-const KernelEntry* reg_entry_rms_v1(int slots, int tpr);
+#define RN_DECL_FAMILY(OPN)                                      \
+    const KernelEntry* reg_entry_##OPN##_v4(int, int);           \
+    const KernelEntry* reg_entry_##OPN##_v4_al(int, int);        \
+    const KernelEntry* reg_entry_##OPN##_v4_pp(int, int);        \
+    const KernelEntry* reg_entry_##OPN##_v1(int, int);           \
+    const KernelEntry* reg_entry_##OPN##_v4_res(int, int);       \
+    const KernelEntry* reg_entry_##OPN##_v4_al_res(int, int);    \
+    const KernelEntry* reg_entry_##OPN##_v4_pp_res(int, int);    \
+    const KernelEntry* reg_entry_##OPN##_v1_res(int, int);
+RN_DECL_FAMILY(ln)
+RN_DECL_FAMILY(rms)
+#undef RN_DECL_FAMILY
 
-const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool al) {
+const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool al, bool res) {
     const bool ln = op == OP_LN;
+    if (res) {
+        if (vec != 4) return ln ? reg_entry_ln_v1_res(slots, tpr) : reg_entry_rms_v1_res(slots, tpr);
+        if (pp) return ln ? reg_entry_ln_v4_pp_res(slots, tpr) : reg_entry_rms_v4_pp_res(slots, tpr);
+        if (al) return ln ? reg_entry_ln_v4_al_res(slots, tpr) : reg_entry_rms_v4_al_res(slots, tpr);
+        return ln ? reg_entry_ln_v4_res(slots, tpr) : reg_entry_rms_v4_res(slots, tpr);
+    }
     if (vec != 4) return ln ? reg_entry_ln_v1(slots, tpr) : reg_entry_rms_v1(slots, tpr);
     if (pp) return ln ? reg_entry_ln_v4_pp(slots, tpr) : reg_entry_rms_v4_pp(slots, tpr);
     if (al) return ln ? reg_entry_ln_v4_al(slots, tpr) : reg_entry_rms_v4_al(slots, tpr);
@@ -38,7 +48,23 @@ __global__ void empty_kernel() {}
 thread_local int g_last_cuda_error = 0;
 
 constexpr int64_t kMaxElems = (int64_t)1 << 61;
-constexpr int kMaxDevices = 64;
+
+// One call, as the entry points received it.
+struct Request {
+    int op;                 // OP_LN or OP_RMS
+    bool res;               // residual variant
+    const float* x;
+    const float* r;         // residual (res only)
+    const float* p0;        // gamma or w
+    const float* p1;        // beta (LN) or NULL
+    float* y;
+    float* h;               // x + r written back (res only; may be NULL)
+    float* mean;            // may be NULL
+    float* rstd;            // may be NULL
+    int64_t rows;
+    int64_t d;
+    float eps;
+};
 
 // Vectors (of `vec` floats) a row of width d needs held, excluding the <= 6
 // scalars of an unaligned head and tail.
@@ -92,18 +118,27 @@ bool staged_shape(int64_t d, int* stages, int* smem) {
     return true;
 }
 
-int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, const void* p0,
-              const void* p1, rn_plan* pl) {
+uintptr_t addr(const void* p) { return (uintptr_t)p; }
+
+int plan_impl(const Request& q, int variant, rn_plan* pl) {
+    const int64_t d = q.d;
     if (d <= 0) return RN_ERR_SIZE;
     std::memset(pl, 0, sizeof(*pl));
-    // 16-byte vectors need x and y in the same 16-byte phase (a row's head
-    // peel then aligns both); otherwise every access is scalar.
-    const int vec = ((((uintptr_t)x ^ (uintptr_t)y) & 15u) == 0) ? 4 : 1;
+    // 16-byte vectors need every streamed array (x, y, and with a residual r
+    // and h) in the same 16-byte phase, so that one head peel aligns them all;
+    // otherwise every access is scalar.
+    uintptr_t phase = addr(q.x) ^ addr(q.y);
+    if (q.res) {
+        phase |= addr(q.x) ^ addr(q.r);
+        if (q.h) phase |= addr(q.x) ^ addr(q.h);
+    }
+    const int vec = (phase & 15u) == 0 ? 4 : 1;
     const int64_t units = row_units(d, vec);
     pl->vec = vec;
     // Every row whole aligned vectors, parameters included.
-    const bool al = vec == 4 && d % 4 == 0 && (((uintptr_t)x | (uintptr_t)p0 |
-                                                 (op == OP_LN ? (uintptr_t)p1 : 0)) & 15u) == 0;
+    uintptr_t bases = addr(q.x) | addr(q.p0) | (q.op == OP_LN ? addr(q.p1) : 0);
+    if (q.res) bases |= addr(q.r) | addr(q.h);
+    const bool al = vec == 4 && d % 4 == 0 && (bases & 15u) == 0;
 
     int v = variant;
     if (v == RN_VARIANT_AUTO) {
@@ -112,13 +147,15 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, cons
         // beats splitting the row over a cluster there; beyond, the cluster
         // keeps the single HBM read that the staged and streaming kernels
         // give up or pay for in shared-memory passes.
+        // With a residual, 1024-thread rows would hold x and the residual in
+        // 64 registers and spill; those rows stream instead.
         if (units <= 32 * kMaxSlots)
             v = RN_VARIANT_WARP;
-        else if (units <= 1024 * kMaxSlots)
+        else if (units <= (q.res ? 512 : 1024) * kMaxSlots)
             v = RN_VARIANT_BLOCK;
-        else if (vec == 4 && cluster_shape(units, &ct, &cc, &cs))
+        else if (!q.res && vec == 4 && cluster_shape(units, &ct, &cc, &cs))
             v = RN_VARIANT_CLUSTER;
-        else if (vec == 4 && staged_shape(d, &st, &sm))
+        else if (!q.res && vec == 4 && staged_shape(d, &st, &sm))
             v = RN_VARIANT_STAGED;
         else
             v = RN_VARIANT_STREAM;
@@ -131,7 +168,7 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, cons
             pl->threads_per_row = 32;
             pl->rows_per_cta = kWarpRowsPerCta;
             pl->threads_per_cta = 32 * kWarpRowsPerCta;
-            pl->prefetch = reg_prefetch(vec, pl->slots, 32);
+            pl->prefetch = reg_prefetch(vec, pl->slots, 32, q.res);
             pl->aligned = al;
             pl->params_held = al && reg_may_hold_params(vec, pl->slots, 32);
             break;
@@ -142,14 +179,14 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, cons
             pl->threads_per_row = tpr;
             pl->rows_per_cta = 1;
             pl->threads_per_cta = tpr;
-            pl->prefetch = reg_prefetch(vec, slots, tpr);
+            pl->prefetch = reg_prefetch(vec, slots, tpr, q.res);
             pl->aligned = al;
             pl->params_held = al && reg_may_hold_params(vec, slots, tpr);
             break;
         }
         case RN_VARIANT_STAGED: {
             int st, sm;
-            if (vec != 4 || !staged_shape(d, &st, &sm)) return RN_ERR_VARIANT;
+            if (q.res || vec != 4 || !staged_shape(d, &st, &sm)) return RN_ERR_VARIANT;
             pl->slots = st;            // row buffers in the ring
             pl->threads_per_row = kStagedThreads;
             pl->rows_per_cta = 1;
@@ -159,7 +196,7 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, cons
         }
         case RN_VARIANT_CLUSTER: {
             int ct, cc, cs;
-            if (vec != 4 || !cluster_shape(units, &ct, &cc, &cs)) return RN_ERR_VARIANT;
+            if (q.res || vec != 4 || !cluster_shape(units, &ct, &cc, &cs)) return RN_ERR_VARIANT;
             pl->slots = cs;
             pl->threads_per_row = ct * cc;
             pl->rows_per_cta = 1;
@@ -178,7 +215,6 @@ int plan_impl(int op, int variant, int64_t d, const void* x, const void* y, cons
             return RN_ERR_VARIANT;
     }
     pl->variant = v;
-    (void)op;
     return RN_OK;
 }
 
@@ -190,26 +226,25 @@ bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
 
 bool misaligned(const void* p) { return p && ((uintptr_t)p & 3u); }
 
-int validate(int op, const float* x, const float* p0, const float* p1, const float* y,
-             const float* mean, const float* rstd, int64_t rows, int64_t d, float eps) {
-    if (rows < 0 || d <= 0) return RN_ERR_SIZE;
-    if (rows > 0 && d > kMaxElems / rows) return RN_ERR_SIZE;
-    if (!std::isfinite(eps) || eps < 0.f) return RN_ERR_EPS;
-    if (rows == 0) return RN_OK;
-    if (!x || !y || !p0 || (op == OP_LN && !p1)) return RN_ERR_NULL;
-    if (misaligned(x) || misaligned(y) || misaligned(p0) || misaligned(p1) || misaligned(mean) ||
-        misaligned(rstd))
-        return RN_ERR_ALIGN;
-    const int64_t nx = rows * d * 4, np = d * 4, ns = rows * 4;
-    // outputs against inputs
-    const void* outs[3] = {y, mean, rstd};
-    const int64_t nouts[3] = {nx, ns, ns};
-    const void* ins[3] = {x, p0, p1};
-    const int64_t nins[3] = {nx, np, np};
-    for (int i = 0; i < 3; ++i) {
-        for (int j = 0; j < 3; ++j)
+int validate(const Request& q) {
+    if (q.rows < 0 || q.d <= 0) return RN_ERR_SIZE;
+    if (q.rows > 0 && q.d > kMaxElems / q.rows) return RN_ERR_SIZE;
+    if (!std::isfinite(q.eps) || q.eps < 0.f) return RN_ERR_EPS;
+    if (q.rows == 0) return RN_OK;
+    if (!q.x || !q.y || !q.p0 || (q.op == OP_LN && !q.p1) || (q.res && !q.r)) return RN_ERR_NULL;
+    const void* all[] = {q.x, q.r, q.p0, q.p1, q.y, q.h, q.mean, q.rstd};
+    for (const void* p : all)
+        if (misaligned(p)) return RN_ERR_ALIGN;
+    const int64_t nx = q.rows * q.d * 4, np = q.d * 4, ns = q.rows * 4;
+    // outputs against inputs and against each other
+    const void* outs[4] = {q.y, q.h, q.mean, q.rstd};
+    const int64_t nouts[4] = {nx, nx, ns, ns};
+    const void* ins[4] = {q.x, q.r, q.p0, q.p1};
+    const int64_t nins[4] = {nx, nx, np, np};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 4; ++j)
             if (overlaps(outs[i], nouts[i], ins[j], nins[j])) return RN_ERR_ALIAS;
-        for (int j = i + 1; j < 3; ++j)
+        for (int j = i + 1; j < 4; ++j)
             if (overlaps(outs[i], nouts[i], outs[j], nouts[j])) return RN_ERR_ALIAS;
     }
     return RN_OK;
@@ -279,67 +314,74 @@ int resident_clusters(const ClusterEntry* ce, cudaError_t* err) {
     return n;
 }
 
-int run(int op, int variant, const float* x, const float* p0, const float* p1, float* y,
-        float* mean, float* rstd, int64_t rows, int64_t d, float eps, void* stream) {
-    int st = validate(op, x, p0, p1, y, mean, rstd, rows, d, eps);
+int fail_cuda(cudaError_t err) {
+    g_last_cuda_error = (int)err;
+    return RN_ERR_CUDA;
+}
+
+int run(const Request& q, int variant, void* stream) {
+    if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
+    int st = validate(q);
     if (st != RN_OK) return st;
-    if (rows == 0) return RN_OK;
+    if (q.rows == 0) return RN_OK;
     rn_plan pl;
-    st = plan_impl(op, variant, d, x, y, p0, p1, &pl);
+    st = plan_impl(q, variant, &pl);
     if (st != RN_OK) return st;
 
     Params prm;
-    prm.x = x;
-    prm.y = y;
-    prm.p0 = p0;
-    prm.p1 = p1;
-    prm.mean = mean;
-    prm.rstd = rstd;
-    prm.rows = rows;
-    prm.d = d;
-    prm.eps = eps;
+    prm.x = q.x;
+    prm.y = q.y;
+    prm.r = q.res ? q.r : nullptr;
+    prm.h = q.res ? q.h : nullptr;
+    prm.p0 = q.p0;
+    prm.p1 = q.p1;
+    prm.mean = q.mean;
+    prm.rstd = q.rstd;
+    prm.rows = q.rows;
+    prm.d = q.d;
+    prm.eps = q.eps;
+    const cudaStream_t s = (cudaStream_t)stream;
 
     if (pl.variant == RN_VARIANT_CLUSTER) {
         const ClusterEntry* ce =
-            cluster_entry(op, pl.slots, pl.threads_per_cta, pl.cluster, pl.aligned != 0);
+            cluster_entry(q.op, pl.slots, pl.threads_per_cta, pl.cluster, pl.aligned != 0);
         if (!ce) return RN_ERR_VARIANT;
         cudaError_t err = cudaSuccess;
         const int nclusters = resident_clusters(ce, &err);
-        if (err == cudaSuccess) {
-            const int64_t want = rows < nclusters ? rows : nclusters;
-            err = ce->launch(prm, (int)want * ce->cl, (cudaStream_t)stream);
-        }
-        if (err != cudaSuccess) {
-            g_last_cuda_error = (int)err;
-            return RN_ERR_CUDA;
-        }
-        return RN_OK;
+        if (err != cudaSuccess) return fail_cuda(err);
+        const int64_t want = q.rows < nclusters ? q.rows : nclusters;
+        err = ce->launch(prm, (int)want * ce->cl, s);
+        return err == cudaSuccess ? RN_OK : fail_cuda(err);
     }
 
     const KernelEntry* e = nullptr;
     if (pl.variant == RN_VARIANT_STREAM)
-        e = stream_entry(op, pl.vec);
+        e = stream_entry(q.op, pl.vec, q.res);
     else if (pl.variant == RN_VARIANT_STAGED)
-        e = staged_entry(op, pl.slots);
+        e = staged_entry(q.op, pl.slots);
     else
-        e = reg_entry(op, pl.vec, pl.slots, pl.threads_per_row, pl.params_held != 0,
-                      pl.aligned != 0);
+        e = reg_entry(q.op, pl.vec, pl.slots, pl.threads_per_row, pl.params_held != 0,
+                      pl.aligned != 0, q.res);
     if (!e) return RN_ERR_VARIANT;
 
     cudaError_t err = cudaSuccess;
     const int resident = resident_ctas(e, pl.smem_bytes, &err);
-    if (err != cudaSuccess) {
-        g_last_cuda_error = (int)err;
-        return RN_ERR_CUDA;
-    }
-    const int64_t want = (rows + e->rows_per_cta - 1) / e->rows_per_cta;
+    if (err != cudaSuccess) return fail_cuda(err);
+    const int64_t want = (q.rows + e->rows_per_cta - 1) / e->rows_per_cta;
     const int grid = (int)(want < resident ? want : resident);
-    err = e->launch(prm, grid, (cudaStream_t)stream);
-    if (err != cudaSuccess) {
-        g_last_cuda_error = (int)err;
-        return RN_ERR_CUDA;
-    }
-    return RN_OK;
+    err = e->launch(prm, grid, s);
+    return err == cudaSuccess ? RN_OK : fail_cuda(err);
+}
+
+Request ln_request(const float* x, const float* res, const float* gamma, const float* beta,
+                   float* h, float* y, float* mean, float* rstd, int64_t rows, int64_t d,
+                   float eps, bool residual) {
+    return Request{OP_LN, residual, x, res, gamma, beta, y, h, mean, rstd, rows, d, eps};
+}
+
+Request rms_request(const float* x, const float* res, const float* w, float* h, float* y,
+                    int64_t rows, int64_t d, float eps, bool residual) {
+    return Request{OP_RMS, residual, x, res, w, nullptr, y, h, nullptr, nullptr, rows, d, eps};
 }
 
 }  // namespace
@@ -348,33 +390,80 @@ extern "C" {
 
 int ln_fwd(const float* x, const float* gamma, const float* beta, float* y, float* mean_out,
            float* rstd_out, int64_t rows, int64_t d, float eps, void* stream) {
-    return run(OP_LN, RN_VARIANT_AUTO, x, gamma, beta, y, mean_out, rstd_out, rows, d, eps, stream);
+    return run(ln_request(x, nullptr, gamma, beta, nullptr, y, mean_out, rstd_out, rows, d, eps,
+                          false),
+               RN_VARIANT_AUTO, stream);
 }
 
 int rms_fwd(const float* x, const float* w, float* y, int64_t rows, int64_t d, float eps,
             void* stream) {
-    return run(OP_RMS, RN_VARIANT_AUTO, x, w, nullptr, y, nullptr, nullptr, rows, d, eps, stream);
+    return run(rms_request(x, nullptr, w, nullptr, y, rows, d, eps, false), RN_VARIANT_AUTO,
+               stream);
 }
 
 int ln_fwd_variant(int variant, const float* x, const float* gamma, const float* beta, float* y,
                    float* mean_out, float* rstd_out, int64_t rows, int64_t d, float eps,
                    void* stream) {
-    if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
-    return run(OP_LN, variant, x, gamma, beta, y, mean_out, rstd_out, rows, d, eps, stream);
+    return run(ln_request(x, nullptr, gamma, beta, nullptr, y, mean_out, rstd_out, rows, d, eps,
+                          false),
+               variant, stream);
 }
 
 int rms_fwd_variant(int variant, const float* x, const float* w, float* y, int64_t rows,
                     int64_t d, float eps, void* stream) {
+    return run(rms_request(x, nullptr, w, nullptr, y, rows, d, eps, false), variant, stream);
+}
+
+int ln_fwd_residual(const float* x, const float* res, const float* gamma, const float* beta,
+                    float* h_out, float* y, float* mean_out, float* rstd_out, int64_t rows,
+                    int64_t d, float eps, void* stream) {
+    return run(ln_request(x, res, gamma, beta, h_out, y, mean_out, rstd_out, rows, d, eps, true),
+               RN_VARIANT_AUTO, stream);
+}
+
+int rms_fwd_residual(const float* x, const float* res, const float* w, float* h_out, float* y,
+                     int64_t rows, int64_t d, float eps, void* stream) {
+    return run(rms_request(x, res, w, h_out, y, rows, d, eps, true), RN_VARIANT_AUTO, stream);
+}
+
+int ln_fwd_residual_variant(int variant, const float* x, const float* res, const float* gamma,
+                            const float* beta, float* h_out, float* y, float* mean_out,
+                            float* rstd_out, int64_t rows, int64_t d, float eps, void* stream) {
+    return run(ln_request(x, res, gamma, beta, h_out, y, mean_out, rstd_out, rows, d, eps, true),
+               variant, stream);
+}
+
+int rms_fwd_residual_variant(int variant, const float* x, const float* res, const float* w,
+                             float* h_out, float* y, int64_t rows, int64_t d, float eps,
+                             void* stream) {
+    return run(rms_request(x, res, w, h_out, y, rows, d, eps, true), variant, stream);
+}
+
+int rn_plan_for_residual(int op, int variant, int64_t d, const void* x, const void* res,
+                         const void* h, const void* y, const void* p0, const void* p1,
+                         rn_plan* plan) {
+    if (!plan) return RN_ERR_NULL;
+    if (op != RN_OP_LN && op != RN_OP_RMS) return RN_ERR_VARIANT;
     if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
-    return run(OP_RMS, variant, x, w, nullptr, y, nullptr, nullptr, rows, d, eps, stream);
+    Request q{op == RN_OP_LN ? OP_LN : OP_RMS,
+              res != nullptr,
+              (const float*)x,
+              (const float*)res,
+              (const float*)p0,
+              (const float*)p1,
+              (float*)y,
+              (float*)h,
+              nullptr,
+              nullptr,
+              1,
+              d,
+              0.f};
+    return plan_impl(q, variant, plan);
 }
 
 int rn_plan_for(int op, int variant, int64_t d, const void* x, const void* y, const void* p0,
                 const void* p1, rn_plan* plan) {
-    if (!plan) return RN_ERR_NULL;
-    if (op != RN_OP_LN && op != RN_OP_RMS) return RN_ERR_VARIANT;
-    if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
-    return plan_impl(op, variant, d, x, y, p0, p1, plan);
+    return rn_plan_for_residual(op, variant, d, x, nullptr, nullptr, y, p0, p1, plan);
 }
 
 const char* rn_status_str(int status) {
@@ -396,11 +485,7 @@ int rn_last_cuda_error(void) { return g_last_cuda_error; }
 int rn_device_error(unsigned int* flags, int clear) {
     if (!flags) return RN_ERR_NULL;
     const cudaError_t err = device_error_word(flags, clear != 0);
-    if (err != cudaSuccess) {
-        g_last_cuda_error = (int)err;
-        return RN_ERR_CUDA;
-    }
-    return RN_OK;
+    return err == cudaSuccess ? RN_OK : fail_cuda(err);
 }
 
 int rn_launch_empty(int64_t grid, int threads, void* stream) {
@@ -408,11 +493,7 @@ int rn_launch_empty(int64_t grid, int threads, void* stream) {
         return RN_ERR_SIZE;
     empty_kernel<<<(unsigned)grid, threads, 0, (cudaStream_t)stream>>>();
     const cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) {
-        g_last_cuda_error = (int)err;
-        return RN_ERR_CUDA;
-    }
-    return RN_OK;
+    return err == cudaSuccess ? RN_OK : fail_cuda(err);
 }
 
 const char* rn_variant_name(int variant) {

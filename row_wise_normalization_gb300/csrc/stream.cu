@@ -2,8 +2,13 @@
 #include "rn_stream.cuh"
 
 namespace rn {
-const KernelEntry* stream_entry(int op, int vec) {
-    if (op == OP_LN) return vec == 4 ? &StreamInst<OP_LN, 4>::entry : &StreamInst<OP_LN, 1>::entry;
-    return vec == 4 ? &StreamInst<OP_RMS, 4>::entry : &StreamInst<OP_RMS, 1>::entry;
+template <int OP, bool RES>
+const KernelEntry* stream_pick(int vec) {
+    return vec == 4 ? &StreamInst<OP, 4, RES>::entry : &StreamInst<OP, 1, RES>::entry;
+}
+
+const KernelEntry* stream_entry(int op, int vec, bool res) {
+    if (op == OP_LN) return res ? stream_pick<OP_LN, true>(vec) : stream_pick<OP_LN, false>(vec);
+    return res ? stream_pick<OP_RMS, true>(vec) : stream_pick<OP_RMS, false>(vec);
 }
 }  // namespace rn

@@ -104,3 +104,43 @@ def variants_for(op, d, x_off=0, y_off=0):
             continue
         out.append(v)
     return out
+
+
+def run_residual(op, x, r, params, eps=1e-5, variant=capi.RN_VARIANT_AUTO, x_off=0, r_off=0,
+                 y_off=0, h_off=0, p_off=0, want_h=True):
+    """ln/rms_fwd_residual_variant through the C ABI; returns (h or None, y,
+    mean, rstd) as FP32 numpy (mean/rstd None for RMSNorm), guards checked."""
+    torch = torch_cuda()
+    rows, d = x.shape
+    xb, xp = dev_copy(x, x_off)
+    rb, rp = dev_copy(r, r_off)
+    pbs = [dev_copy(a, p_off) for a in params]
+    y = Guarded(rows * d, y_off)
+    h = Guarded(rows * d, h_off) if want_h else None
+    if op == capi.RN_OP_LN:
+        m, s = Guarded(rows), Guarded(rows)
+        st = capi.ln_fwd_residual_variant(variant, xp, rp, pbs[0][1], pbs[1][1],
+                                          h.ptr if h else 0, y.ptr, m.ptr, s.ptr, rows, d,
+                                          float(np.float32(eps)), stream_handle())
+    else:
+        m = s = None
+        st = capi.rms_fwd_residual_variant(variant, xp, rp, pbs[0][1], h.ptr if h else 0, y.ptr,
+                                           rows, d, float(np.float32(eps)), stream_handle())
+    capi.check(st)
+    torch.cuda.synchronize()
+    ho = h.fetch("h guard").reshape(rows, d) if h else None
+    yo = y.fetch("y guard").reshape(rows, d)
+    return (ho, yo, m.fetch("mean guard") if m else None, s.fetch("rstd guard") if s else None)
+
+
+def residual_variants_for(op, d, x_off=0, y_off=0):
+    """Every forced variant the residual entry points accept for width d."""
+    out = [capi.RN_VARIANT_AUTO]
+    xa, ya = (1 << 20) + 4 * x_off, (1 << 30) + 4 * y_off
+    for v in range(1, capi.RN_VARIANT_COUNT):
+        try:
+            capi.plan_residual(op, v, d, xa, xa + (1 << 28), ya + (1 << 28), ya)
+        except capi.RowNormError:
+            continue
+        out.append(v)
+    return out

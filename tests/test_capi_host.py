@@ -175,3 +175,37 @@ def test_torch_binding_rejects_cpu_tensors():
         rn.ln_fwd(x, torch.ones(4), torch.zeros(4))
     with pytest.raises(ValueError):
         rn.rms_fwd(x, torch.ones(4))
+
+
+def test_residual_validation(lib):
+    R = A + 0x400000
+    H = A + 0x500000
+    f = lambda **k: capi.ln_fwd_residual(**{**dict(x=A, res=R, gamma=A + 0x100000,
+                                                   beta=A + 0x200000, h_out=H, y=A + 0x300000,
+                                                   mean_out=0, rstd_out=0, rows=4, d=8,
+                                                   eps=1e-5, stream=0), **k})
+    assert f(res=0) == capi.RN_ERR_NULL
+    assert f(h_out=R) == capi.RN_ERR_ALIAS          # in place over the residual
+    assert f(h_out=A) == capi.RN_ERR_ALIAS          # over x
+    assert f(y=R + 16) == capi.RN_ERR_ALIAS         # y over the residual
+    assert f(h_out=A + 0x300000) == capi.RN_ERR_ALIAS   # h over y
+    assert f(res=R + 2) == capi.RN_ERR_ALIGN
+    assert f(rows=0, x=0, res=0) == capi.RN_OK
+    assert capi.rms_fwd_residual(A, 0, A + 0x1000, 0, A + 0x2000, 4, 8, 1e-5, 0) == capi.RN_ERR_NULL
+
+
+def test_residual_plans(lib):
+    X, Y = A, A + 0x1000000
+    p = capi.plan_residual(capi.RN_OP_LN, capi.RN_VARIANT_AUTO, 768, X, X + 0x100000,
+                           Y + 0x100000, Y)
+    assert p.variant == capi.RN_VARIANT_WARP and p.vec == 4 and p.aligned == 1
+    # a residual in another 16-byte phase makes every access scalar
+    p = capi.plan_residual(capi.RN_OP_LN, capi.RN_VARIANT_AUTO, 768, X, X + 0x100004,
+                           Y + 0x100000, Y)
+    assert p.vec == 1
+    # rows past 16384 floats stream
+    p = capi.plan_residual(capi.RN_OP_RMS, capi.RN_VARIANT_AUTO, 20000, X, X + 0x1000000, 0, Y)
+    assert p.variant == capi.RN_VARIANT_STREAM
+    for v in (capi.RN_VARIANT_STAGED, capi.RN_VARIANT_CLUSTER):
+        with pytest.raises(capi.RowNormError):
+            capi.plan_residual(capi.RN_OP_LN, v, 40000, X, X + 0x1000000, 0, Y)
