@@ -534,6 +534,32 @@ def run_ours(args, rank, world, local_rank):
             del xt, rt, ht, yt
         extra["residual_fused_cold_l2"] = fused
 
+        # 16-bit storage (FP32 arithmetic): algorithmic bytes at 2 bytes per element
+        typed = []
+        for op, rows_, d_, dt in (("ln", 4096, 768, torch.bfloat16), ("ln", 32768, 8192, torch.bfloat16),
+                                  ("rms", 32768, 8192, torch.bfloat16),
+                                  ("ln", 32768, 8192, torch.float16)):
+            xw = workloads.Workload(op, rows_, d_, seed=63)
+            xt = torch.from_numpy(xw.x()).to(device).to(dt)
+            pt = [torch.from_numpy(p_).to(device).to(dt) for p_ in xw.params()]
+            yt = torch.empty_like(xt)
+            if op == "ln":
+                mt = torch.empty(rows_, device=device)
+                st_ = torch.empty(rows_, device=device)
+                f = lambda: rn.ln_fwd(xt, *pt, y=yt, mean=mt, rstd=st_)
+            else:
+                f = lambda: rn.rms_fwd(xt, *pt, y=yt)
+            for _ in range(3):
+                flush()
+                f()
+            ms_ = statistics.median(time_launches(torch, f, args.sweep_steps, flush))
+            nb = 4 * rows_ * d_ + (4 if op == "ln" else 2) * d_ + (8 * rows_ if op == "ln" else 0)
+            typed.append({"workload": f"{op}_{str(dt).split('.')[-1]}_{rows_}x{d_}",
+                          "ms_median": ms_, "GBps": gbs(nb, ms_),
+                          "frac_of_measured_hbm": gbs(nb, ms_) / peak})
+            del xt, yt
+        extra["storage_16bit_cold_l2"] = typed
+
     clocks = None
     if sampler:
         sampler.stop()

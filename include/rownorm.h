@@ -68,8 +68,16 @@ typedef enum rn_status {
     RN_ERR_ALIAS = 4,   /* an output overlaps an input or another output      */
     RN_ERR_CUDA = 5,    /* the CUDA runtime reported an error on launch       */
     RN_ERR_ALIGN = 6,   /* a pointer is not 4-byte aligned                     */
-    RN_ERR_VARIANT = 7  /* a forced variant cannot run this shape / alignment  */
+    RN_ERR_VARIANT = 7, /* a forced variant cannot run this shape / alignment  */
+    RN_ERR_DTYPE = 8    /* unknown storage type, or one the entry point lacks  */
 } rn_status;
+
+/* Storage types of x, y and the parameter vectors (statistics are FP32). */
+enum {
+    RN_DTYPE_F32 = 0,
+    RN_DTYPE_BF16 = 1,   /* bfloat16: 8 exponent bits, 7 stored mantissa bits */
+    RN_DTYPE_F16 = 2     /* IEEE binary16                                      */
+};
 
 /*
  * LayerNorm forward.
@@ -115,6 +123,27 @@ int ln_fwd_residual(const float *x, const float *res, const float *gamma, const 
 
 int rms_fwd_residual(const float *x, const float *res, const float *w, float *h_out,
                      float *y, int64_t rows, int64_t d, float eps, void *stream);
+
+/*
+ * LayerNorm / RMSNorm with 16-bit (or FP32) storage and FP32 arithmetic.
+ *   dtype     RN_DTYPE_F32, RN_DTYPE_BF16 or RN_DTYPE_F16: the element type of
+ *             x, y, gamma, beta and w (all the same type)
+ *   variant   RN_VARIANT_AUTO or a forced variant (see below)
+ *   mean_out, rstd_out: FP32 [rows], may be NULL
+ * Values are widened to FP32 on load, every statistic is accumulated in FP32
+ * exactly as in ln_fwd / rms_fwd, and y is rounded to the storage type once,
+ * to nearest even. Pointers must be aligned to the element size (2 bytes for
+ * 16-bit types). With 16-bit storage, AUTO uses the warp / CTA-per-row
+ * kernels up to d = 32768 and the streaming kernel beyond; the staged and
+ * cluster variants are FP32 only (RN_ERR_VARIANT). RN_DTYPE_F32 here is the
+ * same computation as ln_fwd / rms_fwd.
+ */
+int ln_fwd_typed(int dtype, int variant, const void *x, const void *gamma, const void *beta,
+                 void *y, float *mean_out, float *rstd_out, int64_t rows, int64_t d, float eps,
+                 void *stream);
+
+int rms_fwd_typed(int dtype, int variant, const void *x, const void *w, void *y, int64_t rows,
+                  int64_t d, float eps, void *stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *rn_status_str(int status);
@@ -173,6 +202,10 @@ enum { RN_OP_LN = 0, RN_OP_RMS = 1 };
  * RN_ERR_VARIANT. Performs no CUDA call. */
 int rn_plan_for(int op, int variant, int64_t d, const void *x, const void *y,
                 const void *p0, const void *p1, rn_plan *plan);
+
+/* rn_plan_for for a storage type (host-only). */
+int rn_plan_for_typed(int dtype, int op, int variant, int64_t d, const void *x, const void *y,
+                      const void *p0, const void *p1, rn_plan *plan);
 
 /* Short static name of a variant ("warp", "block", ...). */
 const char *rn_variant_name(int variant);

@@ -23,25 +23,38 @@ def _stream_handle(t, stream):
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _empty_like_home(x, shape):
+def _empty_like_home(x, shape, dtype=None):
     import torch
 
+    dtype = torch.float32 if dtype is None else dtype
     if x.is_cuda:
-        return torch.empty(shape, dtype=torch.float32, device=x.device)
-    return torch.empty(shape, dtype=torch.float32, pin_memory=True)
+        return torch.empty(shape, dtype=dtype, device=x.device)
+    return torch.empty(shape, dtype=dtype, pin_memory=True)
 
 
-def _check_f32_cuda(name, t):
-    """FP32, contiguous, and addressable by the GPU: a CUDA tensor or a pinned
-    CPU tensor (which the kernel reads or writes over the host link)."""
+def _dtype_code(t):
+    import torch
+
+    codes = {torch.float32: capi.RN_DTYPE_F32, torch.bfloat16: capi.RN_DTYPE_BF16,
+             torch.float16: capi.RN_DTYPE_F16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype} (float32, bfloat16 or float16)")
+    return codes[t.dtype]
+
+
+def _check_f32_cuda(name, t, dtype=None):
+    """Contiguous, of the expected dtype (FP32 unless given), and addressable
+    by the GPU: a CUDA tensor or a pinned CPU tensor (which the kernel reads or
+    writes over the host link)."""
     import torch
 
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not (t.is_cuda or t.is_pinned()):
         raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
-    if t.dtype != torch.float32:
-        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    want = torch.float32 if dtype is None else dtype
+    if t.dtype != want:
+        raise TypeError(f"{name} must be {want}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
@@ -50,55 +63,58 @@ def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, s
            variant: int = capi.RN_VARIANT_AUTO):
     """LayerNorm forward over the last dimension of ``x``.
 
-    Returns ``(y, mean, rstd)``: y like x; mean and rstd of shape x.shape[:-1]
-    (FP32). Tensors are CUDA tensors or pinned CPU tensors (read or written by
-    the kernel over the host link); outputs not passed in are allocated where
-    x lives.
+    x, gamma, beta (and y) are float32, bfloat16 or float16 -- all the same
+    type; statistics are computed in FP32. Returns ``(y, mean, rstd)``: y like
+    x; mean and rstd FP32 of shape x.shape[:-1]. Tensors are CUDA tensors or
+    pinned CPU tensors (read or written by the kernel over the host link);
+    outputs not passed in are allocated where x lives.
     """
-    import torch
-
-    _check_f32_cuda("x", x)
+    code = _dtype_code(x)
+    _check_f32_cuda("x", x, x.dtype)
     d = x.shape[-1]
     rows = x.numel() // d if d else 0
     for n, t in (("gamma", gamma), ("beta", beta)):
-        _check_f32_cuda(n, t)
+        _check_f32_cuda(n, t, x.dtype)
         if t.numel() != d:
             raise ValueError(f"{n} must have {d} elements")
     if y is None:
-        y = _empty_like_home(x, x.shape)
+        y = _empty_like_home(x, x.shape, x.dtype)
     if mean is None:
         mean = _empty_like_home(x, x.shape[:-1])
     if rstd is None:
         rstd = _empty_like_home(x, x.shape[:-1])
-    for n, t, k in (("y", y, x.numel()), ("mean", mean, rows), ("rstd", rstd, rows)):
+    _check_f32_cuda("y", y, x.dtype)
+    if y.numel() != x.numel():
+        raise ValueError("y must be shaped like x")
+    for n, t in (("mean", mean), ("rstd", rstd)):
         _check_f32_cuda(n, t)
-        if t.numel() != k:
-            raise ValueError(f"{n} must have {k} elements")
-    st = capi.ln_fwd_variant(variant, x.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
-                             y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), rows, d,
-                             float(eps), _stream_handle(x, stream))
+        if t.numel() != rows:
+            raise ValueError(f"{n} must have {rows} elements")
+    st = capi.ln_fwd_typed(code, variant, x.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
+                           y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), rows, d, float(eps),
+                           _stream_handle(x, stream))
     capi.check(st)
     return y, mean, rstd
 
 
 def rms_fwd(x, w, eps: float = 1e-5, *, y=None, stream=None,
             variant: int = capi.RN_VARIANT_AUTO):
-    """RMSNorm forward over the last dimension of ``x``; returns y."""
-    import torch
-
-    _check_f32_cuda("x", x)
+    """RMSNorm forward over the last dimension of ``x`` (float32, bfloat16 or
+    float16; w of the same type); returns y."""
+    code = _dtype_code(x)
+    _check_f32_cuda("x", x, x.dtype)
     d = x.shape[-1]
     rows = x.numel() // d if d else 0
-    _check_f32_cuda("w", w)
+    _check_f32_cuda("w", w, x.dtype)
     if w.numel() != d:
         raise ValueError(f"w must have {d} elements")
     if y is None:
-        y = _empty_like_home(x, x.shape)
-    _check_f32_cuda("y", y)
+        y = _empty_like_home(x, x.shape, x.dtype)
+    _check_f32_cuda("y", y, x.dtype)
     if y.numel() != x.numel():
         raise ValueError("y must be shaped like x")
-    st = capi.rms_fwd_variant(variant, x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, d,
-                              float(eps), _stream_handle(x, stream))
+    st = capi.rms_fwd_typed(code, variant, x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, d,
+                            float(eps), _stream_handle(x, stream))
     capi.check(st)
     return y
 

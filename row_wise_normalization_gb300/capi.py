@@ -23,6 +23,11 @@ RN_ERR_ALIAS = 4
 RN_ERR_CUDA = 5
 RN_ERR_ALIGN = 6
 RN_ERR_VARIANT = 7
+RN_ERR_DTYPE = 8
+
+RN_DTYPE_F32 = 0
+RN_DTYPE_BF16 = 1
+RN_DTYPE_F16 = 2
 
 RN_VARIANT_AUTO = 0
 RN_VARIANT_WARP = 1
@@ -65,6 +70,9 @@ SIGNATURES = {
     "rms_fwd_residual_variant": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
     "rn_plan_for_residual": (_INT, [_INT, _INT, _I64, _P, _P, _P, _P, _P, _P,
                                     ctypes.POINTER(rn_plan)]),
+    "ln_fwd_typed": (_INT, [_INT, _INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+    "rms_fwd_typed": (_INT, [_INT, _INT, _P, _P, _P, _I64, _I64, _F, _P]),
+    "rn_plan_for_typed": (_INT, [_INT, _INT, _INT, _I64, _P, _P, _P, _P, ctypes.POINTER(rn_plan)]),
     "rn_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
 }
 
@@ -122,6 +130,14 @@ def plan_residual(op: int, variant: int, d: int, x: int, res: int, h: int, y: in
     return out
 
 
+def plan_typed(dtype: int, op: int, variant: int, d: int, x: int, y: int, p0: int = 0,
+               p1: int = 0) -> rn_plan:
+    """The kernel configuration a typed call would launch (host only)."""
+    out = rn_plan()
+    check(load().rn_plan_for_typed(dtype, op, variant, d, x, y, p0, p1, ctypes.byref(out)))
+    return out
+
+
 def variant_name(v: int) -> str:
     return load().rn_variant_name(v).decode()
 
@@ -173,3 +189,13 @@ def ln_fwd_residual_variant(variant, x, res, gamma, beta, h_out, y, mean_out, rs
 
 def rms_fwd_residual_variant(variant, x, res, w, h_out, y, rows, d, eps, stream=0) -> int:
     return load().rms_fwd_residual_variant(variant, x, res, w, h_out, y, rows, d, eps, stream)
+
+
+def ln_fwd_typed(dtype, variant, x, gamma, beta, y, mean_out, rstd_out, rows, d, eps,
+                 stream=0) -> int:
+    return load().ln_fwd_typed(dtype, variant, x, gamma, beta, y, mean_out, rstd_out, rows, d,
+                               eps, stream)
+
+
+def rms_fwd_typed(dtype, variant, x, w, y, rows, d, eps, stream=0) -> int:
+    return load().rms_fwd_typed(dtype, variant, x, w, y, rows, d, eps, stream)

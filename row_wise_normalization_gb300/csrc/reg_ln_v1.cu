@@ -2,5 +2,5 @@
 #include "rn_reg.cuh"
 
 namespace rn {
-const KernelEntry* reg_entry_ln_v1(int slots, int tpr) { return reg_pick<OP_LN, 1, false, false>(slots, tpr); }
+const KernelEntry* reg_entry_ln_v1(int slots, int tpr) { return reg_pick<OP_LN, float, 1, false, false>(slots, tpr); }
 }  // namespace rn

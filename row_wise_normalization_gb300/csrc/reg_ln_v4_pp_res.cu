@@ -2,5 +2,5 @@
 #include "rn_reg.cuh"
 
 namespace rn {
-const KernelEntry* reg_entry_ln_v4_pp_res(int slots, int tpr) { return reg_pick<OP_LN, 4,true,true, true>(slots, tpr); }
+const KernelEntry* reg_entry_ln_v4_pp_res(int slots, int tpr) { return reg_pick<OP_LN, float, 4,true,true, true>(slots, tpr); }
 }  // namespace rn

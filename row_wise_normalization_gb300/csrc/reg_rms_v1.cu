@@ -2,5 +2,5 @@
 #include "rn_reg.cuh"
 
 namespace rn {
-const KernelEntry* reg_entry_rms_v1(int slots, int tpr) { return reg_pick<OP_RMS, 1, false, false>(slots, tpr); }
+const KernelEntry* reg_entry_rms_v1(int slots, int tpr) { return reg_pick<OP_RMS, float, 1, false, false>(slots, tpr); }
 }  // namespace rn

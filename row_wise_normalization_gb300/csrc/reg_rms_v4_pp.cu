@@ -2,5 +2,5 @@
 #include "rn_reg.cuh"
 
 namespace rn {
-const KernelEntry* reg_entry_rms_v4_pp(int slots, int tpr) { return reg_pick<OP_RMS, 4, true, true>(slots, tpr); }
+const KernelEntry* reg_entry_rms_v4_pp(int slots, int tpr) { return reg_pick<OP_RMS, float, 4, true, true>(slots, tpr); }
 }  // namespace rn

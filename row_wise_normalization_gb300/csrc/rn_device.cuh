@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "rn_params.h"
@@ -94,6 +96,168 @@ __device__ __forceinline__ void st_y(float* p, const Vec<VEC>& r) {
     } else {
         st_y1(p, r.v[0]);
     }
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit storage (BF16, FP16): rows are read and written in the storage type
+// and held as FP32. A 128-bit access moves 8 elements. BF16 -> FP32 is exact
+// (the BF16 bits are the high half of the FP32 word); FP32 -> BF16/FP16 rounds
+// to nearest even through CUDA's conversion intrinsics.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Elem {
+    static constexpr int kVec = 16 / (int)sizeof(T);   // elements per 128-bit vector
+};
+
+__device__ __forceinline__ void unpack2(uint32_t u, float& lo, float& hi, __nv_bfloat16*) {
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+}
+__device__ __forceinline__ void unpack2(uint32_t u, float& lo, float& hi, __half*) {
+    const __half2 h2 = *reinterpret_cast<const __half2*>(&u);
+    const float2 f = __half22float2(h2);
+    lo = f.x;
+    hi = f.y;
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16*) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __half*) {
+    const __half2 b = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+__device__ __forceinline__ float half_to_f(uint16_t u, __nv_bfloat16*) {
+    return __uint_as_float((uint32_t)u << 16);
+}
+__device__ __forceinline__ float half_to_f(uint16_t u, __half*) {
+    return __half2float(__ushort_as_half(u));
+}
+__device__ __forceinline__ uint16_t f_to_half(float f, __nv_bfloat16*) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ uint16_t f_to_half(float f, __half*) {
+    return __half_as_ushort(__float2half_rn(f));
+}
+
+// Streamed 128-bit load of 8 16-bit elements as FP32.
+template <typename T>
+__device__ __forceinline__ void ld_x8(float* o, const T* p) {
+    uint32_t a, b, c, d;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "l"(p));
+    unpack2(a, o[0], o[1], (T*)nullptr);
+    unpack2(b, o[2], o[3], (T*)nullptr);
+    unpack2(c, o[4], o[5], (T*)nullptr);
+    unpack2(d, o[6], o[7], (T*)nullptr);
+}
+template <typename T>
+__device__ __forceinline__ void ld_p8(float* o, const T* p) {
+    uint32_t a, b, c, d;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "l"(p));
+    unpack2(a, o[0], o[1], (T*)nullptr);
+    unpack2(b, o[2], o[3], (T*)nullptr);
+    unpack2(c, o[4], o[5], (T*)nullptr);
+    unpack2(d, o[6], o[7], (T*)nullptr);
+}
+template <typename T>
+__device__ __forceinline__ float ld_h1(const T* p, bool stream) {
+    uint16_t u;
+    if (stream)
+        asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(u) : "l"(p));
+    else
+        asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(u) : "l"(p));
+    return half_to_f(u, (T*)nullptr);
+}
+template <typename T>
+__device__ __forceinline__ void st_y8(T* p, const float* v) {
+    const uint32_t a = pack2(v[0], v[1], (T*)nullptr), b = pack2(v[2], v[3], (T*)nullptr),
+                   c = pack2(v[4], v[5], (T*)nullptr), d = pack2(v[6], v[7], (T*)nullptr);
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+template <typename T>
+__device__ __forceinline__ void st_h1(T* p, float v) {
+    const uint16_t u = f_to_half(v, (T*)nullptr);
+    asm volatile("st.global.cs.u16 [%0], %1;" ::"l"(p), "h"(u) : "memory");
+}
+
+// Typed accesses: T = float (VEC 4 or 1) or a 16-bit type (VEC 8 or 1).
+template <typename T, int VEC>
+__device__ __forceinline__ void ldt_x(Vec<VEC>& r, const T* p) {
+    if constexpr (sizeof(T) == 4) {
+        ld_x(r, reinterpret_cast<const float*>(p));
+    } else if constexpr (VEC == 8) {
+        ld_x8(r.v, p);
+    } else {
+        r.v[0] = ld_h1(p, true);
+    }
+}
+template <typename T>
+__device__ __forceinline__ float ldt_x1(const T* p) {
+    if constexpr (sizeof(T) == 4)
+        return ld_x1(reinterpret_cast<const float*>(p));
+    else
+        return ld_h1(p, true);
+}
+template <typename T>
+__device__ __forceinline__ float ldt_p1(const T* p) {
+    if constexpr (sizeof(T) == 4)
+        return ld_p1(reinterpret_cast<const float*>(p));
+    else
+        return ld_h1(p, false);
+}
+template <typename T, int VEC>
+__device__ __forceinline__ void ldt_p(Vec<VEC>& r, const T* p, bool aligned) {
+    if constexpr (sizeof(T) == 4) {
+        ld_p(r, reinterpret_cast<const float*>(p), aligned);
+    } else if constexpr (VEC == 8) {
+        if (aligned) {
+            ld_p8(r.v, p);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) r.v[k] = ld_h1(p + k, false);
+        }
+    } else {
+        r.v[0] = ld_h1(p, false);
+    }
+}
+template <typename T, int VEC>
+__device__ __forceinline__ void stt_y(T* p, const Vec<VEC>& r) {
+    if constexpr (sizeof(T) == 4) {
+        st_y(reinterpret_cast<float*>(p), r);
+    } else if constexpr (VEC == 8) {
+        st_y8(p, r.v);
+    } else {
+        st_h1(p, r.v[0]);
+    }
+}
+template <typename T>
+__device__ __forceinline__ void stt_y1(T* p, float v) {
+    if constexpr (sizeof(T) == 4)
+        st_y1(reinterpret_cast<float*>(p), v);
+    else
+        st_h1(p, v);
+}
+
+// Elements of T to the next 16-byte boundary of p (0 .. kVec-1), clamped to d.
+template <typename T>
+__device__ __forceinline__ int head_peel_t(const T* p, int64_t d) {
+    constexpr int LS = sizeof(T) == 4 ? 2 : 1;   // log2(sizeof(T))
+    int h = (int)(((0u - (unsigned)(uintptr_t)p) & 15u) >> LS);
+    return h > d ? (int)d : h;
+}
+
+// True when p + j (elements of T) is 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ bool aligned16(const T* p, int j) {
+    constexpr int LS = sizeof(T) == 4 ? 2 : 1;   // log2(sizeof(T))
+    constexpr unsigned M = 16 / sizeof(T) - 1;
+    return ((((unsigned)(uintptr_t)p >> LS) + (unsigned)j) & M) == 0;
 }
 
 // ---------------------------------------------------------------------------

@@ -9,6 +9,10 @@ namespace rn {
 
 enum Op : int { OP_LN = 0, OP_RMS = 1 };
 
+// Storage types of x, y and the parameters (statistics are always FP32).
+enum Dtype : int { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+constexpr int dtype_size(int dt) { return dt == DT_F32 ? 4 : 2; }
+
 // Arguments of every row-normalization kernel. For RMSNorm p0 = w, p1 = NULL,
 // mean = rstd = NULL. With a residual (r != NULL) the kernels normalise
 // h = x + r and write h to `h` when it is not NULL.
@@ -42,7 +46,8 @@ struct KernelEntry {
 // tail scalars); pp: the parameter vectors are held in registers across rows
 // (requires al, tpr <= 128 and slots <= 6). Returns NULL if the
 // configuration was not compiled.
-const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool al, bool res);
+const KernelEntry* reg_entry(int op, int dtype, int vec, int slots, int tpr, bool pp, bool al,
+                             bool res);
 
 // Register-held configurations, measured on GB300 (cold L2, same-session
 // device-to-device copy as the reference):
@@ -60,15 +65,15 @@ const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool 
 //    most 6 vectors each, when every row starts at the same 16-byte phase
 //    (with 8 vectors the held parameters cost a resident CTA per SM).
 constexpr bool reg_prefetch(int vec, int slots, int tpr, bool res = false) {
-    return vec == 4 && !(slots >= 8 && tpr >= 256) && (!res || slots <= 4) &&
-           (52 + 8 * slots) * tpr <= 65536;   // both rows fit the registers of one CTA
+    return vec > 1 && !(slots * vec >= 32 && tpr >= 256) && (!res || slots <= 4) &&
+           (52 + 2 * slots * vec) * tpr <= 65536;   // both rows fit the registers of one CTA
 }
 constexpr bool reg_may_hold_params(int vec, int slots, int tpr) {
-    return vec == 4 && tpr <= 128 && slots <= 6;
+    return vec > 1 && tpr <= 128 && slots * vec <= 24;
 }
 
-// Streaming two-read kernels (any width); res: with a residual add.
-const KernelEntry* stream_entry(int op, int vec, bool res);
+// Streaming two-read kernels (any width); res: with a residual add (FP32).
+const KernelEntry* stream_entry(int op, int dtype, int vec, bool res);
 
 // Shared-memory-staged kernels with `stages` row buffers (1..kMaxStages).
 const KernelEntry* staged_entry(int op, int stages);

@@ -49,13 +49,14 @@ constexpr int reg_budget(int op, int vec, int slots, bool pf, bool pp, bool res 
 // Resident CTAs each kernel is compiled for, which sets its register cap
 // (65536 registers per SM, allocated in units of 8 per thread). For the wide
 // slices (6+ vectors per thread) the counts are the measured optima on
-// GB300 (cold L2, against a same-session device-to-device copy): with
+// GB300 (cold L2, against a same-session device-to-device copy; "wide" is 24+
+// floats held per thread, 6+ FP32 or 3+ 16-bit vectors): with
 // prefetch about 384 resident threads per SM (the two held rows keep enough
 // bytes in flight, and the spare registers let loads issue early), without
 // it about 768-1024. Narrower slices fill the SM as far as the budget allows.
 constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, bool pp,
                            bool res = false) {
-    if (vec == 4 && slots >= 6 && !res) {
+    if (vec > 1 && slots * vec >= 24 && !res) {
         if (pf) return threads == 64 ? 5 : (threads >= 384 ? 1 : 384 / threads);
         return threads >= 1024 ? 1 : (threads == 512 ? 2 : (768 / threads > 0 ? 768 / threads : 1));
     }
@@ -87,18 +88,20 @@ __device__ __forceinline__ void add_residual(HeldRow<VEC, SLOTS, RES>& r) {
 }
 
 // Loads one row of x (and of the residual rr when RES) at the phase of xr; the
-// residual must share x's 16-byte phase (the host checks).
-template <int VEC, int SLOTS, int TPR, bool AL, bool RES = false>
-__device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const float* xr,
-                                         const float* rr, int d, int t) {
+// residual must share x's 16-byte phase (the host checks). T is the storage
+// type (FP32: VEC 4 or 1; BF16/FP16: VEC 8 or 1); the row is held as FP32.
+template <typename T, int VEC, int SLOTS, int TPR, bool AL, bool RES = false>
+__device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const T* xr,
+                                         const T* rr, int d, int t) {
+    constexpr int LV = VEC == 8 ? 3 : (VEC == 4 ? 2 : 0);   // log2(VEC)
     if constexpr (AL) {
         r.h = 0;
-        r.nv = d >> 2;
+        r.nv = d >> LV;
         r.tl = 0;
-    } else if constexpr (VEC == 4) {
-        r.h = head_peel(xr, d);
-        r.nv = (d - r.h) >> 2;
-        r.tl = d - r.h - 4 * r.nv;
+    } else if constexpr (VEC > 1) {
+        r.h = head_peel_t(xr, d);
+        r.nv = (d - r.h) >> LV;
+        r.tl = d - r.h - VEC * r.nv;
     } else {
         r.h = 0;
         r.nv = d;
@@ -108,8 +111,8 @@ __device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const floa
     for (int s = 0; s < SLOTS; ++s) {
         const int q = t + s * TPR;
         if (q < r.nv) {
-            ld_x(r.v[s], xr + r.h + q * VEC);
-            if constexpr (RES) ld_x(r.vr[s], rr + r.h + q * VEC);
+            ldt_x(r.v[s], xr + r.h + q * VEC);
+            if constexpr (RES) ldt_x(r.vr[s], rr + r.h + q * VEC);
         } else {
 #pragma unroll
             for (int k = 0; k < VEC; ++k) r.v[s].v[k] = 0.f;
@@ -121,21 +124,30 @@ __device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const floa
     }
     r.e = 0.f;
     r.er = 0.f;
-    if constexpr (VEC == 4 && !AL) {
+    if constexpr (VEC > 1 && !AL) {
         if (t < r.h + r.tl) {
-            const int ei = (t < r.h) ? t : r.h + 4 * r.nv + (t - r.h);
-            r.e = ld_x1(xr + ei);
-            if constexpr (RES) r.er = ld_x1(rr + ei);
+            const int ei = (t < r.h) ? t : r.h + VEC * r.nv + (t - r.h);
+            r.e = ldt_x1(xr + ei);
+            if constexpr (RES) r.er = ldt_x1(rr + ei);
         }
     }
 }
 
-template <int OP, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL, bool RES>
+template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL,
+          bool RES>
 __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES))
     reg_kernel(const Params p) {
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
-    static_assert(!PP || VEC == 4, "parameters are held only on the vector path");
-    static_assert(!AL || VEC == 4, "the aligned layout is a vector layout");
+    static_assert(VEC == 1 || VEC == Elem<T>::kVec, "a vector is one 128-bit access");
+    static_assert(!PP || VEC > 1, "parameters are held only on the vector path");
+    static_assert(!AL || VEC > 1, "the aligned layout is a vector layout");
+    static_assert(!RES || sizeof(T) == 4, "the residual form is FP32");
+    const T* X = reinterpret_cast<const T*>(p.x);
+    const T* R = reinterpret_cast<const T*>(p.r);
+    const T* P0 = reinterpret_cast<const T*>(p.p0);
+    const T* P1 = reinterpret_cast<const T*>(p.p1);
+    T* Y = reinterpret_cast<T*>(p.y);
+    T* H = reinterpret_cast<T*>(p.h);
     constexpr int WPR = TPR / 32;                    // warps per row
     constexpr int NST = (OP == OP_LN) ? 4 : 1;       // floats a warp publishes
     constexpr int NBUF = (WPR > 1) ? 2 : 1;
@@ -152,26 +164,26 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     if (row >= p.rows) return;                       // the whole group leaves together
 
     HeldRow<VEC, SLOTS, RES> cur;
-    load_row<VEC, SLOTS, TPR, AL, RES>(cur, p.x + row * p.d, RES ? p.r + row * p.d : nullptr, d, t);
+    load_row<T, VEC, SLOTS, TPR, AL, RES>(cur, X + row * p.d, RES ? R + row * p.d : nullptr, d, t);
 
     // Parameters held across rows (PP): every row has the phase of row 0.
     Vec<VEC> pg[PP ? SLOTS : 1], pb[(PP && OP == OP_LN) ? SLOTS : 1];
     float pge = 0.f, pbe = 0.f;
     if constexpr (PP) {
-        const bool pa0 = AL || ((((uintptr_t)p.p0 >> 2) + cur.h) & 3) == 0;
-        const bool pa1 = AL || OP != OP_LN || ((((uintptr_t)p.p1 >> 2) + cur.h) & 3) == 0;
+        const bool pa0 = AL || aligned16(P0, cur.h);
+        const bool pa1 = AL || OP != OP_LN || aligned16(P1, cur.h);
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             const int q = t + s * TPR;
             if (q < cur.nv) {
-                ld_p(pg[s], p.p0 + cur.h + q * VEC, pa0);
-                if constexpr (OP == OP_LN) ld_p(pb[s], p.p1 + cur.h + q * VEC, pa1);
+                ldt_p(pg[s], P0 + cur.h + q * VEC, pa0);
+                if constexpr (OP == OP_LN) ldt_p(pb[s], P1 + cur.h + q * VEC, pa1);
             }
         }
         if (!AL && t < cur.h + cur.tl) {
-            const int ei = (t < cur.h) ? t : cur.h + 4 * cur.nv + (t - cur.h);
-            pge = ld_p1(p.p0 + ei);
-            if constexpr (OP == OP_LN) pbe = ld_p1(p.p1 + ei);
+            const int ei = (t < cur.h) ? t : cur.h + VEC * cur.nv + (t - cur.h);
+            pge = ldt_p1(P0 + ei);
+            if constexpr (OP == OP_LN) pbe = ldt_p1(P1 + ei);
         }
     }
 
@@ -181,13 +193,13 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         HeldRow<VEC, SLOTS, RES> nxt;
         if constexpr (PF) {
             if (nrow < p.rows)
-                load_row<VEC, SLOTS, TPR, AL, RES>(nxt, p.x + nrow * p.d,
-                                                   RES ? p.r + nrow * p.d : nullptr, d, t);
+                load_row<T, VEC, SLOTS, TPR, AL, RES>(nxt, X + nrow * p.d,
+                                                      RES ? R + nrow * p.d : nullptr, d, t);
         }
         add_residual(cur);
         const int h = cur.h, nv = cur.nv, tl = cur.tl;
-        const bool has_e = (VEC == 4) && !AL && (t < h + tl);
-        const int ei = (t < h) ? t : h + 4 * nv + (t - h);
+        const bool has_e = (VEC > 1) && !AL && (t < h + tl);
+        const int ei = (t < h) ? t : h + VEC * nv + (t - h);
 
         // ---- statistics ------------------------------------------------
         float mu = 0.f, rs;
@@ -260,12 +272,12 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         }
 
         // ---- normalize and store from the held registers ----------------
-        float* yr = p.y + row * p.d;
-        float* hr = RES && p.h ? p.h + row * p.d : nullptr;
+        T* yr = Y + row * p.d;
+        T* hr = RES && p.h ? H + row * p.d : nullptr;
         bool pa = true;   // parameter vectors 16-byte aligned at this row's phase
-        if constexpr (VEC == 4 && !PP && !AL) {
-            pa = ((((uintptr_t)p.p0 >> 2) + h) & 3) == 0;
-            if constexpr (OP == OP_LN) pa = pa && ((((uintptr_t)p.p1 >> 2) + h) & 3) == 0;
+        if constexpr (VEC > 1 && !PP && !AL) {
+            pa = aligned16(P0, h);
+            if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
         }
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
@@ -277,8 +289,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                     a = pg[s];
                     if constexpr (OP == OP_LN) b = pb[s];
                 } else {
-                    ld_p(a, p.p0 + j, pa);
-                    if constexpr (OP == OP_LN) ld_p(b, p.p1 + j, pa);
+                    ldt_p(a, P0 + j, pa);
+                    if constexpr (OP == OP_LN) ldt_p(b, P1 + j, pa);
                 }
                 if constexpr (OP == OP_LN) {
 #pragma unroll
@@ -288,21 +300,21 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
 #pragma unroll
                     for (int k = 0; k < VEC; ++k) o.v[k] = cur.v[s].v[k] * rs * a.v[k];
                 }
-                st_y(yr + j, o);
+                stt_y(yr + j, o);
                 if constexpr (RES) {
-                    if (hr) st_y(hr + j, cur.v[s]);
+                    if (hr) stt_y(hr + j, cur.v[s]);
                 }
             }
         }
-        if (RES && has_e && hr) st_y1(hr + ei, cur.e);
+        if (RES && has_e && hr) stt_y1(hr + ei, cur.e);
         if (has_e) {
-            const float a = PP ? pge : ld_p1(p.p0 + ei);
+            const float a = PP ? pge : ldt_p1(P0 + ei);
             float o;
             if constexpr (OP == OP_LN)
-                o = fmaf((cur.e - mu) * rs, a, PP ? pbe : ld_p1(p.p1 + ei));
+                o = fmaf((cur.e - mu) * rs, a, PP ? pbe : ldt_p1(P1 + ei));
             else
                 o = cur.e * rs * a;
-            st_y1(yr + ei, o);
+            stt_y1(yr + ei, o);
         }
         if constexpr (OP == OP_LN) {
             if (t == 0) {
@@ -316,8 +328,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         if constexpr (PF)
             cur = nxt;
         else
-            load_row<VEC, SLOTS, TPR, AL, RES>(cur, p.x + row * p.d, RES ? p.r + row * p.d : nullptr,
-                                               d, t);
+            load_row<T, VEC, SLOTS, TPR, AL, RES>(cur, X + row * p.d, RES ? R + row * p.d : nullptr,
+                                                  d, t);
     }
 }
 
@@ -329,51 +341,61 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
 // d % 4 == 0, so every row is whole 128-bit vectors -- no head/tail scalars
 // and no per-row alignment tests (the common case: allocators align to 256
 // bytes). PP is only compiled with AL.
-template <int OP, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES>
+template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES>
 struct RegInst {
     static constexpr int RPC = (TPR == 32) ? kWarpRowsPerCta : 1;
     static constexpr bool PF = reg_prefetch(VEC, SLOTS, TPR, RES);
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
-        reg_kernel<OP, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES><<<grid, TPR * RPC, 0, s>>>(p);
+        reg_kernel<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES><<<grid, TPR * RPC, 0, s>>>(p);
         return cudaGetLastError();
     }
     static const KernelEntry entry;
 };
 
-template <int OP, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES>
-const KernelEntry RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::entry = {
-    (const void*)&reg_kernel<OP, VEC, SLOTS, TPR, RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::RPC,
-                             RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::PF, PP, AL, RES>,
-    TPR * RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::RPC,
-    RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::RPC, 0,
-    &RegInst<OP, VEC, SLOTS, TPR, PP, AL, RES>::launch, nullptr};
+template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES>
+const KernelEntry RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::entry = {
+    (const void*)&reg_kernel<OP, T, VEC, SLOTS, TPR,
+                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::RPC,
+                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::PF, PP, AL, RES>,
+    TPR * RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::RPC,
+    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::RPC, 0,
+    &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::launch, nullptr};
 
-template <int OP, int VEC, int TPR, bool PP, bool AL, bool RES>
+// Slots per thread a family is compiled for: up to 8 FP32 vectors (32 floats),
+// 4 16-bit vectors (32 floats) or 8 scalars; held parameters allow 24 floats.
+template <typename T, int VEC, bool PP>
+constexpr int reg_max_slots() {
+    return PP ? 24 / VEC : (VEC == 1 ? 8 : 32 / VEC);
+}
+
+template <int OP, typename T, int VEC, int TPR, bool PP, bool AL, bool RES>
 const KernelEntry* reg_pick_slots(int slots) {
+    constexpr int M = reg_max_slots<T, VEC, PP>();
+    if (slots < 1 || slots > M) return nullptr;
     switch (slots) {
-        case 1: return &RegInst<OP, VEC, 1, TPR, PP, AL, RES>::entry;
-        case 2: return &RegInst<OP, VEC, 2, TPR, PP, AL, RES>::entry;
-        case 3: return &RegInst<OP, VEC, 3, TPR, PP, AL, RES>::entry;
-        case 4: return &RegInst<OP, VEC, 4, TPR, PP, AL, RES>::entry;
-        case 5: return &RegInst<OP, VEC, 5, TPR, PP, AL, RES>::entry;
-        case 6: return &RegInst<OP, VEC, 6, TPR, PP, AL, RES>::entry;
-        case 7: if constexpr (!PP) return &RegInst<OP, VEC, 7, TPR, PP, AL, RES>::entry; else return nullptr;
-        case 8: if constexpr (!PP) return &RegInst<OP, VEC, 8, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 1: return &RegInst<OP, T, VEC, 1, TPR, PP, AL, RES>::entry;
+        case 2: if constexpr (M >= 2) return &RegInst<OP, T, VEC, 2, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 3: if constexpr (M >= 3) return &RegInst<OP, T, VEC, 3, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 4: if constexpr (M >= 4) return &RegInst<OP, T, VEC, 4, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 5: if constexpr (M >= 5) return &RegInst<OP, T, VEC, 5, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 6: if constexpr (M >= 6) return &RegInst<OP, T, VEC, 6, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 7: if constexpr (M >= 7) return &RegInst<OP, T, VEC, 7, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 8: if constexpr (M >= 8) return &RegInst<OP, T, VEC, 8, TPR, PP, AL, RES>::entry; else return nullptr;
         default: return nullptr;
     }
 }
 
 // (slots, tpr) -> entry for one (VEC, PP, AL) family; PP families exist for
 // rows of at most 128 threads and 6 vectors per thread.
-template <int OP, int VEC, bool PP, bool AL, bool RES = false>
+template <int OP, typename T, int VEC, bool PP, bool AL, bool RES = false>
 const KernelEntry* reg_pick(int slots, int tpr) {
     switch (tpr) {
-        case 32: return reg_pick_slots<OP, VEC, 32, PP, AL, RES>(slots);
-        case 64: return reg_pick_slots<OP, VEC, 64, PP, AL, RES>(slots);
-        case 128: return reg_pick_slots<OP, VEC, 128, PP, AL, RES>(slots);
-        case 256: if constexpr (!PP) return reg_pick_slots<OP, VEC, 256, PP, AL, RES>(slots); else return nullptr;
-        case 512: if constexpr (!PP) return reg_pick_slots<OP, VEC, 512, PP, AL, RES>(slots); else return nullptr;
-        case 1024: if constexpr (!PP) return reg_pick_slots<OP, VEC, 1024, PP, AL, RES>(slots); else return nullptr;
+        case 32: return reg_pick_slots<OP, T, VEC, 32, PP, AL, RES>(slots);
+        case 64: return reg_pick_slots<OP, T, VEC, 64, PP, AL, RES>(slots);
+        case 128: return reg_pick_slots<OP, T, VEC, 128, PP, AL, RES>(slots);
+        case 256: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 256, PP, AL, RES>(slots); else return nullptr;
+        case 512: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 512, PP, AL, RES>(slots); else return nullptr;
+        case 1024: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 1024, PP, AL, RES>(slots); else return nullptr;
         default: return nullptr;
     }
 }

@@ -30,25 +30,34 @@ __device__ __forceinline__ void chan_merge(float& n, float& m, float& M, float n
     n = nn;
 }
 
-// Loads VEC floats of x (plus the residual when RES) at element offset j.
-template <int VEC, bool RES>
-__device__ __forceinline__ void ld_xr(Vec<VEC>& v, const float* xr, const float* rr, int64_t j) {
-    ld_x(v, xr + j);
+// Loads VEC elements of x (plus the residual when RES) at element offset j,
+// as FP32.
+template <typename T, int VEC, bool RES>
+__device__ __forceinline__ void ld_xr(Vec<VEC>& v, const T* xr, const T* rr, int64_t j) {
+    ldt_x(v, xr + j);
     if constexpr (RES) {
         Vec<VEC> r;
-        ld_x(r, rr + j);
+        ldt_x(r, rr + j);
 #pragma unroll
         for (int k = 0; k < VEC; ++k) v.v[k] = v.v[k] + r.v[k];
     }
 }
 
-template <bool RES>
-__device__ __forceinline__ float ld_xr1(const float* xr, const float* rr, int64_t j) {
-    return RES ? ld_x1(xr + j) + ld_x1(rr + j) : ld_x1(xr + j);
+template <typename T, bool RES>
+__device__ __forceinline__ float ld_xr1(const T* xr, const T* rr, int64_t j) {
+    return RES ? ldt_x1(xr + j) + ldt_x1(rr + j) : ldt_x1(xr + j);
 }
 
-template <int OP, int VEC, int TPB, bool RES>
+template <int OP, typename T, int VEC, int TPB, bool RES>
 __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p) {
+    static_assert(VEC == 1 || VEC == Elem<T>::kVec, "a vector is one 128-bit access");
+    static_assert(!RES || sizeof(T) == 4, "the residual form is FP32");
+    const T* X = reinterpret_cast<const T*>(p.x);
+    const T* R = reinterpret_cast<const T*>(p.r);
+    const T* P0 = reinterpret_cast<const T*>(p.p0);
+    const T* P1 = reinterpret_cast<const T*>(p.p1);
+    T* Y = reinterpret_cast<T*>(p.y);
+    T* H = reinterpret_cast<T*>(p.h);
     constexpr int W = TPB / 32;
     __shared__ __align__(16) float xch[2][W][4];
     const int t = threadIdx.x;
@@ -58,30 +67,30 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
 
     int it = 0;
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
-        const float* xr = p.x + row * d;
-        const float* rr = RES ? p.r + row * d : nullptr;
-        float* yr = p.y + row * d;
-        float* hr = RES && p.h ? p.h + row * d : nullptr;
+        const T* xr = X + row * d;
+        const T* rr = RES ? R + row * d : nullptr;
+        T* yr = Y + row * d;
+        T* hr = RES && p.h ? H + row * d : nullptr;
         int h = 0, tl = 0;
         int64_t nv;
-        if constexpr (VEC == 4) {
-            h = head_peel(xr, d);
-            nv = (d - h) >> 2;
-            tl = (int)(d - h - 4 * nv);
+        if constexpr (VEC > 1) {
+            h = head_peel_t(xr, d);
+            nv = (d - h) / VEC;
+            tl = (int)(d - h - VEC * nv);
         } else {
             nv = d;
         }
-        const bool has_e = (VEC == 4) && (t < h + tl);
-        const int64_t ei = (t < h) ? (int64_t)t : (int64_t)h + 4 * nv + (t - h);
+        const bool has_e = (VEC > 1) && (t < h + tl);
+        const int64_t ei = (t < h) ? (int64_t)t : (int64_t)h + VEC * nv + (t - h);
         float(*slot)[4] = xch[it & 1];
 
         float mu = 0.f, rs;
         if constexpr (OP == OP_LN) {
-            const float K = ld_xr1<RES>(xr, rr, 0);   // shift (the same address for every thread)
+            const float K = ld_xr1<T, RES>(xr, rr, 0);   // shift (the same address for every thread)
             float n = 0.f, m = 0.f, M = 0.f;
             for (int64_t q = t; q < nv; q += TPB) {
                 Vec<VEC> v;
-                ld_xr<VEC, RES>(v, xr, rr, h + q * VEC);
+                ld_xr<T, VEC, RES>(v, xr, rr, h + q * VEC);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) v.v[k] -= K;
                 float s = 0.f;
@@ -96,7 +105,7 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
                 }
                 chan_merge(n, m, M, (float)VEC, mc, Mc);
             }
-            if (has_e) chan_merge(n, m, M, 1.f, ld_xr1<RES>(xr, rr, ei) - K, 0.f);
+            if (has_e) chan_merge(n, m, M, 1.f, ld_xr1<T, RES>(xr, rr, ei) - K, 0.f);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const float nb = __shfl_xor_sync(0xffffffffu, n, o);
@@ -114,12 +123,12 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
             float ss = 0.f;
             for (int64_t q = t; q < nv; q += TPB) {
                 Vec<VEC> v;
-                ld_xr<VEC, RES>(v, xr, rr, h + q * VEC);
+                ld_xr<T, VEC, RES>(v, xr, rr, h + q * VEC);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) ss = fmaf(v.v[k], v.v[k], ss);
             }
             if (has_e) {
-                const float e = ld_xr1<RES>(xr, rr, ei);
+                const float e = ld_xr1<T, RES>(xr, rr, ei);
                 ss = fmaf(e, e, ss);
             }
             ss = warp_sum(ss);
@@ -130,37 +139,37 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
         }
 
         bool pa = true;
-        if constexpr (VEC == 4) {
-            pa = ((((uintptr_t)p.p0 >> 2) + h) & 3) == 0;
-            if constexpr (OP == OP_LN) pa = pa && ((((uintptr_t)p.p1 >> 2) + h) & 3) == 0;
+        if constexpr (VEC > 1) {
+            pa = aligned16(P0, h);
+            if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
         }
         for (int64_t q = t; q < nv; q += TPB) {
             const int64_t j = h + q * VEC;
             Vec<VEC> v, a, o;
-            ld_xr<VEC, RES>(v, xr, rr, j);
-            if (RES && hr) st_y(hr + j, v);
-            ld_p(a, p.p0 + j, pa);
+            ld_xr<T, VEC, RES>(v, xr, rr, j);
+            if (RES && hr) stt_y(hr + j, v);
+            ldt_p(a, P0 + j, pa);
             if constexpr (OP == OP_LN) {
                 Vec<VEC> b;
-                ld_p(b, p.p1 + j, pa);
+                ldt_p(b, P1 + j, pa);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) o.v[k] = fmaf((v.v[k] - mu) * rs, a.v[k], b.v[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) o.v[k] = v.v[k] * rs * a.v[k];
             }
-            st_y(yr + j, o);
+            stt_y(yr + j, o);
         }
         if (has_e) {
-            const float e = ld_xr1<RES>(xr, rr, ei);
-            if (RES && hr) st_y1(hr + ei, e);
-            const float a = ld_p1(p.p0 + ei);
+            const float e = ld_xr1<T, RES>(xr, rr, ei);
+            if (RES && hr) stt_y1(hr + ei, e);
+            const float a = ldt_p1(P0 + ei);
             float o;
             if constexpr (OP == OP_LN)
-                o = fmaf((e - mu) * rs, a, ld_p1(p.p1 + ei));
+                o = fmaf((e - mu) * rs, a, ldt_p1(P1 + ei));
             else
                 o = e * rs * a;
-            st_y1(yr + ei, o);
+            stt_y1(yr + ei, o);
         }
         if constexpr (OP == OP_LN) {
             if (t == 0) {
@@ -171,18 +180,18 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
     }
 }
 
-template <int OP, int VEC, bool RES>
+template <int OP, typename T, int VEC, bool RES>
 struct StreamInst {
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
-        stream_kernel<OP, VEC, kStreamThreads, RES><<<grid, kStreamThreads, 0, s>>>(p);
+        stream_kernel<OP, T, VEC, kStreamThreads, RES><<<grid, kStreamThreads, 0, s>>>(p);
         return cudaGetLastError();
     }
     static const KernelEntry entry;
 };
 
-template <int OP, int VEC, bool RES>
-const KernelEntry StreamInst<OP, VEC, RES>::entry = {
-    (const void*)&stream_kernel<OP, VEC, kStreamThreads, RES>, kStreamThreads, 1, 0,
-    &StreamInst<OP, VEC, RES>::launch, nullptr};
+template <int OP, typename T, int VEC, bool RES>
+const KernelEntry StreamInst<OP, T, VEC, RES>::entry = {
+    (const void*)&stream_kernel<OP, T, VEC, kStreamThreads, RES>, kStreamThreads, 1, 0,
+    &StreamInst<OP, T, VEC, RES>::launch, nullptr};
 
 }  // namespace rn

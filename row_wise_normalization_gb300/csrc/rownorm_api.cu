@@ -23,9 +23,33 @@ namespace rn {
 RN_DECL_FAMILY(ln)
 RN_DECL_FAMILY(rms)
 #undef RN_DECL_FAMILY
+#define RN_DECL_FAMILY16(OPN, TN)                                 \
+    const KernelEntry* reg_entry_##OPN##_##TN##_v8(int, int);     \
+    const KernelEntry* reg_entry_##OPN##_##TN##_v8_al(int, int);  \
+    const KernelEntry* reg_entry_##OPN##_##TN##_v8_pp(int, int);  \
+    const KernelEntry* reg_entry_##OPN##_##TN##_v1(int, int);
+RN_DECL_FAMILY16(ln, bf16)
+RN_DECL_FAMILY16(rms, bf16)
+RN_DECL_FAMILY16(ln, f16)
+RN_DECL_FAMILY16(rms, f16)
+#undef RN_DECL_FAMILY16
 
-const KernelEntry* reg_entry(int op, int vec, int slots, int tpr, bool pp, bool al, bool res) {
+const KernelEntry* reg_entry(int op, int dtype, int vec, int slots, int tpr, bool pp, bool al,
+                             bool res) {
     const bool ln = op == OP_LN;
+    if (dtype != DT_F32) {
+        if (res) return nullptr;
+#define RN_PICK16(TN)                                                                         \
+    if (vec != 8) return ln ? reg_entry_ln_##TN##_v1(slots, tpr) : reg_entry_rms_##TN##_v1(slots, tpr); \
+    if (pp) return ln ? reg_entry_ln_##TN##_v8_pp(slots, tpr) : reg_entry_rms_##TN##_v8_pp(slots, tpr); \
+    if (al) return ln ? reg_entry_ln_##TN##_v8_al(slots, tpr) : reg_entry_rms_##TN##_v8_al(slots, tpr); \
+    return ln ? reg_entry_ln_##TN##_v8(slots, tpr) : reg_entry_rms_##TN##_v8(slots, tpr);
+        if (dtype == DT_BF16) {
+            RN_PICK16(bf16)
+        }
+        RN_PICK16(f16)
+#undef RN_PICK16
+    }
     if (res) {
         if (vec != 4) return ln ? reg_entry_ln_v1_res(slots, tpr) : reg_entry_rms_v1_res(slots, tpr);
         if (pp) return ln ? reg_entry_ln_v4_pp_res(slots, tpr) : reg_entry_rms_v4_pp_res(slots, tpr);
@@ -52,6 +76,7 @@ constexpr int64_t kMaxElems = (int64_t)1 << 61;
 // One call, as the entry points received it.
 struct Request {
     int op;                 // OP_LN or OP_RMS
+    int dtype;              // DT_F32, DT_BF16 or DT_F16 (x, y, parameters, residual)
     bool res;               // residual variant
     const float* x;
     const float* r;         // residual (res only)
@@ -66,17 +91,21 @@ struct Request {
     float eps;
 };
 
-// Vectors (of `vec` floats) a row of width d needs held, excluding the <= 6
-// scalars of an unaligned head and tail.
-int64_t row_units(int64_t d, int vec) { return vec == 4 ? d / 4 : d; }
+// Vectors (of `vec` elements) a row of width d needs held, excluding the
+// scalars of an unaligned head and tail (fewer than 2 * vec).
+int64_t row_units(int64_t d, int vec) { return d / vec; }
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// Vectors a register-held thread may hold: 8 FP32 or 4 16-bit vectors (32
+// floats either way), or 8 scalars.
+int max_slots(int vec) { return vec == 1 ? kMaxSlots : 32 / vec; }
+
 // Register-held CTA-per-row configuration: the fewest threads (>= 64, a power
-// of two) that hold the row in at most kMaxSlots vectors each.
-bool block_shape(int64_t units, int* tpr, int* slots) {
+// of two) that hold the row in at most `maxs` vectors each.
+bool block_shape(int64_t units, int maxs, int* tpr, int* slots) {
     for (int t = 64; t <= 1024; t *= 2) {
-        if (units <= (int64_t)t * kMaxSlots) {
+        if (units <= (int64_t)t * maxs) {
             *tpr = t;
             *slots = units == 0 ? 1 : ceil_div(units, t);
             return true;
@@ -132,13 +161,15 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
         phase |= addr(q.x) ^ addr(q.r);
         if (q.h) phase |= addr(q.x) ^ addr(q.h);
     }
-    const int vec = (phase & 15u) == 0 ? 4 : 1;
+    const bool f32 = q.dtype == DT_F32;
+    const int vec = (phase & 15u) == 0 ? 16 / dtype_size(q.dtype) : 1;
     const int64_t units = row_units(d, vec);
+    const int maxs = max_slots(vec);
     pl->vec = vec;
     // Every row whole aligned vectors, parameters included.
     uintptr_t bases = addr(q.x) | addr(q.p0) | (q.op == OP_LN ? addr(q.p1) : 0);
     if (q.res) bases |= addr(q.r) | addr(q.h);
-    const bool al = vec == 4 && d % 4 == 0 && (bases & 15u) == 0;
+    const bool al = vec > 1 && d % vec == 0 && (bases & 15u) == 0;
 
     int v = variant;
     if (v == RN_VARIANT_AUTO) {
@@ -149,13 +180,13 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
         // give up or pay for in shared-memory passes.
         // With a residual, 1024-thread rows would hold x and the residual in
         // 64 registers and spill; those rows stream instead.
-        if (units <= 32 * kMaxSlots)
+        if (units <= 32 * maxs)
             v = RN_VARIANT_WARP;
-        else if (units <= (q.res ? 512 : 1024) * kMaxSlots)
+        else if (units <= (q.res ? 512 : 1024) * maxs)
             v = RN_VARIANT_BLOCK;
-        else if (!q.res && vec == 4 && cluster_shape(units, &ct, &cc, &cs))
+        else if (f32 && !q.res && vec == 4 && cluster_shape(units, &ct, &cc, &cs))
             v = RN_VARIANT_CLUSTER;
-        else if (!q.res && vec == 4 && staged_shape(d, &st, &sm))
+        else if (f32 && !q.res && vec == 4 && staged_shape(d, &st, &sm))
             v = RN_VARIANT_STAGED;
         else
             v = RN_VARIANT_STREAM;
@@ -163,7 +194,7 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
     pl->cluster = 1;
     switch (v) {
         case RN_VARIANT_WARP:
-            if (units > 32 * kMaxSlots) return RN_ERR_VARIANT;
+            if (units > 32 * maxs) return RN_ERR_VARIANT;
             pl->slots = units == 0 ? 1 : ceil_div(units, 32);
             pl->threads_per_row = 32;
             pl->rows_per_cta = kWarpRowsPerCta;
@@ -174,7 +205,7 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
             break;
         case RN_VARIANT_BLOCK: {
             int tpr, slots;
-            if (!block_shape(units, &tpr, &slots)) return RN_ERR_VARIANT;
+            if (!block_shape(units, maxs, &tpr, &slots)) return RN_ERR_VARIANT;
             pl->slots = slots;
             pl->threads_per_row = tpr;
             pl->rows_per_cta = 1;
@@ -186,7 +217,7 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
         }
         case RN_VARIANT_STAGED: {
             int st, sm;
-            if (q.res || vec != 4 || !staged_shape(d, &st, &sm)) return RN_ERR_VARIANT;
+            if (!f32 || q.res || vec != 4 || !staged_shape(d, &st, &sm)) return RN_ERR_VARIANT;
             pl->slots = st;            // row buffers in the ring
             pl->threads_per_row = kStagedThreads;
             pl->rows_per_cta = 1;
@@ -196,7 +227,8 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
         }
         case RN_VARIANT_CLUSTER: {
             int ct, cc, cs;
-            if (q.res || vec != 4 || !cluster_shape(units, &ct, &cc, &cs)) return RN_ERR_VARIANT;
+            if (!f32 || q.res || vec != 4 || !cluster_shape(units, &ct, &cc, &cs))
+                return RN_ERR_VARIANT;
             pl->slots = cs;
             pl->threads_per_row = ct * cc;
             pl->rows_per_cta = 1;
@@ -224,18 +256,22 @@ bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
     return pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
 }
 
-bool misaligned(const void* p) { return p && ((uintptr_t)p & 3u); }
+bool misaligned(const void* p, int es) { return p && ((uintptr_t)p & (uintptr_t)(es - 1)); }
 
 int validate(const Request& q) {
+    if (q.dtype != DT_F32 && q.dtype != DT_BF16 && q.dtype != DT_F16) return RN_ERR_DTYPE;
+    if (q.res && q.dtype != DT_F32) return RN_ERR_DTYPE;
     if (q.rows < 0 || q.d <= 0) return RN_ERR_SIZE;
     if (q.rows > 0 && q.d > kMaxElems / q.rows) return RN_ERR_SIZE;
     if (!std::isfinite(q.eps) || q.eps < 0.f) return RN_ERR_EPS;
     if (q.rows == 0) return RN_OK;
     if (!q.x || !q.y || !q.p0 || (q.op == OP_LN && !q.p1) || (q.res && !q.r)) return RN_ERR_NULL;
-    const void* all[] = {q.x, q.r, q.p0, q.p1, q.y, q.h, q.mean, q.rstd};
-    for (const void* p : all)
-        if (misaligned(p)) return RN_ERR_ALIGN;
-    const int64_t nx = q.rows * q.d * 4, np = q.d * 4, ns = q.rows * 4;
+    const int es = dtype_size(q.dtype);
+    const void* data[] = {q.x, q.r, q.p0, q.p1, q.y, q.h};
+    for (const void* p : data)
+        if (misaligned(p, es)) return RN_ERR_ALIGN;
+    if (misaligned(q.mean, 4) || misaligned(q.rstd, 4)) return RN_ERR_ALIGN;
+    const int64_t nx = q.rows * q.d * es, np = q.d * es, ns = q.rows * 4;
     // outputs against inputs and against each other
     const void* outs[4] = {q.y, q.h, q.mean, q.rstd};
     const int64_t nouts[4] = {nx, nx, ns, ns};
@@ -356,11 +392,11 @@ int run(const Request& q, int variant, void* stream) {
 
     const KernelEntry* e = nullptr;
     if (pl.variant == RN_VARIANT_STREAM)
-        e = stream_entry(q.op, pl.vec, q.res);
+        e = stream_entry(q.op, q.dtype, pl.vec, q.res);
     else if (pl.variant == RN_VARIANT_STAGED)
         e = staged_entry(q.op, pl.slots);
     else
-        e = reg_entry(q.op, pl.vec, pl.slots, pl.threads_per_row, pl.params_held != 0,
+        e = reg_entry(q.op, q.dtype, pl.vec, pl.slots, pl.threads_per_row, pl.params_held != 0,
                       pl.aligned != 0, q.res);
     if (!e) return RN_ERR_VARIANT;
 
@@ -375,13 +411,14 @@ int run(const Request& q, int variant, void* stream) {
 
 Request ln_request(const float* x, const float* res, const float* gamma, const float* beta,
                    float* h, float* y, float* mean, float* rstd, int64_t rows, int64_t d,
-                   float eps, bool residual) {
-    return Request{OP_LN, residual, x, res, gamma, beta, y, h, mean, rstd, rows, d, eps};
+                   float eps, bool residual, int dtype = DT_F32) {
+    return Request{OP_LN, dtype, residual, x, res, gamma, beta, y, h, mean, rstd, rows, d, eps};
 }
 
 Request rms_request(const float* x, const float* res, const float* w, float* h, float* y,
-                    int64_t rows, int64_t d, float eps, bool residual) {
-    return Request{OP_RMS, residual, x, res, w, nullptr, y, h, nullptr, nullptr, rows, d, eps};
+                    int64_t rows, int64_t d, float eps, bool residual, int dtype = DT_F32) {
+    return Request{OP_RMS, dtype, residual, x, res, w, nullptr, y, h, nullptr, nullptr, rows, d,
+                   eps};
 }
 
 }  // namespace
@@ -439,13 +476,31 @@ int rms_fwd_residual_variant(int variant, const float* x, const float* res, cons
     return run(rms_request(x, res, w, h_out, y, rows, d, eps, true), variant, stream);
 }
 
-int rn_plan_for_residual(int op, int variant, int64_t d, const void* x, const void* res,
-                         const void* h, const void* y, const void* p0, const void* p1,
-                         rn_plan* plan) {
+int ln_fwd_typed(int dtype, int variant, const void* x, const void* gamma, const void* beta,
+                 void* y, float* mean_out, float* rstd_out, int64_t rows, int64_t d, float eps,
+                 void* stream) {
+    return run(ln_request((const float*)x, nullptr, (const float*)gamma, (const float*)beta,
+                          nullptr, (float*)y, mean_out, rstd_out, rows, d, eps, false, dtype),
+               variant, stream);
+}
+
+int rms_fwd_typed(int dtype, int variant, const void* x, const void* w, void* y, int64_t rows,
+                  int64_t d, float eps, void* stream) {
+    return run(rms_request((const float*)x, nullptr, (const float*)w, nullptr, (float*)y, rows, d,
+                           eps, false, dtype),
+               variant, stream);
+}
+
+static int plan_any(int dtype, int op, int variant, int64_t d, const void* x, const void* res,
+                    const void* h, const void* y, const void* p0, const void* p1, rn_plan* plan) {
     if (!plan) return RN_ERR_NULL;
     if (op != RN_OP_LN && op != RN_OP_RMS) return RN_ERR_VARIANT;
     if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
+    if (dtype != RN_DTYPE_F32 && dtype != RN_DTYPE_BF16 && dtype != RN_DTYPE_F16)
+        return RN_ERR_DTYPE;
+    if (res && dtype != RN_DTYPE_F32) return RN_ERR_DTYPE;
     Request q{op == RN_OP_LN ? OP_LN : OP_RMS,
+              dtype,
               res != nullptr,
               (const float*)x,
               (const float*)res,
@@ -459,6 +514,17 @@ int rn_plan_for_residual(int op, int variant, int64_t d, const void* x, const vo
               d,
               0.f};
     return plan_impl(q, variant, plan);
+}
+
+int rn_plan_for_residual(int op, int variant, int64_t d, const void* x, const void* res,
+                         const void* h, const void* y, const void* p0, const void* p1,
+                         rn_plan* plan) {
+    return plan_any(RN_DTYPE_F32, op, variant, d, x, res, h, y, p0, p1, plan);
+}
+
+int rn_plan_for_typed(int dtype, int op, int variant, int64_t d, const void* x, const void* y,
+                      const void* p0, const void* p1, rn_plan* plan) {
+    return plan_any(dtype, op, variant, d, x, nullptr, nullptr, y, p0, p1, plan);
 }
 
 int rn_plan_for(int op, int variant, int64_t d, const void* x, const void* y, const void* p0,
@@ -476,6 +542,7 @@ const char* rn_status_str(int status) {
         case RN_ERR_CUDA: return "CUDA runtime error (see rn_last_cuda_error)";
         case RN_ERR_ALIGN: return "a pointer is not 4-byte aligned";
         case RN_ERR_VARIANT: return "the requested kernel variant cannot run this request";
+        case RN_ERR_DTYPE: return "unsupported storage type for this entry point";
         default: return "unknown status";
     }
 }

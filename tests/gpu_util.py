@@ -144,3 +144,73 @@ def residual_variants_for(op, d, x_off=0, y_off=0):
             continue
         out.append(v)
     return out
+
+
+DTYPE_CODE = {"f32": capi.RN_DTYPE_F32, "bf16": capi.RN_DTYPE_BF16, "f16": capi.RN_DTYPE_F16}
+
+
+def dev_copy16(bits, offset=0, pad=16):
+    """Upload uint16 patterns, ``offset`` elements into a fresh allocation."""
+    torch = torch_cuda()
+    a = np.ascontiguousarray(bits, np.uint16).reshape(-1).view(np.int16)
+    buf = torch.zeros(a.size + offset + pad, dtype=torch.int16, device="cuda")
+    if a.size:
+        buf[offset:offset + a.size].copy_(torch.from_numpy(a.copy()))
+    return buf, buf.data_ptr() + 2 * offset
+
+
+class Guarded16:
+    """A device output of n 16-bit elements framed by sentinel guards."""
+
+    def __init__(self, n, offset=0):
+        torch = torch_cuda()
+        self.n = n
+        self.head = parity.GUARD + offset
+        host = np.full(n + self.head + parity.GUARD, parity.SENTINEL16, np.uint16).view(np.int16)
+        self.buf = torch.from_numpy(host).to("cuda")
+        self.ptr = self.buf.data_ptr() + 2 * self.head
+
+    def fetch(self, what):
+        h = self.buf.cpu().numpy().view(np.uint16)
+        if not (np.all(h[:self.head] == parity.SENTINEL16)
+                and np.all(h[self.head + self.n:] == parity.SENTINEL16)):
+            raise parity.ParityError(f"{what}: guard region overwritten")
+        return h[self.head:self.head + self.n]
+
+
+def run_typed(op, dtype, xbits, pbits, eps=1e-5, variant=capi.RN_VARIANT_AUTO, x_off=0, y_off=0,
+              p_off=0, stats=True):
+    """ln/rms_fwd_typed on 16-bit patterns; returns (y patterns, mean, rstd)."""
+    torch = torch_cuda()
+    rows, d = xbits.shape
+    xb, xp = dev_copy16(xbits, x_off)
+    pbs = [dev_copy16(p, p_off) for p in pbits]
+    y = Guarded16(rows * d, y_off)
+    code = DTYPE_CODE[dtype]
+    if op == capi.RN_OP_LN:
+        m = Guarded(rows) if stats else None
+        r = Guarded(rows) if stats else None
+        st = capi.ln_fwd_typed(code, variant, xp, pbs[0][1], pbs[1][1], y.ptr,
+                               m.ptr if m else 0, r.ptr if r else 0, rows, d,
+                               float(np.float32(eps)), stream_handle())
+    else:
+        m = r = None
+        st = capi.rms_fwd_typed(code, variant, xp, pbs[0][1], y.ptr, rows, d,
+                                float(np.float32(eps)), stream_handle())
+    capi.check(st)
+    torch.cuda.synchronize()
+    return (y.fetch("y guard").reshape(rows, d), m.fetch("mean guard") if m else None,
+            r.fetch("rstd guard") if r else None)
+
+
+def typed_variants_for(dtype, op, d, x_off=0, y_off=0):
+    out = [capi.RN_VARIANT_AUTO]
+    es = 4 if dtype == "f32" else 2
+    xa, ya = (1 << 20) + es * x_off, (1 << 30) + es * y_off
+    for v in range(1, capi.RN_VARIANT_COUNT):
+        try:
+            capi.plan_typed(DTYPE_CODE[dtype], op, v, d, xa, ya)
+        except capi.RowNormError:
+            continue
+        out.append(v)
+    return out

@@ -95,3 +95,51 @@ def check_guards(buf, n, what="guard", head=GUARD):
 def guarded(n, head=GUARD):
     """A host buffer of n outputs framed by guards, every element a sentinel."""
     return np.full(n + head + GUARD, SENTINEL_BITS, np.uint32).view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# 16-bit storage: y is computed in FP32 and rounded once to the storage type.
+# An element passes if it is within one unit in the last place of the float64
+# reference rounded to that type (the FP32 value can sit on the other side of
+# a rounding boundary, never further), or within the FP32 rule plus one unit
+# in the last place: near-zero outputs of LayerNorm (beta cancelling the
+# normalised term) carry the FP32 computation's absolute error, ~u_32 |mu|
+# rstd, which exceeds one 16-bit ulp there and is what the FP32 rule's
+# absolute term already allows.
+# --------------------------------------------------------------------------
+SENTINEL16 = 0x7FC1   # a NaN in both BF16 and FP16
+
+
+def _round_storage(ref64, dtype):
+    import workloads
+
+    bits, _ = workloads.to_storage(np.asarray(ref64, np.float64).astype(np.float32), dtype)
+    return bits
+
+
+def check_y_storage(bits, y_ref, dtype, what="y"):
+    bits = np.asarray(bits, np.uint16)
+    y_ref = np.asarray(y_ref, np.float64)
+    want = _round_storage(y_ref, dtype)
+    if bits.shape != want.shape:
+        raise ParityError(f"{what}: shape {bits.shape} != {want.shape}")
+    # ordered integer keys: ULP distance of same-type values
+    def key(b):
+        b = b.astype(np.int32)
+        return np.where(b & 0x8000, 0x8000 - b, b)
+    dist = np.abs(key(bits) - key(want))
+    nan = np.isnan(y_ref)
+    import workloads
+
+    got = workloads.from_storage(bits, dtype).astype(np.float64)
+    ulp = np.abs(workloads.from_storage(want ^ np.uint16(0), dtype).astype(np.float64)
+                 - workloads.from_storage((want + np.uint16(1)) & np.uint16(0x7FFF) |
+                                          (want & np.uint16(0x8000)), dtype).astype(np.float64))
+    with np.errstate(invalid="ignore"):
+        loose = np.abs(got - y_ref) <= Y_ATOL + Y_RTOL * np.abs(y_ref) + ulp
+    bad = ((dist > 1) & ~loose & ~nan) | (np.isnan(got) & ~nan)
+    if bad.any():
+        i = _first_bad(bad)
+        raise ParityError(f"{what}: {int(bad.sum())} elements more than 1 ulp off; first at {i}: "
+                          f"got {got[i]!r}, want {y_ref[i]!r}")
+    return int(dist.max()) if dist.size else 0

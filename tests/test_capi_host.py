@@ -209,3 +209,30 @@ def test_residual_plans(lib):
     for v in (capi.RN_VARIANT_STAGED, capi.RN_VARIANT_CLUSTER):
         with pytest.raises(capi.RowNormError):
             capi.plan_residual(capi.RN_OP_LN, v, 40000, X, X + 0x1000000, 0, Y)
+
+
+def test_typed_plans_and_validation(lib):
+    X, Y = A, A + 0x1000000
+    p = capi.plan_typed(capi.RN_DTYPE_BF16, capi.RN_OP_LN, capi.RN_VARIANT_AUTO, 768, X, Y, X, X)
+    assert (p.variant, p.vec, p.slots, p.aligned) == (capi.RN_VARIANT_WARP, 8, 3, 1)
+    p = capi.plan_typed(capi.RN_DTYPE_F16, capi.RN_OP_RMS, capi.RN_VARIANT_AUTO, 4096, X, Y)
+    assert (p.variant, p.vec, p.threads_per_row, p.slots) == (capi.RN_VARIANT_BLOCK, 8, 128, 4)
+    p = capi.plan_typed(capi.RN_DTYPE_BF16, capi.RN_OP_RMS, capi.RN_VARIANT_AUTO, 40000, X, Y)
+    assert p.variant == capi.RN_VARIANT_STREAM
+    # 2-byte phases differ from 16-byte phases: scalar path
+    p = capi.plan_typed(capi.RN_DTYPE_BF16, capi.RN_OP_RMS, capi.RN_VARIANT_AUTO, 768, X + 2, Y)
+    assert p.vec == 1
+    with pytest.raises(capi.RowNormError):
+        capi.plan_typed(capi.RN_DTYPE_BF16, capi.RN_OP_LN, capi.RN_VARIANT_CLUSTER, 40000, X, Y)
+    with pytest.raises(capi.RowNormError):
+        capi.plan_typed(7, capi.RN_OP_LN, capi.RN_VARIANT_AUTO, 64, X, Y)
+    # validation: 2-byte alignment for 16-bit, unknown dtype
+    assert capi.ln_fwd_typed(capi.RN_DTYPE_BF16, 0, X + 1, X + 0x100000, X + 0x200000, Y, 0, 0,
+                             4, 8, 1e-5, 0) == capi.RN_ERR_ALIGN
+    assert capi.ln_fwd_typed(9, 0, X, X + 0x100000, X + 0x200000, Y, 0, 0, 4, 8, 1e-5,
+                             0) == capi.RN_ERR_DTYPE
+    assert capi.rms_fwd_typed(capi.RN_DTYPE_F16, 0, X, X + 0x100000, X + 8, 4, 8, 1e-5,
+                              0) == capi.RN_ERR_ALIAS
+    # statistics stay FP32: 4-byte alignment even with 16-bit data
+    assert capi.ln_fwd_typed(capi.RN_DTYPE_BF16, 0, X, X + 0x100000, X + 0x200000, Y,
+                             X + 0x300002, 0, 4, 8, 1e-5, 0) == capi.RN_ERR_ALIGN

@@ -79,3 +79,48 @@ def test_stat_tolerances_reject_slips():
     # a biased-vs-unbiased slip in rstd is far outside the bound
     with pytest.raises(parity.ParityError):
         parity.check_rstd(r * np.sqrt(767 / 768), r)
+
+
+def test_storage_rounding_matches_torch():
+    """The input generator's BF16/FP16 rounding is torch's (round to nearest even)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    a = (rng.standard_normal(100000) * 10.0 ** rng.integers(-6, 6, 100000)).astype(np.float32)
+    bits, wide = workloads.to_storage(a, "bf16")
+    t = torch.from_numpy(a).to(torch.bfloat16)
+    assert np.array_equal(bits.view(np.int16), t.view(torch.int16).numpy())
+    assert np.array_equal(wide, t.float().numpy())
+    bits, wide = workloads.to_storage(a[np.abs(a) < 6e4], "f16")
+    t = torch.from_numpy(a[np.abs(a) < 6e4]).to(torch.float16)
+    assert np.array_equal(bits.view(np.int16), t.view(torch.int16).numpy())
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_storage_checker(dtype):
+    rng = np.random.default_rng(6)
+    ref = rng.standard_normal(5000) * 3
+    bits, _ = workloads.to_storage(ref.astype(np.float32), dtype)
+    parity.check_y_storage(bits, ref, dtype)               # the rounded reference passes
+    off1 = bits.copy()
+    off1[::7] += 1                                           # 1 ulp away: still accepted
+    parity.check_y_storage(off1, ref, dtype)
+    off2 = bits.copy()
+    off2[3] += 2                                             # 2 ulp away: rejected
+    with pytest.raises(parity.ParityError):
+        parity.check_y_storage(off2, ref, dtype)
+    sent = bits.copy()
+    sent[10] = parity.SENTINEL16                             # an unwritten element: rejected
+    with pytest.raises(parity.ParityError):
+        parity.check_y_storage(sent, ref, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_storage_checker_near_zero_uses_fp32_rule(dtype):
+    """Tiny outputs: an absolute error inside the FP32 rule passes even when it is
+    many 16-bit ulps; a large one does not."""
+    ref = np.array([4.6e-6, -3.0e-5, 1e-3])
+    bits, _ = workloads.to_storage(np.array([2.3e-6, -2.8e-5, 1e-3], np.float32), dtype)
+    parity.check_y_storage(bits, ref, dtype)
+    bits, _ = workloads.to_storage(np.array([4.6e-6, -3.0e-5, 1.2e-3], np.float32), dtype)
+    with pytest.raises(parity.ParityError):
+        parity.check_y_storage(bits, ref, dtype)

@@ -200,3 +200,33 @@ def sweep_offset():
 def large_32768x8192(op: str = "ln") -> Workload:
     """LN or RMS at 32768 x 8192 (1 GiB in, 1 GiB out), x ~ N(0,1), seed 4."""
     return Workload(op, 32768, 8192, seed=4, tag=f"{op}_32768x8192")
+
+
+# --------------------------------------------------------------------------
+# 16-bit storage: FP32 values rounded to BF16 or FP16 (nearest even). Returns
+# the 16-bit patterns (uint16) and their exact FP32 values, which both sides
+# use (the GPU receives the patterns, the oracle the widened values).
+# --------------------------------------------------------------------------
+
+def to_storage(a, dtype: str):
+    a = np.ascontiguousarray(a, np.float32)
+    if dtype == "f32":
+        return a, a
+    if dtype == "f16":
+        h = a.astype(np.float16)
+        return h.view(np.uint16), h.astype(np.float32)
+    if dtype == "bf16":
+        u = a.view(np.uint32)
+        bits = ((u + (((u >> 16) & 1) + np.uint32(0x7FFF))) >> 16).astype(np.uint16)
+        return bits, (bits.astype(np.uint32) << 16).view(np.float32)
+    raise ValueError(dtype)
+
+
+def from_storage(bits, dtype: str):
+    """FP32 values of 16-bit patterns."""
+    bits = np.asarray(bits)
+    if dtype == "f16":
+        return bits.view(np.float16).astype(np.float32)
+    if dtype == "bf16":
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+    raise ValueError(dtype)
