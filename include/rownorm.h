@@ -54,6 +54,7 @@
 #ifndef ROWNORM_H
 #define ROWNORM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -144,6 +145,44 @@ int ln_fwd_typed(int dtype, int variant, const void *x, const void *gamma, const
 
 int rms_fwd_typed(int dtype, int variant, const void *x, const void *w, void *y, int64_t rows,
                   int64_t d, float eps, void *stream);
+
+/*
+ * Backward (FP32). The pages list backward passes as untested; these are the
+ * derivatives of the forward definitions above.
+ *
+ * LayerNorm, from the forward's saved mean and rstd:
+ *   xhat = (x - mean) * rstd, g = dy * gamma,
+ *   dx     = rstd * (g - mean_j g - xhat * mean_j(g * xhat))   [rows][d]
+ *   dgamma = sum_i dy * xhat,  dbeta = sum_i dy                 [d]
+ * RMSNorm, with r = (mean_j x^2 + eps)^-1/2 recomputed from x:
+ *   dx = r * (g - x * r^2 * mean_j(g * x)), g = dy * w;  dw = sum_i dy * x * r.
+ *
+ * dgamma / dbeta / dw may be NULL (not computed; with all NULL no workspace
+ * is needed). Parameter gradients are summed over rows deterministically: each
+ * row group accumulates its rows' column sums in registers, each CTA adds its
+ * groups in order and writes one row of partial sums to `workspace` (device
+ * memory, 16-byte aligned, caller-owned, contents on entry ignored), and a
+ * second kernel adds those rows in a fixed order with Kahan compensation.
+ * *_bwd_workspace_size gives the bytes for the full grid on the current
+ * device; a smaller workspace (at least one partial row: 2*d*4 bytes for LN,
+ * d*4 for RMS) runs fewer CTAs, and one below that returns RN_ERR_SIZE.
+ * Results are bitwise repeatable for a given device and workspace size.
+ * Calls on one stream may share a workspace; calls that may run at the same
+ * time on the GPU need workspaces of their own. Widths up to 16384
+ * (aligned arrays, d % 4 == 0) or 8192 (otherwise); wider rows return
+ * RN_ERR_SIZE. Two kernel launches when parameter gradients are wanted, one
+ * otherwise; rows == 0 zeroes the requested parameter gradients.
+ */
+int ln_bwd_workspace_size(int64_t rows, int64_t d, size_t *bytes);
+
+int ln_bwd(const float *dy, const float *x, const float *gamma, const float *mean,
+           const float *rstd, float *dx, float *dgamma, float *dbeta, int64_t rows, int64_t d,
+           void *workspace, size_t workspace_bytes, void *stream);
+
+int rms_bwd_workspace_size(int64_t rows, int64_t d, size_t *bytes);
+
+int rms_bwd(const float *dy, const float *x, const float *w, float *dx, float *dw, int64_t rows,
+            int64_t d, float eps, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *rn_status_str(int status);

@@ -16,5 +16,5 @@ compute the plain definitions; both are pinned by ``tests/test_oracle_*.py``
 (closed forms, invariants, exact brute force on tiny rows, a float64 library
 cross-check and planted mistakes that the pins must catch).
 """
-from .reference import (layer_norm, layer_norm_residual, residual_sum, rms_norm,  # noqa: F401
-                        rms_norm_residual)
+from .reference import (layer_norm, layer_norm_backward, layer_norm_residual,  # noqa: F401
+                        residual_sum, rms_norm, rms_norm_backward, rms_norm_residual)

@@ -96,3 +96,48 @@ def rms_norm_residual(x, res, w, eps=1e-5):
     h = residual_sum(x, res)
     y, r = rms_norm(h, w, eps)
     return h, y, r
+
+
+def layer_norm_backward(dy, x, gamma, mean, rstd):
+    """Gradients of LayerNorm for upstream gradient ``dy``, from the saved
+    per-row mean and rstd (float64 of the given values).
+
+    With xhat = (x - mean) * rstd and g = dy * gamma (the derivative of the
+    output definition above, written out):
+
+        dbeta_j  = sum_i dy_ij
+        dgamma_j = sum_i dy_ij * xhat_ij
+        dx_ij    = rstd_i * (g_ij - (1/d) sum_k g_ik - xhat_ij (1/d) sum_k g_ik xhat_ik)
+
+    Returns float64 (dx [rows, d], dgamma [d], dbeta [d]).
+    """
+    dy64 = np.asarray(dy, dtype=np.float32).astype(np.float64)
+    x64 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    g64 = np.asarray(gamma, dtype=np.float32).astype(np.float64)
+    mu = np.asarray(mean, dtype=np.float64).reshape(-1, 1)
+    rs = np.asarray(rstd, dtype=np.float64).reshape(-1, 1)
+    xhat = (x64 - mu) * rs
+    g = dy64 * g64[None, :]
+    dx = rs * (g - g.mean(axis=1, keepdims=True) - xhat * (g * xhat).mean(axis=1, keepdims=True))
+    return dx, (dy64 * xhat).sum(axis=0), dy64.sum(axis=0)
+
+
+def rms_norm_backward(dy, x, w, eps=1e-5):
+    """Gradients of RMSNorm for upstream gradient ``dy`` (the per-row scale r
+    recomputed from x as in the forward definition).
+
+    With r = (mean_j x^2 + eps)^(-1/2) and g = dy * w:
+
+        dw_j  = sum_i dy_ij * x_ij * r_i
+        dx_ij = r_i * g_ij - x_ij * r_i^3 * (1/d) sum_k g_ik x_ik
+
+    Returns float64 (dx [rows, d], dw [d]).
+    """
+    dy64 = np.asarray(dy, dtype=np.float32).astype(np.float64)
+    x64 = np.asarray(x, dtype=np.float32).astype(np.float64)
+    w64 = np.asarray(w, dtype=np.float32).astype(np.float64)
+    _, r = rms_norm(x, w, eps)
+    r = r.reshape(-1, 1)
+    g = dy64 * w64[None, :]
+    dx = r * g - x64 * r ** 3 * (g * x64).mean(axis=1, keepdims=True)
+    return dx, (dy64 * x64 * r).sum(axis=0)

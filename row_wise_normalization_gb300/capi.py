@@ -71,6 +71,10 @@ SIGNATURES = {
     "rn_plan_for_residual": (_INT, [_INT, _INT, _I64, _P, _P, _P, _P, _P, _P,
                                     ctypes.POINTER(rn_plan)]),
     "ln_fwd_typed": (_INT, [_INT, _INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
+    "ln_bwd_workspace_size": (_INT, [_I64, _I64, ctypes.POINTER(ctypes.c_size_t)]),
+    "rms_bwd_workspace_size": (_INT, [_I64, _I64, ctypes.POINTER(ctypes.c_size_t)]),
+    "ln_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
+    "rms_bwd": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
     "rms_fwd_typed": (_INT, [_INT, _INT, _P, _P, _P, _I64, _I64, _F, _P]),
     "rn_plan_for_typed": (_INT, [_INT, _INT, _INT, _I64, _P, _P, _P, _P, ctypes.POINTER(rn_plan)]),
     "rn_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
@@ -199,3 +203,20 @@ def ln_fwd_typed(dtype, variant, x, gamma, beta, y, mean_out, rstd_out, rows, d,
 
 def rms_fwd_typed(dtype, variant, x, w, y, rows, d, eps, stream=0) -> int:
     return load().rms_fwd_typed(dtype, variant, x, w, y, rows, d, eps, stream)
+
+
+def bwd_workspace_size(op: int, rows: int, d: int) -> int:
+    out = ctypes.c_size_t(0)
+    fn = load().ln_bwd_workspace_size if op == RN_OP_LN else load().rms_bwd_workspace_size
+    check(fn(rows, d, ctypes.byref(out)))
+    return out.value
+
+
+def ln_bwd(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, workspace, workspace_bytes,
+           stream=0) -> int:
+    return load().ln_bwd(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, workspace,
+                         workspace_bytes, stream)
+
+
+def rms_bwd(dy, x, w, dx, dw, rows, d, eps, workspace, workspace_bytes, stream=0) -> int:
+    return load().rms_bwd(dy, x, w, dx, dw, rows, d, eps, workspace, workspace_bytes, stream)

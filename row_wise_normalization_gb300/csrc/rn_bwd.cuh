@@ -1,0 +1,308 @@
+// rn_bwd.cuh -- LayerNorm / RMSNorm backward (FP32).
+//
+// Row part (dx), one row group per row at a time, row slice in registers as in
+// the forward kernels:
+//   LayerNorm, from the saved mean and rstd of the forward:
+//     xhat = (x - mean) * rstd,  g = dy * gamma,
+//     dx = rstd * (g - mean_j(g) - xhat * mean_j(g * xhat));
+//   RMSNorm, with r = (mean_j x^2 + eps)^-1/2 recomputed from the held row:
+//     g = dy * w,  dx = r * (g - x * r^2 * mean_j(g * x)).
+// Both need two row sums, which meet in one exchange (warp xor shuffles, then
+// one named barrier when several warps share a row). g is rounded once
+// (__fmul_rn, never contracted into a later fma), so the g the sums saw is the
+// g that dx subtracts from: for a one-element row g - mean(g) is exactly 0,
+// where a contracted product would leave its rounding residue times rstd.
+//
+// Parameter part (dgamma/dbeta, dw): a thread owns the same columns for every
+// row it processes (whole aligned vectors, or single elements when the
+// arrays are not all 16-byte aligned with d % 4 == 0), so it accumulates its
+// columns' sums over its rows in registers. A CTA holds 256 / TPR row groups
+// (at least one); when its rows are done the groups' sums are added through
+// shared memory in group order and the CTA writes one partial row to the
+// workspace. column_reduce_kernel then adds the CTAs' rows in a fixed order
+// with Kahan compensation: deterministic for a given grid, no atomics. It is
+// launched as a programmatic dependent of the row kernel, so its launch
+// overlaps the row kernel's tail and it waits (griddepcontrol.wait) for the
+// row kernel's writes before reading.
+#pragma once
+
+#include "rn_device.cuh"
+
+namespace rn {
+
+// Registers a thread is budgeted: x, dy, the held parameters and (PG) two
+// accumulators per held element, plus indices and addresses; the CTAs per SM
+// follow from it (65536 registers, allocated in units of 8 per thread).
+constexpr int bwd_min_ctas(int threads, int held, bool pg) {
+    const int budget = 56 + held * (pg ? 5 : 3);
+    const int n = 65536 / (((budget + 7) / 8) * 8 * threads);
+    return n < 1 ? 1 : (n > 32 ? 32 : n);
+}
+
+template <int OP, int VEC, int SLOTS, int TPR, int RPC, bool PG>
+__global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC, PG))
+    bwd_kernel(const BwdParams p) {
+    static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
+    constexpr int WPR = TPR / 32;
+    constexpr int NBUF = WPR > 1 ? 2 : 1;
+    __shared__ __align__(16) float xch[NBUF][RPC][WPR][2];
+
+    const int g = threadIdx.x / TPR;
+    const int t = threadIdx.x - g * TPR;
+    const int w = t >> 5, lane = t & 31;
+    const int d = (int)p.d;
+    const int nv = d / VEC;               // VEC 4 only when d % 4 == 0 (host checks)
+    const float inv_d = 1.0f / (float)d;
+    const int64_t group = (int64_t)blockIdx.x * RPC + g;
+    const int64_t ngroups = (int64_t)gridDim.x * RPC;
+
+    // parameters of my columns, held for every row
+    Vec<VEC> par[SLOTS];
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        const int q = t + s * TPR;
+        if (q < nv) {
+            ld_p(par[s], p.p0 + q * VEC, true);
+        } else {
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) par[s].v[k] = 0.f;
+        }
+    }
+    Vec<VEC> acc0[PG ? SLOTS : 1], acc1[(PG && OP == OP_LN) ? SLOTS : 1];
+    if constexpr (PG) {
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+                acc0[s].v[k] = 0.f;
+                if constexpr (OP == OP_LN) acc1[s].v[k] = 0.f;
+            }
+    }
+
+    int it = 0;
+    for (int64_t row = group; row < p.rows; row += ngroups, ++it) {
+        const float* xr = p.x + row * p.d;
+        const float* dyr = p.dy + row * p.d;
+        Vec<VEC> xv[SLOTS], dv[SLOTS];
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            const int q = t + s * TPR;
+            if (q < nv) {
+                ld_x(xv[s], xr + q * VEC);
+                ld_x(dv[s], dyr + q * VEC);
+            } else {
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) xv[s].v[k] = dv[s].v[k] = 0.f;
+            }
+        }
+        float mu = 0.f, rs = 0.f;
+        if constexpr (OP == OP_LN) {
+            mu = ld_p1(p.mean + row);
+            rs = ld_p1(p.rstd + row);
+        }
+        // two row sums: LN (sum g, sum g*xhat); RMS (sum x^2, sum g*x)
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            if (t + s * TPR < nv) {
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) {
+                    const float gk = __fmul_rn(dv[s].v[k], par[s].v[k]);
+                    if constexpr (OP == OP_LN) {
+                        const float xh = (xv[s].v[k] - mu) * rs;
+                        s1 += gk;
+                        s2 = fmaf(gk, xh, s2);
+                    } else {
+                        s1 = fmaf(xv[s].v[k], xv[s].v[k], s1);
+                        s2 = fmaf(gk, xv[s].v[k], s2);
+                    }
+                }
+            }
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        if constexpr (WPR > 1) {
+            float(*slot)[2] = xch[it & (NBUF - 1)][g];
+            if (lane == 0) {
+                slot[w][0] = s1;
+                slot[w][1] = s2;
+            }
+            named_sync(1 + g, TPR);
+            s1 = 0.f;
+            s2 = 0.f;
+#pragma unroll
+            for (int k = 0; k < WPR; ++k) {
+                s1 += slot[k][0];
+                s2 += slot[k][1];
+            }
+        }
+        float c1, c2;
+        if constexpr (OP == OP_LN) {
+            c1 = s1 * inv_d;
+            c2 = s2 * inv_d;
+        } else {
+            rs = rsqrtf(s1 * inv_d + p.eps);
+            c1 = 0.f;
+            c2 = s2 * inv_d * rs * rs;
+        }
+        float* dxr = p.dx + row * p.d;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            const int q = t + s * TPR;
+            if (q < nv) {
+                Vec<VEC> o;
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) {
+                    const float gk = __fmul_rn(dv[s].v[k], par[s].v[k]);
+                    if constexpr (OP == OP_LN) {
+                        const float xh = (xv[s].v[k] - mu) * rs;
+                        o.v[k] = rs * (gk - c1 - xh * c2);
+                        if constexpr (PG) {
+                            acc0[s].v[k] += dv[s].v[k];
+                            acc1[s].v[k] = fmaf(dv[s].v[k], xh, acc1[s].v[k]);
+                        }
+                    } else {
+                        o.v[k] = rs * (gk - xv[s].v[k] * c2);
+                        if constexpr (PG) acc0[s].v[k] = fmaf(dv[s].v[k], xv[s].v[k] * rs, acc0[s].v[k]);
+                    }
+                }
+                st_y(dxr + q * VEC, o);
+            }
+        }
+    }
+
+    // let the column reduction's CTAs launch; they wait for this grid's writes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if constexpr (PG) {
+        float* wr = p.ws + (int64_t)blockIdx.x * p.ws_width;
+        if constexpr (RPC == 1) {
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int q = t + s * TPR;
+                if (q < nv) {
+                    st_y(wr + q * VEC, acc0[s]);
+                    if constexpr (OP == OP_LN) st_y(wr + d + q * VEC, acc1[s]);
+                }
+            }
+        } else {
+            // add the CTA's row groups, in group order, one slot at a time
+            __shared__ __align__(16) float red[RPC][TPR * VEC];
+            constexpr int HALVES = OP == OP_LN ? 2 : 1;
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+#pragma unroll
+                for (int hf = 0; hf < HALVES; ++hf) {
+                    const Vec<VEC>& a = hf ? acc1[s] : acc0[s];
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) red[g][t * VEC + k] = a.v[k];
+                    __syncthreads();
+                    const int q = t + s * TPR;
+                    if (g == 0 && q < nv) {
+                        Vec<VEC> sum;
+#pragma unroll
+                        for (int k = 0; k < VEC; ++k) sum.v[k] = red[0][t * VEC + k];
+#pragma unroll
+                        for (int gg = 1; gg < RPC; ++gg)
+#pragma unroll
+                            for (int k = 0; k < VEC; ++k) sum.v[k] += red[gg][t * VEC + k];
+                        st_y(wr + hf * d + q * VEC, sum);
+                    }
+                    __syncthreads();
+                }
+            }
+        }
+    }
+}
+
+// Sum of the workspace's rows: out0[j] = sum_c ws[c][j] for j < d, out1[j - d]
+// for d <= j < width (either output may be NULL). A CTA takes 32 columns and
+// 32 slices of the rows: lane l of warp w adds rows w, w + 32, ... of column
+// l with Kahan compensation (a warp reads 128 contiguous bytes per row), and
+// warp 0 adds the 32 slice sums in slice order, again compensated.
+constexpr int kReduceCols = 32;
+constexpr int kReduceSlices = 32;
+
+__global__ void __launch_bounds__(kReduceCols * kReduceSlices)
+    column_reduce_kernel(const float* __restrict__ ws, int64_t rows, int64_t width, int64_t d,
+                         float* out0, float* out1) {
+    __shared__ float part[kReduceSlices][kReduceCols + 1];
+    // wait until the row kernel's partials are written and visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31, slice = threadIdx.x >> 5;
+    const int64_t j = (int64_t)blockIdx.x * kReduceCols + lane;
+    float s = 0.f, c = 0.f;
+    if (j < width) {
+#pragma unroll 4
+        for (int64_t r = slice; r < rows; r += kReduceSlices) {
+            const float v = __ldcg(ws + r * width + j) - c;
+            const float tsum = s + v;
+            c = (tsum - s) - v;
+            s = tsum;
+        }
+    }
+    part[slice][lane] = s;
+    __syncthreads();
+    if (slice == 0 && j < width) {
+        float u = 0.f, e = 0.f;
+#pragma unroll
+        for (int k = 0; k < kReduceSlices; ++k) {
+            const float v = part[k][lane] - e;
+            const float tsum = u + v;
+            e = (tsum - u) - v;
+            u = tsum;
+        }
+        if (j < d) {
+            if (out0) out0[j] = u;
+        } else if (out1) {
+            out1[j - d] = u;
+        }
+    }
+}
+
+}  // namespace rn
+
+namespace rn {
+
+template <int OP, int VEC, int SLOTS, int TPR, bool PG>
+struct BwdInst {
+    static constexpr int RPC = TPR < 256 ? 256 / TPR : 1;
+    static cudaError_t launch(const BwdParams& p, int grid, cudaStream_t s) {
+        bwd_kernel<OP, VEC, SLOTS, TPR, RPC, PG><<<grid, TPR * RPC, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    static const BwdEntry entry;
+};
+
+template <int OP, int VEC, int SLOTS, int TPR, bool PG>
+const BwdEntry BwdInst<OP, VEC, SLOTS, TPR, PG>::entry = {
+    (const void*)&bwd_kernel<OP, VEC, SLOTS, TPR, BwdInst<OP, VEC, SLOTS, TPR, PG>::RPC, PG>,
+    TPR * BwdInst<OP, VEC, SLOTS, TPR, PG>::RPC, BwdInst<OP, VEC, SLOTS, TPR, PG>::RPC,
+    &BwdInst<OP, VEC, SLOTS, TPR, PG>::launch};
+
+template <int OP, int VEC, int TPR, bool PG>
+const BwdEntry* bwd_pick_slots(int slots) {
+    switch (slots) {
+        case 1: return &BwdInst<OP, VEC, 1, TPR, PG>::entry;
+        case 2: return &BwdInst<OP, VEC, 2, TPR, PG>::entry;
+        case 3: return &BwdInst<OP, VEC, 3, TPR, PG>::entry;
+        case 4: return &BwdInst<OP, VEC, 4, TPR, PG>::entry;
+        case 8: if constexpr (VEC == 1) return &BwdInst<OP, VEC, 8, TPR, PG>::entry; else return nullptr;
+        default: return nullptr;
+    }
+}
+
+template <int OP, int VEC, bool PG>
+const BwdEntry* bwd_pick(int slots, int tpr) {
+    switch (tpr) {
+        case 32: return bwd_pick_slots<OP, VEC, 32, PG>(slots);
+        case 64: return bwd_pick_slots<OP, VEC, 64, PG>(slots);
+        case 128: return bwd_pick_slots<OP, VEC, 128, PG>(slots);
+        case 256: return bwd_pick_slots<OP, VEC, 256, PG>(slots);
+        case 512: return bwd_pick_slots<OP, VEC, 512, PG>(slots);
+        case 1024: return bwd_pick_slots<OP, VEC, 1024, PG>(slots);
+        default: return nullptr;
+    }
+}
+
+}  // namespace rn

@@ -92,6 +92,34 @@ const ClusterEntry* cluster_entry(int op, int slots, int threads, int cl, bool a
 constexpr int kMaxCluster = 16;
 constexpr int kClusterMaxQuads = 1024 * 8 * kMaxCluster;   // 524288 floats per row
 
+// Arguments of the backward kernels (rn_bwd.cuh).
+struct BwdParams {
+    const float* dy;
+    const float* x;
+    const float* p0;      // gamma or w
+    const float* mean;    // LN: saved mean
+    const float* rstd;    // LN: saved rstd
+    float* dx;
+    float* ws;            // [grid][ws_width] partial column sums (NULL: no parameter grads)
+    int64_t rows;
+    int64_t d;
+    int64_t ws_width;     // 2d (LN: dbeta part, dgamma part) or d (RMS: dw)
+    float eps;            // RMS only
+};
+
+// Backward kernels. slots: 1, 2, 3, 4 (and 8 with vec 1).
+struct BwdEntry {
+    const void* fn;
+    int threads;
+    int rows_per_cta;
+    cudaError_t (*launch)(const BwdParams&, int grid, cudaStream_t);
+};
+const BwdEntry* bwd_entry(int op, int vec, int slots, int tpr, bool pg);
+cudaError_t column_reduce(const float* ws, int64_t groups, int64_t width, int64_t d, float* out0,
+                          float* out1, cudaStream_t s);
+constexpr int kBwdHeld = 16;   // floats of a row a backward thread holds (x and dy each)
+constexpr int kBwdMinRowsPerGroup = 4;   // rows a backward row group takes at least (with grads)
+
 // Reads (and optionally clears) the device error word of the current device.
 cudaError_t device_error_word(unsigned int* out, bool clear);
 

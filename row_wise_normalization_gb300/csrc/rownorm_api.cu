@@ -421,9 +421,210 @@ Request rms_request(const float* x, const float* res, const float* w, float* h, 
                    eps};
 }
 
+// ---------------------------------------------------------------------------
+// Backward.
+// ---------------------------------------------------------------------------
+struct BwdRequest {
+    int op;
+    const float* dy;
+    const float* x;
+    const float* p0;     // gamma or w
+    const float* mean;   // LN
+    const float* rstd;   // LN
+    float* dx;
+    float* dp0;          // dgamma or dw (may be NULL)
+    float* dp1;          // dbeta (LN; may be NULL)
+    int64_t rows;
+    int64_t d;
+    float eps;           // RMS
+    void* ws;
+    size_t ws_bytes;
+};
+
+struct BwdPlan {
+    const BwdEntry* e;
+    int vec, slots, tpr, grid;
+    int64_t width;       // floats per workspace row
+    int64_t groups;      // workspace rows written (one per CTA)
+};
+
+int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaError_t* err) {
+    *err = cudaSuccess;
+    const bool al = q.d % 4 == 0 &&
+                    ((addr(q.dy) | addr(q.x) | addr(q.p0) | addr(q.dx) | addr(q.ws)) & 15u) == 0;
+    const int vec = al ? 4 : 1;
+    const int maxs = vec == 4 ? kBwdHeld / 4 : 8;
+    const int64_t units = q.d / vec;
+    int tpr = 0, slots = 0;
+    for (int t = 32; t <= 1024; t *= 2)
+        if (units <= (int64_t)t * maxs) {
+            tpr = t;
+            break;
+        }
+    if (!tpr) return RN_ERR_SIZE;
+    const int need = (int)((units + tpr - 1) / tpr);
+    slots = need <= 4 ? need : 8;
+    const BwdEntry* e = bwd_entry(q.op, vec, slots, tpr, pg);
+    if (!e) return RN_ERR_VARIANT;
+    // resident CTAs
+    int dev = 0, sms = 0, per = 0;
+    if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return RN_ERR_CUDA;
+    if ((*err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return RN_ERR_CUDA;
+    if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, e->fn, e->threads, 0)) !=
+        cudaSuccess)
+        return RN_ERR_CUDA;
+    int64_t grid = (int64_t)(per > 0 ? per : 1) * sms;
+    const int64_t rows_ctas = (q.rows + e->rows_per_cta - 1) / e->rows_per_cta;
+    if (rows_ctas < grid) grid = rows_ctas;
+    if (pg) {
+        // every CTA writes one partial row of the parameter sums: give each
+        // row group several rows, but keep at least one CTA per SM busy
+        const int64_t per_cta = (int64_t)e->rows_per_cta * kBwdMinRowsPerGroup;
+        int64_t want = (q.rows + per_cta - 1) / per_cta;
+        const int64_t floor_ = rows_ctas < sms ? rows_ctas : sms;
+        if (want < floor_) want = floor_;
+        if (want < grid) grid = want;
+    }
+    if (grid < 1) grid = 1;
+    const int64_t width = q.op == OP_LN ? 2 * q.d : q.d;
+    if (pg && !size_only) {
+        const int64_t cap = (int64_t)(q.ws_bytes / ((size_t)width * 4));
+        if (cap < 1) return RN_ERR_SIZE;   // workspace smaller than one CTA's partial row
+        if (cap < grid) grid = cap;
+    }
+    bp->e = e;
+    bp->vec = vec;
+    bp->slots = slots;
+    bp->tpr = tpr;
+    bp->grid = (int)grid;
+    bp->width = width;
+    bp->groups = grid;
+    return RN_OK;
+}
+
+int bwd_validate(const BwdRequest& q, bool pg) {
+    if (q.rows < 0 || q.d <= 0) return RN_ERR_SIZE;
+    if (q.rows > 0 && q.d > kMaxElems / q.rows) return RN_ERR_SIZE;
+    if (q.op == OP_RMS && (!std::isfinite(q.eps) || q.eps < 0.f)) return RN_ERR_EPS;
+    if (q.rows == 0) return RN_OK;
+    if (!q.dy || !q.x || !q.p0 || !q.dx) return RN_ERR_NULL;
+    if (q.op == OP_LN && (!q.mean || !q.rstd)) return RN_ERR_NULL;
+    if (pg && !q.ws) return RN_ERR_NULL;
+    const void* all[] = {q.dy, q.x, q.p0, q.mean, q.rstd, q.dx, q.dp0, q.dp1};
+    for (const void* p : all)
+        if (misaligned(p, 4)) return RN_ERR_ALIGN;
+    if (pg && (addr(q.ws) & 15u)) return RN_ERR_ALIGN;
+    const int64_t nx = q.rows * q.d * 4, np = q.d * 4, ns = q.rows * 4;
+    const int64_t nws = pg ? (int64_t)q.ws_bytes : 0;
+    const void* outs[4] = {q.dx, q.dp0, q.dp1, pg ? q.ws : nullptr};
+    const int64_t nouts[4] = {nx, np, np, nws};
+    const void* ins[5] = {q.dy, q.x, q.p0, q.mean, q.rstd};
+    const int64_t nins[5] = {nx, nx, np, ns, ns};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 5; ++j)
+            if (overlaps(outs[i], nouts[i], ins[j], nins[j])) return RN_ERR_ALIAS;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(outs[i], nouts[i], outs[j], nouts[j])) return RN_ERR_ALIAS;
+    }
+    return RN_OK;
+}
+
+int run_bwd(const BwdRequest& q, void* stream) {
+    const bool pg = q.dp0 || q.dp1;
+    int st = bwd_validate(q, pg);
+    if (st != RN_OK) return st;
+    if (q.rows == 0) {
+        // an empty batch still defines the parameter gradients: zero
+        const cudaStream_t s = (cudaStream_t)stream;
+        cudaError_t err = cudaSuccess;
+        if (q.dp0) err = cudaMemsetAsync(q.dp0, 0, (size_t)q.d * 4, s);
+        if (err == cudaSuccess && q.dp1) err = cudaMemsetAsync(q.dp1, 0, (size_t)q.d * 4, s);
+        return err == cudaSuccess ? RN_OK : fail_cuda(err);
+    }
+    BwdPlan bp;
+    cudaError_t err;
+    st = bwd_plan(q, pg, false, &bp, &err);
+    if (st == RN_ERR_CUDA) return fail_cuda(err);
+    if (st != RN_OK) return st;
+    BwdParams prm;
+    prm.dy = q.dy;
+    prm.x = q.x;
+    prm.p0 = q.p0;
+    prm.mean = q.mean;
+    prm.rstd = q.rstd;
+    prm.dx = q.dx;
+    prm.ws = pg ? (float*)q.ws : nullptr;
+    prm.rows = q.rows;
+    prm.d = q.d;
+    prm.ws_width = bp.width;
+    prm.eps = q.eps;
+    const cudaStream_t s = (cudaStream_t)stream;
+    err = bp.e->launch(prm, bp.grid, s);
+    if (err != cudaSuccess) return fail_cuda(err);
+    if (pg) {
+        // LN workspace rows: [0, d) dbeta partials, [d, 2d) dgamma partials
+        float* out0 = q.op == OP_LN ? q.dp1 : q.dp0;
+        float* out1 = q.op == OP_LN ? q.dp0 : nullptr;
+        err = column_reduce((const float*)q.ws, bp.groups, bp.width, q.d, out0, out1, s);
+        if (err != cudaSuccess) return fail_cuda(err);
+    }
+    return RN_OK;
+}
+
+int bwd_workspace(int op, int64_t rows, int64_t d, size_t* bytes) {
+    if (!bytes) return RN_ERR_NULL;
+    if (rows < 0 || d <= 0) return RN_ERR_SIZE;
+    *bytes = 0;
+    if (rows == 0) return RN_OK;
+    BwdRequest q{};
+    q.op = op;
+    q.rows = rows;
+    q.d = d;
+    // the vector and the scalar layout may run different grids: size for
+    // the larger (one workspace row per CTA in both)
+    BwdPlan bp;
+    cudaError_t err;
+    const int st = bwd_plan(q, true, true, &bp, &err);
+    if (st == RN_ERR_CUDA) return fail_cuda(err);
+    if (st != RN_OK) return st;
+    // the scalar layout may fit more CTAs per SM than the vector one
+    BwdRequest qs = q;
+    qs.x = (const float*)4;   // any unaligned address selects the scalar layout
+    BwdPlan bs;
+    const int st2 = bwd_plan(qs, true, true, &bs, &err);
+    int64_t groups = bp.groups;
+    if (st2 == RN_OK && bs.groups > groups) groups = bs.groups;
+    *bytes = (size_t)(groups * bp.width * 4);
+    return RN_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int ln_bwd_workspace_size(int64_t rows, int64_t d, size_t* bytes) {
+    return bwd_workspace(OP_LN, rows, d, bytes);
+}
+
+int rms_bwd_workspace_size(int64_t rows, int64_t d, size_t* bytes) {
+    return bwd_workspace(OP_RMS, rows, d, bytes);
+}
+
+int ln_bwd(const float* dy, const float* x, const float* gamma, const float* mean,
+           const float* rstd, float* dx, float* dgamma, float* dbeta, int64_t rows, int64_t d,
+           void* workspace, size_t workspace_bytes, void* stream) {
+    BwdRequest q{OP_LN, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, 0.f,
+                 workspace, workspace_bytes};
+    return run_bwd(q, stream);
+}
+
+int rms_bwd(const float* dy, const float* x, const float* w, float* dx, float* dw, int64_t rows,
+            int64_t d, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+    BwdRequest q{OP_RMS, dy, x, w, nullptr, nullptr, dx, dw, nullptr, rows, d, eps,
+                 workspace, workspace_bytes};
+    return run_bwd(q, stream);
+}
 
 int ln_fwd(const float* x, const float* gamma, const float* beta, float* y, float* mean_out,
            float* rstd_out, int64_t rows, int64_t d, float eps, void* stream) {

@@ -143,3 +143,26 @@ def check_y_storage(bits, y_ref, dtype, what="y"):
         raise ParityError(f"{what}: {int(bad.sum())} elements more than 1 ulp off; first at {i}: "
                           f"got {got[i]!r}, want {y_ref[i]!r}")
     return int(dist.max()) if dist.size else 0
+
+
+# --------------------------------------------------------------------------
+# Sums over rows (parameter gradients). FP32 recursive summation of n terms
+# errs by at most about n u |terms|_1 (Higham, "Accuracy and Stability of
+# Numerical Algorithms", recursive summation bound); the kernels sum at most
+# `chain` rows in sequence per partial and add the partials with Kahan
+# compensation, so |err_j| <= (chain + 4) u sum_i |term_ij| + 1e-4 |ref_j|.
+# --------------------------------------------------------------------------
+U32 = 2.0 ** -24
+
+
+def check_colsum(got, ref, abs_terms, chain, what="colsum"):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    lim = (chain + 4) * U32 * np.asarray(abs_terms, np.float64) + 1e-4 * np.abs(ref) + 1e-7
+    err = np.abs(got - ref)
+    bad = ~(err <= lim)
+    if bad.any():
+        i = _first_bad(bad)
+        raise ParityError(f"{what}: {int(bad.sum())} columns out of tolerance; first {i}: "
+                          f"got {got[i]!r}, want {ref[i]!r} (limit {lim[i]:.3e})")
+    return float((err / np.maximum(lim, 1e-300)).max()) if err.size else 0.0
