@@ -70,7 +70,8 @@ typedef enum rn_status {
     RN_ERR_CUDA = 5,    /* the CUDA runtime reported an error on launch       */
     RN_ERR_ALIGN = 6,   /* a pointer is not 4-byte aligned                     */
     RN_ERR_VARIANT = 7, /* a forced variant cannot run this shape / alignment  */
-    RN_ERR_DTYPE = 8    /* unknown storage type, or one the entry point lacks  */
+    RN_ERR_DTYPE = 8,   /* unknown storage type, or one the entry point lacks  */
+    RN_ERR_SCRATCH = 9  /* the request needs more than a static scratch holds  */
 } rn_status;
 
 /* Storage types of x, y and the parameter vectors (statistics are FP32). */
@@ -183,6 +184,31 @@ int rms_bwd_workspace_size(int64_t rows, int64_t d, size_t *bytes);
 
 int rms_bwd(const float *dy, const float *x, const float *w, float *dx, float *dw, int64_t rows,
             int64_t d, float eps, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * LayerNorm backward without any allocation. The paper has no counterpart to
+ * this entry point; it serves callers that cannot allocate device memory
+ * where they run the backward: a process whose caching allocator already
+ * holds nearly all of HBM, a loop that cannot afford cudaFree's device-wide
+ * synchronisation, or C code with no allocator. Arguments, layouts, results
+ * and errors are those of ln_bwd, without the workspace: the parameter-
+ * gradient partials go to one static device array of RN_NOALLOC_SCRATCH_BYTES
+ * (8 MiB), which every GPU that loads the library holds until exit.
+ * d > RN_NOALLOC_MAX_D (4096) returns RN_ERR_SCRATCH and launches nothing; at
+ * d <= 4096 the array holds at least 256 partial rows, so the grid matches
+ * ln_bwd's with a workspace of that size, and the results are the same bits.
+ * The first call on each device looks the array up (cudaGetSymbolAddress,
+ * with that device current); make that call before any stream capture on the
+ * device. Nothing here calls cudaMalloc, cudaFree or another allocating
+ * routine. All calls share the array and nothing in it has to start at zero;
+ * calls that can overlap on the GPU (two streams, two threads) race on it.
+ */
+#define RN_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define RN_NOALLOC_MAX_D 4096
+
+int ln_bwd_noalloc(const float *dy, const float *x, const float *gamma, const float *mean,
+                   const float *rstd, float *dx, float *dgamma, float *dbeta, int64_t rows,
+                   int64_t d, void *stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *rn_status_str(int status);

@@ -24,6 +24,11 @@ RN_ERR_CUDA = 5
 RN_ERR_ALIGN = 6
 RN_ERR_VARIANT = 7
 RN_ERR_DTYPE = 8
+RN_ERR_SCRATCH = 9
+
+# static scratch of ln_bwd_noalloc
+RN_NOALLOC_SCRATCH_BYTES = 8 << 20
+RN_NOALLOC_MAX_D = 4096
 
 RN_DTYPE_F32 = 0
 RN_DTYPE_BF16 = 1
@@ -75,6 +80,7 @@ SIGNATURES = {
     "rms_bwd_workspace_size": (_INT, [_I64, _I64, ctypes.POINTER(ctypes.c_size_t)]),
     "ln_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
     "rms_bwd": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
+    "ln_bwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "rms_fwd_typed": (_INT, [_INT, _INT, _P, _P, _P, _I64, _I64, _F, _P]),
     "rn_plan_for_typed": (_INT, [_INT, _INT, _INT, _I64, _P, _P, _P, _P, ctypes.POINTER(rn_plan)]),
     "rn_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
@@ -220,3 +226,11 @@ def ln_bwd(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, workspace, work
 
 def rms_bwd(dy, x, w, dx, dw, rows, d, eps, workspace, workspace_bytes, stream=0) -> int:
     return load().rms_bwd(dy, x, w, dx, dw, rows, d, eps, workspace, workspace_bytes, stream)
+
+
+def ln_bwd_noalloc(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, stream=0) -> int:
+    """ln_bwd with its partials in the library's static scratch: for callers
+    that cannot allocate device memory at that point (an allocator that holds
+    nearly all of HBM, a loop that cannot take cudaFree's synchronisation).
+    d <= RN_NOALLOC_MAX_D; calls that overlap on the GPU race on the scratch."""
+    return load().ln_bwd_noalloc(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, stream)

@@ -120,6 +120,9 @@ cudaError_t column_reduce(const float* ws, int64_t groups, int64_t width, int64_
 constexpr int kBwdHeld = 16;   // floats of a row a backward thread holds (x and dy each)
 constexpr int kBwdMinRowsPerGroup = 4;   // rows a backward row group takes at least (with grads)
 
+// Records err as this thread's last CUDA error; returns RN_ERR_CUDA.
+int record_cuda_error(cudaError_t err);
+
 // Reads (and optionally clears) the device error word of the current device.
 cudaError_t device_error_word(unsigned int* out, bool clear);
 

@@ -601,6 +601,10 @@ int bwd_workspace(int op, int64_t rows, int64_t d, size_t* bytes) {
 
 }  // namespace
 
+namespace rn {
+int record_cuda_error(cudaError_t err) { return fail_cuda(err); }
+}  // namespace rn
+
 extern "C" {
 
 int ln_bwd_workspace_size(int64_t rows, int64_t d, size_t* bytes) {
@@ -744,6 +748,9 @@ const char* rn_status_str(int status) {
         case RN_ERR_ALIGN: return "a pointer is not 4-byte aligned";
         case RN_ERR_VARIANT: return "the requested kernel variant cannot run this request";
         case RN_ERR_DTYPE: return "unsupported storage type for this entry point";
+        case RN_ERR_SCRATCH:
+            return "the request needs more than the static scratch holds (ln_bwd_noalloc: "
+                   "d <= 4096)";
         default: return "unknown status";
     }
 }
