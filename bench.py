@@ -14,8 +14,9 @@ Also reported in the same JSON line: the e2e number (pinned host x in,
 device result back to pinned host, through the public API), the oracle on
 the host cores (``cpu_baseline``), the warm-L2 and CUDA-graph numbers of the
 headline shape, the empty-kernel launch floor, a same-session
-device-to-device copy, and the large / sweep shapes (cold L2) for both
-LayerNorm and RMSNorm.
+device-to-device copy, the large / sweep shapes (cold L2) for both
+LayerNorm and RMSNorm, the fused residual add against add-then-normalise,
+BF16/FP16 storage, and the backward (dx plus parameter gradients).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -71,19 +72,31 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# Sources of the FP32 register-held forward kernels (the headline kernel's
+# family): a change to any of them invalidates recorded ncu counters.
+KERNEL_SOURCES = ("rn_reg.cuh", "rn_device.cuh", "rn_params.h", "reg_ln_v4.cu", "reg_ln_v4_al.cu",
+                  "reg_ln_v4_pp.cu", "reg_ln_v1.cu", "reg_rms_v4.cu", "reg_rms_v4_al.cu",
+                  "reg_rms_v4_pp.cu", "reg_rms_v1.cu")
+
+
+CLOCK_WINDOW_S = 0.3
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "row_wise_normalization_gb300", "csrc", "*"))):
-        if p.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(p).encode())
-            h.update(open(p, "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "rownorm.h"), "rb").read())
+    for name in KERNEL_SOURCES:
+        h.update(name.encode())
+        h.update(open(os.path.join(ROOT, "row_wise_normalization_gb300", "csrc", name), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_tag: str, current_hash: str):
+def plan_key(pl: dict) -> str:
+    return "{variant}/vec{vec}/slots{slots}/tpr{threads_per_row}/cta{threads_per_cta}".format(**pl)
+
+
+def recorded_traffic(kernel_tag: str, current_hash: str, plan: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+    the current kernel sources and launch plan (else None)."""
     path = os.path.join(PROFILES, f"{kernel_tag}.traffic.txt")
     if not os.path.exists(path):
         return None
@@ -92,7 +105,7 @@ def recorded_traffic(kernel_tag: str, current_hash: str):
         if "=" in line and not line.lstrip().startswith("#"):
             k, v = line.split("=", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("source_hash") != current_hash:
+    if kv.get("source_hash") != current_hash or kv.get("plan") != plan:
         return None
     try:
         return int(kv["dram_bytes_per_launch"])
@@ -169,7 +182,8 @@ class ClockSampler:
         for name, t0, t1 in self.windows:
             if name == window:
                 sel = [r for r in rows if t0 - 0.01 <= r["t"] <= t1 + 0.01]
-        label = window
+        label = (f"{window} steps (continued untimed with the same step to "
+                 f"{int(CLOCK_WINDOW_S * 1000)} ms when shorter)")
         if len(sel) < 3:
             # the timed region is shorter than a few sampling intervals: use
             # every sample taken while the benchmark kept the GPU busy
@@ -376,7 +390,16 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     t1 = time.time()
     if sampler:
-        sampler.mark("timed", t0, t1)
+        # nvidia-smi samples every few tens of ms: when the K steps end
+        # sooner than CLOCK_WINDOW_S, keep running the same step (untimed)
+        # until the window is that long, so that the clock record covers
+        # this load and not idle time
+        while time.time() - t0 < CLOCK_WINDOW_S:
+            for _ in range(50):
+                flush()
+                case.launch()
+            torch.cuda.synchronize()
+        sampler.mark("timed", t0, time.time())
     step_ms = statistics.fmean(times)
     if dist is not None:
         tt = torch.tensor([step_ms], device=device)
@@ -604,7 +627,7 @@ def run_ours(args, rank, world, local_rank):
         print(f"parity gate failed: {parity}", file=sys.stderr)
 
     h = source_hash()
-    traffic = recorded_traffic(wl.tag, h)
+    traffic = recorded_traffic(wl.tag, h, plan_key(pl))
     achieved = gbs(case.bytes, statistics.fmean(times))
     line = {
         "metric": METRIC,
@@ -696,7 +719,7 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--sweep-steps", type=int, default=20)
