@@ -64,7 +64,7 @@ extern "C" {
 typedef enum rn_status {
     RN_OK = 0,
     RN_ERR_NULL = 1,    /* a required pointer is NULL while rows > 0          */
-    RN_ERR_SIZE = 2,    /* rows < 0, d <= 0, or rows * d too large             */
+    RN_ERR_SIZE = 2,    /* rows < 0, d <= 0, rows * d too large, stride < d    */
     RN_ERR_EPS = 3,     /* eps < 0, NaN or infinite                            */
     RN_ERR_ALIAS = 4,   /* an output overlaps an input or another output      */
     RN_ERR_CUDA = 5,    /* the CUDA runtime reported an error on launch       */
@@ -146,6 +146,28 @@ int ln_fwd_typed(int dtype, int variant, const void *x, const void *gamma, const
 
 int rms_fwd_typed(int dtype, int variant, const void *x, const void *w, void *y, int64_t rows,
                   int64_t d, float eps, void *stream);
+
+/*
+ * Strided rows: as ln_fwd_typed / rms_fwd_typed, with row i of x at
+ * x + i*ldx and row i of y at y + i*ldy (strides in elements, each >= d;
+ * the d elements of a row stay contiguous). This normalises a column block
+ * of a wider matrix (e.g. one head's slice of a fused projection output) or
+ * rows with a padded pitch, in place of a copy to a contiguous buffer. The
+ * elements between rows are neither read nor written. Strides below d
+ * return RN_ERR_SIZE. Aliasing is checked on spans (first to last element),
+ * so an output interleaved with an input in the same rows is rejected
+ * (RN_ERR_ALIAS). The 128-bit path needs x and y in the same 16-byte phase
+ * on every row: equal base phases and ldx - ldy a multiple of the vector
+ * (4 FP32 or 8 16-bit elements); otherwise every access is scalar. The
+ * pages test contiguous rows only ("RMSNorm on an RTX 5070 ...", section
+ * "The operator and the change", names arbitrary strides as untested).
+ */
+int ln_fwd_strided(int dtype, int variant, const void *x, int64_t ldx, const void *gamma,
+                   const void *beta, void *y, int64_t ldy, float *mean_out, float *rstd_out,
+                   int64_t rows, int64_t d, float eps, void *stream);
+
+int rms_fwd_strided(int dtype, int variant, const void *x, int64_t ldx, const void *w, void *y,
+                    int64_t ldy, int64_t rows, int64_t d, float eps, void *stream);
 
 /*
  * Backward (FP32). The pages list backward passes as untested; these are the
@@ -267,6 +289,11 @@ enum { RN_OP_LN = 0, RN_OP_RMS = 1 };
  * RN_ERR_VARIANT. Performs no CUDA call. */
 int rn_plan_for(int op, int variant, int64_t d, const void *x, const void *y,
                 const void *p0, const void *p1, rn_plan *plan);
+
+/* The plan of a strided call (ln_fwd_strided / rms_fwd_strided). */
+int rn_plan_for_strided(int dtype, int op, int variant, int64_t d, const void *x, int64_t ldx,
+                        const void *y, int64_t ldy, const void *p0, const void *p1,
+                        rn_plan *plan);
 
 /* rn_plan_for for a storage type (host-only). */
 int rn_plan_for_typed(int dtype, int op, int variant, int64_t d, const void *x, const void *y,

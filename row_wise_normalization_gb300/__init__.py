@@ -42,7 +42,7 @@ def _dtype_code(t):
     return codes[t.dtype]
 
 
-def _check_f32_cuda(name, t, dtype=None):
+def _check_f32_cuda(name, t, dtype=None, contiguous=True):
     """Contiguous, of the expected dtype (FP32 unless given), and addressable
     by the GPU: a CUDA tensor or a pinned CPU tensor (which the kernel reads or
     writes over the host link)."""
@@ -55,8 +55,20 @@ def _check_f32_cuda(name, t, dtype=None):
     want = torch.float32 if dtype is None else dtype
     if t.dtype != want:
         raise TypeError(f"{name} must be {want}, got {t.dtype}")
-    if not t.is_contiguous():
+    if contiguous and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _rows_of(name, t, d):
+    """(rows, row stride) of x or y: a contiguous tensor of rows of d, or a
+    2-D tensor whose rows are d contiguous elements at a stride >= d (a column
+    block of a wider matrix)."""
+    if t.is_contiguous():
+        return (t.numel() // d if d else 0), d
+    if t.dim() == 2 and t.shape[1] == d and t.stride(1) == 1 and t.stride(0) >= d:
+        return t.shape[0], t.stride(0)
+    raise ValueError(f"{name} must be contiguous, or 2-D with unit column stride and a row "
+                     f"stride >= its width")
 
 
 def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, stream=None,
@@ -67,12 +79,14 @@ def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, s
     type; statistics are computed in FP32. Returns ``(y, mean, rstd)``: y like
     x; mean and rstd FP32 of shape x.shape[:-1]. Tensors are CUDA tensors or
     pinned CPU tensors (read or written by the kernel over the host link);
-    outputs not passed in are allocated where x lives.
+    outputs not passed in are allocated where x lives. x and y may also be
+    2-D row-strided views (``big[:, a:a + d]``): the kernels then read and
+    write the rows in place.
     """
     code = _dtype_code(x)
-    _check_f32_cuda("x", x, x.dtype)
+    _check_f32_cuda("x", x, x.dtype, contiguous=False)
     d = x.shape[-1]
-    rows = x.numel() // d if d else 0
+    rows, ldx = _rows_of("x", x, d)
     for n, t in (("gamma", gamma), ("beta", beta)):
         _check_f32_cuda(n, t, x.dtype)
         if t.numel() != d:
@@ -83,16 +97,22 @@ def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, s
         mean = _empty_like_home(x, x.shape[:-1])
     if rstd is None:
         rstd = _empty_like_home(x, x.shape[:-1])
-    _check_f32_cuda("y", y, x.dtype)
-    if y.numel() != x.numel():
+    _check_f32_cuda("y", y, x.dtype, contiguous=False)
+    if y.numel() != x.numel() or y.shape[-1] != d:
         raise ValueError("y must be shaped like x")
+    _, ldy = _rows_of("y", y, d)
     for n, t in (("mean", mean), ("rstd", rstd)):
         _check_f32_cuda(n, t)
         if t.numel() != rows:
             raise ValueError(f"{n} must have {rows} elements")
-    st = capi.ln_fwd_typed(code, variant, x.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
-                           y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), rows, d, float(eps),
-                           _stream_handle(x, stream))
+    if ldx == d and ldy == d:
+        st = capi.ln_fwd_typed(code, variant, x.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
+                               y.data_ptr(), mean.data_ptr(), rstd.data_ptr(), rows, d,
+                               float(eps), _stream_handle(x, stream))
+    else:
+        st = capi.ln_fwd_strided(code, variant, x.data_ptr(), ldx, gamma.data_ptr(),
+                                 beta.data_ptr(), y.data_ptr(), ldy, mean.data_ptr(),
+                                 rstd.data_ptr(), rows, d, float(eps), _stream_handle(x, stream))
     capi.check(st)
     return y, mean, rstd
 
@@ -100,21 +120,27 @@ def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, s
 def rms_fwd(x, w, eps: float = 1e-5, *, y=None, stream=None,
             variant: int = capi.RN_VARIANT_AUTO):
     """RMSNorm forward over the last dimension of ``x`` (float32, bfloat16 or
-    float16; w of the same type); returns y."""
+    float16; w of the same type); returns y. x and y may be 2-D row-strided
+    views, as in ln_fwd."""
     code = _dtype_code(x)
-    _check_f32_cuda("x", x, x.dtype)
+    _check_f32_cuda("x", x, x.dtype, contiguous=False)
     d = x.shape[-1]
-    rows = x.numel() // d if d else 0
+    rows, ldx = _rows_of("x", x, d)
     _check_f32_cuda("w", w, x.dtype)
     if w.numel() != d:
         raise ValueError(f"w must have {d} elements")
     if y is None:
         y = _empty_like_home(x, x.shape, x.dtype)
-    _check_f32_cuda("y", y, x.dtype)
-    if y.numel() != x.numel():
+    _check_f32_cuda("y", y, x.dtype, contiguous=False)
+    if y.numel() != x.numel() or y.shape[-1] != d:
         raise ValueError("y must be shaped like x")
-    st = capi.rms_fwd_typed(code, variant, x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, d,
-                            float(eps), _stream_handle(x, stream))
+    _, ldy = _rows_of("y", y, d)
+    if ldx == d and ldy == d:
+        st = capi.rms_fwd_typed(code, variant, x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, d,
+                                float(eps), _stream_handle(x, stream))
+    else:
+        st = capi.rms_fwd_strided(code, variant, x.data_ptr(), ldx, w.data_ptr(), y.data_ptr(),
+                                  ldy, rows, d, float(eps), _stream_handle(x, stream))
     capi.check(st)
     return y
 

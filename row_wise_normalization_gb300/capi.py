@@ -81,6 +81,10 @@ SIGNATURES = {
     "ln_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
     "rms_bwd": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
     "ln_bwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "ln_fwd_strided": (_INT, [_INT, _INT, _P, _I64, _P, _P, _P, _I64, _P, _P, _I64, _I64, _F, _P]),
+    "rms_fwd_strided": (_INT, [_INT, _INT, _P, _I64, _P, _P, _I64, _I64, _I64, _F, _P]),
+    "rn_plan_for_strided": (_INT, [_INT, _INT, _INT, _I64, _P, _I64, _P, _I64, _P, _P,
+                                   ctypes.POINTER(rn_plan)]),
     "rms_fwd_typed": (_INT, [_INT, _INT, _P, _P, _P, _I64, _I64, _F, _P]),
     "rn_plan_for_typed": (_INT, [_INT, _INT, _INT, _I64, _P, _P, _P, _P, ctypes.POINTER(rn_plan)]),
     "rn_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
@@ -145,6 +149,15 @@ def plan_typed(dtype: int, op: int, variant: int, d: int, x: int, y: int, p0: in
     """The kernel configuration a typed call would launch (host only)."""
     out = rn_plan()
     check(load().rn_plan_for_typed(dtype, op, variant, d, x, y, p0, p1, ctypes.byref(out)))
+    return out
+
+
+def plan_strided(dtype: int, op: int, variant: int, d: int, x: int, ldx: int, y: int, ldy: int,
+                 p0: int = 0, p1: int = 0) -> rn_plan:
+    """The kernel configuration a strided call would launch (host only)."""
+    out = rn_plan()
+    check(load().rn_plan_for_strided(dtype, op, variant, d, x, ldx, y, ldy, p0, p1,
+                                     ctypes.byref(out)))
     return out
 
 
@@ -234,3 +247,13 @@ def ln_bwd_noalloc(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, stream=
     nearly all of HBM, a loop that cannot take cudaFree's synchronisation).
     d <= RN_NOALLOC_MAX_D; calls that overlap on the GPU race on the scratch."""
     return load().ln_bwd_noalloc(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, stream)
+
+
+def ln_fwd_strided(dtype, variant, x, ldx, gamma, beta, y, ldy, mean, rstd, rows, d, eps,
+                   stream=0) -> int:
+    return load().ln_fwd_strided(dtype, variant, x, ldx, gamma, beta, y, ldy, mean, rstd, rows,
+                                 d, eps, stream)
+
+
+def rms_fwd_strided(dtype, variant, x, ldx, w, y, ldy, rows, d, eps, stream=0) -> int:
+    return load().rms_fwd_strided(dtype, variant, x, ldx, w, y, ldy, rows, d, eps, stream)

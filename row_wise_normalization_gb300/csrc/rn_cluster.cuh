@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
         int h, nv, tl, q0, nq;   // row layout and this CTA's quads [q0, q0 + nq)
     };
     auto load = [&](Slice& s, int64_t row) {
-        const float* xr = p.x + row * p.d;
+        const float* xr = p.x + row * p.ldx;
         if constexpr (AL) {
             s.h = 0;
             s.nv = d >> 2;
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
         }
 
         // ---- normalize and store from the held registers ----------------
-        float* yr = p.y + row * p.d;
+        float* yr = p.y + row * p.ldy;
         bool pa = true;
         if constexpr (!AL) {
             pa = ((((uintptr_t)p.p0 >> 2) + h) & 3) == 0;

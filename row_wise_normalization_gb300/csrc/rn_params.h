@@ -27,6 +27,8 @@ struct Params {
     float* rstd;       // may be NULL
     int64_t rows;
     int64_t d;
+    int64_t ldx, ldy;  // row strides of x and y, in elements (>= d; d when contiguous)
+    int64_t ldr, ldh;  // row strides of r and h
     float eps;
 };
 

@@ -164,9 +164,9 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     if (row >= p.rows) return;                       // the whole group leaves together
 
     HeldRow<VEC, SLOTS, RES> cur;
-    load_row<T, VEC, SLOTS, TPR, AL, RES>(cur, X + row * p.d, RES ? R + row * p.d : nullptr, d, t);
+    load_row<T, VEC, SLOTS, TPR, AL, RES>(cur, X + row * p.ldx, RES ? R + row * p.ldr : nullptr, d, t);
 
-    // Parameters held across rows (PP): every row has the phase of row 0.
+    // Parameters held across rows (PP, only with AL): every row is aligned.
     Vec<VEC> pg[PP ? SLOTS : 1], pb[(PP && OP == OP_LN) ? SLOTS : 1];
     float pge = 0.f, pbe = 0.f;
     if constexpr (PP) {
@@ -193,8 +193,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         HeldRow<VEC, SLOTS, RES> nxt;
         if constexpr (PF) {
             if (nrow < p.rows)
-                load_row<T, VEC, SLOTS, TPR, AL, RES>(nxt, X + nrow * p.d,
-                                                      RES ? R + nrow * p.d : nullptr, d, t);
+                load_row<T, VEC, SLOTS, TPR, AL, RES>(nxt, X + nrow * p.ldx,
+                                                      RES ? R + nrow * p.ldr : nullptr, d, t);
         }
         add_residual(cur);
         const int h = cur.h, nv = cur.nv, tl = cur.tl;
@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         }
 
         // ---- normalize and store from the held registers ----------------
-        T* yr = Y + row * p.d;
-        T* hr = RES && p.h ? H + row * p.d : nullptr;
+        T* yr = Y + row * p.ldy;
+        T* hr = RES && p.h ? H + row * p.ldh : nullptr;
         bool pa = true;   // parameter vectors 16-byte aligned at this row's phase
         if constexpr (VEC > 1 && !PP && !AL) {
             pa = aligned16(P0, h);
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         if constexpr (PF)
             cur = nxt;
         else
-            load_row<T, VEC, SLOTS, TPR, AL, RES>(cur, X + row * p.d, RES ? R + row * p.d : nullptr,
+            load_row<T, VEC, SLOTS, TPR, AL, RES>(cur, X + row * p.ldx, RES ? R + row * p.ldr : nullptr,
                                                   d, t);
     }
 }

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(TPB, 1) staged_kernel(const Params p) {
     // Issue the copy of my i-th row into stage i % STAGES (thread 0 only).
     auto issue = [&](int64_t i) {
         const int64_t row = first + i * stride;
-        const float* xr = p.x + row * p.d;
+        const float* xr = p.x + row * p.ldx;
         const int h = head_peel(xr, d);
         const int nv = (d - h) >> 2;
         const int s = (int)(i % STAGES);
@@ -168,8 +168,8 @@ __global__ void __launch_bounds__(TPB, 1) staged_kernel(const Params p) {
     int rot = 0;
     for (int64_t i = 0; i < nmine; ++i) {
         const int64_t row = first + i * stride;
-        const float* xr = p.x + row * p.d;
-        float* yr = p.y + row * p.d;
+        const float* xr = p.x + row * p.ldx;
+        float* yr = p.y + row * p.ldy;
         const int h = head_peel(xr, d);
         const int nv = (d - h) >> 2;
         const int tl = d - h - 4 * nv;

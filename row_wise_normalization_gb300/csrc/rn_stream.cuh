@@ -67,10 +67,10 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
 
     int it = 0;
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
-        const T* xr = X + row * d;
-        const T* rr = RES ? R + row * d : nullptr;
-        T* yr = Y + row * d;
-        T* hr = RES && p.h ? H + row * d : nullptr;
+        const T* xr = X + row * p.ldx;
+        const T* rr = RES ? R + row * p.ldr : nullptr;
+        T* yr = Y + row * p.ldy;
+        T* hr = RES && p.h ? H + row * p.ldh : nullptr;
         int h = 0, tl = 0;
         int64_t nv;
         if constexpr (VEC > 1) {

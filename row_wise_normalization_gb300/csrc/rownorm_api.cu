@@ -89,7 +89,17 @@ struct Request {
     int64_t rows;
     int64_t d;
     float eps;
+    // row strides in elements; 0 means contiguous (d). The strided entry
+    // points reject strides below d before they get here.
+    int64_t ldx = 0, ldy = 0;
 };
+
+int64_t ldx_of(const Request& q) { return q.ldx > 0 ? q.ldx : q.d; }
+int64_t ldy_of(const Request& q) { return q.ldy > 0 ? q.ldy : q.d; }
+
+// Elements from the first to the last element of a [rows][d] array with row
+// stride ld (0 if rows == 0).
+int64_t span(int64_t rows, int64_t d, int64_t ld) { return rows > 0 ? (rows - 1) * ld + d : 0; }
 
 // Vectors (of `vec` elements) a row of width d needs held, excluding the
 // scalars of an unaligned head and tail (fewer than 2 * vec).
@@ -156,20 +166,27 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
     // 16-byte vectors need every streamed array (x, y, and with a residual r
     // and h) in the same 16-byte phase, so that one head peel aligns them all;
     // otherwise every access is scalar.
+    // With row strides, rows keep that common phase when the strides agree
+    // modulo a vector (residual rows are contiguous: their stride is d).
     uintptr_t phase = addr(q.x) ^ addr(q.y);
     if (q.res) {
         phase |= addr(q.x) ^ addr(q.r);
         if (q.h) phase |= addr(q.x) ^ addr(q.h);
     }
     const bool f32 = q.dtype == DT_F32;
-    const int vec = (phase & 15u) == 0 ? 16 / dtype_size(q.dtype) : 1;
+    const int64_t vv = 16 / dtype_size(q.dtype);
+    const int64_t ldx = ldx_of(q), ldy = ldy_of(q);
+    const bool strides_agree =
+        (ldx - ldy) % vv == 0 && (!q.res || (ldx - d) % vv == 0);
+    const int vec = ((phase & 15u) == 0 && strides_agree) ? (int)vv : 1;
     const int64_t units = row_units(d, vec);
     const int maxs = max_slots(vec);
     pl->vec = vec;
     // Every row whole aligned vectors, parameters included.
     uintptr_t bases = addr(q.x) | addr(q.p0) | (q.op == OP_LN ? addr(q.p1) : 0);
     if (q.res) bases |= addr(q.r) | addr(q.h);
-    const bool al = vec > 1 && d % vec == 0 && (bases & 15u) == 0;
+    const bool al = vec > 1 && d % vec == 0 && (bases & 15u) == 0 && ldx % vec == 0 &&
+                    ldy % vec == 0;
 
     int v = variant;
     if (v == RN_VARIANT_AUTO) {
@@ -262,7 +279,10 @@ int validate(const Request& q) {
     if (q.dtype != DT_F32 && q.dtype != DT_BF16 && q.dtype != DT_F16) return RN_ERR_DTYPE;
     if (q.res && q.dtype != DT_F32) return RN_ERR_DTYPE;
     if (q.rows < 0 || q.d <= 0) return RN_ERR_SIZE;
-    if (q.rows > 0 && q.d > kMaxElems / q.rows) return RN_ERR_SIZE;
+    const int64_t ldx = ldx_of(q), ldy = ldy_of(q);
+    if (ldx < q.d || ldy < q.d) return RN_ERR_SIZE;
+    const int64_t ldmax = ldx > ldy ? ldx : ldy;
+    if (q.rows > 0 && (q.rows - 1) > (kMaxElems - q.d) / ldmax) return RN_ERR_SIZE;
     if (!std::isfinite(q.eps) || q.eps < 0.f) return RN_ERR_EPS;
     if (q.rows == 0) return RN_OK;
     if (!q.x || !q.y || !q.p0 || (q.op == OP_LN && !q.p1) || (q.res && !q.r)) return RN_ERR_NULL;
@@ -271,12 +291,14 @@ int validate(const Request& q) {
     for (const void* p : data)
         if (misaligned(p, es)) return RN_ERR_ALIGN;
     if (misaligned(q.mean, 4) || misaligned(q.rstd, 4)) return RN_ERR_ALIGN;
-    const int64_t nx = q.rows * q.d * es, np = q.d * es, ns = q.rows * 4;
+    // spans from the first to the last element (strided rows: the gaps count)
+    const int64_t nx = span(q.rows, q.d, ldx) * es, ny = span(q.rows, q.d, ldy) * es;
+    const int64_t nd = q.rows * q.d * es, np = q.d * es, ns = q.rows * 4;
     // outputs against inputs and against each other
     const void* outs[4] = {q.y, q.h, q.mean, q.rstd};
-    const int64_t nouts[4] = {nx, nx, ns, ns};
+    const int64_t nouts[4] = {ny, nd, ns, ns};
     const void* ins[4] = {q.x, q.r, q.p0, q.p1};
-    const int64_t nins[4] = {nx, nx, np, np};
+    const int64_t nins[4] = {nx, nd, np, np};
     for (int i = 0; i < 4; ++i) {
         for (int j = 0; j < 4; ++j)
             if (overlaps(outs[i], nouts[i], ins[j], nins[j])) return RN_ERR_ALIAS;
@@ -375,6 +397,10 @@ int run(const Request& q, int variant, void* stream) {
     prm.rstd = q.rstd;
     prm.rows = q.rows;
     prm.d = q.d;
+    prm.ldx = ldx_of(q);
+    prm.ldy = ldy_of(q);
+    prm.ldr = q.d;
+    prm.ldh = q.d;
     prm.eps = q.eps;
     const cudaStream_t s = (cudaStream_t)stream;
 
@@ -696,8 +722,30 @@ int rms_fwd_typed(int dtype, int variant, const void* x, const void* w, void* y,
                variant, stream);
 }
 
+int ln_fwd_strided(int dtype, int variant, const void* x, int64_t ldx, const void* gamma,
+                   const void* beta, void* y, int64_t ldy, float* mean_out, float* rstd_out,
+                   int64_t rows, int64_t d, float eps, void* stream) {
+    if (ldx < d || ldy < d || ldx <= 0) return RN_ERR_SIZE;
+    Request q = ln_request((const float*)x, nullptr, (const float*)gamma, (const float*)beta,
+                           nullptr, (float*)y, mean_out, rstd_out, rows, d, eps, false, dtype);
+    q.ldx = ldx;
+    q.ldy = ldy;
+    return run(q, variant, stream);
+}
+
+int rms_fwd_strided(int dtype, int variant, const void* x, int64_t ldx, const void* w, void* y,
+                    int64_t ldy, int64_t rows, int64_t d, float eps, void* stream) {
+    if (ldx < d || ldy < d || ldx <= 0) return RN_ERR_SIZE;
+    Request q = rms_request((const float*)x, nullptr, (const float*)w, nullptr, (float*)y, rows, d,
+                           eps, false, dtype);
+    q.ldx = ldx;
+    q.ldy = ldy;
+    return run(q, variant, stream);
+}
+
 static int plan_any(int dtype, int op, int variant, int64_t d, const void* x, const void* res,
-                    const void* h, const void* y, const void* p0, const void* p1, rn_plan* plan) {
+                    const void* h, const void* y, const void* p0, const void* p1, rn_plan* plan,
+                    int64_t ldx = 0, int64_t ldy = 0) {
     if (!plan) return RN_ERR_NULL;
     if (op != RN_OP_LN && op != RN_OP_RMS) return RN_ERR_VARIANT;
     if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
@@ -718,6 +766,11 @@ static int plan_any(int dtype, int op, int variant, int64_t d, const void* x, co
               1,
               d,
               0.f};
+    if (ldx != 0 || ldy != 0) {
+        if (ldx < d || ldy < d) return RN_ERR_SIZE;
+        q.ldx = ldx;
+        q.ldy = ldy;
+    }
     return plan_impl(q, variant, plan);
 }
 
@@ -732,6 +785,13 @@ int rn_plan_for_typed(int dtype, int op, int variant, int64_t d, const void* x, 
     return plan_any(dtype, op, variant, d, x, nullptr, nullptr, y, p0, p1, plan);
 }
 
+int rn_plan_for_strided(int dtype, int op, int variant, int64_t d, const void* x, int64_t ldx,
+                        const void* y, int64_t ldy, const void* p0, const void* p1,
+                        rn_plan* plan) {
+    if (ldx <= 0 || ldy <= 0) return RN_ERR_SIZE;
+    return plan_any(dtype, op, variant, d, x, nullptr, nullptr, y, p0, p1, plan, ldx, ldy);
+}
+
 int rn_plan_for(int op, int variant, int64_t d, const void* x, const void* y, const void* p0,
                 const void* p1, rn_plan* plan) {
     return rn_plan_for_residual(op, variant, d, x, nullptr, nullptr, y, p0, p1, plan);
@@ -741,7 +801,8 @@ const char* rn_status_str(int status) {
     switch (status) {
         case RN_OK: return "ok";
         case RN_ERR_NULL: return "a required pointer is NULL";
-        case RN_ERR_SIZE: return "invalid size (rows < 0, d <= 0 or rows*d too large)";
+        case RN_ERR_SIZE:
+            return "invalid size (rows < 0, d <= 0, rows*d too large or a row stride below d)";
         case RN_ERR_EPS: return "eps must be finite and >= 0";
         case RN_ERR_ALIAS: return "an output overlaps an input or another output";
         case RN_ERR_CUDA: return "CUDA runtime error (see rn_last_cuda_error)";

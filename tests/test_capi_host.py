@@ -236,3 +236,48 @@ def test_typed_plans_and_validation(lib):
     # statistics stay FP32: 4-byte alignment even with 16-bit data
     assert capi.ln_fwd_typed(capi.RN_DTYPE_BF16, 0, X, X + 0x100000, X + 0x200000, Y,
                              X + 0x300002, 0, 4, 8, 1e-5, 0) == capi.RN_ERR_ALIGN
+
+
+def test_strided_plans_and_validation(lib):
+    X, Y = A, A + 0x1000000
+    F32, BF16 = capi.RN_DTYPE_F32, capi.RN_DTYPE_BF16
+    LN, AUTO = capi.RN_OP_LN, capi.RN_VARIANT_AUTO
+    # a column block of a wider matrix: strides a multiple of 4, everything aligned
+    p = capi.plan_strided(F32, LN, AUTO, 768, X, 3 * 768, Y, 768, X, X)
+    assert (p.variant, p.vec, p.aligned) == (capi.RN_VARIANT_WARP, 4, 1)
+    # strides that agree modulo 4 but are not multiples of 4: vector path with head peel
+    p = capi.plan_strided(F32, LN, AUTO, 768, X, 771, Y, 775, X, X)
+    assert (p.vec, p.aligned) == (4, 0)
+    # strides that disagree modulo 4: rows change relative phase, scalar path
+    p = capi.plan_strided(F32, LN, AUTO, 768, X, 770, Y, 768, X, X)
+    assert p.vec == 1
+    # 16-bit: agreement modulo 8 elements
+    p = capi.plan_strided(BF16, LN, AUTO, 1024, X, 1032, Y, 1024, X, X)
+    assert (p.vec, p.aligned) == (8, 1)
+    p = capi.plan_strided(BF16, LN, AUTO, 1024, X, 1028, Y, 1024, X, X)
+    assert p.vec == 1
+    # wide rows keep their variants when the phases agree
+    p = capi.plan_strided(F32, LN, AUTO, 65536, X, 65540, Y, 65536, X, X)
+    assert p.variant == capi.RN_VARIANT_CLUSTER
+    p = capi.plan_strided(F32, LN, capi.RN_VARIANT_STAGED, 20000, X, 20004, Y, 20000, X, X)
+    assert p.variant == capi.RN_VARIANT_STAGED
+    with pytest.raises(capi.RowNormError):
+        capi.plan_strided(F32, LN, capi.RN_VARIANT_STAGED, 20000, X, 20002, Y, 20000, X, X)
+    with pytest.raises(capi.RowNormError):
+        capi.plan_strided(F32, LN, AUTO, 768, X, 700, Y, 768, X, X)
+    G, B, M, S = X + 0x2000000, X + 0x2100000, X + 0x2200000, X + 0x2300000
+    # strides below d are rejected before anything runs
+    assert capi.ln_fwd_strided(F32, AUTO, X, 767, G, B, Y, 768, M, S, 4, 768, 1e-5,
+                               0) == capi.RN_ERR_SIZE
+    assert capi.ln_fwd_strided(F32, AUTO, X, 768, G, B, Y, 0, M, S, 4, 768, 1e-5,
+                               0) == capi.RN_ERR_SIZE
+    assert capi.rms_fwd_strided(F32, AUTO, X, -4, G, Y, 768, 4, 768, 1e-5, 0) == capi.RN_ERR_SIZE
+    # spans: y interleaved with x's rows (y = x + d, both with stride 2d) is an alias
+    assert capi.ln_fwd_strided(F32, AUTO, X, 1536, G, B, X + 4 * 768, 1536, M, S, 4, 768, 1e-5,
+                               0) == capi.RN_ERR_ALIAS
+    # a stride that makes the span overflow
+    assert capi.ln_fwd_strided(F32, AUTO, X, 1 << 60, G, B, Y, 768, M, S, 16, 768, 1e-5,
+                               0) == capi.RN_ERR_SIZE
+    # empty batch: nothing runs
+    assert capi.ln_fwd_strided(F32, AUTO, 0, 1000, 0, 0, 0, 1000, 0, 0, 0, 768, 1e-5,
+                               0) == capi.RN_OK
