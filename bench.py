@@ -16,7 +16,8 @@ the host cores (``cpu_baseline``), the warm-L2 and CUDA-graph numbers of the
 headline shape, the empty-kernel launch floor, a same-session
 device-to-device copy, the large / sweep shapes (cold L2) for both
 LayerNorm and RMSNorm, the fused residual add against add-then-normalise,
-BF16/FP16 storage, and the backward (dx plus parameter gradients).
+BF16/FP16 storage, the backward (dx plus parameter gradients), and 64 small
+problems as single calls, a CUDA graph of them and one batched call.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -350,6 +351,26 @@ def cpu_baseline_leg(case_wl, gpu_result=None, seconds=10.0):
             "host_cores_available": len(os.sched_getaffinity(0))}, parity
 
 
+def rank_workload(base: workloads.Workload, rank: int) -> workloads.Workload:
+    """Weak scaling: every rank normalises its own batch of the base shape;
+    the rows are independent, so a rank's batch is just other seeded data
+    (seed shifted by 1000 per rank) and no data crosses ranks."""
+    return workloads.Workload(base.op, base.rows, base.d, base.seed + 1000 * rank, base.x_dist,
+                              base.x_std, base.eps, tag=base.tag)
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time (one all-reduce of a scalar; not on the data
+    path). Without a process group, the value itself."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -368,10 +389,7 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
-    seed_shift = 1000 * rank
-    base = pick_workload(args.workload)
-    wl = workloads.Workload(base.op, base.rows, base.d, base.seed + seed_shift,
-                            base.x_dist, base.x_std, base.eps, tag=base.tag)
+    wl = rank_workload(pick_workload(args.workload), rank)
     case = LnCase(torch, wl, device)
     flush = Flusher(torch, device)
     sampler = ClockSampler(local_rank) if rank == 0 else None
@@ -400,11 +418,7 @@ def run_ours(args, rank, world, local_rank):
                 case.launch()
             torch.cuda.synchronize()
         sampler.mark("timed", t0, time.time())
-    step_ms = statistics.fmean(times)
-    if dist is not None:
-        tt = torch.tensor([step_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = max_over_ranks(statistics.fmean(times), dist, device)
     value = gbs(case.bytes * world, step_ms)
 
     # ---- e2e through the public API with pinned host buffers ----------------
@@ -448,11 +462,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     if sampler:
         sampler.mark("e2e", t2, time.time())
-    e2e_ms = statistics.fmean(e2e_times)
-    if dist is not None:
-        tt = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(statistics.fmean(e2e_times), dist, device)
     # the host-resident result must equal the device-resident one (same x)
     e2e_match = bool(torch.equal(yh, case.y.cpu()))
     for _ in range(3):
@@ -614,6 +624,53 @@ def run_ours(args, rank, world, local_rank):
                         "launches_per_call": 2})
             del xt, dyt, dxt, wst
         extra["backward_cold_l2"] = bwd
+
+        # 64 small problems (LayerNorm 512x128 each): 64 single calls, the
+        # same 64 calls replayed from a CUDA graph, and one batched call
+        nprob, rows_, d_ = 64, 512, 128
+        probs = []
+        for i in range(nprob):
+            xw = workloads.Workload("ln", rows_, d_, seed=70 + i)
+            xt = torch.from_numpy(xw.x()).to(device)
+            gt, bt = (torch.from_numpy(p_).to(device) for p_ in xw.params())
+            probs.append((xt, gt, bt, torch.empty_like(xt), torch.empty(rows_, device=device),
+                          torch.empty(rows_, device=device)))
+        table = capi.problems([(x_.data_ptr(), g_.data_ptr(), b_.data_ptr(), y_.data_ptr(),
+                                m_.data_ptr(), s_.data_ptr(), rows_, d_)
+                               for x_, g_, b_, y_, m_, s_ in probs])
+        eps32 = float(np.float32(1e-5))
+
+        def singles():
+            s_ = torch.cuda.current_stream().cuda_stream
+            for x_, g_, b_, y_, m_, r_ in probs:
+                capi.ln_fwd(x_.data_ptr(), g_.data_ptr(), b_.data_ptr(), y_.data_ptr(),
+                            m_.data_ptr(), r_.data_ptr(), rows_, d_, eps32, s_)
+
+        def batched():
+            capi.ln_fwd_batched(capi.RN_DTYPE_F32, table, nprob, eps32,
+                                torch.cuda.current_stream().cuda_stream)
+
+        singles()
+        batched()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            singles()
+        tiny = {}
+        for name, f in (("single_calls", singles), ("graph_of_single_calls", graph.replay),
+                        ("batched_call", batched)):
+            for _ in range(3):
+                flush()
+                f()
+            tiny[name + "_us"] = 1e3 * statistics.median(time_launches(torch, f, args.sweep_steps,
+                                                                        flush))
+        nb = nprob * algorithmic_bytes("ln", rows_, d_)
+        tiny.update({"workload": f"{nprob} x ln_{rows_}x{d_}", "cold_l2": True,
+                     "batched_GBps": gbs(nb, tiny["batched_call_us"] / 1e3),
+                     "launches": {"single_calls": nprob, "graph_of_single_calls": nprob,
+                                  "batched_call": 1}})
+        extra["many_small_problems"] = tiny
+        del probs, graph
 
     clocks = None
     if sampler:

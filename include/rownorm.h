@@ -170,6 +170,38 @@ int rms_fwd_strided(int dtype, int variant, const void *x, int64_t ldx, const vo
                     int64_t ldy, int64_t rows, int64_t d, float eps, void *stream);
 
 /*
+ * Many small problems in one launch. A tensor of a few hundred KB is
+ * normalised in a few microseconds of DRAM time but pays a whole kernel
+ * launch; a step that normalises many of them is launch-bound (the RMSNorm
+ * page times its kernels inside CUDA graphs of 64 launches for this reason:
+ * "RMSNorm on an RTX 5070 ...", section "What the timer included"). These
+ * entry points take `count` independent problems, each as ln_fwd_typed /
+ * rms_fwd_typed would (contiguous rows, one storage type `dtype` and one eps
+ * for all), and run every problem of width d <= 1024 whose x and y share a
+ * 16-byte phase in one launch per 128 such problems; the others get launches
+ * of their own (the same kernels ln_fwd_typed would pick), on the same
+ * stream. `problems` is host memory, read during the call only. Each
+ * problem is validated as its single call would be, and no problem may
+ * write what another reads or writes (RN_ERR_ALIAS); nothing runs unless all
+ * pass. Results are those of the single calls, bit for bit, for problems of
+ * width <= 1024.
+ */
+typedef struct rn_problem {
+    const void *x;      /* [rows][d] */
+    const void *p0;     /* gamma (LN) or w (RMS), [d] */
+    const void *p1;     /* beta (LN), [d]; ignored by RMS */
+    void *y;            /* [rows][d] */
+    float *mean_out;    /* LN: [rows] FP32, may be NULL; ignored by RMS */
+    float *rstd_out;    /* LN: [rows] FP32, may be NULL; ignored by RMS */
+    int64_t rows;
+    int64_t d;
+} rn_problem;
+
+int ln_fwd_batched(int dtype, const rn_problem *problems, int count, float eps, void *stream);
+
+int rms_fwd_batched(int dtype, const rn_problem *problems, int count, float eps, void *stream);
+
+/*
  * Backward (FP32). The pages list backward passes as untested; these are the
  * derivatives of the forward definitions above.
  *

@@ -11,8 +11,8 @@ from __future__ import annotations
 from . import capi
 from .capi import RowNormError, load  # noqa: F401
 
-__all__ = ["ln_fwd", "rms_fwd", "ln_fwd_residual", "rms_fwd_residual", "ln_bwd", "rms_bwd",
-           "capi", "RowNormError", "load"]
+__all__ = ["ln_fwd", "rms_fwd", "ln_fwd_residual", "rms_fwd_residual", "ln_fwd_batched",
+           "rms_fwd_batched", "ln_bwd", "rms_bwd", "capi", "RowNormError", "load"]
 
 
 def _stream_handle(t, stream):
@@ -143,6 +143,53 @@ def rms_fwd(x, w, eps: float = 1e-5, *, y=None, stream=None,
                                   ldy, rows, d, float(eps), _stream_handle(x, stream))
     capi.check(st)
     return y
+
+
+def _batched(op, problems, eps, stream):
+    if not problems:
+        return []
+    x0 = problems[0][0]
+    code = _dtype_code(x0)
+    items, outs = [], []
+    for k, pr in enumerate(problems):
+        x, params = pr[0], pr[1:]
+        _check_f32_cuda(f"problem {k} x", x, x0.dtype)
+        d = x.shape[-1]
+        rows = x.numel() // d if d else 0
+        for t in params:
+            _check_f32_cuda(f"problem {k} parameter", t, x0.dtype)
+            if t.numel() != d:
+                raise ValueError(f"problem {k}: parameters must have {d} elements")
+        y = _empty_like_home(x, x.shape, x.dtype)
+        if op == capi.RN_OP_LN:
+            mean = _empty_like_home(x, x.shape[:-1])
+            rstd = _empty_like_home(x, x.shape[:-1])
+            items.append((x.data_ptr(), params[0].data_ptr(), params[1].data_ptr(), y.data_ptr(),
+                          mean.data_ptr(), rstd.data_ptr(), rows, d))
+            outs.append((y, mean, rstd))
+        else:
+            items.append((x.data_ptr(), params[0].data_ptr(), 0, y.data_ptr(), 0, 0, rows, d))
+            outs.append(y)
+    fn = capi.ln_fwd_batched if op == capi.RN_OP_LN else capi.rms_fwd_batched
+    capi.check(fn(code, capi.problems(items), len(items), float(eps), _stream_handle(x0, stream)))
+    return outs
+
+
+def ln_fwd_batched(problems, eps: float = 1e-5, *, stream=None):
+    """LayerNorm of many small tensors in as few launches as possible.
+
+    ``problems``: a sequence of ``(x, gamma, beta)``, contiguous, all of one
+    dtype (float32, bfloat16 or float16). Returns a list of ``(y, mean,
+    rstd)``, one per problem. Problems of width <= 1024 share one launch per
+    128; wider ones get their own.
+    """
+    return _batched(capi.RN_OP_LN, problems, eps, stream)
+
+
+def rms_fwd_batched(problems, eps: float = 1e-5, *, stream=None):
+    """RMSNorm of many small tensors: ``problems`` is a sequence of ``(x, w)``;
+    returns the list of y."""
+    return _batched(capi.RN_OP_RMS, problems, eps, stream)
 
 
 def _check_like(name, t, numel):

@@ -59,6 +59,13 @@ class rn_plan(ctypes.Structure):
                 ("cluster", _INT)]
 
 
+class rn_problem(ctypes.Structure):
+    """One problem of ln_fwd_batched / rms_fwd_batched (pointers as ints)."""
+    _fields_ = [("x", ctypes.c_void_p), ("p0", ctypes.c_void_p), ("p1", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("mean_out", ctypes.c_void_p),
+                ("rstd_out", ctypes.c_void_p), ("rows", ctypes.c_int64), ("d", ctypes.c_int64)]
+
+
 SIGNATURES = {
     "ln_fwd": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P]),
     "rms_fwd": (_INT, [_P, _P, _P, _I64, _I64, _F, _P]),
@@ -81,6 +88,8 @@ SIGNATURES = {
     "ln_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
     "rms_bwd": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
     "ln_bwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "ln_fwd_batched": (_INT, [_INT, ctypes.POINTER(rn_problem), _INT, _F, _P]),
+    "rms_fwd_batched": (_INT, [_INT, ctypes.POINTER(rn_problem), _INT, _F, _P]),
     "ln_fwd_strided": (_INT, [_INT, _INT, _P, _I64, _P, _P, _P, _I64, _P, _P, _I64, _I64, _F, _P]),
     "rms_fwd_strided": (_INT, [_INT, _INT, _P, _I64, _P, _P, _I64, _I64, _I64, _F, _P]),
     "rn_plan_for_strided": (_INT, [_INT, _INT, _INT, _I64, _P, _I64, _P, _I64, _P, _P,
@@ -257,3 +266,20 @@ def ln_fwd_strided(dtype, variant, x, ldx, gamma, beta, y, ldy, mean, rstd, rows
 
 def rms_fwd_strided(dtype, variant, x, ldx, w, y, ldy, rows, d, eps, stream=0) -> int:
     return load().rms_fwd_strided(dtype, variant, x, ldx, w, y, ldy, rows, d, eps, stream)
+
+
+def problems(items) -> "ctypes.Array":
+    """A ctypes array of rn_problem from (x, p0, p1, y, mean, rstd, rows, d)
+    tuples of ints."""
+    arr = (rn_problem * max(len(items), 1))()
+    for i, it in enumerate(items):
+        arr[i] = rn_problem(*it)
+    return arr
+
+
+def ln_fwd_batched(dtype, probs, count, eps, stream=0) -> int:
+    return load().ln_fwd_batched(dtype, probs, count, eps, stream)
+
+
+def rms_fwd_batched(dtype, probs, count, eps, stream=0) -> int:
+    return load().rms_fwd_batched(dtype, probs, count, eps, stream)

@@ -94,6 +94,36 @@ const ClusterEntry* cluster_entry(int op, int slots, int threads, int cl, bool a
 constexpr int kMaxCluster = 16;
 constexpr int kClusterMaxQuads = 1024 * 8 * kMaxCluster;   // 524288 floats per row
 
+// Batched small problems (rn_batched.cuh): one launch over the rows of up to
+// kBatchMax independent problems of width <= kBatchMaxD whose x and y share a
+// 16-byte phase. The table is the kernel's (__grid_constant__) parameter.
+constexpr int kBatchMax = 128;
+constexpr int kBatchMaxD = 1024;
+constexpr int kBatchThreads = 128;
+struct BatchProblem {
+    const void* x;     // [rows][d], contiguous
+    const void* p0;    // gamma or w
+    const void* p1;    // beta (LN) or NULL
+    void* y;
+    float* mean;       // may be NULL
+    float* rstd;       // may be NULL
+    int64_t rows;
+    int64_t d;
+};
+struct BatchParams {
+    int n;                         // problems in the table (>= 1, each with rows > 0)
+    float eps;
+    int64_t start[kBatchMax + 1];  // start[k]: first global row of problem k
+    BatchProblem pr[kBatchMax];
+};
+struct BatchEntry {
+    const void* fn;
+    int threads;
+    cudaError_t (*launch)(const BatchParams&, int grid, cudaStream_t);
+};
+// slots: vectors per lane, 1, 2, 4 or 8 (FP32) / 1, 2 or 4 (16-bit).
+const BatchEntry* batched_entry(int op, int dtype, int slots);
+
 // Arguments of the backward kernels (rn_bwd.cuh).
 struct BwdParams {
     const float* dy;

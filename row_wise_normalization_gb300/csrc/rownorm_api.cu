@@ -448,6 +448,149 @@ Request rms_request(const float* x, const float* res, const float* w, float* h, 
 }
 
 // ---------------------------------------------------------------------------
+// Batched small problems.
+// ---------------------------------------------------------------------------
+int batch_resident(const BatchEntry* e, cudaError_t* err) {
+    struct Cache {
+        const BatchEntry* e;
+        int dev;
+        int n;
+    };
+    static thread_local Cache cache[8];
+    static thread_local int cache_next = 0;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return 0;
+    for (auto& c : cache)
+        if (c.e == e && c.dev == dev && c.n > 0) return c.n;
+    int sms = 0, per = 0;
+    *err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (*err != cudaSuccess) return 0;
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, e->fn, e->threads, 0);
+    if (*err != cudaSuccess) return 0;
+    if (per < 1) {
+        *err = cudaErrorInvalidConfiguration;
+        return 0;
+    }
+    cache[cache_next] = {e, dev, per * sms};
+    cache_next = (cache_next + 1) % 8;
+    return per * sms;
+}
+
+Request problem_request(int op, int dtype, const rn_problem& pr, float eps) {
+    Request q = op == OP_LN
+                    ? ln_request((const float*)pr.x, nullptr, (const float*)pr.p0,
+                                 (const float*)pr.p1, nullptr, (float*)pr.y, pr.mean_out,
+                                 pr.rstd_out, pr.rows, pr.d, eps, false, dtype)
+                    : rms_request((const float*)pr.x, nullptr, (const float*)pr.p0, nullptr,
+                                  (float*)pr.y, pr.rows, pr.d, eps, false, dtype);
+    return q;
+}
+
+// Byte ranges a problem reads and writes.
+void problem_ranges(int op, int dtype, const rn_problem& pr, const void* in[3], int64_t nin[3],
+                    const void* out[3], int64_t nout[3]) {
+    const int64_t es = dtype_size(dtype), n = pr.rows * pr.d * es;
+    in[0] = pr.x;
+    nin[0] = n;
+    in[1] = pr.p0;
+    nin[1] = pr.d * es;
+    in[2] = op == OP_LN ? pr.p1 : nullptr;
+    nin[2] = pr.d * es;
+    out[0] = pr.y;
+    nout[0] = n;
+    out[1] = op == OP_LN ? pr.mean_out : nullptr;
+    nout[1] = pr.rows * 4;
+    out[2] = op == OP_LN ? pr.rstd_out : nullptr;
+    nout[2] = pr.rows * 4;
+}
+
+int run_batched(int op, int dtype, const rn_problem* prs, int count, float eps, void* stream) {
+    if (count < 0) return RN_ERR_SIZE;
+    if (count == 0) return RN_OK;
+    if (!prs) return RN_ERR_NULL;
+    if (dtype != DT_F32 && dtype != DT_BF16 && dtype != DT_F16) return RN_ERR_DTYPE;
+    if (!std::isfinite(eps) || eps < 0.f) return RN_ERR_EPS;
+    // every problem on its own, then no problem writing what another touches
+    for (int i = 0; i < count; ++i) {
+        const int st = validate(problem_request(op, dtype, prs[i], eps));
+        if (st != RN_OK) return st;
+    }
+    for (int i = 0; i < count; ++i) {
+        if (prs[i].rows == 0) continue;
+        const void *ii[3], *io[3];
+        int64_t nii[3], nio[3];
+        problem_ranges(op, dtype, prs[i], ii, nii, io, nio);
+        for (int j = i + 1; j < count; ++j) {
+            if (prs[j].rows == 0) continue;
+            const void *ji[3], *jo[3];
+            int64_t nji[3], njo[3];
+            problem_ranges(op, dtype, prs[j], ji, nji, jo, njo);
+            for (int a = 0; a < 3; ++a)
+                for (int b = 0; b < 3; ++b)
+                    if (overlaps(io[a], nio[a], ji[b], nji[b]) ||
+                        overlaps(jo[a], njo[a], ii[b], nii[b]) ||
+                        overlaps(io[a], nio[a], jo[b], njo[b]))
+                        return RN_ERR_ALIAS;
+        }
+    }
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t err = cudaSuccess;
+    const int vec = 16 / dtype_size(dtype);
+    BatchParams bp;
+    bp.n = 0;
+    bp.eps = eps;
+    bp.start[0] = 0;
+    int64_t widest = 0;   // vectors per row of the table's widest problem
+    auto flush = [&]() -> int {
+        if (bp.n == 0) return RN_OK;
+        // the fewest vectors per lane (1, 2, 4, 8) that hold the widest row
+        int slots = 1;
+        while ((int64_t)slots * 32 < widest) slots *= 2;
+        const BatchEntry* e = batched_entry(op, dtype, slots);
+        if (!e) return RN_ERR_VARIANT;
+        const int resident = batch_resident(e, &err);
+        if (err != cudaSuccess) return fail_cuda(err);
+        widest = 0;
+        const int64_t rows = bp.start[bp.n];
+        const int64_t rows_per_cta = e->threads / 32;
+        const int64_t want = (rows + rows_per_cta - 1) / rows_per_cta;
+        err = e->launch(bp, (int)(want < resident ? want : resident), s);
+        bp.n = 0;
+        return err == cudaSuccess ? RN_OK : fail_cuda(err);
+    };
+    for (int i = 0; i < count; ++i) {
+        const rn_problem& pr = prs[i];
+        if (pr.rows == 0) continue;
+        const bool same_phase = ((addr(pr.x) ^ addr(pr.y)) & 15u) == 0;
+        if (pr.d > kBatchMaxD || !same_phase) {
+            // wide rows, or x and y in different 16-byte phases: own launch
+            const int st = run(problem_request(op, dtype, pr, eps), RN_VARIANT_AUTO, stream);
+            if (st != RN_OK) return st;
+            continue;
+        }
+        BatchProblem& b = bp.pr[bp.n];
+        b.x = pr.x;
+        b.p0 = pr.p0;
+        b.p1 = op == OP_LN ? pr.p1 : nullptr;
+        b.y = pr.y;
+        b.mean = op == OP_LN ? pr.mean_out : nullptr;
+        b.rstd = op == OP_LN ? pr.rstd_out : nullptr;
+        b.rows = pr.rows;
+        b.d = pr.d;
+        if (pr.d / vec > widest) widest = pr.d / vec;
+        bp.start[bp.n + 1] = bp.start[bp.n] + pr.rows;
+        ++bp.n;
+        if (bp.n == kBatchMax) {
+            const int st = flush();
+            if (st != RN_OK) return st;
+            bp.start[0] = 0;
+        }
+    }
+    return flush();
+}
+
+// ---------------------------------------------------------------------------
 // Backward.
 // ---------------------------------------------------------------------------
 struct BwdRequest {
@@ -741,6 +884,14 @@ int rms_fwd_strided(int dtype, int variant, const void* x, int64_t ldx, const vo
     q.ldx = ldx;
     q.ldy = ldy;
     return run(q, variant, stream);
+}
+
+int ln_fwd_batched(int dtype, const rn_problem* problems, int count, float eps, void* stream) {
+    return run_batched(OP_LN, dtype, problems, count, eps, stream);
+}
+
+int rms_fwd_batched(int dtype, const rn_problem* problems, int count, float eps, void* stream) {
+    return run_batched(OP_RMS, dtype, problems, count, eps, stream);
 }
 
 static int plan_any(int dtype, int op, int variant, int64_t d, const void* x, const void* res,

@@ -281,3 +281,34 @@ def test_strided_plans_and_validation(lib):
     # empty batch: nothing runs
     assert capi.ln_fwd_strided(F32, AUTO, 0, 1000, 0, 0, 0, 1000, 0, 0, 0, 768, 1e-5,
                                0) == capi.RN_OK
+
+
+def test_batched_validation_without_launch(lib):
+    X = A
+    F32 = capi.RN_DTYPE_F32
+    ok = (X, X + 0x100000, X + 0x200000, X + 0x300000, 0, 0, 4, 64)
+    assert capi.ln_fwd_batched(F32, capi.problems([]), 0, 1e-5, 0) == capi.RN_OK
+    assert capi.ln_fwd_batched(F32, capi.problems([ok]), -1, 1e-5, 0) == capi.RN_ERR_SIZE
+    assert capi.ln_fwd_batched(F32, None, 3, 1e-5, 0) == capi.RN_ERR_NULL
+    assert capi.ln_fwd_batched(7, capi.problems([ok]), 1, 1e-5, 0) == capi.RN_ERR_DTYPE
+    assert capi.ln_fwd_batched(F32, capi.problems([ok]), 1, -1.0, 0) == capi.RN_ERR_EPS
+    # a bad problem anywhere stops the whole call before anything runs
+    bad_null = (0, X + 0x100000, X + 0x200000, X + 0x400000, 0, 0, 4, 64)
+    assert capi.ln_fwd_batched(F32, capi.problems([ok, bad_null]), 2, 1e-5,
+                               0) == capi.RN_ERR_NULL
+    bad_size = (X + 0x500000, X + 0x100000, X + 0x200000, X + 0x600000, 0, 0, 4, 0)
+    assert capi.ln_fwd_batched(F32, capi.problems([ok, bad_size]), 2, 1e-5,
+                               0) == capi.RN_ERR_SIZE
+    # problem 2 writes problem 1's input
+    clash = (X + 0x700000, X + 0x100000, X + 0x200000, X + 16, 0, 0, 4, 64)
+    assert capi.ln_fwd_batched(F32, capi.problems([ok, clash]), 2, 1e-5,
+                               0) == capi.RN_ERR_ALIAS
+    # two problems writing the same y
+    twin = (X + 0x800000, X + 0x100000, X + 0x200000, X + 0x300000, 0, 0, 4, 64)
+    assert capi.rms_fwd_batched(F32, capi.problems([ok, twin]), 2, 1e-5,
+                                0) == capi.RN_ERR_ALIAS
+    # sharing read-only parameters is fine (only checked here up to validation:
+    # rows == 0 problems run nothing)
+    empty = [(X + 0x900000 * (i + 1), X + 0x100000, X + 0x200000, X + 0x300000 + 0x900000 * (i + 1),
+              0, 0, 0, 64) for i in range(3)]
+    assert capi.ln_fwd_batched(F32, capi.problems(empty), 3, 1e-5, 0) == capi.RN_OK
