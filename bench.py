@@ -656,9 +656,12 @@ def run_ours(args, rank, world, local_rank):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             singles()
+        graph_b = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_b):
+            batched()
         tiny = {}
         for name, f in (("single_calls", singles), ("graph_of_single_calls", graph.replay),
-                        ("batched_call", batched)):
+                        ("batched_call", batched), ("batched_call_from_graph", graph_b.replay)):
             for _ in range(3):
                 flush()
                 f()
@@ -668,9 +671,9 @@ def run_ours(args, rank, world, local_rank):
         tiny.update({"workload": f"{nprob} x ln_{rows_}x{d_}", "cold_l2": True,
                      "batched_GBps": gbs(nb, tiny["batched_call_us"] / 1e3),
                      "launches": {"single_calls": nprob, "graph_of_single_calls": nprob,
-                                  "batched_call": 1}})
+                                  "batched_call": 1, "batched_call_from_graph": 1}})
         extra["many_small_problems"] = tiny
-        del probs, graph
+        del probs, graph, graph_b
 
     clocks = None
     if sampler:

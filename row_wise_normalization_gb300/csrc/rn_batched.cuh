@@ -6,9 +6,10 @@
 // tensors is launch-bound. Here the table of up to kBatchMax problems travels
 // in the kernel's parameter space (a __grid_constant__ struct: no device
 // allocation, no copy), the rows of all problems form one index space
-// [0, start[n]), and every warp takes rows of it grid-stride, finding the
-// problem of a row by binary search over the row offsets (constant-cache
-// broadcasts, the same for the whole warp). A row is handled exactly as in
+// [0, start[n]), and every warp takes a contiguous chunk of it, finding its
+// first problem by binary search over the row offsets and then walking
+// forward (the problem's fields stay in registers while its rows last). A
+// row is handled exactly as in
 // the warp-per-row kernel: held in registers as 128-bit vectors after a
 // head peel to the row's 16-byte boundary (x and y share that phase -- the
 // host sends other problems to their own launches), mean then centred sum
@@ -23,9 +24,94 @@
 
 namespace rn {
 
-// Register budget per SLOTS: about 12 per held float and 30 fixed.
+// One row, as the warp-per-row kernel computes it (the same operations in
+// the same order, so the results match a single call's bit for bit). AL: the
+// problem's arrays are 16-byte aligned and d is a multiple of the vector.
+template <int OP, typename T, int SLOTS, bool AL>
+__device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, const T* P1,
+                                            float* mean, float* rstd, int64_t row, int d,
+                                            float eps, int lane) {
+    constexpr int VEC = Elem<T>::kVec;
+    const float fd = (float)d;
+    HeldRow<VEC, SLOTS, false> cur;
+    load_row<T, VEC, SLOTS, 32, AL, false>(cur, xr, nullptr, d, lane);
+    const int h = cur.h, nv = cur.nv, tl = cur.tl;
+    const bool has_e = !AL && lane < h + tl;
+    const int ei = (lane < h) ? lane : h + VEC * nv + (lane - h);
+
+    float mu = 0.f, rs;
+    if constexpr (OP == OP_LN) {
+        float sum = cur.e;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
+        mu = warp_sum(sum) / fd;
+        float m2 = has_e ? (cur.e - mu) * (cur.e - mu) : 0.f;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            if (lane + s * 32 < nv) {
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) {
+                    const float c = cur.v[s].v[k] - mu;
+                    m2 = fmaf(c, c, m2);
+                }
+            }
+        }
+        rs = rsqrtf(warp_sum(m2) / fd + eps);
+    } else {
+        float ss = cur.e * cur.e;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) ss = fmaf(cur.v[s].v[k], cur.v[s].v[k], ss);
+        rs = rsqrtf(warp_sum(ss) / fd + eps);
+    }
+
+    bool pa = true;
+    if constexpr (!AL) {
+        pa = aligned16(P0, h);
+        if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
+    }
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        const int q = lane + s * 32;
+        if (q < nv) {
+            const int j = h + q * VEC;
+            Vec<VEC> a, b, o;
+            ldt_p(a, P0 + j, pa);
+            if constexpr (OP == OP_LN) {
+                ldt_p(b, P1 + j, pa);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k)
+                    o.v[k] = fmaf((cur.v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) o.v[k] = cur.v[s].v[k] * rs * a.v[k];
+            }
+            stt_y(yr + j, o);
+        }
+    }
+    if (has_e) {
+        const float a = ldt_p1(P0 + ei);
+        float o;
+        if constexpr (OP == OP_LN)
+            o = fmaf((cur.e - mu) * rs, a, ldt_p1(P1 + ei));
+        else
+            o = cur.e * rs * a;
+        stt_y1(yr + ei, o);
+    }
+    if constexpr (OP == OP_LN) {
+        if (lane == 0) {
+            if (mean) mean[row] = mu;
+            if (rstd) rstd[row] = rs;
+        }
+    }
+}
+
+// Register budget per SLOTS: about 12 per held float and 40 fixed.
 constexpr int batch_min_ctas(int slots, int vec) {
-    const int regs = 30 + 12 * slots * vec / 4;
+    const int regs = 40 + 12 * slots * vec / 4;
     const int n = 65536 / (((regs + 7) / 8) * 8 * kBatchThreads);
     return n < 1 ? 1 : (n > 16 ? 16 : n);
 }
@@ -33,102 +119,51 @@ constexpr int batch_min_ctas(int slots, int vec) {
 template <int OP, typename T, int SLOTS>
 __global__ void __launch_bounds__(kBatchThreads, batch_min_ctas(SLOTS, Elem<T>::kVec))
     batched_kernel(const __grid_constant__ BatchParams p) {
-    constexpr int VEC = Elem<T>::kVec;
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t total = p.start[p.n];
-
-    for (int64_t gr = warp; gr < total; gr += nwarps) {
-        // the problem holding global row gr: the last k with start[k] <= gr
-        int lo = 0, hi = p.n - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.start[mid] <= gr)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        const BatchProblem& pr = p.pr[lo];
-        const int64_t row = gr - p.start[lo];
-        const int d = (int)pr.d;
-        const float fd = (float)d;
-        const T* xr = reinterpret_cast<const T*>(pr.x) + row * pr.d;
-        T* yr = reinterpret_cast<T*>(pr.y) + row * pr.d;
+    // a contiguous chunk of rows per warp: the problem is looked up once and
+    // then advanced as the chunk crosses into the next problem
+    const int64_t chunk = (total + nwarps - 1) / nwarps;
+    int64_t r = warp * chunk;
+    const int64_t r_end = r + chunk < total ? r + chunk : total;
+    if (r >= r_end) return;
+    int k = 0, hi = p.n - 1;   // the last k with start[k] <= r
+    while (k < hi) {
+        const int mid = (k + hi + 1) >> 1;
+        if (p.start[mid] <= r)
+            k = mid;
+        else
+            hi = mid - 1;
+    }
+    for (;;) {
+        const BatchProblem& pr = p.pr[k];
+        const int64_t first = p.start[k];
+        const int64_t last = p.start[k + 1] < r_end ? p.start[k + 1] : r_end;
+        const int d = pr.d;
+        const T* X = reinterpret_cast<const T*>(pr.x);
+        T* Y = reinterpret_cast<T*>(pr.y);
         const T* P0 = reinterpret_cast<const T*>(pr.p0);
         const T* P1 = reinterpret_cast<const T*>(pr.p1);
-
-        HeldRow<VEC, SLOTS, false> cur;
-        load_row<T, VEC, SLOTS, 32, false, false>(cur, xr, nullptr, d, lane);
-        const int h = cur.h, nv = cur.nv, tl = cur.tl;
-        const bool has_e = lane < h + tl;
-        const int ei = (lane < h) ? lane : h + VEC * nv + (lane - h);
-
-        float mu = 0.f, rs;
-        if constexpr (OP == OP_LN) {
-            float sum = cur.e;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s)
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
-            mu = warp_sum(sum) / fd;
-            float m2 = has_e ? (cur.e - mu) * (cur.e - mu) : 0.f;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                if (lane + s * 32 < nv) {
-#pragma unroll
-                    for (int k = 0; k < VEC; ++k) {
-                        const float c = cur.v[s].v[k] - mu;
-                        m2 = fmaf(c, c, m2);
-                    }
-                }
+        float* mean = pr.mean;
+        float* rstd = pr.rstd;
+        const float eps = p.eps;
+        if (pr.al) {
+            for (; r < last; ++r) {
+                const int64_t row = r - first;
+                batched_row<OP, T, SLOTS, true>(X + row * d, Y + row * d, P0, P1, mean, rstd,
+                                                row, d, eps, lane);
             }
-            rs = rsqrtf(warp_sum(m2) / fd + p.eps);
         } else {
-            float ss = cur.e * cur.e;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s)
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) ss = fmaf(cur.v[s].v[k], cur.v[s].v[k], ss);
-            rs = rsqrtf(warp_sum(ss) / fd + p.eps);
-        }
-
-        bool pa = aligned16(P0, h);
-        if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s) {
-            const int q = lane + s * 32;
-            if (q < nv) {
-                const int j = h + q * VEC;
-                Vec<VEC> a, b, o;
-                ldt_p(a, P0 + j, pa);
-                if constexpr (OP == OP_LN) {
-                    ldt_p(b, P1 + j, pa);
-#pragma unroll
-                    for (int k = 0; k < VEC; ++k)
-                        o.v[k] = fmaf((cur.v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < VEC; ++k) o.v[k] = cur.v[s].v[k] * rs * a.v[k];
-                }
-                stt_y(yr + j, o);
+            for (; r < last; ++r) {
+                const int64_t row = r - first;
+                batched_row<OP, T, SLOTS, false>(X + row * d, Y + row * d, P0, P1, mean, rstd,
+                                                 row, d, eps, lane);
             }
         }
-        if (has_e) {
-            const float a = ldt_p1(P0 + ei);
-            float o;
-            if constexpr (OP == OP_LN)
-                o = fmaf((cur.e - mu) * rs, a, ldt_p1(P1 + ei));
-            else
-                o = cur.e * rs * a;
-            stt_y1(yr + ei, o);
-        }
-        if constexpr (OP == OP_LN) {
-            if (lane == 0) {
-                if (pr.mean) pr.mean[row] = mu;
-                if (pr.rstd) pr.rstd[row] = rs;
-            }
-        }
+        if (r >= r_end) break;
+        ++k;   // problems in the table all have rows > 0
     }
 }
 

@@ -108,7 +108,8 @@ struct BatchProblem {
     float* mean;       // may be NULL
     float* rstd;       // may be NULL
     int64_t rows;
-    int64_t d;
+    int d;             // <= kBatchMaxD
+    int al;            // x, y and the parameters 16-byte aligned, d % vector == 0
 };
 struct BatchParams {
     int n;                         // problems in the table (>= 1, each with rows > 0)

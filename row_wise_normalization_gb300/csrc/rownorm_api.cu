@@ -3,7 +3,11 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
+#include <iterator>
+#include <utility>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -516,22 +520,31 @@ int run_batched(int op, int dtype, const rn_problem* prs, int count, float eps, 
         const int st = validate(problem_request(op, dtype, prs[i], eps));
         if (st != RN_OK) return st;
     }
-    for (int i = 0; i < count; ++i) {
-        if (prs[i].rows == 0) continue;
-        const void *ii[3], *io[3];
-        int64_t nii[3], nio[3];
-        problem_ranges(op, dtype, prs[i], ii, nii, io, nio);
-        for (int j = i + 1; j < count; ++j) {
-            if (prs[j].rows == 0) continue;
-            const void *ji[3], *jo[3];
-            int64_t nji[3], njo[3];
-            problem_ranges(op, dtype, prs[j], ji, nji, jo, njo);
-            for (int a = 0; a < 3; ++a)
-                for (int b = 0; b < 3; ++b)
-                    if (overlaps(io[a], nio[a], ji[b], nji[b]) ||
-                        overlaps(jo[a], njo[a], ii[b], nii[b]) ||
-                        overlaps(io[a], nio[a], jo[b], njo[b]))
-                        return RN_ERR_ALIAS;
+    {
+        // Outputs may overlap nothing: no other output, no input (inputs may
+        // share memory among themselves, e.g. one gamma for all problems).
+        // Sort the outputs; adjacent ones must be disjoint; then each input
+        // can only meet the last output starting below its end.
+        std::vector<std::pair<uintptr_t, uintptr_t>> outs, ins;   // [begin, end)
+        outs.reserve(3 * (size_t)count);
+        ins.reserve(3 * (size_t)count);
+        for (int i = 0; i < count; ++i) {
+            if (prs[i].rows == 0) continue;
+            const void *pi[3], *po[3];
+            int64_t ni[3], no[3];
+            problem_ranges(op, dtype, prs[i], pi, ni, po, no);
+            for (int a = 0; a < 3; ++a) {
+                if (po[a] && no[a] > 0) outs.emplace_back(addr(po[a]), addr(po[a]) + no[a]);
+                if (pi[a] && ni[a] > 0) ins.emplace_back(addr(pi[a]), addr(pi[a]) + ni[a]);
+            }
+        }
+        std::sort(outs.begin(), outs.end());
+        for (size_t i = 1; i < outs.size(); ++i)
+            if (outs[i].first < outs[i - 1].second) return RN_ERR_ALIAS;
+        for (const auto& in : ins) {
+            auto it = std::lower_bound(outs.begin(), outs.end(),
+                                       std::make_pair(in.second, (uintptr_t)0));
+            if (it != outs.begin() && std::prev(it)->second > in.first) return RN_ERR_ALIAS;
         }
     }
     const cudaStream_t s = (cudaStream_t)stream;
@@ -577,7 +590,10 @@ int run_batched(int op, int dtype, const rn_problem* prs, int count, float eps, 
         b.mean = op == OP_LN ? pr.mean_out : nullptr;
         b.rstd = op == OP_LN ? pr.rstd_out : nullptr;
         b.rows = pr.rows;
-        b.d = pr.d;
+        b.d = (int)pr.d;
+        b.al = pr.d % vec == 0 &&
+               ((addr(pr.x) | addr(pr.y) | addr(pr.p0) | (op == OP_LN ? addr(pr.p1) : 0)) &
+                15u) == 0;
         if (pr.d / vec > widest) widest = pr.d / vec;
         bp.start[bp.n + 1] = bp.start[bp.n] + pr.rows;
         ++bp.n;
