@@ -63,11 +63,16 @@ const KernelEntry* reg_entry(int op, int dtype, int vec, int slots, int tpr, boo
 //  * with a residual the prefetched row holds x and the residual apart until
 //    it is processed (three slices live), so only slices of <= 4 vectors
 //    prefetch;
+//  * 16-bit storage moves half the bytes per held float, so for slices of
+//    24+ floats on rows of 128+ threads the resident threads (1024 per SM)
+//    keep more bytes in flight than a prefetched second row does: no
+//    prefetch there (LayerNorm BF16 32768 x 4096: 123 -> 96 us);
 //  * parameters held across rows for rows of up to 128 threads holding at
 //    most 6 vectors each, when every row starts at the same 16-byte phase
 //    (with 8 vectors the held parameters cost a resident CTA per SM).
 constexpr bool reg_prefetch(int vec, int slots, int tpr, bool res = false) {
     return vec > 1 && !(slots * vec >= 32 && tpr >= 256) && (!res || slots <= 4) &&
+           !(vec == 8 && slots * vec >= 24 && tpr >= 128) &&   // 16-bit: occupancy wins
            (52 + 2 * slots * vec) * tpr <= 65536;   // both rows fit the registers of one CTA
 }
 constexpr bool reg_may_hold_params(int vec, int slots, int tpr) {

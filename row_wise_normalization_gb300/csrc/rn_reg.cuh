@@ -53,9 +53,16 @@ constexpr int reg_budget(int op, int vec, int slots, bool pf, bool pp, bool res 
 // floats held per thread, 6+ FP32 or 3+ 16-bit vectors): with
 // prefetch about 384 resident threads per SM (the two held rows keep enough
 // bytes in flight, and the spare registers let loads issue early), without
-// it about 768-1024. Narrower slices fill the SM as far as the budget allows.
+// it about 768-1024. 16-bit storage runs its wide slices on rows of 128+
+// threads without prefetch (see reg_prefetch) at 1024 resident threads per
+// SM, LayerNorm rows of 256 threads at 768. Narrower slices fill the SM as
+// far as the budget allows.
 constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, bool pp,
                            bool res = false) {
+    if (vec == 8 && slots * vec >= 24 && !pf && threads >= 128) {
+        const int target = (op == 0 && threads == 256) ? 768 : 1024;
+        return target / threads > 0 ? target / threads : 1;
+    }
     if (vec > 1 && slots * vec >= 24 && !res) {
         if (pf) return threads == 64 ? 5 : (threads >= 384 ? 1 : 384 / threads);
         return threads >= 1024 ? 1 : (threads == 512 ? 2 : (768 / threads > 0 ? 768 / threads : 1));
