@@ -65,7 +65,11 @@ constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, boo
     }
     if (vec > 1 && slots * vec >= 24 && !res) {
         if (pf) return threads == 64 ? 5 : (threads >= 384 ? 1 : 384 / threads);
-        return threads >= 1024 ? 1 : (threads == 512 ? 2 : (768 / threads > 0 ? 768 / threads : 1));
+        // without prefetch: 768 threads on 256-thread rows; below 256 threads
+        // (the one-wave instances) 512, which leaves 128 registers (a wide
+        // LayerNorm slice needs about 100) and no spills
+        if (threads < 256) return 512 / threads;
+        return threads >= 1024 ? 1 : (threads == 512 ? 2 : 768 / threads);
     }
     const int per = ((reg_budget(op, vec, slots, pf, pp, res) + 7) / 8) * 8;
     const int n = 65536 / (per * threads);
@@ -348,10 +352,14 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
 // d % 4 == 0, so every row is whole 128-bit vectors -- no head/tail scalars
 // and no per-row alignment tests (the common case: allocators align to 256
 // bytes). PP is only compiled with AL.
-template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES>
+// NOPF: the same configuration compiled without prefetch at the no-prefetch
+// occupancy, for calls whose rows all fit in one wave of it (nothing to
+// overlap a prefetch with); only where the default instance prefetches.
+template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES,
+          bool NOPF = false>
 struct RegInst {
     static constexpr int RPC = (TPR == 32) ? kWarpRowsPerCta : 1;
-    static constexpr bool PF = reg_prefetch(VEC, SLOTS, TPR, RES);
+    static constexpr bool PF = NOPF ? false : reg_prefetch(VEC, SLOTS, TPR, RES);
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
         reg_kernel<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES><<<grid, TPR * RPC, 0, s>>>(p);
         return cudaGetLastError();
@@ -359,14 +367,14 @@ struct RegInst {
     static const KernelEntry entry;
 };
 
-template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES>
-const KernelEntry RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::entry = {
+template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES, bool NOPF>
+const KernelEntry RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::entry = {
     (const void*)&reg_kernel<OP, T, VEC, SLOTS, TPR,
-                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::RPC,
-                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::PF, PP, AL, RES>,
-    TPR * RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::RPC,
-    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::RPC, 0,
-    &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES>::launch, nullptr};
+                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::RPC,
+                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::PF, PP, AL, RES>,
+    TPR * RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::RPC,
+    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::RPC, 0,
+    &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::launch, nullptr};
 
 // Slots per thread a family is compiled for: up to 8 FP32 vectors (32 floats),
 // 4 16-bit vectors (32 floats) or 8 scalars; held parameters allow 24 floats.
@@ -375,34 +383,42 @@ constexpr int reg_max_slots() {
     return PP ? 24 / VEC : (VEC == 1 ? 8 : 32 / VEC);
 }
 
-template <int OP, typename T, int VEC, int TPR, bool PP, bool AL, bool RES>
+template <int OP, typename T, int VEC, int S, int TPR, bool PP, bool AL, bool RES, bool NOPF>
+const KernelEntry* reg_inst_entry() {
+    if constexpr (NOPF && !reg_prefetch(VEC, S, TPR, RES))
+        return nullptr;   // the default instance already runs without prefetch
+    else
+        return &RegInst<OP, T, VEC, S, TPR, PP, AL, RES, NOPF>::entry;
+}
+
+template <int OP, typename T, int VEC, int TPR, bool PP, bool AL, bool RES, bool NOPF = false>
 const KernelEntry* reg_pick_slots(int slots) {
     constexpr int M = reg_max_slots<T, VEC, PP>();
     if (slots < 1 || slots > M) return nullptr;
     switch (slots) {
-        case 1: return &RegInst<OP, T, VEC, 1, TPR, PP, AL, RES>::entry;
-        case 2: if constexpr (M >= 2) return &RegInst<OP, T, VEC, 2, TPR, PP, AL, RES>::entry; else return nullptr;
-        case 3: if constexpr (M >= 3) return &RegInst<OP, T, VEC, 3, TPR, PP, AL, RES>::entry; else return nullptr;
-        case 4: if constexpr (M >= 4) return &RegInst<OP, T, VEC, 4, TPR, PP, AL, RES>::entry; else return nullptr;
-        case 5: if constexpr (M >= 5) return &RegInst<OP, T, VEC, 5, TPR, PP, AL, RES>::entry; else return nullptr;
-        case 6: if constexpr (M >= 6) return &RegInst<OP, T, VEC, 6, TPR, PP, AL, RES>::entry; else return nullptr;
-        case 7: if constexpr (M >= 7) return &RegInst<OP, T, VEC, 7, TPR, PP, AL, RES>::entry; else return nullptr;
-        case 8: if constexpr (M >= 8) return &RegInst<OP, T, VEC, 8, TPR, PP, AL, RES>::entry; else return nullptr;
+        case 1: return reg_inst_entry<OP, T, VEC, 1, TPR, PP, AL, RES, NOPF>();
+        case 2: if constexpr (M >= 2) return reg_inst_entry<OP, T, VEC, 2, TPR, PP, AL, RES, NOPF>(); else return nullptr;
+        case 3: if constexpr (M >= 3) return reg_inst_entry<OP, T, VEC, 3, TPR, PP, AL, RES, NOPF>(); else return nullptr;
+        case 4: if constexpr (M >= 4) return reg_inst_entry<OP, T, VEC, 4, TPR, PP, AL, RES, NOPF>(); else return nullptr;
+        case 5: if constexpr (M >= 5) return reg_inst_entry<OP, T, VEC, 5, TPR, PP, AL, RES, NOPF>(); else return nullptr;
+        case 6: if constexpr (M >= 6) return reg_inst_entry<OP, T, VEC, 6, TPR, PP, AL, RES, NOPF>(); else return nullptr;
+        case 7: if constexpr (M >= 7) return reg_inst_entry<OP, T, VEC, 7, TPR, PP, AL, RES, NOPF>(); else return nullptr;
+        case 8: if constexpr (M >= 8) return reg_inst_entry<OP, T, VEC, 8, TPR, PP, AL, RES, NOPF>(); else return nullptr;
         default: return nullptr;
     }
 }
 
 // (slots, tpr) -> entry for one (VEC, PP, AL) family; PP families exist for
 // rows of at most 128 threads and 6 vectors per thread.
-template <int OP, typename T, int VEC, bool PP, bool AL, bool RES = false>
+template <int OP, typename T, int VEC, bool PP, bool AL, bool RES = false, bool NOPF = false>
 const KernelEntry* reg_pick(int slots, int tpr) {
     switch (tpr) {
-        case 32: return reg_pick_slots<OP, T, VEC, 32, PP, AL, RES>(slots);
-        case 64: return reg_pick_slots<OP, T, VEC, 64, PP, AL, RES>(slots);
-        case 128: return reg_pick_slots<OP, T, VEC, 128, PP, AL, RES>(slots);
-        case 256: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 256, PP, AL, RES>(slots); else return nullptr;
-        case 512: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 512, PP, AL, RES>(slots); else return nullptr;
-        case 1024: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 1024, PP, AL, RES>(slots); else return nullptr;
+        case 32: return reg_pick_slots<OP, T, VEC, 32, PP, AL, RES, NOPF>(slots);
+        case 64: return reg_pick_slots<OP, T, VEC, 64, PP, AL, RES, NOPF>(slots);
+        case 128: return reg_pick_slots<OP, T, VEC, 128, PP, AL, RES, NOPF>(slots);
+        case 256: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 256, PP, AL, RES, NOPF>(slots); else return nullptr;
+        case 512: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 512, PP, AL, RES, NOPF>(slots); else return nullptr;
+        case 1024: if constexpr (!PP) return reg_pick_slots<OP, T, VEC, 1024, PP, AL, RES, NOPF>(slots); else return nullptr;
         default: return nullptr;
     }
 }

@@ -27,6 +27,10 @@ namespace rn {
 RN_DECL_FAMILY(ln)
 RN_DECL_FAMILY(rms)
 #undef RN_DECL_FAMILY
+const KernelEntry* reg_entry_ln_v4_al_nopf(int, int);
+const KernelEntry* reg_entry_rms_v4_al_nopf(int, int);
+const KernelEntry* reg_entry_ln_v4_pp_nopf(int, int);
+const KernelEntry* reg_entry_rms_v4_pp_nopf(int, int);
 #define RN_DECL_FAMILY16(OPN, TN)                                 \
     const KernelEntry* reg_entry_##OPN##_##TN##_v8(int, int);     \
     const KernelEntry* reg_entry_##OPN##_##TN##_v8_al(int, int);  \
@@ -431,9 +435,31 @@ int run(const Request& q, int variant, void* stream) {
     if (!e) return RN_ERR_VARIANT;
 
     cudaError_t err = cudaSuccess;
-    const int resident = resident_ctas(e, pl.smem_bytes, &err);
+    int resident = resident_ctas(e, pl.smem_bytes, &err);
     if (err != cudaSuccess) return fail_cuda(err);
     const int64_t want = (q.rows + e->rows_per_cta - 1) / e->rows_per_cta;
+    // Aligned FP32 rows that prefetch: when every row fits in one wave of
+    // the no-prefetch instance (more CTAs resident, no next row to overlap
+    // with), run that instead. Measured on GB300: LayerNorm 1024 x 2048
+    // 9.8 -> 8.4 us, 512 x 4096 10.2 -> 9.2 us (cold L2).
+    if ((pl.variant == RN_VARIANT_WARP || pl.variant == RN_VARIANT_BLOCK) && pl.prefetch &&
+        pl.aligned && q.dtype == DT_F32 && !q.res) {
+        const bool ln = q.op == OP_LN;
+        const KernelEntry* e1 =
+            pl.params_held
+                ? (ln ? reg_entry_ln_v4_pp_nopf(pl.slots, pl.threads_per_row)
+                      : reg_entry_rms_v4_pp_nopf(pl.slots, pl.threads_per_row))
+                : (ln ? reg_entry_ln_v4_al_nopf(pl.slots, pl.threads_per_row)
+                      : reg_entry_rms_v4_al_nopf(pl.slots, pl.threads_per_row));
+        if (e1 && want > resident) {
+            const int r1 = resident_ctas(e1, 0, &err);
+            if (err != cudaSuccess) return fail_cuda(err);
+            if (want <= r1) {
+                e = e1;
+                resident = r1;
+            }
+        }
+    }
     const int grid = (int)(want < resident ? want : resident);
     err = e->launch(prm, grid, s);
     return err == cudaSuccess ? RN_OK : fail_cuda(err);
