@@ -332,6 +332,32 @@ def cpu_baseline_leg(case_wl, gpu_result=None, seconds=10.0):
             break
     el = time.perf_counter() - t0
     nbytes = algorithmic_bytes(case_wl.op, case_wl.rows, case_wl.d)
+
+    # the same oracle function on every host core at once: the rows split
+    # into one contiguous block per thread (ctypes releases the GIL during
+    # the call), whole passes for about half the single-thread time
+    from concurrent.futures import ThreadPoolExecutor
+
+    cores = len(os.sched_getaffinity(0))
+    bounds = [(case_wl.rows * i // cores, case_wl.rows * (i + 1) // cores) for i in range(cores)]
+    parts = [(np.ascontiguousarray(x[a:b]), a, b) for a, b in bounds if b > a]
+
+    def one(part):
+        fn(part[0], *params, case_wl.eps)
+
+    with ThreadPoolExecutor(len(parts)) as ex:
+        list(ex.map(one, parts))
+        t1 = time.perf_counter()
+        n_all = 0
+        while True:
+            list(ex.map(one, parts))
+            n_all += 1
+            if time.perf_counter() - t1 >= seconds / 2:
+                break
+        el_all = time.perf_counter() - t1
+    all_cores = {"value": nbytes * n_all / el_all / 1e9, "unit": UNIT, "cores": len(parts),
+                 "sample": f"{n_all} whole passes over {case_wl.rows}x{case_wl.d}, rows split "
+                           f"over {len(parts)} threads, {el_all:.1f} s"}
     parity = None
     if gpu_result is not None:
         import parity as P
@@ -348,7 +374,7 @@ def cpu_baseline_leg(case_wl, gpu_result=None, seconds=10.0):
             "sample": f"{n} whole passes of the C float64 oracle over {case_wl.rows}x{case_wl.d} "
                       f"({case_wl.op}), single thread, {el:.1f} s",
             "cpu": platform.processor() or platform.machine(),
-            "host_cores_available": len(os.sched_getaffinity(0))}, parity
+            "host_cores_available": cores, "all_cores": all_cores}, parity
 
 
 def rank_workload(base: workloads.Workload, rank: int) -> workloads.Workload:
