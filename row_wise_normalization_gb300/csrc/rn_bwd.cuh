@@ -34,7 +34,8 @@ namespace rn {
 // accumulators per held element, plus indices and addresses; the CTAs per SM
 // follow from it (65536 registers, allocated in units of 8 per thread).
 constexpr int bwd_min_ctas(int threads, int held, bool pg) {
-    const int budget = 56 + held * (pg ? 5 : 3);
+    const int need = 40 + held * (pg ? 5 : 3);
+    const int budget = need < 64 ? 64 : need;
     const int n = 65536 / (((budget + 7) / 8) * 8 * threads);
     return n < 1 ? 1 : (n > 32 ? 32 : n);
 }
