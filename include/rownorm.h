@@ -365,6 +365,15 @@ int rn_plan_for_residual(int op, int variant, int64_t d, const void *x, const vo
 enum { RN_DEVERR_STAGED_TIMEOUT = 1 };
 int rn_device_error(unsigned int *flags, int clear);
 
+/* Self-test of the failure path above (library infrastructure; the paper has
+ * no counterpart): launches one CTA on `stream` whose thread waits, through
+ * the same bounded wait the staged kernels use, on an mbarrier that nothing
+ * ever arrives at. After timeout_us microseconds (1 .. 1000000, else
+ * RN_ERR_SIZE) the wait gives up, sets RN_DEVERR_STAGED_TIMEOUT in the
+ * device error word and the kernel returns; the context stays usable. No
+ * memory other than that word is touched. */
+int rn_selftest_bounded_wait(unsigned int timeout_us, void *stream);
+
 /* Measurement aid: launch an empty kernel with `grid` CTAs of `threads`
  * threads on `stream` (the launch-latency floor small shapes are compared
  * against). grid in [1, 2^31), threads in [1, 1024], else RN_ERR_SIZE. */

@@ -26,6 +26,9 @@ RN_ERR_VARIANT = 7
 RN_ERR_DTYPE = 8
 RN_ERR_SCRATCH = 9
 
+# device error word bits
+RN_DEVERR_STAGED_TIMEOUT = 1
+
 # static scratch of ln_bwd_noalloc
 RN_NOALLOC_SCRATCH_BYTES = 8 << 20
 RN_NOALLOC_MAX_D = 4096
@@ -88,6 +91,7 @@ SIGNATURES = {
     "ln_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
     "rms_bwd": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
     "ln_bwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "rn_selftest_bounded_wait": (_INT, [ctypes.c_uint, _P]),
     "ln_fwd_batched": (_INT, [_INT, ctypes.POINTER(rn_problem), _INT, _F, _P]),
     "rms_fwd_batched": (_INT, [_INT, ctypes.POINTER(rn_problem), _INT, _F, _P]),
     "ln_fwd_strided": (_INT, [_INT, _INT, _P, _I64, _P, _P, _P, _I64, _P, _P, _I64, _I64, _F, _P]),
@@ -283,3 +287,8 @@ def ln_fwd_batched(dtype, probs, count, eps, stream=0) -> int:
 
 def rms_fwd_batched(dtype, probs, count, eps, stream=0) -> int:
     return load().rms_fwd_batched(dtype, probs, count, eps, stream)
+
+
+def selftest_bounded_wait(timeout_us: int, stream=0) -> int:
+    """Launch the bounded-wait self-test (see include/rownorm.h)."""
+    return load().rn_selftest_bounded_wait(timeout_us, stream)

@@ -163,6 +163,9 @@ constexpr int kBwdMinRowsPerGroup = 4;   // rows a backward row group takes at l
 // Records err as this thread's last CUDA error; returns RN_ERR_CUDA.
 int record_cuda_error(cudaError_t err);
 
+// Launches the bounded-wait self-test (one CTA, a wait nothing completes).
+cudaError_t bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
+
 // Reads (and optionally clears) the device error word of the current device.
 cudaError_t device_error_word(unsigned int* out, bool clear);
 

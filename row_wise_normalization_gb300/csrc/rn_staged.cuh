@@ -74,13 +74,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+// Self-test of the bounded wait: thread 0 waits on an mbarrier that nothing
+// arrives at, through the wait above, and records the timeout exactly as a
+// staged kernel does. Touches no data.
+__global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait_bounded(smem_addr(&bar), 0, limit_ns))
+        atomicOr(&g_device_error, kErrStagedTimeout);
 }
 
 // 1-D bulk copy global -> this CTA's shared memory, completing `bytes` on bar.

@@ -1017,6 +1017,12 @@ int rn_device_error(unsigned int* flags, int clear) {
     return err == cudaSuccess ? RN_OK : fail_cuda(err);
 }
 
+int rn_selftest_bounded_wait(unsigned int timeout_us, void* stream) {
+    if (timeout_us < 1 || timeout_us > 1000000) return RN_ERR_SIZE;
+    const cudaError_t e = bounded_wait_selftest(1000ull * timeout_us, (cudaStream_t)stream);
+    return e == cudaSuccess ? RN_OK : fail_cuda(e);
+}
+
 int rn_launch_empty(int64_t grid, int threads, void* stream) {
     if (grid < 1 || grid >= ((int64_t)1 << 31) || threads < 1 || threads > 1024)
         return RN_ERR_SIZE;

@@ -18,6 +18,11 @@ const KernelEntry* staged_entry(int op, int stages) {
     return op == OP_LN ? staged_pick<OP_LN>(stages) : staged_pick<OP_RMS>(stages);
 }
 
+cudaError_t bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
+    bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t device_error_word(unsigned int* out, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(out, g_device_error, sizeof(unsigned int));
     if (e != cudaSuccess || !clear) return e;

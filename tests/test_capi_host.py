@@ -312,3 +312,8 @@ def test_batched_validation_without_launch(lib):
     empty = [(X + 0x900000 * (i + 1), X + 0x100000, X + 0x200000, X + 0x300000 + 0x900000 * (i + 1),
               0, 0, 0, 64) for i in range(3)]
     assert capi.ln_fwd_batched(F32, capi.problems(empty), 3, 1e-5, 0) == capi.RN_OK
+
+
+def test_bounded_wait_selftest_rejects_out_of_range_limits(lib):
+    assert capi.selftest_bounded_wait(0, 0) == capi.RN_ERR_SIZE
+    assert capi.selftest_bounded_wait(2000000, 0) == capi.RN_ERR_SIZE
