@@ -1,7 +1,9 @@
 /*
  * rownorm.h -- C ABI of the GB300 (sm_103a) row-wise normalization library.
  *
- * Two operations over a contiguous, row-major FP32 matrix x[rows][d]:
+ * Two operations over the rows of a row-major matrix x[rows][d] (FP32, or
+ * BF16 / FP16 storage with FP32 arithmetic in the *_typed, *_strided and
+ * *_batched entry points), with their backward passes (FP32):
  *
  *   LayerNorm:  mu_i      = (1/d) sum_j x_ij
  *               sigma_i^2 = (1/d) sum_j (x_ij - mu_i)^2
@@ -26,12 +28,14 @@
  *               page tables (GB300 over NVLink-C2C), ordinary pageable host
  *               memory. Host-resident x is then read and host-resident y
  *               written by the kernel itself over the host link, with no
- *               staging copies. The caller owns every buffer; the library
- *               allocates nothing and never synchronizes. Rows are
- *               contiguous with row stride d (in elements). Every pointer
- *               must be 4-byte aligned; no other alignment is required
- *               (16-byte aligned rows take the vector path, others a scalar
- *               head/tail or the scalar path).
+ *               staging copies. The caller owns every buffer (the
+ *               backward's workspace included); no entry point allocates
+ *               or synchronizes, except the diagnostics that say so. Rows
+ *               are contiguous with row stride d (in elements), except in
+ *               the *_strided entry points. Every pointer must be aligned
+ *               to its element (4 bytes for FP32, 2 for 16-bit storage); no
+ *               other alignment is required (16-byte aligned rows take the
+ *               vector path, others a scalar head/tail or the scalar path).
  *   Stream      `stream` is a cudaStream_t passed as void*; NULL means the
  *               legacy default stream. Work is enqueued asynchronously; the
  *               results are valid once the stream has reached that point.
