@@ -546,6 +546,7 @@ def run_ours(args, rank, world, local_rank):
         cases = [workloads.large_32768x8192("ln"), workloads.large_32768x8192("rms")]
         cases += [w for w in workloads.sweep_offset()]
         t3 = time.time()
+        clean = Flusher(torch, device, mode="clean")
         for w in cases:
             c = LnCase(torch, w, device)
             for _ in range(3):
@@ -553,10 +554,22 @@ def run_ours(args, rank, world, local_rank):
                 c.launch()
             ts = time_launches(torch, c.launch, args.sweep_steps, flush)
             med = statistics.median(ts)
+            # the same with the L2 holding clean, unrelated lines (no
+            # write-backs of the flush buffer during the kernel)
+            tc = statistics.median(time_launches(torch, c.launch, args.sweep_steps, clean))
+            # a device copy of x into a y-sized buffer, timed the same way
+            yc = torch.empty_like(c.x)
+            tcp = statistics.median(time_launches(torch, lambda: yc.copy_(c.x), args.sweep_steps,
+                                                  flush))
+            del yc
             sweep.append({"workload": w.tag, "op": w.op, "rows": w.rows, "d": w.d,
+                          "same_size_copy_ms_median": tcp, "kernel_over_copy_time": med / tcp,
                           "plan": c.plan(), "ms_median": med, "GBps": gbs(c.bytes, med),
-                          "frac_of_measured_hbm": gbs(c.bytes, med) / peak})
+                          "frac_of_measured_hbm": gbs(c.bytes, med) / peak,
+                          "clean_l2": {"ms_median": tc, "GBps": gbs(c.bytes, tc),
+                                       "frac_of_measured_hbm": gbs(c.bytes, tc) / peak}})
             del c
+        del clean
         # same-session roofline control: a device-to-device copy of 1 GiB
         src = torch.empty(1 << 28, dtype=torch.float32, device=device)
         dst = torch.empty_like(src)
