@@ -296,6 +296,64 @@ NAMED = {
 }
 
 
+def latency_bound_check(torch, capi, wl, device, flush, peak, steps):
+    """Is a small shape launch-latency-bound? Its cold time must be within
+    the same-grid empty kernel's time plus its bytes at the measured HBM
+    bandwidth plus 1 us, and its CUDA-graph-replayed time per launch within
+    1.5x the empty kernel's replayed the same way. A device copy of the same
+    bytes, timed both ways, is reported beside it: unlike the empty kernel
+    it pays the DRAM round trip and the store drain a real kernel pays."""
+    c = LnCase(torch, wl, device)
+    pl = c.plan()
+    rpc = max(1, pl["threads_per_cta"] // pl["threads_per_row"])
+    grid = max(1, -(-wl.rows // rpc))
+
+    def empty():
+        capi.check(capi.launch_empty(grid, pl["threads_per_cta"],
+                                     torch.cuda.current_stream().cuda_stream))
+
+    def graph_per_launch(f):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            f()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(64):
+                    f()
+        torch.cuda.current_stream().wait_stream(s)
+        g.replay()
+        torch.cuda.synchronize()
+        return statistics.median(time_launches(torch, g.replay, 15)) / 64
+
+    ycopy = torch.empty_like(c.x)
+
+    def copy():
+        ycopy.copy_(c.x)
+
+    out = {}
+    for name, f in (("kernel", c.launch), ("empty", empty), ("copy", copy)):
+        for _ in range(3):
+            flush()
+            f()
+        out[name] = statistics.median(time_launches(torch, f, steps, flush))
+        out[name + "_graph"] = graph_per_launch(f)
+    at_peak_ms = c.bytes / (peak * 1e9) * 1e3
+    ok = (out["kernel"] <= out["empty"] + at_peak_ms + 1e-3 and
+          out["kernel_graph"] <= 1.5 * out["empty_graph"])
+    return {"workload": wl.tag or f"{wl.op}_{wl.rows}x{wl.d}", "plan": pl, "grid": grid,
+            "kernel_cold_us": 1e3 * out["kernel"], "empty_cold_us": 1e3 * out["empty"],
+            "bytes_at_measured_peak_us": 1e3 * at_peak_ms,
+            "kernel_graph_us_per_launch": 1e3 * out["kernel_graph"],
+            "empty_graph_us_per_launch": 1e3 * out["empty_graph"],
+            "launch_latency_bound": ok,
+            "same_size_copy_cold_us": 1e3 * out["copy"],
+            "same_size_copy_graph_us_per_launch": 1e3 * out["copy_graph"],
+            "kernel_over_copy_cold": out["kernel"] / out["copy"],
+            "kernel_over_copy_graph": out["kernel_graph"] / out["copy_graph"]}
+
+
 def pick_workload(name: str) -> workloads.Workload:
     """A named workload, or op:rows:d (seed 1, x ~ N(0,1))."""
     if name in NAMED:
@@ -580,6 +638,14 @@ def run_ours(args, rank, world, local_rank):
         if sampler:
             sampler.mark("sweep", t3, time.time())
     extra["sweep_cold_l2"] = sweep
+
+    # the small shapes against the launch-latency floor
+    if not args.no_sweep:
+        small = [workloads.ln_512x128()]
+        small += [w for w in workloads.rms_512_matrix() if w.x_dist == "normal"]
+        extra["small_shapes_latency_bound"] = [
+            latency_bound_check(torch, capi, w, device, flush, peak, args.sweep_steps)
+            for w in small]
 
     # residual add fused with the normalization, against the same work done
     # as a separate add followed by the normalization (cold L2)
