@@ -24,6 +24,27 @@
 
 namespace rn {
 
+// The parameters of one row's vectors and head/tail scalar.
+template <int OP, typename T, int VEC, int SLOTS>
+__device__ __forceinline__ void batched_params(Vec<VEC> (&a)[SLOTS],
+                                               Vec<VEC> (&b)[OP == OP_LN ? SLOTS : 1],
+                                               float& ae, float& be, const T* P0, const T* P1,
+                                               int h, int nv, bool has_e, int ei, bool aligned,
+                                               int lane) {
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        const int q = lane + s * 32;
+        if (q < nv) {
+            ldt_p(a[s], P0 + h + q * VEC, aligned);
+            if constexpr (OP == OP_LN) ldt_p(b[s], P1 + h + q * VEC, aligned);
+        }
+    }
+    if (has_e) {
+        ae = ldt_p1(P0 + ei);
+        if constexpr (OP == OP_LN) be = ldt_p1(P1 + ei);
+    }
+}
+
 // One row, as the warp-per-row kernel computes it (the same operations in
 // the same order, so the results match a single call's bit for bit). AL: the
 // problem's arrays are 16-byte aligned and d is a multiple of the vector.
@@ -38,6 +59,19 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
     const int h = cur.h, nv = cur.nv, tl = cur.tl;
     const bool has_e = !AL && lane < h + tl;
     const int ei = (lane < h) ? lane : h + VEC * nv + (lane - h);
+
+    // slices of at most 8 floats load the parameters with the row, before
+    // the reduction (as the single-call kernel does); wider ones after it
+    constexpr bool EP = SLOTS * VEC <= 8;
+    bool pa = true;
+    if constexpr (!AL) {
+        pa = aligned16(P0, h);
+        if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
+    }
+    Vec<VEC> pa0[SLOTS], pa1[OP == OP_LN ? SLOTS : 1];
+    float pe0 = 0.f, pe1 = 0.f;
+    if constexpr (EP)
+        batched_params<OP, T, VEC, SLOTS>(pa0, pa1, pe0, pe1, P0, P1, h, nv, has_e, ei, pa, lane);
 
     float mu = 0.f, rs;
     if constexpr (OP == OP_LN) {
@@ -68,20 +102,20 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
         rs = rsqrtf(warp_sum(ss) / fd + eps);
     }
 
-    bool pa = true;
-    if constexpr (!AL) {
-        pa = aligned16(P0, h);
-        if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
-    }
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
         const int q = lane + s * 32;
         if (q < nv) {
             const int j = h + q * VEC;
             Vec<VEC> a, b, o;
-            ldt_p(a, P0 + j, pa);
+            if constexpr (EP) {
+                a = pa0[s];
+                if constexpr (OP == OP_LN) b = pa1[s];
+            } else {
+                ldt_p(a, P0 + j, pa);
+                if constexpr (OP == OP_LN) ldt_p(b, P1 + j, pa);
+            }
             if constexpr (OP == OP_LN) {
-                ldt_p(b, P1 + j, pa);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
                     o.v[k] = fmaf((cur.v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
@@ -92,13 +126,18 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
             stt_y(yr + j, o);
         }
     }
+    if constexpr (!EP) {
+        if (has_e) {
+            pe0 = ldt_p1(P0 + ei);
+            if constexpr (OP == OP_LN) pe1 = ldt_p1(P1 + ei);
+        }
+    }
     if (has_e) {
-        const float a = ldt_p1(P0 + ei);
         float o;
         if constexpr (OP == OP_LN)
-            o = fmaf((cur.e - mu) * rs, a, ldt_p1(P1 + ei));
+            o = fmaf((cur.e - mu) * rs, pe0, pe1);
         else
-            o = cur.e * rs * a;
+            o = cur.e * rs * pe0;
         stt_y1(yr + ei, o);
     }
     if constexpr (OP == OP_LN) {
@@ -109,9 +148,10 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
     }
 }
 
-// Register budget per SLOTS: about 12 per held float and 40 fixed.
+// Register budget per SLOTS: about 12 per held float and 40 fixed, plus the
+// early-loaded parameters of slices of at most 8 floats.
 constexpr int batch_min_ctas(int slots, int vec) {
-    const int regs = 40 + 12 * slots * vec / 4;
+    const int regs = 40 + 12 * slots * vec / 4 + (slots * vec <= 8 ? 2 * slots * vec : 0);
     const int n = 65536 / (((regs + 7) / 8) * 8 * kBatchThreads);
     return n < 1 ? 1 : (n > 16 ? 16 : n);
 }

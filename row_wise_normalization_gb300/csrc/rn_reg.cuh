@@ -212,6 +212,33 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         const bool has_e = (VEC > 1) && !AL && (t < h + tl);
         const int ei = (t < h) ? t : h + VEC * nv + (t - h);
 
+        // EP (early parameters): slices of at most 8 floats without held
+        // parameters load this row's gamma/beta (w) now, so that the loads
+        // overlap the reduction instead of following it -- on the short,
+        // launch-bound rows the dependent chain is the whole kernel
+        constexpr bool EP = !PP && SLOTS * VEC <= 8;
+        Vec<VEC> ea[EP ? SLOTS : 1], eb[(EP && OP == OP_LN) ? SLOTS : 1];
+        float eae = 0.f, ebe = 0.f;
+        if constexpr (EP) {
+            bool epa = true;
+            if constexpr (VEC > 1 && !AL) {
+                epa = aligned16(P0, h);
+                if constexpr (OP == OP_LN) epa = epa && aligned16(P1, h);
+            }
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int q = t + s * TPR;
+                if (q < nv) {
+                    ldt_p(ea[s], P0 + h + q * VEC, epa);
+                    if constexpr (OP == OP_LN) ldt_p(eb[s], P1 + h + q * VEC, epa);
+                }
+            }
+            if (has_e) {
+                eae = ldt_p1(P0 + ei);
+                if constexpr (OP == OP_LN) ebe = ldt_p1(P1 + ei);
+            }
+        }
+
         // ---- statistics ------------------------------------------------
         float mu = 0.f, rs;
         if constexpr (OP == OP_LN) {
@@ -286,7 +313,7 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         T* yr = Y + row * p.ldy;
         T* hr = RES && p.h ? H + row * p.ldh : nullptr;
         bool pa = true;   // parameter vectors 16-byte aligned at this row's phase
-        if constexpr (VEC > 1 && !PP && !AL) {
+        if constexpr (VEC > 1 && !PP && !EP && !AL) {
             pa = aligned16(P0, h);
             if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
         }
@@ -299,6 +326,9 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                 if constexpr (PP) {
                     a = pg[s];
                     if constexpr (OP == OP_LN) b = pb[s];
+                } else if constexpr (EP) {
+                    a = ea[s];
+                    if constexpr (OP == OP_LN) b = eb[s];
                 } else {
                     ldt_p(a, P0 + j, pa);
                     if constexpr (OP == OP_LN) ldt_p(b, P1 + j, pa);
@@ -319,10 +349,10 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         }
         if (RES && has_e && hr) stt_y1(hr + ei, cur.e);
         if (has_e) {
-            const float a = PP ? pge : ldt_p1(P0 + ei);
+            const float a = PP ? pge : (EP ? eae : ldt_p1(P0 + ei));
             float o;
             if constexpr (OP == OP_LN)
-                o = fmaf((cur.e - mu) * rs, a, PP ? pbe : ldt_p1(P1 + ei));
+                o = fmaf((cur.e - mu) * rs, a, PP ? pbe : (EP ? ebe : ldt_p1(P1 + ei)));
             else
                 o = cur.e * rs * a;
             stt_y1(yr + ei, o);
