@@ -75,12 +75,30 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
 
     float mu = 0.f, rs;
     if constexpr (OP == OP_LN) {
-        float sum = cur.e;
+        // FP32 rows: the sum of x - K, K the row's first element (as the
+        // warp-per-row kernel computes it)
+        constexpr bool SHIFT = sizeof(T) == 4;
+        float K = 0.f, sum;
+        if constexpr (SHIFT) {
+            const float first = (h > 0 || nv == 0) ? cur.e : cur.v[0].v[0];
+            K = __shfl_sync(0xffffffffu, first, 0);
+            sum = has_e ? cur.e - K : 0.f;
 #pragma unroll
-        for (int s = 0; s < SLOTS; ++s)
+            for (int s = 0; s < SLOTS; ++s) {
+                if (lane + s * 32 < nv) {
 #pragma unroll
-            for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
-        mu = warp_sum(sum) / fd;
+                    for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k] - K;
+                }
+            }
+            mu = K + warp_sum(sum) / fd;
+        } else {
+            sum = cur.e;
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
+            mu = warp_sum(sum) / fd;
+        }
         float m2 = has_e ? (cur.e - mu) * (cur.e - mu) : 0.f;
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {

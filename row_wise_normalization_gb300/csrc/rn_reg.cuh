@@ -84,6 +84,7 @@ struct HeldRow {
     Vec<VEC> v[SLOTS];
     Vec<VEC> vr[RES ? SLOTS : 1];
     float e, er;      // the thread's head/tail scalar (0 if none), its residual
+    float k, kr;      // the row's first element and its residual (KLOAD only)
     int h, nv, tl;    // head peel, aligned vectors, tail of this row
 };
 
@@ -95,13 +96,16 @@ __device__ __forceinline__ void add_residual(HeldRow<VEC, SLOTS, RES>& r) {
 #pragma unroll
             for (int k = 0; k < VEC; ++k) r.v[s].v[k] = r.v[s].v[k] + r.vr[s].v[k];
         r.e = r.e + r.er;
+        r.k = r.k + r.kr;
     }
 }
 
 // Loads one row of x (and of the residual rr when RES) at the phase of xr; the
 // residual must share x's 16-byte phase (the host checks). T is the storage
 // type (FP32: VEC 4 or 1; BF16/FP16: VEC 8 or 1); the row is held as FP32.
-template <typename T, int VEC, int SLOTS, int TPR, bool AL, bool RES = false>
+// KLOAD: every thread also loads the row's first element (the shift of the
+// LayerNorm mean when several warps share the row).
+template <typename T, int VEC, int SLOTS, int TPR, bool AL, bool RES = false, bool KLOAD = false>
 __device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const T* xr,
                                          const T* rr, int d, int t) {
     constexpr int LV = VEC == 8 ? 3 : (VEC == 4 ? 2 : 0);   // log2(VEC)
@@ -135,6 +139,12 @@ __device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const T* x
     }
     r.e = 0.f;
     r.er = 0.f;
+    r.k = 0.f;
+    r.kr = 0.f;
+    if constexpr (KLOAD) {
+        r.k = ldt_x1(xr);
+        if constexpr (RES) r.kr = ldt_x1(rr);
+    }
     if constexpr (VEC > 1 && !AL) {
         if (t < r.h + r.tl) {
             const int ei = (t < r.h) ? t : r.h + VEC * r.nv + (t - r.h);
@@ -170,12 +180,20 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     const int lane = t & 31;
     const int d = (int)p.d;                          // register-held rows are < 2^31 wide
     const float fd = (float)d;
+    // FP32 LayerNorm sums x - K, K the row's first element, and takes the
+    // mean as K + sum / d: the summands are of the order of the row's spread,
+    // not of its mean, so a row with |mean| >> sigma keeps a mean within
+    // about half an ulp (y inherits the mean's error times rstd). 16-bit
+    // storage carries 8-11 significant bits, far coarser than that error.
+    constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
+    constexpr bool KLOAD = SHIFT && WPR > 1;
     const int64_t step = (int64_t)gridDim.x * RPC;
     int64_t row = (int64_t)blockIdx.x * RPC + g;
     if (row >= p.rows) return;                       // the whole group leaves together
 
     HeldRow<VEC, SLOTS, RES> cur;
-    load_row<T, VEC, SLOTS, TPR, AL, RES>(cur, X + row * p.ldx, RES ? R + row * p.ldr : nullptr, d, t);
+    load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
+                                                 RES ? R + row * p.ldr : nullptr, d, t);
 
     // Parameters held across rows (PP, only with AL): every row is aligned.
     Vec<VEC> pg[PP ? SLOTS : 1], pb[(PP && OP == OP_LN) ? SLOTS : 1];
@@ -204,8 +222,9 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         HeldRow<VEC, SLOTS, RES> nxt;
         if constexpr (PF) {
             if (nrow < p.rows)
-                load_row<T, VEC, SLOTS, TPR, AL, RES>(nxt, X + nrow * p.ldx,
-                                                      RES ? R + nrow * p.ldr : nullptr, d, t);
+                load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(nxt, X + nrow * p.ldx,
+                                                             RES ? R + nrow * p.ldr : nullptr, d,
+                                                             t);
         }
         add_residual(cur);
         const int h = cur.h, nv = cur.nv, tl = cur.tl;
@@ -242,14 +261,34 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         // ---- statistics ------------------------------------------------
         float mu = 0.f, rs;
         if constexpr (OP == OP_LN) {
-            float sum = cur.e;
+            float K = 0.f, sum;
+            if constexpr (SHIFT) {
+                if constexpr (WPR == 1) {
+                    // lane 0 holds the row's first element: its head scalar,
+                    // else its first vector, else (no vectors) its tail scalar
+                    const float first = (h > 0 || nv == 0) ? cur.e : cur.v[0].v[0];
+                    K = __shfl_sync(0xffffffffu, first, 0);
+                } else {
+                    K = cur.k;
+                }
+                sum = has_e ? cur.e - K : 0.f;
 #pragma unroll
-            for (int s = 0; s < SLOTS; ++s)
+                for (int s = 0; s < SLOTS; ++s) {
+                    if (t + s * TPR < nv) {
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
+                        for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k] - K;
+                    }
+                }
+            } else {
+                sum = cur.e;
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
+            }
 
             if constexpr (WPR == 1) {
-                mu = warp_sum(sum) / fd;
+                mu = SHIFT ? K + warp_sum(sum) / fd : warp_sum(sum) / fd;
                 float m2 = has_e ? (cur.e - mu) * (cur.e - mu) : 0.f;
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
@@ -270,7 +309,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                     const int rem = nv - s * TPR - 32 * w;
                     nw += VEC * (rem <= 0 ? 0 : (rem >= 32 ? 32 : rem));
                 }
-                const float wmean = nw > 0 ? wsum / (float)nw : 0.f;
+                const float wmean_s = nw > 0 ? wsum / (float)nw : 0.f;   // shifted by K
+                const float wmean = SHIFT ? K + wmean_s : wmean_s;
                 float m2 = has_e ? (cur.e - wmean) * (cur.e - wmean) : 0.f;
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
@@ -284,11 +324,15 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                 }
                 m2 = warp_sum(m2);
                 float(*slot)[NST] = xch[it & (NBUF - 1)][g];
+                // the per-warp centred M2 about the rounded wmean differs from
+                // the one about the exact warp mean only at second order;
+                // the merge works on the shifted sums and means
                 if (lane == 0)
-                    *reinterpret_cast<float4*>(slot[w]) = make_float4((float)nw, wsum, wmean, m2);
+                    *reinterpret_cast<float4*>(slot[w]) = make_float4((float)nw, wsum, wmean_s, m2);
                 named_sync(1 + g, TPR);
-                float M2;
-                merge_ln_warps<WPR>(slot, lane, fd, mu, M2);
+                float M2, mu_s;
+                merge_ln_warps<WPR>(slot, lane, fd, mu_s, M2);
+                mu = SHIFT ? K + mu_s : mu_s;
                 rs = rsqrtf(M2 / fd + p.eps);
             }
         } else {
@@ -369,8 +413,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         if constexpr (PF)
             cur = nxt;
         else
-            load_row<T, VEC, SLOTS, TPR, AL, RES>(cur, X + row * p.ldx, RES ? R + row * p.ldr : nullptr,
-                                                  d, t);
+            load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
+                                                         RES ? R + row * p.ldr : nullptr, d, t);
     }
 }
 

@@ -1,0 +1,108 @@
+"""Seeded random configurations against the oracle (GPU).
+
+The other parity tests walk chosen shapes; these draw the call itself: the
+operation, the row count, the width (log-uniform from 1 to 70000, so every
+kernel family and both sides of every dispatch boundary come up), the
+16-byte phases of x, y and the parameters, the value distribution, the eps
+and a forced variant among those that accept the call. The draws are fixed
+by the case number, so a failure names a reproducible case. Sizes stay
+small enough for the float64 oracle (at most ~2M elements per case).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import gpu_util as G
+import parity
+import workloads
+from oracle import reference
+from row_wise_normalization_gb300 import capi
+
+pytestmark = pytest.mark.gpu
+
+LN, RMS = capi.RN_OP_LN, capi.RN_OP_RMS
+DISTS = ("normal", "offset", "small", "zeros", "alternating")
+
+
+def _draw(case):
+    rng = np.random.default_rng([77, case])
+    d = int(math.exp(rng.uniform(0.0, math.log(70000.0))))
+    d = max(1, d)
+    rows = int(rng.integers(1, max(2, min(700, 2_000_000 // d)) + 1))
+    op = LN if rng.random() < 0.5 else RMS
+    dist = DISTS[int(rng.integers(0, len(DISTS)))]
+    x_off, y_off, p_off = (int(v) for v in rng.integers(0, 4, size=3))
+    if rng.random() < 0.5:
+        y_off = x_off          # half the cases keep x and y in one phase
+    eps = float(np.float32(10.0 ** rng.uniform(-7, -2)))
+    return rng, op, rows, d, dist, x_off, y_off, p_off, eps
+
+
+@pytest.mark.parametrize("case", range(200))
+def test_fuzz_forward(case):
+    rng, op, rows, d, dist, x_off, y_off, p_off, eps = _draw(case)
+    wl = workloads.Workload("ln" if op == LN else "rms", rows, d, seed=1000 + case,
+                            x_dist=dist, x_std=float(rng.uniform(0.5, 3.0)), eps=eps)
+    x = wl.x()
+    params = wl.params()
+    variants = G.variants_for(op, d, x_off, y_off)
+    v = variants[int(rng.integers(0, len(variants)))]
+    if op == LN:
+        y, m, r = G.run_ln(x, *params, eps=eps, variant=v, x_off=x_off, y_off=y_off, p_off=p_off)
+        yr, mr, rr = reference.layer_norm(x, *params, eps)
+        parity.check_y(y, yr, what=f"case {case} y")
+        parity.check_mean(m, mr, x, what=f"case {case} mean")
+        parity.check_rstd(r, rr, what=f"case {case} rstd")
+    else:
+        y = G.run_rms(x, *params, eps=eps, variant=v, x_off=x_off, y_off=y_off, p_off=p_off)
+        yr, _ = reference.rms_norm(x, *params, eps)
+        parity.check_y(y, yr, what=f"case {case} y")
+    assert capi.device_error() == 0
+
+
+@pytest.mark.parametrize("case", range(48))
+def test_fuzz_residual(case):
+    rng, op, rows, d, dist, x_off, y_off, p_off, eps = _draw(1000 + case)
+    wl = workloads.Workload("ln" if op == LN else "rms", rows, d, seed=2000 + case,
+                            x_dist=dist, eps=eps)
+    x = wl.x()
+    res = workloads.Workload("ln", rows, d, seed=3000 + case).x()
+    params = wl.params()
+    variants = G.residual_variants_for(op, d, x_off, y_off)
+    v = variants[int(rng.integers(0, len(variants)))]
+    h, y, m, r = G.run_residual(op, x, res, params, eps=eps, variant=v, x_off=x_off,
+                                r_off=x_off, y_off=y_off, h_off=y_off, p_off=p_off)
+    hr = reference.residual_sum(x, res)
+    assert np.array_equal(h.view(np.uint32), hr.view(np.uint32)), f"case {case} h"
+    if op == LN:
+        _, yr, mr, rr = reference.layer_norm_residual(x, res, *params, eps)
+        parity.check_mean(m, mr, hr, what=f"case {case} mean")
+        parity.check_rstd(r, rr, what=f"case {case} rstd")
+    else:
+        _, yr, _ = reference.rms_norm_residual(x, res, *params, eps)
+    parity.check_y(y, yr, what=f"case {case} y")
+
+
+@pytest.mark.parametrize("case", range(48))
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_fuzz_16bit(case, dtype):
+    rng, op, rows, d, dist, x_off, y_off, p_off, eps = _draw(2000 + case)
+    if dist == "offset" and dtype == "f16":
+        dist = "normal"            # FP16's range and step do not carry the +-100 offsets well
+    wl = workloads.Workload("ln" if op == LN else "rms", rows, d, seed=4000 + case,
+                            x_dist=dist, eps=eps)
+    xb, xw = workloads.to_storage(wl.x(), dtype)
+    pst = [workloads.to_storage(p_, dtype) for p_ in wl.params()]
+    variants = G.typed_variants_for(dtype, op, d, x_off, y_off)
+    v = variants[int(rng.integers(0, len(variants)))]
+    y, m, r = G.run_typed(op, dtype, xb, [p_[0] for p_ in pst], eps=eps, variant=v, x_off=x_off,
+                          y_off=y_off, p_off=p_off)
+    pw = [p_[1] for p_ in pst]
+    if op == LN:
+        yr, mr, rr = reference.layer_norm(xw, *pw, eps)
+        parity.check_mean(m, mr, xw, what=f"case {case} mean")
+        parity.check_rstd(r, rr, what=f"case {case} rstd")
+    else:
+        yr, _ = reference.rms_norm(xw, *pw, eps)
+    parity.check_y_storage(y, yr, dtype, what=f"case {case} y")
