@@ -73,12 +73,12 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
     if constexpr (EP)
         batched_params<OP, T, VEC, SLOTS>(pa0, pa1, pe0, pe1, P0, P1, h, nv, has_e, ei, pa, lane);
 
-    float mu = 0.f, rs;
+    // FP32 LayerNorm rows work in the frame shifted by the row's first
+    // element K, as the warp-per-row kernel does
+    constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
+    float mu = 0.f, rs, K = 0.f, mu_s = 0.f;
     if constexpr (OP == OP_LN) {
-        // FP32 rows: the sum of x - K, K the row's first element (as the
-        // warp-per-row kernel computes it)
-        constexpr bool SHIFT = sizeof(T) == 4;
-        float K = 0.f, sum;
+        float sum;
         if constexpr (SHIFT) {
             const float first = (h > 0 || nv == 0) ? cur.e : cur.v[0].v[0];
             K = __shfl_sync(0xffffffffu, first, 0);
@@ -90,7 +90,8 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
                     for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k] - K;
                 }
             }
-            mu = K + warp_sum(sum) / fd;
+            mu_s = warp_sum(sum) / fd;
+            mu = K + mu_s;
         } else {
             sum = cur.e;
 #pragma unroll
@@ -136,7 +137,8 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
             if constexpr (OP == OP_LN) {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
-                    o.v[k] = fmaf((cur.v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
+                    o.v[k] = SHIFT ? fmaf(((cur.v[s].v[k] - K) - mu_s) * rs, a.v[k], b.v[k])
+                                   : fmaf((cur.v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) o.v[k] = cur.v[s].v[k] * rs * a.v[k];
@@ -153,7 +155,7 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
     if (has_e) {
         float o;
         if constexpr (OP == OP_LN)
-            o = fmaf((cur.e - mu) * rs, pe0, pe1);
+            o = fmaf((SHIFT ? (cur.e - K) - mu_s : cur.e - mu) * rs, pe0, pe1);
         else
             o = cur.e * rs * pe0;
         stt_y1(yr + ei, o);

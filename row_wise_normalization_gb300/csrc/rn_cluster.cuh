@@ -172,14 +172,14 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
         cluster_sync_all();
 
         // ---- merge the CL * WPR partials (every thread) -----------------
-        float mu = 0.f, rs;
+        float mu = 0.f, rs, mus = 0.f;   // mus = mu - K; the output is formed as (x - K) - mus
         {
             float s1 = 0.f;
 #pragma unroll
             for (int k = lane; k < NE; k += 32) s1 += buf[k].y;
             s1 = warp_sum(s1);
             if constexpr (OP == OP_LN) {
-                const float mus = s1 / fd;            // mean of x - K
+                mus = s1 / fd;                        // mean of x - K
                 float m2 = 0.f;
 #pragma unroll
                 for (int k = lane; k < NE; k += 32) {
@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
                 if constexpr (OP == OP_LN) {
                     ld_p(b, p.p1 + j, pa);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) o.v[u] = fmaf((cur.v[k].v[u] - mu) * rs, a.v[u], b.v[u]);
+                    for (int u = 0; u < 4; ++u)
+                        o.v[u] = fmaf(((cur.v[k].v[u] - cur.K) - mus) * rs, a.v[u], b.v[u]);
                 } else {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) o.v[u] = cur.v[k].v[u] * rs * a.v[u];
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
             const float a = ld_p1(p.p0 + ei);
             float o;
             if constexpr (OP == OP_LN)
-                o = fmaf((cur.e - mu) * rs, a, ld_p1(p.p1 + ei));
+                o = fmaf(((cur.e - cur.K) - mus) * rs, a, ld_p1(p.p1 + ei));
             else
                 o = cur.e * rs * a;
             st_y1(yr + ei, o);

@@ -180,11 +180,12 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     const int lane = t & 31;
     const int d = (int)p.d;                          // register-held rows are < 2^31 wide
     const float fd = (float)d;
-    // FP32 LayerNorm sums x - K, K the row's first element, and takes the
-    // mean as K + sum / d: the summands are of the order of the row's spread,
-    // not of its mean, so a row with |mean| >> sigma keeps a mean within
-    // about half an ulp (y inherits the mean's error times rstd). 16-bit
-    // storage carries 8-11 significant bits, far coarser than that error.
+    // FP32 LayerNorm works in the frame shifted by K, the row's first
+    // element: it sums x - K (summands of the order of the row's spread, not
+    // of its mean), keeps mu_s = mean - K, and forms the output from
+    // (x - K) - mu_s, so y's error does not grow with |mean| / sigma (with
+    // the mean rounded to FP32, y would carry half an ulp of the mean times
+    // rstd). 16-bit storage carries 8-11 significant bits, far coarser.
     constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
     constexpr bool KLOAD = SHIFT && WPR > 1;
     const int64_t step = (int64_t)gridDim.x * RPC;
@@ -259,9 +260,9 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         }
 
         // ---- statistics ------------------------------------------------
-        float mu = 0.f, rs;
+        float mu = 0.f, rs, K = 0.f, mu_s = 0.f;   // mu_s = mu - K (SHIFT)
         if constexpr (OP == OP_LN) {
-            float K = 0.f, sum;
+            float sum;
             if constexpr (SHIFT) {
                 if constexpr (WPR == 1) {
                     // lane 0 holds the row's first element: its head scalar,
@@ -288,7 +289,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
             }
 
             if constexpr (WPR == 1) {
-                mu = SHIFT ? K + warp_sum(sum) / fd : warp_sum(sum) / fd;
+                mu_s = warp_sum(sum) / fd;
+                mu = SHIFT ? K + mu_s : mu_s;
                 float m2 = has_e ? (cur.e - mu) * (cur.e - mu) : 0.f;
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                 if (lane == 0)
                     *reinterpret_cast<float4*>(slot[w]) = make_float4((float)nw, wsum, wmean_s, m2);
                 named_sync(1 + g, TPR);
-                float M2, mu_s;
+                float M2;
                 merge_ln_warps<WPR>(slot, lane, fd, mu_s, M2);
                 mu = SHIFT ? K + mu_s : mu_s;
                 rs = rsqrtf(M2 / fd + p.eps);
@@ -380,7 +382,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                 if constexpr (OP == OP_LN) {
 #pragma unroll
                     for (int k = 0; k < VEC; ++k)
-                        o.v[k] = fmaf((cur.v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
+                        o.v[k] = SHIFT ? fmaf(((cur.v[s].v[k] - K) - mu_s) * rs, a.v[k], b.v[k])
+                                       : fmaf((cur.v[s].v[k] - mu) * rs, a.v[k], b.v[k]);
                 } else {
 #pragma unroll
                     for (int k = 0; k < VEC; ++k) o.v[k] = cur.v[s].v[k] * rs * a.v[k];
@@ -396,7 +399,8 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
             const float a = PP ? pge : (EP ? eae : ldt_p1(P0 + ei));
             float o;
             if constexpr (OP == OP_LN)
-                o = fmaf((cur.e - mu) * rs, a, PP ? pbe : (EP ? ebe : ldt_p1(P1 + ei)));
+                o = fmaf((SHIFT ? (cur.e - K) - mu_s : cur.e - mu) * rs, a,
+                         PP ? pbe : (EP ? ebe : ldt_p1(P1 + ei)));
             else
                 o = cur.e * rs * a;
             stt_y1(yr + ei, o);

@@ -204,16 +204,18 @@ __global__ void __launch_bounds__(TPB, 1) staged_kernel(const Params p) {
         __syncthreads();
         if (abort_flag) break;
 
-        float mu = 0.f, rs;
+        float mu = 0.f, rs, K = 0.f, mus = 0.f;   // mus = mu - K
         if constexpr (OP == OP_LN) {
-            // pass 1: mean (shifted by the row's first element)
-            const float K = d > 0 ? ld_x1(xr) : 0.f;
+            // pass 1: mean (shifted by the row's first element); the output
+            // is formed in the shifted frame too, (x - K) - mus
+            K = d > 0 ? ld_x1(xr) : 0.f;
             float s1 = has_e ? e - K : 0.f;
             for (int q = t; q < nv; q += TPB) {
                 const float4 v = buf[q];
                 s1 += ((v.x - K) + (v.y - K)) + ((v.z - K) + (v.w - K));
             }
-            mu = K + block_sum<TPB>(s1, red[rot], lane, w) / fd;
+            mus = block_sum<TPB>(s1, red[rot], lane, w) / fd;
+            mu = K + mus;
             rot = rot == 2 ? 0 : rot + 1;
             // pass 2: centred sum of squares
             float s2 = has_e ? (e - mu) * (e - mu) : 0.f;
@@ -251,10 +253,10 @@ __global__ void __launch_bounds__(TPB, 1) staged_kernel(const Params p) {
             if constexpr (OP == OP_LN) {
                 Vec<4> b;
                 ld_p(b, p.p1 + j, pa);
-                o.v[0] = fmaf((v.x - mu) * rs, a.v[0], b.v[0]);
-                o.v[1] = fmaf((v.y - mu) * rs, a.v[1], b.v[1]);
-                o.v[2] = fmaf((v.z - mu) * rs, a.v[2], b.v[2]);
-                o.v[3] = fmaf((v.w - mu) * rs, a.v[3], b.v[3]);
+                o.v[0] = fmaf(((v.x - K) - mus) * rs, a.v[0], b.v[0]);
+                o.v[1] = fmaf(((v.y - K) - mus) * rs, a.v[1], b.v[1]);
+                o.v[2] = fmaf(((v.z - K) - mus) * rs, a.v[2], b.v[2]);
+                o.v[3] = fmaf(((v.w - K) - mus) * rs, a.v[3], b.v[3]);
             } else {
                 o.v[0] = v.x * rs * a.v[0];
                 o.v[1] = v.y * rs * a.v[1];
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(TPB, 1) staged_kernel(const Params p) {
             const float a = ld_p1(p.p0 + ei);
             float o;
             if constexpr (OP == OP_LN)
-                o = fmaf((e - mu) * rs, a, ld_p1(p.p1 + ei));
+                o = fmaf(((e - K) - mus) * rs, a, ld_p1(p.p1 + ei));
             else
                 o = e * rs * a;
             st_y1(yr + ei, o);

@@ -84,9 +84,12 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
         const int64_t ei = (t < h) ? (int64_t)t : (int64_t)h + VEC * nv + (t - h);
         float(*slot)[4] = xch[it & 1];
 
-        float mu = 0.f, rs;
+        // FP32 output is formed in the shifted frame, (x - K) - mus, so that
+        // its error does not grow with |mean| / sigma
+        constexpr bool SHIFT_OUT = sizeof(T) == 4;
+        float mu = 0.f, rs, K = 0.f, mus = 0.f;
         if constexpr (OP == OP_LN) {
-            const float K = ld_xr1<T, RES>(xr, rr, 0);   // shift (the same address for every thread)
+            K = ld_xr1<T, RES>(xr, rr, 0);   // shift (the same address for every thread)
             float n = 0.f, m = 0.f, M = 0.f;
             for (int64_t q = t; q < nv; q += TPB) {
                 Vec<VEC> v;
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
             }
             if (lane == 0) *reinterpret_cast<float4*>(slot[w]) = make_float4(n, n * m, m, M);
             __syncthreads();
-            float M2, mus;
+            float M2;
             merge_ln_warps<W>(slot, lane, fd, mus, M2);
             mu = K + mus;
             rs = rsqrtf(M2 / fd + p.eps);
@@ -153,7 +156,9 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
                 Vec<VEC> b;
                 ldt_p(b, P1 + j, pa);
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) o.v[k] = fmaf((v.v[k] - mu) * rs, a.v[k], b.v[k]);
+                for (int k = 0; k < VEC; ++k)
+                    o.v[k] = SHIFT_OUT ? fmaf(((v.v[k] - K) - mus) * rs, a.v[k], b.v[k])
+                                       : fmaf((v.v[k] - mu) * rs, a.v[k], b.v[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) o.v[k] = v.v[k] * rs * a.v[k];
@@ -166,7 +171,7 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
             const float a = ldt_p1(P0 + ei);
             float o;
             if constexpr (OP == OP_LN)
-                o = fmaf((e - mu) * rs, a, ldt_p1(P1 + ei));
+                o = fmaf((SHIFT_OUT ? (e - K) - mus : e - mu) * rs, a, ldt_p1(P1 + ei));
             else
                 o = e * rs * a;
             stt_y1(yr + ei, o);
