@@ -6,7 +6,8 @@ kernel family and both sides of every dispatch boundary come up), the
 16-byte phases of x, y and the parameters, the value distribution, the eps
 and a forced variant among those that accept the call. The draws are fixed
 by the case number, so a failure names a reproducible case. Sizes stay
-small enough for the float64 oracle (at most ~2M elements per case).
+small enough for the float64 oracle (at most ~2M elements per case). The
+strided, batched and backward entry points are drawn the same way.
 """
 import math
 
@@ -68,9 +69,12 @@ def test_fuzz_forward(case):
 def test_fuzz_residual(case):
     rng, op, rows, d, dist, x_off, y_off, p_off, eps = _draw(1000 + case)
     wl = workloads.Workload("ln" if op == LN else "rms", rows, d, seed=2000 + case,
-                            x_dist=dist, eps=eps)
+                            x_dist=dist, x_std=_x_std(rng), eps=eps)
     x = wl.x()
-    res = workloads.Workload("ln", rows, d, seed=3000 + case).x()
+    # a residual of random scale: h = x + res keeps x's offset and a spread
+    # down to 0.05
+    res = (workloads.Workload("ln", rows, d, seed=3000 + case).x()
+           * np.float32(_x_std(rng))).astype(np.float32)
     params = wl.params()
     variants = G.residual_variants_for(op, d, x_off, y_off)
     v = variants[int(rng.integers(0, len(variants)))]
@@ -109,3 +113,95 @@ def test_fuzz_16bit(case, dtype):
     else:
         yr, _ = reference.rms_norm(xw, *pw, eps)
     parity.check_y_storage(y, yr, dtype, what=f"case {case} y")
+
+
+def _x_std(rng):
+    return float(math.exp(rng.uniform(math.log(0.05), math.log(3.0))))
+
+
+@pytest.mark.parametrize("case", range(64))
+def test_fuzz_strided(case):
+    """Random row strides (>= d) and phases through ln_fwd_strided /
+    rms_fwd_strided, every accepted variant drawn; gaps must stay untouched."""
+    import test_gpu_strided as S
+
+    rng, op, rows, d, dist, x_off, y_off, p_off, eps = _draw(3000 + case)
+    rows = min(rows, max(1, 400_000 // d))
+    ldx = d + int(rng.integers(0, 9))
+    ldy = d + int(rng.integers(0, 9))
+    dtype = capi.RN_DTYPE_F32 if rng.random() < 0.75 else capi.RN_DTYPE_BF16
+    wl = workloads.Workload("ln" if op == LN else "rms", rows, d, seed=5000 + case, x_dist=dist,
+                            x_std=_x_std(rng))
+    x = wl.x()
+    params = wl.params()
+    variants = S._variants(dtype, op, d, ldx, ldy, x_off, y_off)
+    v = variants[int(rng.integers(0, len(variants)))]
+    S._check(op, dtype, x, params, S._run(op, dtype, x, params, ldx, ldy, v, x_off, y_off))
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_batched(case):
+    """A random table of problems (widths, rows, phases, empty ones) through
+    ln_fwd_batched / rms_fwd_batched, each against the oracle and, bit for
+    bit, against its single call."""
+    import test_gpu_batched as B
+
+    rng = np.random.default_rng([78, case])
+    op = LN if rng.random() < 0.5 else RMS
+    dtype = capi.RN_DTYPE_F32 if rng.random() < 0.75 else capi.RN_DTYPE_BF16
+    n = int(rng.integers(1, 150))
+    shapes = []
+    for _ in range(n):
+        d = int(math.exp(rng.uniform(0.0, math.log(1500.0))))
+        rows = int(rng.integers(0, 40))
+        xo = int(rng.integers(0, 4))
+        yo = xo if rng.random() < 0.7 else int(rng.integers(0, 4))
+        if dtype == capi.RN_DTYPE_BF16:
+            xo, yo = 2 * xo, 2 * yo
+        shapes.append((rows, max(1, d), xo, yo))
+    B._run_batch(op, dtype, shapes, 7000 + 1000 * case)
+
+
+@pytest.mark.parametrize("case", range(48))
+def test_fuzz_backward(case):
+    """Random LayerNorm / RMSNorm backward calls: widths up to 16384, offset
+    rows with small spreads, aligned or not, and a random workspace size
+    between one partial row and the full one."""
+    import test_gpu_backward as W
+
+    rng, op, rows, d, dist, x_off, y_off, p_off, eps = _draw(4000 + case)
+    d = min(d, 16384)
+    rows = max(1, min(rows, 600_000 // d))
+    off = int(rng.integers(0, 4)) if d <= 8192 else 0
+    wl = workloads.Workload("ln", rows, d, seed=9000 + case, x_dist=dist, x_std=_x_std(rng))
+    x = wl.x()
+    dy = workloads.Workload("ln", rows, d, seed=9500 + case).x()
+    g, _ = wl.params()
+    width = 2 * d if op == LN else d
+    if d > 8192 and d % 4:
+        # beyond the scalar layout's 8192 floats: a documented size error,
+        # from the workspace query and from the call itself
+        with pytest.raises(capi.RowNormError) as err:
+            capi.bwd_workspace_size(op, rows, d)
+        assert err.value.status == capi.RN_ERR_SIZE
+        with pytest.raises(capi.RowNormError) as err:
+            if op == LN:
+                m32, r32 = W._stats(x, g)
+                W._run_ln(x, dy, g, m32, r32, off=off, ws_bytes=4 * width * 4)
+            else:
+                W._run_rms(x, dy, g, off=off, ws_bytes=4 * width * 4)
+        assert err.value.status == capi.RN_ERR_SIZE
+        return
+    full = capi.bwd_workspace_size(op, rows, d)
+    ws = int(rng.integers(1, max(2, full // (4 * width)) + 1)) * 4 * width
+    chain = max(4, -(-rows // 152)) + 16 if ws >= full else rows + 16
+    if op == LN:
+        m32, r32 = W._stats(x, g)
+        W._check_ln(x, dy, g, W._run_ln(x, dy, g, m32, r32, off=off, ws_bytes=ws), chain=chain)
+    else:
+        dx, dw = W._run_rms(x, dy, g, off=off, ws_bytes=ws)
+        dxr, dwr = reference.rms_norm_backward(dy, x, g)
+        parity.check_y(dx, dxr, what=f"case {case} dx")
+        _, r = reference.rms_norm(x, g)
+        terms = np.abs(dy.astype(np.float64) * x * r[:, None]).sum(axis=0)
+        parity.check_colsum(dw, dwr, terms, chain, f"case {case} dw")
