@@ -100,13 +100,14 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
                 for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
             mu = warp_sum(sum) / fd;
         }
-        float m2 = has_e ? (cur.e - mu) * (cur.e - mu) : 0.f;
+        const float ce = SHIFT ? (cur.e - K) - mu_s : cur.e - mu;
+        float m2 = has_e ? ce * ce : 0.f;
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             if (lane + s * 32 < nv) {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) {
-                    const float c = cur.v[s].v[k] - mu;
+                    const float c = SHIFT ? (cur.v[s].v[k] - K) - mu_s : cur.v[s].v[k] - mu;
                     m2 = fmaf(c, c, m2);
                 }
             }

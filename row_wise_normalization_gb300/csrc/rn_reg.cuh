@@ -182,10 +182,11 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     const float fd = (float)d;
     // FP32 LayerNorm works in the frame shifted by K, the row's first
     // element: it sums x - K (summands of the order of the row's spread, not
-    // of its mean), keeps mu_s = mean - K, and forms the output from
-    // (x - K) - mu_s, so y's error does not grow with |mean| / sigma (with
-    // the mean rounded to FP32, y would carry half an ulp of the mean times
-    // rstd). 16-bit storage carries 8-11 significant bits, far coarser.
+    // of its mean), keeps mu_s = mean - K, and takes every deviation --
+    // for the sum of squares and for the output -- as (x - K) - mu_s, so
+    // neither rstd nor y loses accuracy as |mean| / sigma grows (with the
+    // mean rounded to FP32, every deviation would carry half an ulp of the
+    // mean). 16-bit storage carries 8-11 significant bits, far coarser.
     constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
     constexpr bool KLOAD = SHIFT && WPR > 1;
     const int64_t step = (int64_t)gridDim.x * RPC;
@@ -291,13 +292,15 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
             if constexpr (WPR == 1) {
                 mu_s = warp_sum(sum) / fd;
                 mu = SHIFT ? K + mu_s : mu_s;
-                float m2 = has_e ? (cur.e - mu) * (cur.e - mu) : 0.f;
+                // deviations in the shifted frame too: (x - K) - mu_s
+                const float ce = SHIFT ? (cur.e - K) - mu_s : cur.e - mu;
+                float m2 = has_e ? ce * ce : 0.f;
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
                     if (t + s * TPR < nv) {
 #pragma unroll
                         for (int k = 0; k < VEC; ++k) {
-                            const float c = cur.v[s].v[k] - mu;
+                            const float c = SHIFT ? (cur.v[s].v[k] - K) - mu_s : cur.v[s].v[k] - mu;
                             m2 = fmaf(c, c, m2);
                         }
                     }
@@ -312,22 +315,22 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                     nw += VEC * (rem <= 0 ? 0 : (rem >= 32 ? 32 : rem));
                 }
                 const float wmean_s = nw > 0 ? wsum / (float)nw : 0.f;   // shifted by K
-                const float wmean = SHIFT ? K + wmean_s : wmean_s;
-                float m2 = has_e ? (cur.e - wmean) * (cur.e - wmean) : 0.f;
+                // deviations from the warp mean, taken in the shifted frame
+                const float ce = SHIFT ? (cur.e - K) - wmean_s : cur.e - wmean_s;
+                float m2 = has_e ? ce * ce : 0.f;
 #pragma unroll
                 for (int s = 0; s < SLOTS; ++s) {
                     if (t + s * TPR < nv) {
 #pragma unroll
                         for (int k = 0; k < VEC; ++k) {
-                            const float c = cur.v[s].v[k] - wmean;
+                            const float c = SHIFT ? (cur.v[s].v[k] - K) - wmean_s
+                                                  : cur.v[s].v[k] - wmean_s;
                             m2 = fmaf(c, c, m2);
                         }
                     }
                 }
                 m2 = warp_sum(m2);
                 float(*slot)[NST] = xch[it & (NBUF - 1)][g];
-                // the per-warp centred M2 about the rounded wmean differs from
-                // the one about the exact warp mean only at second order;
                 // the merge works on the shifted sums and means
                 if (lane == 0)
                     *reinterpret_cast<float4*>(slot[w]) = make_float4((float)nw, wsum, wmean_s, m2);

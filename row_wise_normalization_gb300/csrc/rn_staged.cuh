@@ -218,10 +218,11 @@ __global__ void __launch_bounds__(TPB, 1) staged_kernel(const Params p) {
             mu = K + mus;
             rot = rot == 2 ? 0 : rot + 1;
             // pass 2: centred sum of squares
-            float s2 = has_e ? (e - mu) * (e - mu) : 0.f;
+            float s2 = has_e ? ((e - K) - mus) * ((e - K) - mus) : 0.f;
             for (int q = t; q < nv; q += TPB) {
                 const float4 v = buf[q];
-                const float a = v.x - mu, b = v.y - mu, c = v.z - mu, dd = v.w - mu;
+                const float a = (v.x - K) - mus, b = (v.y - K) - mus, c = (v.z - K) - mus,
+                            dd = (v.w - K) - mus;
                 s2 = fmaf(a, a, s2);
                 s2 = fmaf(b, b, s2);
                 s2 = fmaf(c, c, s2);

@@ -295,3 +295,22 @@ def test_full_size_32768x8192(op):
         else:
             yr, _ = reference.rms_norm(xs, p[0], wl.eps)
             parity.check_y(yh[r0:r0 + step], yr, what=f"y rows {r0}+")
+
+
+# ---------------------------------------------------------------------------
+# rows far from zero with a tiny spread: |mean| / sigma = 1e6
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d", [5, 127, 768, 4096, 20000, 70001])
+def test_large_offset_tiny_spread_every_variant(d):
+    """x = 1e4 + N(0, 0.01^2): an FP32 mean is only good to half an ulp of
+    1e4 (5e-4, 5% of sigma), so deviations taken from the rounded mean would
+    miss rstd by ~1e-3 and y by far more than the tolerance; the kernels take
+    every deviation in the frame shifted by the row's first element."""
+    rng = np.random.default_rng([97, d])
+    rows = 24
+    x = (1e4 + 0.01 * rng.standard_normal((rows, d))).astype(np.float32)
+    g = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    b = (0.1 * rng.standard_normal(d)).astype(np.float32)
+    for x_off, y_off in ((0, 0), (1, 1), (0, 2)):
+        for v in G.variants_for(LN, d, x_off, y_off):
+            _check_ln(x, g, b, G.run_ln(x, g, b, variant=v, x_off=x_off, y_off=y_off))
