@@ -435,6 +435,25 @@ def cpu_baseline_leg(case_wl, gpu_result=None, seconds=10.0):
             "host_cores_available": cores, "all_cores": all_cores}, parity
 
 
+def environment(torch, device) -> dict:
+    """What the numbers were measured on."""
+    props = torch.cuda.get_device_properties(device)
+    env = {"gpu": torch.cuda.get_device_name(device), "sms": props.multi_processor_count,
+           "l2_bytes": getattr(props, "L2_cache_size", None),
+           "compute_capability": f"{props.major}.{props.minor}",
+           "torch": torch.__version__, "cuda_runtime": torch.version.cuda,
+           "host": platform.machine(), "host_cores": len(os.sched_getaffinity(0))}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version,memory.total",
+                              "--format=csv,noheader", f"--id={device.index or 0}"],
+                             capture_output=True, text=True, timeout=20)
+        drv, mem = [v.strip() for v in out.stdout.strip().split(",")[:2]]
+        env.update({"driver": drv, "gpu_memory": mem})
+    except (OSError, ValueError, subprocess.SubprocessError):
+        pass
+    return env
+
+
 def rank_workload(base: workloads.Workload, rank: int) -> workloads.Workload:
     """Weak scaling: every rank normalises its own batch of the base shape;
     the rows are independent, so a rank's batch is just other seeded data
@@ -852,6 +871,8 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "parity": parity,
         "clocks": clocks,
+        "environment": environment(torch, device),
+        "samples_ms": [round(t_, 6) for t_ in times],
         "extra": extra,
         "source_hash": h,
     }
