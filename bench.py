@@ -731,29 +731,36 @@ def run_ours(args, rank, world, local_rank):
         # algorithmic bytes: read dy and x, write dx, read the parameters (and
         # LN's saved mean/rstd), write the parameter gradients
         bwd = []
-        for op, rows_, d_ in (("ln", 4096, 768), ("ln", 32768, 1024), ("ln", 16384, 4096),
-                              ("rms", 16384, 4096)):
+        for op, rows_, d_, dt in (("ln", 4096, 768, torch.float32),
+                                  ("ln", 32768, 1024, torch.float32),
+                                  ("ln", 16384, 4096, torch.float32),
+                                  ("rms", 16384, 4096, torch.float32),
+                                  ("ln", 16384, 4096, torch.bfloat16),
+                                  ("rms", 16384, 4096, torch.bfloat16)):
             xw = workloads.Workload(op, rows_, d_, seed=65)
-            xt = torch.from_numpy(xw.x()).to(device)
-            dyt = torch.from_numpy(workloads.Workload(op, rows_, d_, seed=66).x()).to(device)
-            pt = [torch.from_numpy(p_).to(device) for p_ in xw.params()]
+            xt = torch.from_numpy(xw.x()).to(device).to(dt)
+            dyt = torch.from_numpy(workloads.Workload(op, rows_, d_, seed=66).x()).to(device).to(dt)
+            pt = [torch.from_numpy(p_).to(device).to(dt) for p_ in xw.params()]
             dxt = torch.empty_like(xt)
-            g0, g1 = torch.empty(d_, device=device), torch.empty(d_, device=device)
+            g0 = torch.empty(d_, device=device, dtype=dt)
+            g1 = torch.empty(d_, device=device, dtype=dt)
             wst = torch.empty(capi.bwd_workspace_size(capi.RN_OP_LN if op == "ln" else capi.RN_OP_RMS,
                                                       rows_, d_) // 4 + 4, device=device)
+            es = xt.element_size()
             if op == "ln":
                 _, mt, st_ = rn.ln_fwd(xt, *pt)
                 f = lambda: rn.ln_bwd(dyt, xt, pt[0], mt, st_, dx=dxt, dgamma=g0, dbeta=g1,
                                       workspace=wst)
-                nb = 12 * rows_ * d_ + 12 * d_ + 8 * rows_
+                nb = 3 * es * rows_ * d_ + 3 * es * d_ + 8 * rows_
             else:
                 f = lambda: rn.rms_bwd(dyt, xt, pt[0], dx=dxt, dw=g0, workspace=wst)
-                nb = 12 * rows_ * d_ + 8 * d_
+                nb = 3 * es * rows_ * d_ + 2 * es * d_
             for _ in range(3):
                 flush()
                 f()
             ms_ = statistics.median(time_launches(torch, f, args.sweep_steps, flush))
-            bwd.append({"workload": f"{op}_bwd_{rows_}x{d_}", "ms_median": ms_,
+            bwd.append({"workload": f"{op}_bwd_{str(dt).split('.')[-1]}_{rows_}x{d_}",
+                        "ms_median": ms_,
                         "GBps": gbs(nb, ms_), "frac_of_measured_hbm": gbs(nb, ms_) / peak,
                         "launches_per_call": 2})
             del xt, dyt, dxt, wst

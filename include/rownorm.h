@@ -244,6 +244,26 @@ int rms_bwd(const float *dy, const float *x, const float *w, float *dx, float *d
             int64_t d, float eps, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Backward with 16-bit (or FP32) storage: as ln_bwd / rms_bwd, with dy, x,
+ * dx, gamma (w) and dgamma / dbeta (dw) all of type `dtype` (RN_DTYPE_F32,
+ * RN_DTYPE_BF16 or RN_DTYPE_F16; pointers aligned to the element size);
+ * mean and rstd stay FP32. Values are widened to FP32 on load, all
+ * arithmetic and the workspace partials are FP32, and dx and the parameter
+ * gradients are rounded once to the storage type, to nearest even. The
+ * *_bwd_workspace_size figure covers every storage type. Widths up to 16384
+ * (all of dy, x, dx, gamma and the workspace 16-byte aligned and d a multiple
+ * of the 16-byte vector: 4 FP32 or 8 16-bit elements) or 8192 (otherwise).
+ * Unknown dtype: RN_ERR_DTYPE.
+ */
+int ln_bwd_typed(int dtype, const void *dy, const void *x, const void *gamma, const float *mean,
+                 const float *rstd, void *dx, void *dgamma, void *dbeta, int64_t rows, int64_t d,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+int rms_bwd_typed(int dtype, const void *dy, const void *x, const void *w, void *dx, void *dw,
+                  int64_t rows, int64_t d, float eps, void *workspace, size_t workspace_bytes,
+                  void *stream);
+
+/*
  * LayerNorm backward without any allocation. The paper has no counterpart to
  * this entry point; it serves callers that cannot allocate device memory
  * where they run the backward: a process whose caching allocator already

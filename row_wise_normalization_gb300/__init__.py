@@ -265,50 +265,58 @@ def _workspace(op, rows, d, device, workspace):
 
 def ln_bwd(dy, x, gamma, mean, rstd, *, dx=None, dgamma=None, dbeta=None,
            param_grads: bool = True, workspace=None, stream=None):
-    """LayerNorm backward from the forward's saved mean and rstd (FP32 CUDA
-    tensors). Returns ``(dx, dgamma, dbeta)`` (the last two None when
-    ``param_grads`` is False). ``workspace``: a float32 CUDA tensor for the
-    parameter-gradient partials (allocated if not given)."""
+    """LayerNorm backward from the forward's saved mean and rstd. dy, x and
+    gamma are float32, bfloat16 or float16 (one type; dx and the parameter
+    gradients come back in it); mean and rstd are FP32. Returns ``(dx,
+    dgamma, dbeta)`` (the last two None when ``param_grads`` is False).
+    ``workspace``: a float32 CUDA tensor for the parameter-gradient partials
+    (allocated if not given)."""
     import torch
 
-    for n, t in (("dy", dy), ("x", x), ("gamma", gamma), ("mean", mean), ("rstd", rstd)):
+    code = _dtype_code(x)
+    for n, t in (("dy", dy), ("x", x), ("gamma", gamma)):
+        _check_f32_cuda(n, t, x.dtype)
+    for n, t in (("mean", mean), ("rstd", rstd)):
         _check_f32_cuda(n, t)
     d = x.shape[-1]
     rows = x.numel() // d if d else 0
     dx = torch.empty_like(x) if dx is None else dx
     if param_grads:
-        dgamma = torch.empty(d, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
-        dbeta = torch.empty(d, dtype=torch.float32, device=x.device) if dbeta is None else dbeta
+        dgamma = torch.empty(d, dtype=x.dtype, device=x.device) if dgamma is None else dgamma
+        dbeta = torch.empty(d, dtype=x.dtype, device=x.device) if dbeta is None else dbeta
         ws = _workspace(capi.RN_OP_LN, rows, d, x.device, workspace)
     else:
         dgamma = dbeta = ws = None
-    st = capi.ln_bwd(dy.data_ptr(), x.data_ptr(), gamma.data_ptr(), mean.data_ptr(),
-                     rstd.data_ptr(), dx.data_ptr(), dgamma.data_ptr() if dgamma is not None else 0,
-                     dbeta.data_ptr() if dbeta is not None else 0, rows, d,
-                     ws.data_ptr() if ws is not None else 0,
-                     ws.numel() * 4 if ws is not None else 0, _stream_handle(x, stream))
+    st = capi.ln_bwd_typed(code, dy.data_ptr(), x.data_ptr(), gamma.data_ptr(), mean.data_ptr(),
+                           rstd.data_ptr(), dx.data_ptr(),
+                           dgamma.data_ptr() if dgamma is not None else 0,
+                           dbeta.data_ptr() if dbeta is not None else 0, rows, d,
+                           ws.data_ptr() if ws is not None else 0,
+                           ws.numel() * 4 if ws is not None else 0, _stream_handle(x, stream))
     capi.check(st)
     return dx, dgamma, dbeta
 
 
 def rms_bwd(dy, x, w, eps: float = 1e-5, *, dx=None, dw=None, param_grads: bool = True,
             workspace=None, stream=None):
-    """RMSNorm backward (FP32 CUDA tensors). Returns ``(dx, dw)``."""
+    """RMSNorm backward (float32, bfloat16 or float16 tensors of one type).
+    Returns ``(dx, dw)``."""
     import torch
 
+    code = _dtype_code(x)
     for n, t in (("dy", dy), ("x", x), ("w", w)):
-        _check_f32_cuda(n, t)
+        _check_f32_cuda(n, t, x.dtype)
     d = x.shape[-1]
     rows = x.numel() // d if d else 0
     dx = torch.empty_like(x) if dx is None else dx
     if param_grads:
-        dw = torch.empty(d, dtype=torch.float32, device=x.device) if dw is None else dw
+        dw = torch.empty(d, dtype=x.dtype, device=x.device) if dw is None else dw
         ws = _workspace(capi.RN_OP_RMS, rows, d, x.device, workspace)
     else:
         dw = ws = None
-    st = capi.rms_bwd(dy.data_ptr(), x.data_ptr(), w.data_ptr(), dx.data_ptr(),
-                      dw.data_ptr() if dw is not None else 0, rows, d, float(eps),
-                      ws.data_ptr() if ws is not None else 0, ws.numel() * 4 if ws is not None else 0,
-                      _stream_handle(x, stream))
+    st = capi.rms_bwd_typed(code, dy.data_ptr(), x.data_ptr(), w.data_ptr(), dx.data_ptr(),
+                            dw.data_ptr() if dw is not None else 0, rows, d, float(eps),
+                            ws.data_ptr() if ws is not None else 0,
+                            ws.numel() * 4 if ws is not None else 0, _stream_handle(x, stream))
     capi.check(st)
     return dx, dw

@@ -91,6 +91,9 @@ SIGNATURES = {
     "ln_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
     "rms_bwd": (_INT, [_P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
     "ln_bwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "ln_bwd_typed": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, ctypes.c_size_t,
+                            _P]),
+    "rms_bwd_typed": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _F, _P, ctypes.c_size_t, _P]),
     "rn_selftest_bounded_wait": (_INT, [ctypes.c_uint, _P]),
     "ln_fwd_batched": (_INT, [_INT, ctypes.POINTER(rn_problem), _INT, _F, _P]),
     "rms_fwd_batched": (_INT, [_INT, ctypes.POINTER(rn_problem), _INT, _F, _P]),
@@ -292,3 +295,15 @@ def rms_fwd_batched(dtype, probs, count, eps, stream=0) -> int:
 def selftest_bounded_wait(timeout_us: int, stream=0) -> int:
     """Launch the bounded-wait self-test (see include/rownorm.h)."""
     return load().rn_selftest_bounded_wait(timeout_us, stream)
+
+
+def ln_bwd_typed(dtype, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, workspace,
+                 workspace_bytes, stream=0) -> int:
+    return load().ln_bwd_typed(dtype, dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d,
+                               workspace, workspace_bytes, stream)
+
+
+def rms_bwd_typed(dtype, dy, x, w, dx, dw, rows, d, eps, workspace, workspace_bytes,
+                  stream=0) -> int:
+    return load().rms_bwd_typed(dtype, dy, x, w, dx, dw, rows, d, eps, workspace,
+                                workspace_bytes, stream)

@@ -1,29 +1,32 @@
-// Backward kernels and the column reduction of parameter-gradient partials.
+// Backward kernels (FP32 storage), the dispatch over storage types and the
+// column reduction of parameter-gradient partials.
 #include "rn_bwd.cuh"
 
 namespace rn {
 
-const BwdEntry* bwd_entry(int op, int vec, int slots, int tpr, bool pg) {
-    if (op == OP_LN) {
-        if (vec == 4) return pg ? bwd_pick<OP_LN, 4, true>(slots, tpr) : bwd_pick<OP_LN, 4, false>(slots, tpr);
-        return pg ? bwd_pick<OP_LN, 1, true>(slots, tpr) : bwd_pick<OP_LN, 1, false>(slots, tpr);
+const BwdEntry* bwd_entry_bf16(int op, int vec, int slots, int tpr, bool pg);
+const BwdEntry* bwd_entry_f16(int op, int vec, int slots, int tpr, bool pg);
+cudaError_t column_reduce_bf16(const float* ws, int64_t rows, int64_t width, int64_t d,
+                               void* out0, void* out1, cudaStream_t s);
+cudaError_t column_reduce_f16(const float* ws, int64_t rows, int64_t width, int64_t d,
+                              void* out0, void* out1, cudaStream_t s);
+
+const BwdEntry* bwd_entry(int op, int dtype, int vec, int slots, int tpr, bool pg) {
+    switch (dtype) {
+        case DT_F32: return bwd_pick_type<float>(op, vec, slots, tpr, pg);
+        case DT_BF16: return bwd_entry_bf16(op, vec, slots, tpr, pg);
+        case DT_F16: return bwd_entry_f16(op, vec, slots, tpr, pg);
+        default: return nullptr;
     }
-    if (vec == 4) return pg ? bwd_pick<OP_RMS, 4, true>(slots, tpr) : bwd_pick<OP_RMS, 4, false>(slots, tpr);
-    return pg ? bwd_pick<OP_RMS, 1, true>(slots, tpr) : bwd_pick<OP_RMS, 1, false>(slots, tpr);
 }
 
-cudaError_t column_reduce(const float* ws, int64_t rows, int64_t width, int64_t d, float* out0,
-                          float* out1, cudaStream_t s) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((width + kReduceCols - 1) / kReduceCols));
-    cfg.blockDim = dim3(kReduceCols * kReduceSlices);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, column_reduce_kernel, ws, rows, width, d, out0, out1);
+cudaError_t column_reduce(int dtype, const float* ws, int64_t rows, int64_t width, int64_t d,
+                          void* out0, void* out1, cudaStream_t s) {
+    switch (dtype) {
+        case DT_BF16: return column_reduce_bf16(ws, rows, width, d, out0, out1, s);
+        case DT_F16: return column_reduce_f16(ws, rows, width, d, out0, out1, s);
+        default: return column_reduce_t<float>(ws, rows, width, d, out0, out1, s);
+    }
 }
 
 }  // namespace rn

@@ -13,6 +13,11 @@
 // g that dx subtracts from: for a one-element row g - mean(g) is exactly 0,
 // where a contracted product would leave its rounding residue times rstd.
 //
+// T is the storage type of dy, x, dx and the parameter vector (FP32, BF16 or
+// FP16; 16-bit values are widened on load, dx rounded once on store); all
+// arithmetic, the saved statistics and the workspace partials are FP32, and
+// the parameter gradients are rounded once, into T, by the column reduction.
+//
 // Parameter part (dgamma/dbeta, dw): a thread owns the same columns for every
 // row it processes (whole aligned vectors, or single elements when the
 // arrays are not all 16-byte aligned with d % 4 == 0), so it accumulates its
@@ -34,16 +39,38 @@ namespace rn {
 // accumulators per held element, plus indices and addresses; the CTAs per SM
 // follow from it (65536 registers, allocated in units of 8 per thread).
 constexpr int bwd_min_ctas(int threads, int held, bool pg) {
-    const int need = 40 + held * (pg ? 5 : 3);
+    const int need = 48 + held * (pg ? 5 : 3);
     const int budget = need < 64 ? 64 : need;
     const int n = 65536 / (((budget + 7) / 8) * 8 * threads);
     return n < 1 ? 1 : (n > 32 ? 32 : n);
 }
 
-template <int OP, int VEC, int SLOTS, int TPR, int RPC, bool PG>
+// FP32 store of one thread's partial sums to the workspace (VEC 1, 4 or 8).
+template <int VEC>
+__device__ __forceinline__ void st_ws(float* p, const Vec<VEC>& r) {
+    if constexpr (VEC == 8) {
+        Vec<4> a, b;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            a.v[k] = r.v[k];
+            b.v[k] = r.v[4 + k];
+        }
+        st_y(p, a);
+        st_y(p + 4, b);
+    } else {
+        st_y(p, r);
+    }
+}
+
+template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PG>
 __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC, PG))
     bwd_kernel(const BwdParams p) {
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
+    static_assert(VEC == 1 || VEC == Elem<T>::kVec, "a vector is one 128-bit access");
+    const T* X = reinterpret_cast<const T*>(p.x);
+    const T* DY = reinterpret_cast<const T*>(p.dy);
+    const T* P0 = reinterpret_cast<const T*>(p.p0);
+    T* DX = reinterpret_cast<T*>(p.dx);
     constexpr int WPR = TPR / 32;
     constexpr int NBUF = WPR > 1 ? 2 : 1;
     __shared__ __align__(16) float xch[NBUF][RPC][WPR][2];
@@ -52,7 +79,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
     const int t = threadIdx.x - g * TPR;
     const int w = t >> 5, lane = t & 31;
     const int d = (int)p.d;
-    const int nv = d / VEC;               // VEC 4 only when d % 4 == 0 (host checks)
+    const int nv = d / VEC;               // vectors only when d % VEC == 0 (host checks)
     const float inv_d = 1.0f / (float)d;
     const int64_t group = (int64_t)blockIdx.x * RPC + g;
     const int64_t ngroups = (int64_t)gridDim.x * RPC;
@@ -63,7 +90,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
     for (int s = 0; s < SLOTS; ++s) {
         const int q = t + s * TPR;
         if (q < nv) {
-            ld_p(par[s], p.p0 + q * VEC, true);
+            ldt_p(par[s], P0 + q * VEC, true);
         } else {
 #pragma unroll
             for (int k = 0; k < VEC; ++k) par[s].v[k] = 0.f;
@@ -82,15 +109,15 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
 
     int it = 0;
     for (int64_t row = group; row < p.rows; row += ngroups, ++it) {
-        const float* xr = p.x + row * p.d;
-        const float* dyr = p.dy + row * p.d;
+        const T* xr = X + row * p.d;
+        const T* dyr = DY + row * p.d;
         Vec<VEC> xv[SLOTS], dv[SLOTS];
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             const int q = t + s * TPR;
             if (q < nv) {
-                ld_x(xv[s], xr + q * VEC);
-                ld_x(dv[s], dyr + q * VEC);
+                ldt_x(xv[s], xr + q * VEC);
+                ldt_x(dv[s], dyr + q * VEC);
             } else {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) xv[s].v[k] = dv[s].v[k] = 0.f;
@@ -146,7 +173,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
             c1 = 0.f;
             c2 = s2 * inv_d * rs * rs;
         }
-        float* dxr = p.dx + row * p.d;
+        T* dxr = DX + row * p.d;
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             const int q = t + s * TPR;
@@ -167,7 +194,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
                         if constexpr (PG) acc0[s].v[k] = fmaf(dv[s].v[k], xv[s].v[k] * rs, acc0[s].v[k]);
                     }
                 }
-                st_y(dxr + q * VEC, o);
+                stt_y(dxr + q * VEC, o);
             }
         }
     }
@@ -182,8 +209,8 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
             for (int s = 0; s < SLOTS; ++s) {
                 const int q = t + s * TPR;
                 if (q < nv) {
-                    st_y(wr + q * VEC, acc0[s]);
-                    if constexpr (OP == OP_LN) st_y(wr + d + q * VEC, acc1[s]);
+                    st_ws(wr + q * VEC, acc0[s]);
+                    if constexpr (OP == OP_LN) st_ws(wr + d + q * VEC, acc1[s]);
                 }
             }
         } else {
@@ -207,7 +234,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
                         for (int gg = 1; gg < RPC; ++gg)
 #pragma unroll
                             for (int k = 0; k < VEC; ++k) sum.v[k] += red[gg][t * VEC + k];
-                        st_y(wr + hf * d + q * VEC, sum);
+                        st_ws(wr + hf * d + q * VEC, sum);
                     }
                     __syncthreads();
                 }
@@ -217,16 +244,17 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
 }
 
 // Sum of the workspace's rows: out0[j] = sum_c ws[c][j] for j < d, out1[j - d]
-// for d <= j < width (either output may be NULL). A CTA takes 32 columns and
+// for d <= j < width (either output may be NULL), rounded once into TO. A CTA takes 32 columns and
 // 32 slices of the rows: lane l of warp w adds rows w, w + 32, ... of column
 // l with Kahan compensation (a warp reads 128 contiguous bytes per row), and
 // warp 0 adds the 32 slice sums in slice order, again compensated.
 constexpr int kReduceCols = 32;
 constexpr int kReduceSlices = 32;
 
+template <typename TO>
 __global__ void __launch_bounds__(kReduceCols * kReduceSlices)
     column_reduce_kernel(const float* __restrict__ ws, int64_t rows, int64_t width, int64_t d,
-                         float* out0, float* out1) {
+                         TO* out0, TO* out1) {
     __shared__ float part[kReduceSlices][kReduceCols + 1];
     // wait until the row kernel's partials are written and visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -254,9 +282,9 @@ __global__ void __launch_bounds__(kReduceCols * kReduceSlices)
             u = tsum;
         }
         if (j < d) {
-            if (out0) out0[j] = u;
+            if (out0) stt_y1(out0 + j, u);
         } else if (out1) {
-            out1[j - d] = u;
+            stt_y1(out1 + (j - d), u);
         }
     }
 }
@@ -265,45 +293,81 @@ __global__ void __launch_bounds__(kReduceCols * kReduceSlices)
 
 namespace rn {
 
-template <int OP, int VEC, int SLOTS, int TPR, bool PG>
+template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PG>
 struct BwdInst {
     static constexpr int RPC = TPR < 256 ? 256 / TPR : 1;
     static cudaError_t launch(const BwdParams& p, int grid, cudaStream_t s) {
-        bwd_kernel<OP, VEC, SLOTS, TPR, RPC, PG><<<grid, TPR * RPC, 0, s>>>(p);
+        bwd_kernel<OP, T, VEC, SLOTS, TPR, RPC, PG><<<grid, TPR * RPC, 0, s>>>(p);
         return cudaGetLastError();
     }
     static const BwdEntry entry;
 };
 
-template <int OP, int VEC, int SLOTS, int TPR, bool PG>
-const BwdEntry BwdInst<OP, VEC, SLOTS, TPR, PG>::entry = {
-    (const void*)&bwd_kernel<OP, VEC, SLOTS, TPR, BwdInst<OP, VEC, SLOTS, TPR, PG>::RPC, PG>,
-    TPR * BwdInst<OP, VEC, SLOTS, TPR, PG>::RPC, BwdInst<OP, VEC, SLOTS, TPR, PG>::RPC,
-    &BwdInst<OP, VEC, SLOTS, TPR, PG>::launch};
+template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PG>
+const BwdEntry BwdInst<OP, T, VEC, SLOTS, TPR, PG>::entry = {
+    (const void*)&bwd_kernel<OP, T, VEC, SLOTS, TPR, BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC, PG>,
+    TPR * BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC, BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC,
+    &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::launch};
 
-template <int OP, int VEC, int TPR, bool PG>
+// Vectors a backward thread holds: up to 16 floats of x and of dy (4 FP32 or
+// 2 16-bit vectors), or 8 scalars.
+template <int VEC>
+constexpr int bwd_max_slots() {
+    return VEC == 1 ? 8 : 16 / VEC;
+}
+
+template <int OP, typename T, int VEC, int TPR, bool PG>
 const BwdEntry* bwd_pick_slots(int slots) {
+    constexpr int M = bwd_max_slots<VEC>();
     switch (slots) {
-        case 1: return &BwdInst<OP, VEC, 1, TPR, PG>::entry;
-        case 2: return &BwdInst<OP, VEC, 2, TPR, PG>::entry;
-        case 3: return &BwdInst<OP, VEC, 3, TPR, PG>::entry;
-        case 4: return &BwdInst<OP, VEC, 4, TPR, PG>::entry;
-        case 8: if constexpr (VEC == 1) return &BwdInst<OP, VEC, 8, TPR, PG>::entry; else return nullptr;
+        case 1: return &BwdInst<OP, T, VEC, 1, TPR, PG>::entry;
+        case 2: return &BwdInst<OP, T, VEC, 2, TPR, PG>::entry;
+        case 3: if constexpr (M >= 3) return &BwdInst<OP, T, VEC, 3, TPR, PG>::entry; else return nullptr;
+        case 4: if constexpr (M >= 4) return &BwdInst<OP, T, VEC, 4, TPR, PG>::entry; else return nullptr;
+        case 8: if constexpr (M >= 8) return &BwdInst<OP, T, VEC, 8, TPR, PG>::entry; else return nullptr;
         default: return nullptr;
     }
 }
 
-template <int OP, int VEC, bool PG>
+template <int OP, typename T, int VEC, bool PG>
 const BwdEntry* bwd_pick(int slots, int tpr) {
     switch (tpr) {
-        case 32: return bwd_pick_slots<OP, VEC, 32, PG>(slots);
-        case 64: return bwd_pick_slots<OP, VEC, 64, PG>(slots);
-        case 128: return bwd_pick_slots<OP, VEC, 128, PG>(slots);
-        case 256: return bwd_pick_slots<OP, VEC, 256, PG>(slots);
-        case 512: return bwd_pick_slots<OP, VEC, 512, PG>(slots);
-        case 1024: return bwd_pick_slots<OP, VEC, 1024, PG>(slots);
+        case 32: return bwd_pick_slots<OP, T, VEC, 32, PG>(slots);
+        case 64: return bwd_pick_slots<OP, T, VEC, 64, PG>(slots);
+        case 128: return bwd_pick_slots<OP, T, VEC, 128, PG>(slots);
+        case 256: return bwd_pick_slots<OP, T, VEC, 256, PG>(slots);
+        case 512: return bwd_pick_slots<OP, T, VEC, 512, PG>(slots);
+        case 1024: return bwd_pick_slots<OP, T, VEC, 1024, PG>(slots);
         default: return nullptr;
     }
+}
+
+// Every (op, vector width, parameter-gradient) family of one storage type.
+template <typename T>
+const BwdEntry* bwd_pick_type(int op, int vec, int slots, int tpr, bool pg) {
+    constexpr int V = Elem<T>::kVec;
+    if (op == OP_LN) {
+        if (vec == V) return pg ? bwd_pick<OP_LN, T, V, true>(slots, tpr) : bwd_pick<OP_LN, T, V, false>(slots, tpr);
+        return pg ? bwd_pick<OP_LN, T, 1, true>(slots, tpr) : bwd_pick<OP_LN, T, 1, false>(slots, tpr);
+    }
+    if (vec == V) return pg ? bwd_pick<OP_RMS, T, V, true>(slots, tpr) : bwd_pick<OP_RMS, T, V, false>(slots, tpr);
+    return pg ? bwd_pick<OP_RMS, T, 1, true>(slots, tpr) : bwd_pick<OP_RMS, T, 1, false>(slots, tpr);
+}
+
+template <typename TO>
+cudaError_t column_reduce_t(const float* ws, int64_t rows, int64_t width, int64_t d, void* out0,
+                            void* out1, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((width + kReduceCols - 1) / kReduceCols));
+    cfg.blockDim = dim3(kReduceCols * kReduceSlices);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, column_reduce_kernel<TO>, ws, rows, width, d,
+                              static_cast<TO*>(out0), static_cast<TO*>(out1));
 }
 
 }  // namespace rn

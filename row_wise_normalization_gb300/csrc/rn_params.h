@@ -132,7 +132,8 @@ struct BatchEntry {
 // slots: vectors per lane, 1, 2, 4 or 8 (FP32) / 1, 2 or 4 (16-bit).
 const BatchEntry* batched_entry(int op, int dtype, int slots);
 
-// Arguments of the backward kernels (rn_bwd.cuh).
+// Arguments of the backward kernels (rn_bwd.cuh). dy, x, dx and p0 are of the
+// call's storage type (the float pointers are reinterpreted).
 struct BwdParams {
     const float* dy;
     const float* x;
@@ -147,16 +148,18 @@ struct BwdParams {
     float eps;            // RMS only
 };
 
-// Backward kernels. slots: 1, 2, 3, 4 (and 8 with vec 1).
+// Backward kernels. slots: 1-4 (FP32 vectors), 1-2 (16-bit vectors), 1-4 and 8
+// (scalars).
 struct BwdEntry {
     const void* fn;
     int threads;
     int rows_per_cta;
     cudaError_t (*launch)(const BwdParams&, int grid, cudaStream_t);
 };
-const BwdEntry* bwd_entry(int op, int vec, int slots, int tpr, bool pg);
-cudaError_t column_reduce(const float* ws, int64_t groups, int64_t width, int64_t d, float* out0,
-                          float* out1, cudaStream_t s);
+const BwdEntry* bwd_entry(int op, int dtype, int vec, int slots, int tpr, bool pg);
+// out0/out1: the parameter gradients in the storage type `dtype` (or NULL).
+cudaError_t column_reduce(int dtype, const float* ws, int64_t rows, int64_t width, int64_t d,
+                          void* out0, void* out1, cudaStream_t s);
 constexpr int kBwdHeld = 16;   // floats of a row a backward thread holds (x and dy each)
 constexpr int kBwdMinRowsPerGroup = 4;   // rows a backward row group takes at least (with grads)
 

@@ -650,6 +650,7 @@ struct BwdRequest {
     float eps;           // RMS
     void* ws;
     size_t ws_bytes;
+    int dtype = DT_F32;  // storage of dy, x, dx and the parameters and their gradients
 };
 
 struct BwdPlan {
@@ -661,10 +662,11 @@ struct BwdPlan {
 
 int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaError_t* err) {
     *err = cudaSuccess;
-    const bool al = q.d % 4 == 0 &&
+    const int vv = 16 / dtype_size(q.dtype);   // elements of one 128-bit vector
+    const bool al = q.d % vv == 0 &&
                     ((addr(q.dy) | addr(q.x) | addr(q.p0) | addr(q.dx) | addr(q.ws)) & 15u) == 0;
-    const int vec = al ? 4 : 1;
-    const int maxs = vec == 4 ? kBwdHeld / 4 : 8;
+    const int vec = al ? vv : 1;
+    const int maxs = vec == 1 ? 8 : kBwdHeld / vec;
     const int64_t units = q.d / vec;
     int tpr = 0, slots = 0;
     for (int t = 32; t <= 1024; t *= 2)
@@ -675,7 +677,7 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
     if (!tpr) return RN_ERR_SIZE;
     const int need = (int)((units + tpr - 1) / tpr);
     slots = need <= 4 ? need : 8;
-    const BwdEntry* e = bwd_entry(q.op, vec, slots, tpr, pg);
+    const BwdEntry* e = bwd_entry(q.op, q.dtype, vec, slots, tpr, pg);
     if (!e) return RN_ERR_VARIANT;
     // resident CTAs
     int dev = 0, sms = 0, per = 0;
@@ -715,6 +717,7 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
 }
 
 int bwd_validate(const BwdRequest& q, bool pg) {
+    if (q.dtype != DT_F32 && q.dtype != DT_BF16 && q.dtype != DT_F16) return RN_ERR_DTYPE;
     if (q.rows < 0 || q.d <= 0) return RN_ERR_SIZE;
     if (q.rows > 0 && q.d > kMaxElems / q.rows) return RN_ERR_SIZE;
     if (q.op == OP_RMS && (!std::isfinite(q.eps) || q.eps < 0.f)) return RN_ERR_EPS;
@@ -722,11 +725,13 @@ int bwd_validate(const BwdRequest& q, bool pg) {
     if (!q.dy || !q.x || !q.p0 || !q.dx) return RN_ERR_NULL;
     if (q.op == OP_LN && (!q.mean || !q.rstd)) return RN_ERR_NULL;
     if (pg && !q.ws) return RN_ERR_NULL;
-    const void* all[] = {q.dy, q.x, q.p0, q.mean, q.rstd, q.dx, q.dp0, q.dp1};
-    for (const void* p : all)
-        if (misaligned(p, 4)) return RN_ERR_ALIGN;
+    const int es = dtype_size(q.dtype);
+    const void* data[] = {q.dy, q.x, q.p0, q.dx, q.dp0, q.dp1};
+    for (const void* p : data)
+        if (misaligned(p, es)) return RN_ERR_ALIGN;
+    if (misaligned(q.mean, 4) || misaligned(q.rstd, 4)) return RN_ERR_ALIGN;
     if (pg && (addr(q.ws) & 15u)) return RN_ERR_ALIGN;
-    const int64_t nx = q.rows * q.d * 4, np = q.d * 4, ns = q.rows * 4;
+    const int64_t nx = q.rows * q.d * es, np = q.d * es, ns = q.rows * 4;
     const int64_t nws = pg ? (int64_t)q.ws_bytes : 0;
     const void* outs[4] = {q.dx, q.dp0, q.dp1, pg ? q.ws : nullptr};
     const int64_t nouts[4] = {nx, np, np, nws};
@@ -749,8 +754,9 @@ int run_bwd(const BwdRequest& q, void* stream) {
         // an empty batch still defines the parameter gradients: zero
         const cudaStream_t s = (cudaStream_t)stream;
         cudaError_t err = cudaSuccess;
-        if (q.dp0) err = cudaMemsetAsync(q.dp0, 0, (size_t)q.d * 4, s);
-        if (err == cudaSuccess && q.dp1) err = cudaMemsetAsync(q.dp1, 0, (size_t)q.d * 4, s);
+        const size_t np = (size_t)q.d * dtype_size(q.dtype);   // zero is all-zero bits in every type
+        if (q.dp0) err = cudaMemsetAsync(q.dp0, 0, np, s);
+        if (err == cudaSuccess && q.dp1) err = cudaMemsetAsync(q.dp1, 0, np, s);
         return err == cudaSuccess ? RN_OK : fail_cuda(err);
     }
     BwdPlan bp;
@@ -775,9 +781,9 @@ int run_bwd(const BwdRequest& q, void* stream) {
     if (err != cudaSuccess) return fail_cuda(err);
     if (pg) {
         // LN workspace rows: [0, d) dbeta partials, [d, 2d) dgamma partials
-        float* out0 = q.op == OP_LN ? q.dp1 : q.dp0;
-        float* out1 = q.op == OP_LN ? q.dp0 : nullptr;
-        err = column_reduce((const float*)q.ws, bp.groups, bp.width, q.d, out0, out1, s);
+        void* out0 = q.op == OP_LN ? q.dp1 : q.dp0;
+        void* out1 = q.op == OP_LN ? q.dp0 : nullptr;
+        err = column_reduce(q.dtype, (const float*)q.ws, bp.groups, bp.width, q.d, out0, out1, s);
         if (err != cudaSuccess) return fail_cuda(err);
     }
     return RN_OK;
@@ -788,25 +794,30 @@ int bwd_workspace(int op, int64_t rows, int64_t d, size_t* bytes) {
     if (rows < 0 || d <= 0) return RN_ERR_SIZE;
     *bytes = 0;
     if (rows == 0) return RN_OK;
-    BwdRequest q{};
-    q.op = op;
-    q.rows = rows;
-    q.d = d;
-    // the vector and the scalar layout may run different grids: size for
-    // the larger (one workspace row per CTA in both)
-    BwdPlan bp;
-    cudaError_t err;
-    const int st = bwd_plan(q, true, true, &bp, &err);
-    if (st == RN_ERR_CUDA) return fail_cuda(err);
-    if (st != RN_OK) return st;
-    // the scalar layout may fit more CTAs per SM than the vector one
-    BwdRequest qs = q;
-    qs.x = (const float*)4;   // any unaligned address selects the scalar layout
-    BwdPlan bs;
-    const int st2 = bwd_plan(qs, true, true, &bs, &err);
-    int64_t groups = bp.groups;
-    if (st2 == RN_OK && bs.groups > groups) groups = bs.groups;
-    *bytes = (size_t)(groups * bp.width * 4);
+    // every storage type, vector or scalar layout, may run a different grid:
+    // size for the largest (one workspace row of FP32 partials per CTA)
+    int64_t groups = 0, width = 0;
+    int first = RN_ERR_SIZE;
+    for (int dt : {DT_F32, DT_BF16, DT_F16}) {
+        for (uintptr_t xa : {(uintptr_t)0, (uintptr_t)4}) {   // 4: an unaligned address
+            BwdRequest q{};
+            q.op = op;
+            q.rows = rows;
+            q.d = d;
+            q.dtype = dt;
+            q.x = (const float*)xa;
+            BwdPlan bp;
+            cudaError_t err;
+            const int st = bwd_plan(q, true, true, &bp, &err);
+            if (st == RN_ERR_CUDA) return fail_cuda(err);
+            if (dt == DT_F32 && xa == 0) first = st;
+            if (st != RN_OK) continue;
+            if (bp.groups > groups) groups = bp.groups;
+            width = bp.width;
+        }
+    }
+    if (first != RN_OK) return first;   // the FP32 vector layout decides what is valid
+    *bytes = (size_t)(groups * width * 4);
     return RN_OK;
 }
 
@@ -838,6 +849,25 @@ int rms_bwd(const float* dy, const float* x, const float* w, float* dx, float* d
             int64_t d, float eps, void* workspace, size_t workspace_bytes, void* stream) {
     BwdRequest q{OP_RMS, dy, x, w, nullptr, nullptr, dx, dw, nullptr, rows, d, eps,
                  workspace, workspace_bytes};
+    return run_bwd(q, stream);
+}
+
+int ln_bwd_typed(int dtype, const void* dy, const void* x, const void* gamma, const float* mean,
+                 const float* rstd, void* dx, void* dgamma, void* dbeta, int64_t rows, int64_t d,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    BwdRequest q{OP_LN, (const float*)dy, (const float*)x, (const float*)gamma, mean, rstd,
+                 (float*)dx, (float*)dgamma, (float*)dbeta, rows, d, 0.f, workspace,
+                 workspace_bytes};
+    q.dtype = dtype;
+    return run_bwd(q, stream);
+}
+
+int rms_bwd_typed(int dtype, const void* dy, const void* x, const void* w, void* dx, void* dw,
+                  int64_t rows, int64_t d, float eps, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+    BwdRequest q{OP_RMS, (const float*)dy, (const float*)x, (const float*)w, nullptr, nullptr,
+                 (float*)dx, (float*)dw, nullptr, rows, d, eps, workspace, workspace_bytes};
+    q.dtype = dtype;
     return run_bwd(q, stream);
 }
 
