@@ -24,7 +24,10 @@
 // columns' sums over its rows in registers. A CTA holds 256 / TPR row groups
 // (at least one); when its rows are done the groups' sums are added through
 // shared memory in group order and the CTA writes one partial row to the
-// workspace. column_reduce_kernel then adds the CTAs' rows in a fixed order
+// workspace. A 1024-thread row group (rows wider than 8192) has 64 registers
+// a thread, which hold x and dy but not also the parameters and the
+// accumulators: there those live in shared memory instead (SMS), each
+// thread reading and writing only its own entries. column_reduce_kernel then adds the CTAs' rows in a fixed order
 // with Kahan compensation: deterministic for a given grid, no atomics. It is
 // launched as a programmatic dependent of the row kernel, so its launch
 // overlaps the row kernel's tail and it waits (griddepcontrol.wait) for the
@@ -62,6 +65,44 @@ __device__ __forceinline__ void st_ws(float* p, const Vec<VEC>& r) {
     }
 }
 
+// Whether an instance keeps its per-thread state in shared memory, and how
+// many bytes of it: the parameters, and (PG) one or two accumulators, each
+// SLOTS x TPR vectors.
+constexpr bool bwd_sms(int threads) { return threads == 1024; }
+constexpr int bwd_sms_bytes(int op, int vec, int slots, int tpr, bool pg) {
+    return bwd_sms(tpr) ? (1 + (pg ? (op == OP_LN ? 2 : 1) : 0)) * slots * vec * tpr * 4 : 0;
+}
+
+// A thread's vector `s` of one shared-memory plane set: planes of TPR
+// 16-byte chunks (VEC 4 or 8) or floats (VEC 1), so that a warp's accesses to
+// one plane are contiguous and free of bank conflicts.
+template <int VEC, int TPR>
+__device__ __forceinline__ void sms_ld(Vec<VEC>& v, const float* base, int s, int t) {
+    if constexpr (VEC == 1) {
+        v.v[0] = base[s * TPR + t];
+    } else {
+#pragma unroll
+        for (int c = 0; c < VEC / 4; ++c) {
+            const float4 q = reinterpret_cast<const float4*>(base)[(s * (VEC / 4) + c) * TPR + t];
+            v.v[4 * c] = q.x;
+            v.v[4 * c + 1] = q.y;
+            v.v[4 * c + 2] = q.z;
+            v.v[4 * c + 3] = q.w;
+        }
+    }
+}
+template <int VEC, int TPR>
+__device__ __forceinline__ void sms_st(float* base, int s, int t, const Vec<VEC>& v) {
+    if constexpr (VEC == 1) {
+        base[s * TPR + t] = v.v[0];
+    } else {
+#pragma unroll
+        for (int c = 0; c < VEC / 4; ++c)
+            reinterpret_cast<float4*>(base)[(s * (VEC / 4) + c) * TPR + t] =
+                make_float4(v.v[4 * c], v.v[4 * c + 1], v.v[4 * c + 2], v.v[4 * c + 3]);
+    }
+}
+
 template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PG>
 __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC, PG))
     bwd_kernel(const BwdParams p) {
@@ -84,31 +125,52 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
     const int64_t group = (int64_t)blockIdx.x * RPC + g;
     const int64_t ngroups = (int64_t)gridDim.x * RPC;
 
-    // parameters of my columns, held for every row
-    Vec<VEC> par[SLOTS];
+    // parameters of my columns, held for every row (in registers, or SMS:
+    // in shared memory, as are the accumulators)
+    constexpr bool SMS = bwd_sms(TPR * RPC);
+    constexpr int NR = SMS ? 1 : SLOTS;   // vectors of state held in registers
+    extern __shared__ __align__(16) float bwd_state[];
+    float* const s_par = bwd_state;
+    float* const s_acc0 = bwd_state + SLOTS * VEC * TPR;
+    float* const s_acc1 = s_acc0 + SLOTS * VEC * TPR;
+    Vec<VEC> par[NR];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
         const int q = t + s * TPR;
+        Vec<VEC> v;
         if (q < nv) {
-            ldt_p(par[s], P0 + q * VEC, true);
+            ldt_p(v, P0 + q * VEC, true);
         } else {
 #pragma unroll
-            for (int k = 0; k < VEC; ++k) par[s].v[k] = 0.f;
+            for (int k = 0; k < VEC; ++k) v.v[k] = 0.f;
         }
+        if constexpr (SMS)
+            sms_st<VEC, TPR>(s_par, s, t, v);
+        else
+            par[s] = v;
     }
-    Vec<VEC> acc0[PG ? SLOTS : 1], acc1[(PG && OP == OP_LN) ? SLOTS : 1];
+    Vec<VEC> acc0[PG ? NR : 1], acc1[(PG && OP == OP_LN) ? NR : 1];
     if constexpr (PG) {
+        Vec<VEC> z;
 #pragma unroll
-        for (int s = 0; s < SLOTS; ++s)
+        for (int k = 0; k < VEC; ++k) z.v[k] = 0.f;
 #pragma unroll
-            for (int k = 0; k < VEC; ++k) {
-                acc0[s].v[k] = 0.f;
-                if constexpr (OP == OP_LN) acc1[s].v[k] = 0.f;
+        for (int s = 0; s < SLOTS; ++s) {
+            if constexpr (SMS) {
+                sms_st<VEC, TPR>(s_acc0, s, t, z);
+                if constexpr (OP == OP_LN) sms_st<VEC, TPR>(s_acc1, s, t, z);
+            } else {
+                acc0[s] = z;
+                if constexpr (OP == OP_LN) acc1[s] = z;
             }
+        }
     }
 
     int it = 0;
     for (int64_t row = group; row < p.rows; row += ngroups, ++it) {
+        // SMS: re-read the state every row rather than let it be hoisted
+        // into registers that the held row needs
+        if constexpr (SMS) asm volatile("" ::: "memory");
         const T* xr = X + row * p.d;
         const T* dyr = DY + row * p.d;
         Vec<VEC> xv[SLOTS], dv[SLOTS];
@@ -123,6 +185,15 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
                 for (int k = 0; k < VEC; ++k) xv[s].v[k] = dv[s].v[k] = 0.f;
             }
         }
+        // vector layout (every row whole 16-byte chunks): the group's next
+        // row is fetched into L2 while this one is reduced and written
+        if constexpr (VEC > 1) {
+            const int64_t nx = row + ngroups;
+            if (t == 0 && nx < p.rows) {
+                prefetch_l2_bulk(X + nx * p.d, (uint32_t)(p.d * (int64_t)sizeof(T)));
+                prefetch_l2_bulk(DY + nx * p.d, (uint32_t)(p.d * (int64_t)sizeof(T)));
+            }
+        }
         float mu = 0.f, rs = 0.f;
         if constexpr (OP == OP_LN) {
             mu = ld_p1(p.mean + row);
@@ -133,9 +204,14 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             if (t + s * TPR < nv) {
+                Vec<VEC> ps;
+                if constexpr (SMS)
+                    sms_ld<VEC, TPR>(ps, s_par, s, t);
+                else
+                    ps = par[s];
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) {
-                    const float gk = __fmul_rn(dv[s].v[k], par[s].v[k]);
+                    const float gk = __fmul_rn(dv[s].v[k], ps.v[k]);
                     if constexpr (OP == OP_LN) {
                         const float xh = (xv[s].v[k] - mu) * rs;
                         s1 += gk;
@@ -178,20 +254,42 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
         for (int s = 0; s < SLOTS; ++s) {
             const int q = t + s * TPR;
             if (q < nv) {
-                Vec<VEC> o;
+                Vec<VEC> o, ps, a0, a1;
+                if constexpr (SMS) {
+                    sms_ld<VEC, TPR>(ps, s_par, s, t);
+                    if constexpr (PG) {
+                        sms_ld<VEC, TPR>(a0, s_acc0, s, t);
+                        if constexpr (OP == OP_LN) sms_ld<VEC, TPR>(a1, s_acc1, s, t);
+                    }
+                } else {
+                    ps = par[s];
+                    if constexpr (PG) {
+                        a0 = acc0[s];
+                        if constexpr (OP == OP_LN) a1 = acc1[s];
+                    }
+                }
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) {
-                    const float gk = __fmul_rn(dv[s].v[k], par[s].v[k]);
+                    const float gk = __fmul_rn(dv[s].v[k], ps.v[k]);
                     if constexpr (OP == OP_LN) {
                         const float xh = (xv[s].v[k] - mu) * rs;
                         o.v[k] = rs * (gk - c1 - xh * c2);
                         if constexpr (PG) {
-                            acc0[s].v[k] += dv[s].v[k];
-                            acc1[s].v[k] = fmaf(dv[s].v[k], xh, acc1[s].v[k]);
+                            a0.v[k] += dv[s].v[k];
+                            a1.v[k] = fmaf(dv[s].v[k], xh, a1.v[k]);
                         }
                     } else {
                         o.v[k] = rs * (gk - xv[s].v[k] * c2);
-                        if constexpr (PG) acc0[s].v[k] = fmaf(dv[s].v[k], xv[s].v[k] * rs, acc0[s].v[k]);
+                        if constexpr (PG) a0.v[k] = fmaf(dv[s].v[k], xv[s].v[k] * rs, a0.v[k]);
+                    }
+                }
+                if constexpr (PG) {
+                    if constexpr (SMS) {
+                        sms_st<VEC, TPR>(s_acc0, s, t, a0);
+                        if constexpr (OP == OP_LN) sms_st<VEC, TPR>(s_acc1, s, t, a1);
+                    } else {
+                        acc0[s] = a0;
+                        if constexpr (OP == OP_LN) acc1[s] = a1;
                     }
                 }
                 stt_y(dxr + q * VEC, o);
@@ -204,7 +302,21 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
 
     if constexpr (PG) {
         float* wr = p.ws + (int64_t)blockIdx.x * p.ws_width;
-        if constexpr (RPC == 1) {
+        if constexpr (SMS) {
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int q = t + s * TPR;
+                if (q < nv) {
+                    Vec<VEC> a;
+                    sms_ld<VEC, TPR>(a, s_acc0, s, t);
+                    st_ws(wr + q * VEC, a);
+                    if constexpr (OP == OP_LN) {
+                        sms_ld<VEC, TPR>(a, s_acc1, s, t);
+                        st_ws(wr + d + q * VEC, a);
+                    }
+                }
+            }
+        } else if constexpr (RPC == 1) {
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
                 const int q = t + s * TPR;
@@ -296,9 +408,15 @@ namespace rn {
 template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PG>
 struct BwdInst {
     static constexpr int RPC = TPR < 256 ? 256 / TPR : 1;
+    static constexpr int SMEM = bwd_sms_bytes(OP, VEC, SLOTS, TPR * RPC, PG);
     static cudaError_t launch(const BwdParams& p, int grid, cudaStream_t s) {
-        bwd_kernel<OP, T, VEC, SLOTS, TPR, RPC, PG><<<grid, TPR * RPC, 0, s>>>(p);
+        bwd_kernel<OP, T, VEC, SLOTS, TPR, RPC, PG><<<grid, TPR * RPC, SMEM, s>>>(p);
         return cudaGetLastError();
+    }
+    // the limit is per function and process-wide; raising it again is harmless
+    static cudaError_t prepare() {
+        return cudaFuncSetAttribute(bwd_kernel<OP, T, VEC, SLOTS, TPR, RPC, PG>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     }
     static const BwdEntry entry;
 };
@@ -307,7 +425,9 @@ template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PG>
 const BwdEntry BwdInst<OP, T, VEC, SLOTS, TPR, PG>::entry = {
     (const void*)&bwd_kernel<OP, T, VEC, SLOTS, TPR, BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC, PG>,
     TPR * BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC, BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC,
-    &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::launch};
+    BwdInst<OP, T, VEC, SLOTS, TPR, PG>::SMEM, &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::launch,
+    BwdInst<OP, T, VEC, SLOTS, TPR, PG>::SMEM > 48 * 1024 ? &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::prepare
+                                                          : nullptr};
 
 // Vectors a backward thread holds: up to 16 floats of x and of dy (4 FP32 or
 // 2 16-bit vectors), or 8 scalars.

@@ -19,6 +19,12 @@ namespace rn {
 // they go through the read-only path with L1 allocation. y is written once and
 // never re-read by the kernel, so it is stored with the streaming (.cs) hint.
 // ---------------------------------------------------------------------------
+// Asks the bulk-copy engine to bring `bytes` (a multiple of 16) from a
+// 16-byte-aligned global address into L2, without waiting for them.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float4 ld_x4(const float* p) {
     float4 v;
     asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"

@@ -71,14 +71,18 @@ const KernelEntry* reg_entry(int op, int dtype, int vec, int slots, int tpr, boo
 //    prefetch there (LayerNorm BF16 32768 x 4096: 123 -> 96 us);
 //  * parameters held across rows for rows of up to 128 threads holding at
 //    most 6 vectors each, when every row starts at the same 16-byte phase
-//    (with 8 vectors the held parameters cost a resident CTA per SM).
+//    (with 8 vectors the held parameters cost a resident CTA per SM) --
+//    except the 16-bit slices of 24 floats on 128-thread rows, which run at
+//    1024 resident threads per SM where the held parameters would spill
+//    (LayerNorm BF16 32768 x 3072: 90.4 -> 76.2 us without them).
 constexpr bool reg_prefetch(int vec, int slots, int tpr, bool res = false) {
     return vec > 1 && !(slots * vec >= 32 && tpr == 256) && (!res || slots <= 4) &&
            !(vec == 8 && slots * vec >= 24 && tpr >= 128) &&   // 16-bit: occupancy wins
            (52 + 2 * slots * vec) * tpr <= 65536;   // both rows fit the registers of one CTA
 }
 constexpr bool reg_may_hold_params(int vec, int slots, int tpr) {
-    return vec > 1 && tpr <= 128 && slots * vec <= 24;
+    return vec > 1 && tpr <= 128 && slots * vec <= 24 &&
+           !(vec == 8 && slots * vec >= 24 && tpr >= 128);   // 16-bit: occupancy wins
 }
 
 // Streaming two-read kernels (any width); res: with a residual add (FP32).
@@ -154,7 +158,10 @@ struct BwdEntry {
     const void* fn;
     int threads;
     int rows_per_cta;
+    int smem_bytes;       // dynamic shared memory per CTA (the 1024-thread instances)
     cudaError_t (*launch)(const BwdParams&, int grid, cudaStream_t);
+    // Raises the kernel's dynamic shared memory limit (NULL if not needed).
+    cudaError_t (*prepare)();
 };
 const BwdEntry* bwd_entry(int op, int dtype, int vec, int slots, int tpr, bool pg);
 // out0/out1: the parameter gradients in the storage type `dtype` (or NULL).

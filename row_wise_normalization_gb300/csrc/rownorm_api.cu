@@ -684,8 +684,9 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
     if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return RN_ERR_CUDA;
     if ((*err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return RN_ERR_CUDA;
-    if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, e->fn, e->threads, 0)) !=
-        cudaSuccess)
+    if (e->prepare && (*err = e->prepare()) != cudaSuccess) return RN_ERR_CUDA;
+    if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, e->fn, e->threads,
+                                                              e->smem_bytes)) != cudaSuccess)
         return RN_ERR_CUDA;
     int64_t grid = (int64_t)(per > 0 ? per : 1) * sms;
     const int64_t rows_ctas = (q.rows + e->rows_per_cta - 1) / e->rows_per_cta;

@@ -44,7 +44,8 @@ def _check(op, dtype, wide, out):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("d", [1, 7, 8, 9, 33, 128, 768, 1029, 4099, 8193, 20000, 40003])
+@pytest.mark.parametrize("d", [1, 7, 8, 9, 33, 128, 768, 1029, 3072, 4099, 8193, 20000,
+                               40003])
 def test_16bit_every_variant_and_phase(dtype, d):
     bits, wide = _case(23, d, seed=71, dtype=dtype)
     for x_off, y_off, p_off in ((0, 0, 0), (1, 1, 3), (5, 5, 1), (7, 7, 0), (0, 3, 0)):
@@ -57,8 +58,8 @@ def test_16bit_every_variant_and_phase(dtype, d):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("wl", [workloads.ln_4096x768(), workloads.Workload("ln", 32768, 4096,
-                                                                            seed=73)],
+@pytest.mark.parametrize("wl", [workloads.ln_4096x768(), workloads.Workload("ln", 4096, 3072, seed=74),
+                                workloads.Workload("ln", 32768, 4096, seed=73)],
                          ids=lambda w: f"{w.rows}x{w.d}")
 def test_16bit_larger_shapes(dtype, wl):
     xb, xw = workloads.to_storage(wl.x(), dtype)

@@ -82,7 +82,7 @@ def _stats(x, g):
     return mean.astype(np.float32), rstd.astype(np.float32)
 
 
-@pytest.mark.parametrize("d", [1, 3, 31, 128, 768, 1029, 4096, 8192, 16384])
+@pytest.mark.parametrize("d", [1, 3, 31, 128, 768, 1029, 4096, 8192, 12288, 16384])
 @pytest.mark.parametrize("off", [0, 1])
 def test_ln_backward(d, off):
     rows = 300
@@ -94,7 +94,7 @@ def test_ln_backward(d, off):
     _check_ln(x, dy, g, out, chain=_chain(rows))
 
 
-@pytest.mark.parametrize("d", [1, 33, 768, 4096, 16384])
+@pytest.mark.parametrize("d", [1, 33, 768, 4096, 8192, 12288, 16384])
 @pytest.mark.parametrize("off", [0, 3])
 def test_rms_backward(d, off):
     rows = 257
@@ -109,7 +109,8 @@ def test_rms_backward(d, off):
     parity.check_colsum(dw, dwr, terms, _chain(rows), "dw")
 
 
-@pytest.mark.parametrize("rows,d", [(4096, 768), (32768, 1024), (8192, 4096)])
+@pytest.mark.parametrize("rows,d", [(4096, 768), (32768, 1024), (8192, 4096), (1000, 12288),
+                                    (700, 16384)])
 def test_backward_larger(rows, d):
     x, dy, g, _ = _case(rows, d, seed=85, dist="normal")
     m32, r32 = _stats(x, g)

@@ -103,7 +103,7 @@ def _stats(xw, gw, bw):
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("op", [LN, RMS])
 @pytest.mark.parametrize("d,off", [(1, 0), (33, 1), (768, 0), (768, 1), (1000, 0), (1000, 3),
-                                   (4096, 0), (8192, 2), (16384, 0)])
+                                   (4096, 0), (8192, 2), (12288, 0), (16384, 0)])
 def test_backward_16bit(dtype, op, d, off):
     rows = 300 if d <= 4096 else 61
     dist = "offset" if dtype == "bf16" else "normal"
