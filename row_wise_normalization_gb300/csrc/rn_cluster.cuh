@@ -119,6 +119,14 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
         if constexpr (PF) {
             if (nrow < p.rows) load(nxt, nrow);
         }
+        // aligned rows: the bulk-copy engine fetches this CTA's slice of the
+        // row after the ones held into L2 (one instruction, one thread)
+        if constexpr (AL) {
+            const int64_t frow = PF ? nrow + nclusters : nrow;
+            if (t == 0 && frow < p.rows && cur.nq > 0)
+                prefetch_l2_bulk(p.x + frow * p.ldx + 4 * (int64_t)cur.q0,
+                                 (uint32_t)cur.nq * 16u);
+        }
         const int h = cur.h, nv = cur.nv, tl = cur.tl, q0 = cur.q0, nq = cur.nq;
         const bool has_e = !AL && c == 0 && t < h + tl;
         const int ei = (t < h) ? t : h + 4 * nv + (t - h);
