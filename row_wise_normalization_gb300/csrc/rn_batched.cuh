@@ -169,10 +169,11 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
     }
 }
 
-// Register budget per SLOTS: about 12 per held float and 40 fixed, plus the
+// Register budget per SLOTS: about 12 per held float and 52 fixed (the
+// problem's fields, the row's head/tail and alignment state), plus the
 // early-loaded parameters of slices of at most 8 floats.
 constexpr int batch_min_ctas(int slots, int vec) {
-    const int regs = 40 + 12 * slots * vec / 4 + (slots * vec <= 8 ? 2 * slots * vec : 0);
+    const int regs = 52 + 12 * slots * vec / 4 + (slots * vec <= 8 ? 2 * slots * vec : 0);
     const int n = 65536 / (((regs + 7) / 8) * 8 * kBatchThreads);
     return n < 1 ? 1 : (n > 16 ? 16 : n);
 }

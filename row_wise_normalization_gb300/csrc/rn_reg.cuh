@@ -58,7 +58,7 @@ constexpr int reg_budget(int op, int vec, int slots, bool pf, bool pp, bool res 
 // SM, LayerNorm rows of 256 threads at 768. Narrower slices fill the SM as
 // far as the budget allows.
 constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, bool pp,
-                           bool res = false) {
+                           bool res = false, bool al = true) {
     if (vec == 8 && slots * vec >= 24 && !pf && threads >= 128) {
         const int target = (op == 0 && threads == 256) ? 768 : 1024;
         return target / threads > 0 ? target / threads : 1;
@@ -71,7 +71,10 @@ constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, boo
         if (threads < 256) return 512 / threads;
         return threads >= 1024 ? 1 : (threads == 512 ? 2 : 768 / threads);
     }
-    const int per = ((reg_budget(op, vec, slots, pf, pp, res) + 7) / 8) * 8;
+    // the general (unaligned) vector layout also carries the row's head
+    // and tail scalars, their parameters and per-row alignment tests
+    const int extra = (!al && vec > 1) ? 12 : 0;
+    const int per = ((reg_budget(op, vec, slots, pf, pp, res) + extra + 7) / 8) * 8;
     const int n = 65536 / (per * threads);
     return n < 1 ? 1 : (n > 32 ? 32 : n);
 }
@@ -156,7 +159,7 @@ __device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const T* x
 
 template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL,
           bool RES>
-__global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES))
+__global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES, AL))
     reg_kernel(const Params p) {
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
     static_assert(VEC == 1 || VEC == Elem<T>::kVec, "a vector is one 128-bit access");
@@ -475,10 +478,18 @@ const KernelEntry RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::entry = {
     &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::launch, nullptr};
 
 // Slots per thread a family is compiled for: up to 8 FP32 vectors (32 floats),
-// 4 16-bit vectors (32 floats) or 8 scalars; held parameters allow 24 floats.
-template <typename T, int VEC, bool PP>
+// 4 16-bit vectors (32 floats) or 8 scalars; held parameters allow 24 floats,
+// on the rows where the planner holds them (reg_may_hold_params).
+template <typename T, int VEC, bool PP, int TPR>
 constexpr int reg_max_slots() {
-    return PP ? 24 / VEC : (VEC == 1 ? 8 : 32 / VEC);
+    if constexpr (PP) {
+        int m = 0;
+        for (int s = 1; s <= 24 / VEC; ++s)
+            if (reg_may_hold_params(VEC, s, TPR)) m = s;
+        return m;
+    } else {
+        return VEC == 1 ? 8 : 32 / VEC;
+    }
 }
 
 template <int OP, typename T, int VEC, int S, int TPR, bool PP, bool AL, bool RES, bool NOPF>
@@ -491,7 +502,7 @@ const KernelEntry* reg_inst_entry() {
 
 template <int OP, typename T, int VEC, int TPR, bool PP, bool AL, bool RES, bool NOPF = false>
 const KernelEntry* reg_pick_slots(int slots) {
-    constexpr int M = reg_max_slots<T, VEC, PP>();
+    constexpr int M = reg_max_slots<T, VEC, PP, TPR>();
     if (slots < 1 || slots > M) return nullptr;
     switch (slots) {
         case 1: return reg_inst_entry<OP, T, VEC, 1, TPR, PP, AL, RES, NOPF>();
