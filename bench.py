@@ -1019,6 +1019,80 @@ def run_reference(args, rank, world):
     return line
 
 
+VARIANTS = ("auto", "warp", "block", "staged", "stream", "cluster")
+
+
+def run_case(args):
+    """One forward call, variant forced, timed alone: W warm-up launches, K
+    launches each after the L2 flush (cold), then K launches back to back on
+    the same buffers behind a GPU spin (warm). Prints one JSON line. The
+    launch order is fixed so that an ncu capture can select a cold launch
+    (any launch under --cache-control all) or a warm one (launch W + K + 2
+    under --cache-control none: a warm launch that follows another)."""
+    import torch
+
+    import row_wise_normalization_gb300 as rn
+    from row_wise_normalization_gb300 import capi
+
+    capi.load()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    peak, _ = hbm_peak()
+    op, rows, d = args.case.split(":")
+    rows, d = int(rows), int(d)
+    if op not in ("ln", "rms"):
+        raise SystemExit("--case takes ln:rows:d or rms:rows:d")
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[args.dtype]
+    esz = 4 if args.dtype == "f32" else 2
+    wl = workloads.Workload(op, rows, d, seed=1)
+    x = torch.from_numpy(wl.x()).to(device).to(dt)
+    ps = [torch.from_numpy(p_).to(device).to(dt) for p_ in wl.params()]
+    y = torch.empty_like(x)
+    variant = VARIANTS.index(args.variant)
+    if args.residual:
+        r = torch.from_numpy(workloads.Workload(op, rows, d, seed=2).x()).to(device).to(dt)
+        h = torch.empty_like(x)
+    if op == "ln":
+        mean = torch.empty(rows, device=device)
+        rstd = torch.empty(rows, device=device)
+        if args.residual:
+            f = lambda: rn.ln_fwd_residual(x, r, ps[0], ps[1], wl.eps, h=h, y=y, mean=mean,
+                                           rstd=rstd, variant=variant)
+        else:
+            f = lambda: rn.ln_fwd(x, ps[0], ps[1], wl.eps, y=y, mean=mean, rstd=rstd,
+                                  variant=variant)
+        nbytes = (2 * esz * rows * d + 2 * esz * d + 8 * rows)
+    else:
+        if args.residual:
+            f = lambda: rn.rms_fwd_residual(x, r, ps[0], wl.eps, h=h, y=y, variant=variant)
+        else:
+            f = lambda: rn.rms_fwd(x, ps[0], wl.eps, y=y, variant=variant)
+        nbytes = 2 * esz * rows * d + esz * d
+    if args.residual:
+        nbytes += 2 * esz * rows * d
+    for _ in range(args.warmup):
+        f()
+    torch.cuda.synchronize()
+    flush = Flusher(torch, device)
+    cold = time_launches(torch, f, args.steps, flush)
+    warm = time_launches(torch, f, args.steps)
+    opc = capi.RN_OP_LN if op == "ln" else capi.RN_OP_RMS
+    if args.residual:
+        pl = capi.plan_residual(opc, variant, d, x.data_ptr(), r.data_ptr(), h.data_ptr(),
+                                y.data_ptr())
+    else:
+        pl = capi.plan_typed(("f32", "bf16", "f16").index(args.dtype), opc, variant, d,
+                             x.data_ptr(), y.data_ptr())
+    out = {"case": f"{op}{'_residual' if args.residual else ''}_{args.dtype}_{rows}x{d}",
+           "variant": args.variant, "planned": capi.variant_name(pl.variant),
+           "bytes": nbytes}
+    for name, ts in (("cold", cold), ("warm", warm)):
+        med = statistics.median(ts)
+        out[name] = {"ms_median": med, "GBps": gbs(nbytes, med),
+                     "frac_of_measured_hbm": gbs(nbytes, med) / peak}
+    print(json.dumps(out))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1030,7 +1104,15 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="ln_4096x768",
                     help="named workload or op:rows:d (default: the 4096x768 LayerNorm)")
+    ap.add_argument("--case", default=None,
+                    help="op:rows:d -- time one forward call alone, cold and warm (see run_case)")
+    ap.add_argument("--variant", choices=VARIANTS, default="auto")
+    ap.add_argument("--dtype", choices=("f32", "bf16", "f16"), default="f32")
+    ap.add_argument("--residual", action="store_true")
     args = ap.parse_args(argv)
+    if args.case is not None:
+        run_case(args)
+        return 0
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
