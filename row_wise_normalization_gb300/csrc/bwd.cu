@@ -6,6 +6,8 @@ namespace rn {
 
 const BwdEntry* bwd_entry_bf16(int op, int vec, int slots, int tpr, bool pg);
 const BwdEntry* bwd_entry_f16(int op, int vec, int slots, int tpr, bool pg);
+const BwdEntry* bwd_staged_entry_bf16(int op, int slots, int tpr, bool pg);
+const BwdEntry* bwd_staged_entry_f16(int op, int slots, int tpr, bool pg);
 cudaError_t column_reduce_bf16(const float* ws, int64_t rows, int64_t width, int64_t d,
                                void* out0, void* out1, cudaStream_t s);
 cudaError_t column_reduce_f16(const float* ws, int64_t rows, int64_t width, int64_t d,
@@ -16,6 +18,15 @@ const BwdEntry* bwd_entry(int op, int dtype, int vec, int slots, int tpr, bool p
         case DT_F32: return bwd_pick_type<float>(op, vec, slots, tpr, pg);
         case DT_BF16: return bwd_entry_bf16(op, vec, slots, tpr, pg);
         case DT_F16: return bwd_entry_f16(op, vec, slots, tpr, pg);
+        default: return nullptr;
+    }
+}
+
+const BwdEntry* bwd_staged_entry(int op, int dtype, int slots, int tpr, bool pg) {
+    switch (dtype) {
+        case DT_F32: return bwd_staged_pick_type<float>(op, slots, tpr, pg);
+        case DT_BF16: return bwd_staged_entry_bf16(op, slots, tpr, pg);
+        case DT_F16: return bwd_staged_entry_f16(op, slots, tpr, pg);
         default: return nullptr;
     }
 }

@@ -34,7 +34,7 @@
 // row kernel's writes before reading.
 #pragma once
 
-#include "rn_device.cuh"
+#include "rn_async.cuh"
 
 namespace rn {
 
@@ -103,11 +103,22 @@ __device__ __forceinline__ void sms_st(float* base, int s, int t, const Vec<VEC>
     }
 }
 
-template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PG>
+// STG (staged): one CTA is one row group (RPC == 1, 256 or 512 threads,
+// vector layout) and thread 0 has the bulk-copy engine bring the CTA's rows
+// of x and dy into a ring of p.stages (2..kBwdMaxStages) shared-memory
+// stages, p.stages - 1 rows ahead of the row being reduced: the bytes in flight no longer depend on the
+// registers the accumulators leave. A stage is refilled once every thread
+// has passed the next row's exchange barrier (all its reads of the stage are
+// done). Each wait is bounded; a CTA whose wait runs out (the vote at that
+// barrier) sets a bit in p.err, waits (bounded) for its copies still in
+// flight and returns.
+template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PG, bool STG = false>
 __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC, PG))
     bwd_kernel(const BwdParams p) {
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
     static_assert(VEC == 1 || VEC == Elem<T>::kVec, "a vector is one 128-bit access");
+    static_assert(!STG || (RPC == 1 && VEC > 1 && TPR >= 64 && !bwd_sms(TPR)),
+                  "staged: one row group per CTA, vector layout, state in registers");
     const T* X = reinterpret_cast<const T*>(p.x);
     const T* DY = reinterpret_cast<const T*>(p.dy);
     const T* P0 = reinterpret_cast<const T*>(p.p0);
@@ -125,11 +136,37 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
     const int64_t group = (int64_t)blockIdx.x * RPC + g;
     const int64_t ngroups = (int64_t)gridDim.x * RPC;
 
+    // staged: the ring (in dynamic shared memory; SMS is off) and the
+    // issue of the CTA's k-th row into stage k % nst (thread 0)
+    extern __shared__ __align__(16) float bwd_state[];
+    __shared__ __align__(8) unsigned long long sbar[STG ? kBwdMaxStages : 1];
+    const int nst = STG ? p.stages : 1;
+    const int64_t rowbytes = (int64_t)d * (int64_t)sizeof(T);
+    const int64_t rpad = (rowbytes + 127) / 128 * 128;
+    unsigned char* const ring = reinterpret_cast<unsigned char*>(bwd_state);
+    auto issue = [&](int k) {
+        const int64_t r = group + (int64_t)k * ngroups;
+        if (r >= p.rows) return;
+        const int st = k % nst;
+        const uint32_t bar = smem_addr(&sbar[st]);
+        unsigned char* const base = ring + (size_t)st * 2 * rpad;
+        mbar_arrive_expect_tx(bar, (uint32_t)(2 * rowbytes));
+        bulk_g2s(smem_addr(base), X + r * p.d, (uint32_t)rowbytes, bar);
+        bulk_g2s(smem_addr(base + rpad), DY + r * p.d, (uint32_t)rowbytes, bar);
+    };
+    if constexpr (STG) {
+        if (t == 0) {
+            for (int k = 0; k < nst; ++k) mbar_init(smem_addr(&sbar[k]), 1);
+            mbar_fence_init();
+            for (int k = 0; k < nst; ++k) issue(k);
+        }
+        __syncthreads();
+    }
+
     // parameters of my columns, held for every row (in registers, or SMS:
     // in shared memory, as are the accumulators)
     constexpr bool SMS = bwd_sms(TPR * RPC);
     constexpr int NR = SMS ? 1 : SLOTS;   // vectors of state held in registers
-    extern __shared__ __align__(16) float bwd_state[];
     float* const s_par = bwd_state;
     float* const s_acc0 = bwd_state + SLOTS * VEC * TPR;
     float* const s_acc1 = s_acc0 + SLOTS * VEC * TPR;
@@ -174,30 +211,53 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
         const T* xr = X + row * p.d;
         const T* dyr = DY + row * p.d;
         Vec<VEC> xv[SLOTS], dv[SLOTS];
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s) {
-            const int q = t + s * TPR;
-            if (q < nv) {
-                ldt_x(xv[s], xr + q * VEC);
-                ldt_x(dv[s], dyr + q * VEC);
-            } else {
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) xv[s].v[k] = dv[s].v[k] = 0.f;
-            }
-        }
-        // vector layout (every row whole 16-byte chunks): the group's next
-        // row is fetched into L2 while this one is reduced and written
-        if constexpr (VEC > 1) {
-            const int64_t nx = row + ngroups;
-            if (t == 0 && nx < p.rows) {
-                prefetch_l2_bulk(X + nx * p.d, (uint32_t)(p.d * (int64_t)sizeof(T)));
-                prefetch_l2_bulk(DY + nx * p.d, (uint32_t)(p.d * (int64_t)sizeof(T)));
-            }
-        }
         float mu = 0.f, rs = 0.f;
-        if constexpr (OP == OP_LN) {
-            mu = ld_p1(p.mean + row);
-            rs = ld_p1(p.rstd + row);
+        bool ok = true;   // staged: this thread's wait for the row completed
+        if constexpr (STG) {
+            if constexpr (OP == OP_LN) {
+                mu = ld_p1(p.mean + row);
+                rs = ld_p1(p.rstd + row);
+            }
+            const int st = it % nst;
+            ok = mbar_wait_bounded(smem_addr(&sbar[st]), (uint32_t)((it / nst) & 1));
+            const T* sx = reinterpret_cast<const T*>(ring + (size_t)st * 2 * rpad);
+            const T* sdy = reinterpret_cast<const T*>(ring + (size_t)st * 2 * rpad + rpad);
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int q = t + s * TPR;
+                if (ok && q < nv) {
+                    lds_vec<T, VEC>(xv[s], sx + q * VEC);
+                    lds_vec<T, VEC>(dv[s], sdy + q * VEC);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) xv[s].v[k] = dv[s].v[k] = 0.f;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                const int q = t + s * TPR;
+                if (q < nv) {
+                    ldt_x(xv[s], xr + q * VEC);
+                    ldt_x(dv[s], dyr + q * VEC);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) xv[s].v[k] = dv[s].v[k] = 0.f;
+                }
+            }
+            // vector layout (every row whole 16-byte chunks): the group's next
+            // row is fetched into L2 while this one is reduced and written
+            if constexpr (VEC > 1) {
+                const int64_t nx = row + ngroups;
+                if (t == 0 && nx < p.rows) {
+                    prefetch_l2_bulk(X + nx * p.d, (uint32_t)(p.d * (int64_t)sizeof(T)));
+                    prefetch_l2_bulk(DY + nx * p.d, (uint32_t)(p.d * (int64_t)sizeof(T)));
+                }
+            }
+            if constexpr (OP == OP_LN) {
+                mu = ld_p1(p.mean + row);
+                rs = ld_p1(p.rstd + row);
+            }
         }
         // two row sums: LN (sum g, sum g*xhat); RMS (sum x^2, sum g*x)
         float s1 = 0.f, s2 = 0.f;
@@ -231,7 +291,27 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
                 slot[w][0] = s1;
                 slot[w][1] = s2;
             }
-            named_sync(1 + g, TPR);
+            if constexpr (STG) {
+                if (!__syncthreads_and(ok)) {
+                    // a wait ran out: record it, let this CTA's copies still
+                    // in flight (rows it .. it + nst - 2) land, and leave
+                    if (t == 0) {
+                        if (p.err) atomicOr(p.err, kErrStagedTimeout);
+                        for (int k = it; k < it + nst - 1; ++k)
+                            if (group + (int64_t)k * ngroups < p.rows)
+                                (void)mbar_wait_bounded(smem_addr(&sbar[k % nst]),
+                                                        (uint32_t)((k / nst) & 1));
+                    }
+                    return;
+                }
+                // every thread is past its reads of the previous row's stage
+                if (t == 0 && it >= 1) {
+                    fence_proxy_async_smem();
+                    issue(it - 1 + nst);
+                }
+            } else {
+                named_sync(1 + g, TPR);
+            }
             s1 = 0.f;
             s2 = 0.f;
 #pragma unroll
@@ -428,6 +508,57 @@ const BwdEntry BwdInst<OP, T, VEC, SLOTS, TPR, PG>::entry = {
     BwdInst<OP, T, VEC, SLOTS, TPR, PG>::SMEM, &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::launch,
     BwdInst<OP, T, VEC, SLOTS, TPR, PG>::SMEM > 48 * 1024 ? &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::prepare
                                                           : nullptr};
+
+// Staged instances: the ring's size follows d and p.stages, so the dynamic
+// shared memory is set per launch and its limit raised once to the whole
+// budget.
+template <int OP, typename T, int SLOTS, int TPR, bool PG>
+struct BwdStagedInst {
+    static constexpr int VEC = Elem<T>::kVec;
+    static cudaError_t launch(const BwdParams& p, int grid, cudaStream_t s) {
+        const int smem = (int)(p.stages * bwd_stage_bytes(p.d, (int)sizeof(T)));
+        bwd_kernel<OP, T, VEC, SLOTS, TPR, 1, PG, true><<<grid, TPR, smem, s>>>(p);
+        return cudaGetLastError();
+    }
+    static cudaError_t prepare() {
+        return cudaFuncSetAttribute(bwd_kernel<OP, T, VEC, SLOTS, TPR, 1, PG, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kBwdStagedSmemBudget);
+    }
+    static const BwdEntry entry;
+};
+
+template <int OP, typename T, int SLOTS, int TPR, bool PG>
+const BwdEntry BwdStagedInst<OP, T, SLOTS, TPR, PG>::entry = {
+    (const void*)&bwd_kernel<OP, T, Elem<T>::kVec, SLOTS, TPR, 1, PG, true>, TPR, 1, 0,
+    &BwdStagedInst<OP, T, SLOTS, TPR, PG>::launch, &BwdStagedInst<OP, T, SLOTS, TPR, PG>::prepare,
+    1};
+
+// The staged shapes the planner reaches: 256 or 512 threads per row and,
+// since it takes the fewest threads that hold the row, more than half the
+// held vectors per thread (FP32: 3 or 4 quads; 16-bit: 2 vectors of 8).
+template <int OP, typename T, bool PG>
+const BwdEntry* bwd_staged_pick(int slots, int tpr) {
+    if constexpr (sizeof(T) == 4) {
+        if (tpr == 256 && slots == 3) return &BwdStagedInst<OP, T, 3, 256, PG>::entry;
+        if (tpr == 256 && slots == 4) return &BwdStagedInst<OP, T, 4, 256, PG>::entry;
+        if (tpr == 512 && slots == 3) return &BwdStagedInst<OP, T, 3, 512, PG>::entry;
+        if (tpr == 512 && slots == 4) return &BwdStagedInst<OP, T, 4, 512, PG>::entry;
+    } else {
+        if (tpr == 256 && slots == 2) return &BwdStagedInst<OP, T, 2, 256, PG>::entry;
+        if (tpr == 512 && slots == 2) return &BwdStagedInst<OP, T, 2, 512, PG>::entry;
+    }
+    return nullptr;
+}
+
+template <typename T>
+const BwdEntry* bwd_staged_pick_type(int op, int slots, int tpr, bool pg) {
+    if (op == OP_LN)
+        return pg ? bwd_staged_pick<OP_LN, T, true>(slots, tpr)
+                  : bwd_staged_pick<OP_LN, T, false>(slots, tpr);
+    return pg ? bwd_staged_pick<OP_RMS, T, true>(slots, tpr)
+              : bwd_staged_pick<OP_RMS, T, false>(slots, tpr);
+}
 
 // Vectors a backward thread holds: up to 16 floats of x and of dy (4 FP32 or
 // 2 16-bit vectors), or 8 scalars.

@@ -150,6 +150,8 @@ struct BwdParams {
     int64_t d;
     int64_t ws_width;     // 2d (LN: dbeta part, dgamma part) or d (RMS: dw)
     float eps;            // RMS only
+    unsigned int* err;    // the device error word (the staged instances' bounded waits)
+    int stages;           // staged instances: row buffers in the ring (2..kBwdMaxStages)
 };
 
 // Backward kernels. slots: 1-4 (FP32 vectors), 1-2 (16-bit vectors), 1-4 and 8
@@ -162,8 +164,19 @@ struct BwdEntry {
     cudaError_t (*launch)(const BwdParams&, int grid, cudaStream_t);
     // Raises the kernel's dynamic shared memory limit (NULL if not needed).
     cudaError_t (*prepare)();
+    int staged;           // 1: a staged instance (ring depth set per call)
 };
 const BwdEntry* bwd_entry(int op, int dtype, int vec, int slots, int tpr, bool pg);
+// The staged form of a CTA-per-row backward instance (vector layout, 256 or
+// 512 threads): x and dy rows reach shared memory by bulk copies, ahead of
+// the row being reduced. NULL where no staged instance is compiled.
+const BwdEntry* bwd_staged_entry(int op, int dtype, int slots, int tpr, bool pg);
+// Bytes of shared memory one stage of the staged backward holds: a row of x
+// and a row of dy, each padded to 128 bytes.
+constexpr int64_t bwd_stage_bytes(int64_t d, int es) { return 2 * ((d * es + 127) / 128 * 128); }
+constexpr int kBwdMaxStages = 8;    // row buffers of the staged backward, at most
+constexpr int kBwdRingStages = 4;   // the depth the planner asks for (when it fits)
+constexpr int kBwdStagedSmemBudget = 232448 - 2048;   // per CTA, dynamic
 // out0/out1: the parameter gradients in the storage type `dtype` (or NULL).
 cudaError_t column_reduce(int dtype, const float* ws, int64_t rows, int64_t width, int64_t d,
                           void* out0, void* out1, cudaStream_t s);
@@ -178,6 +191,9 @@ cudaError_t bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
 
 // Reads (and optionally clears) the device error word of the current device.
 cudaError_t device_error_word(unsigned int* out, bool clear);
+// The device address of that word on the current device (for kernels built in
+// other translation units, which receive it as a parameter).
+cudaError_t device_error_address(unsigned int** out);
 
 // Compiled configuration space of the register-held kernels.
 constexpr int kMaxSlots = 8;

@@ -22,7 +22,7 @@
 // CTA's copies still in flight, and the CTA returns.
 #pragma once
 
-#include "rn_device.cuh"
+#include "rn_async.cuh"
 
 namespace rn {
 
@@ -30,59 +30,6 @@ namespace rn {
 // compiled into one translation unit only (staged.cu), which also holds the
 // host accessor.
 __device__ unsigned int g_device_error = 0;
-
-constexpr unsigned kErrStagedTimeout = 1u;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_fence_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  unsigned long long limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > limit_ns) return false;
-    }
-    return true;
-}
 
 // Self-test of the bounded wait: thread 0 waits on an mbarrier that nothing
 // arrives at, through the wait above, and records the timeout exactly as a
@@ -96,20 +43,6 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
     __syncthreads();
     if (threadIdx.x == 0 && !mbar_wait_bounded(smem_addr(&bar), 0, limit_ns))
         atomicOr(&g_device_error, kErrStagedTimeout);
-}
-
-// 1-D bulk copy global -> this CTA's shared memory, completing `bytes` on bar.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Sum of one float per thread over the CTA; every thread gets the result.

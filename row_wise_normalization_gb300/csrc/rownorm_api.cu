@@ -655,6 +655,7 @@ struct BwdRequest {
 
 struct BwdPlan {
     const BwdEntry* e;
+    int stages;          // staged instances: ring depth (0 otherwise)
     int vec, slots, tpr, grid;
     int64_t width;       // floats per workspace row
     int64_t groups;      // workspace rows written (one per CTA)
@@ -677,16 +678,51 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
     if (!tpr) return RN_ERR_SIZE;
     const int need = (int)((units + tpr - 1) / tpr);
     slots = need <= 4 ? need : 8;
-    const BwdEntry* e = bwd_entry(q.op, q.dtype, vec, slots, tpr, pg);
-    if (!e) return RN_ERR_VARIANT;
-    // resident CTAs
+    // Rows of 256 or 512 threads on the vector layout run the staged form
+    // when its ring fits: the bulk-copy engine keeps kBwdStages - 1 rows of
+    // x and dy in flight per CTA beyond what the registers hold.
+    const BwdEntry* e = nullptr;
+    int smem = 0, stages = 0;
     int dev = 0, sms = 0, per = 0;
     if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return RN_ERR_CUDA;
     if ((*err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return RN_ERR_CUDA;
+    if (vec > 1 && (tpr == 256 || tpr == 512)) {
+        const BwdEntry* se = bwd_staged_entry(q.op, q.dtype, slots, tpr, pg);
+        if (se) {
+            // as many stages (up to kBwdRingStages) as the SM's shared memory
+            // gives each of the CTAs its registers allow
+            int regs_ctas = 0, smem_sm = 0;
+            if ((*err = se->prepare()) != cudaSuccess) return RN_ERR_CUDA;
+            if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&regs_ctas, se->fn,
+                                                                      se->threads, 0)) !=
+                cudaSuccess)
+                return RN_ERR_CUDA;
+            if ((*err = cudaDeviceGetAttribute(&smem_sm,
+                                               cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                               dev)) != cudaSuccess)
+                return RN_ERR_CUDA;
+            const int64_t sb = bwd_stage_bytes(q.d, dtype_size(q.dtype));
+            int64_t per_cta = smem_sm / (regs_ctas > 0 ? regs_ctas : 1) - 2048;
+            if (per_cta > kBwdStagedSmemBudget) per_cta = kBwdStagedSmemBudget;
+            int64_t n = per_cta / sb;
+            if (n > kBwdRingStages) n = kBwdRingStages;
+            if (n >= 2) {
+                e = se;
+                stages = (int)n;
+                smem = (int)(n * sb);
+            }
+        }
+    }
+    if (!e) {
+        e = bwd_entry(q.op, q.dtype, vec, slots, tpr, pg);
+        if (!e) return RN_ERR_VARIANT;
+        smem = e->smem_bytes;
+    }
+    // resident CTAs
     if (e->prepare && (*err = e->prepare()) != cudaSuccess) return RN_ERR_CUDA;
-    if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, e->fn, e->threads,
-                                                              e->smem_bytes)) != cudaSuccess)
+    if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, e->fn, e->threads, smem)) !=
+        cudaSuccess)
         return RN_ERR_CUDA;
     int64_t grid = (int64_t)(per > 0 ? per : 1) * sms;
     const int64_t rows_ctas = (q.rows + e->rows_per_cta - 1) / e->rows_per_cta;
@@ -708,6 +744,7 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
         if (cap < grid) grid = cap;
     }
     bp->e = e;
+    bp->stages = stages;
     bp->vec = vec;
     bp->slots = slots;
     bp->tpr = tpr;
@@ -777,6 +814,10 @@ int run_bwd(const BwdRequest& q, void* stream) {
     prm.d = q.d;
     prm.ws_width = bp.width;
     prm.eps = q.eps;
+    prm.err = nullptr;
+    prm.stages = bp.stages;
+    if (bp.e->staged && (err = device_error_address(&prm.err)) != cudaSuccess)
+        return fail_cuda(err);
     const cudaStream_t s = (cudaStream_t)stream;
     err = bp.e->launch(prm, bp.grid, s);
     if (err != cudaSuccess) return fail_cuda(err);

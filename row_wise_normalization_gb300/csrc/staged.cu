@@ -30,4 +30,11 @@ cudaError_t device_error_word(unsigned int* out, bool clear) {
     return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
 }
 
+cudaError_t device_error_address(unsigned int** out) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_device_error);
+    *out = static_cast<unsigned int*>(p);
+    return e;
+}
+
 }  // namespace rn

@@ -180,3 +180,37 @@ def test_backward_repeatable():
     b = _run_ln(x, dy, g, m32, r32)
     for u, v in zip(a, b):
         assert np.array_equal(u.view(np.uint32), v.view(np.uint32))
+
+
+# FP32 rows of 256 or 512 threads (3 or 4 quads a thread) on the vector
+# layout run the staged backward: single rows, ragged row counts, and a
+# one-CTA grid (a workspace of one partial row) whose ring wraps many times.
+@pytest.mark.parametrize("d", [3072, 4096, 6144, 8192])
+@pytest.mark.parametrize("rows", [1, 9, 1207])
+def test_backward_staged_fp32(d, rows):
+    x, dy, g, _ = _case(rows, d, seed=93)
+    m32, r32 = _stats(x, g)
+    capi.device_error(clear=True)
+    _check_ln(x, dy, g, _run_ln(x, dy, g, m32, r32), chain=_chain(rows))
+    dx, dw = _run_rms(x, dy, g)
+    dxr, dwr = reference.rms_norm_backward(dy, x, g)
+    parity.check_y(dx, dxr, what="rms dx")
+    _, r = reference.rms_norm(x, g)
+    terms = np.abs(dy.astype(np.float64) * x * r[:, None]).sum(axis=0)
+    parity.check_colsum(dw, dwr, terms, _chain(rows), "dw")
+    assert capi.device_error() == 0
+
+
+def test_backward_staged_fp32_one_cta():
+    rows, d = 517, 4096
+    x, dy, g, _ = _case(rows, d, seed=95)
+    m32, r32 = _stats(x, g)
+    _check_ln(x, dy, g, _run_ln(x, dy, g, m32, r32, ws_bytes=2 * d * 4), chain=rows + CHAIN_PAD)
+    _check_ln(x, dy, g, _run_ln(x, dy, g, m32, r32, param_grads=False), chain=0)
+    dx, dw = _run_rms(x, dy, g, ws_bytes=d * 4)
+    dxr, dwr = reference.rms_norm_backward(dy, x, g)
+    parity.check_y(dx, dxr, what="rms dx")
+    _, r = reference.rms_norm(x, g)
+    terms = np.abs(dy.astype(np.float64) * x * r[:, None]).sum(axis=0)
+    parity.check_colsum(dw, dwr, terms, rows + CHAIN_PAD, "dw")
+    assert capi.device_error() == 0

@@ -164,3 +164,34 @@ def test_backward_16bit_rejects_unknown_type_and_misalignment():
                              0, 0, 0) == capi.RN_ERR_DTYPE
     assert capi.ln_bwd_typed(capi.RN_DTYPE_BF16, p + 1, p + 1024, p + 2048, stats, stats + 64,
                              p + 4096, 0, 0, 4, 8, 0, 0, 0) == capi.RN_ERR_ALIGN
+
+
+# Rows of 256 or 512 threads on the vector layout run the staged backward
+# (x and dy rows brought into a shared-memory ring by bulk copies). Widths on
+# both thread counts, single rows, ragged row counts, and a one-CTA grid
+# (workspace of one partial row) whose ring wraps hundreds of times.
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("op", [LN, RMS])
+@pytest.mark.parametrize("d", [2056, 4096, 4104, 8192])
+@pytest.mark.parametrize("rows", [1, 7, 1531])
+def test_backward_16bit_staged_rows(dtype, op, d, rows):
+    xb, xw, dyb, dyw, gb, gw, bw = _inputs(rows, d, dtype, 817, "offset")
+    m32, r32 = _stats(xw, gw, bw)
+    capi.device_error(clear=True)
+    out = _run(op, dtype, xb, dyb, gb, m32, r32)
+    _check(op, dtype, xw, dyw, gw, bw, out, chain=max(4, -(-rows // 152)) + 16)
+    assert capi.device_error() == 0
+
+
+@pytest.mark.parametrize("op", [LN, RMS])
+@pytest.mark.parametrize("d", [4096, 8192])
+def test_backward_16bit_staged_one_cta_and_no_grads(op, d):
+    rows = 613
+    xb, xw, dyb, dyw, gb, gw, bw = _inputs(rows, d, "bf16", 819, "normal")
+    m32, r32 = _stats(xw, gw, bw)
+    width = 2 * d if op == LN else d
+    out = _run(op, "bf16", xb, dyb, gb, m32, r32, ws_bytes=width * 4)   # one CTA
+    _check(op, "bf16", xw, dyw, gw, bw, out, chain=rows + 16)
+    out = _run(op, "bf16", xb, dyb, gb, m32, r32, grads=False)
+    _check(op, "bf16", xw, dyw, gw, bw, out, chain=0)
+    assert capi.device_error() == 0
