@@ -1070,6 +1070,22 @@ def run_case(args):
         nbytes = 2 * esz * rows * d + esz * d
     if args.residual:
         nbytes += 2 * esz * rows * d
+    if args.backward:
+        # the backward of the same call: dy, x (and the saved statistics) in,
+        # dx and the parameter gradients out, through a caller workspace
+        dy = torch.from_numpy(workloads.Workload(op, rows, d, seed=3).x()).to(device).to(dt)
+        dx = torch.empty_like(x)
+        g0 = torch.empty_like(ps[0])
+        opc_ = capi.RN_OP_LN if op == "ln" else capi.RN_OP_RMS
+        ws = torch.empty(capi.bwd_workspace_size(opc_, rows, d) // 4 + 4, device=device)
+        if op == "ln":
+            _, sm, sr = rn.ln_fwd(x, ps[0], ps[1], wl.eps)
+            g1 = torch.empty_like(ps[1])
+            f = lambda: rn.ln_bwd(dy, x, ps[0], sm, sr, dx=dx, dgamma=g0, dbeta=g1, workspace=ws)
+            nbytes = 3 * esz * rows * d + 3 * esz * d + 8 * rows
+        else:
+            f = lambda: rn.rms_bwd(dy, x, ps[0], wl.eps, dx=dx, dw=g0, workspace=ws)
+            nbytes = 3 * esz * rows * d + 2 * esz * d
     for _ in range(args.warmup):
         f()
     torch.cuda.synchronize()
@@ -1083,8 +1099,11 @@ def run_case(args):
     else:
         pl = capi.plan_typed(("f32", "bf16", "f16").index(args.dtype), opc, variant, d,
                              x.data_ptr(), y.data_ptr())
-    out = {"case": f"{op}{'_residual' if args.residual else ''}_{args.dtype}_{rows}x{d}",
-           "variant": args.variant, "planned": capi.variant_name(pl.variant),
+    kind = "_backward" if args.backward else ("_residual" if args.residual else "")
+    out = {"case": f"{op}{kind}_{args.dtype}_{rows}x{d}",
+           "variant": args.variant,
+           "planned": ("backward row kernel + column reduction" if args.backward
+                       else capi.variant_name(pl.variant)),
            "bytes": nbytes}
     for name, ts in (("cold", cold), ("warm", warm)):
         med = statistics.median(ts)
@@ -1109,6 +1128,8 @@ def main(argv=None):
     ap.add_argument("--variant", choices=VARIANTS, default="auto")
     ap.add_argument("--dtype", choices=("f32", "bf16", "f16"), default="f32")
     ap.add_argument("--residual", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="with --case: time the backward (dx and parameter gradients)")
     args = ap.parse_args(argv)
     if args.case is not None:
         run_case(args)

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
         }
         // two row sums: LN (sum g, sum g*xhat); RMS (sum x^2, sum g*x)
         float s1 = 0.f, s2 = 0.f;
+        F2 s1p = f2s(0.f), s2p = f2s(0.f);
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             if (t + s * TPR < nv) {
@@ -269,19 +270,42 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
                     sms_ld<VEC, TPR>(ps, s_par, s, t);
                 else
                     ps = par[s];
+                if constexpr (VEC > 1) {
+                    // adjacent elements in pairs (packed FP32): the two
+                    // halves of s1p/s2p are the even and odd partial sums
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    const float gk = __fmul_rn(dv[s].v[k], ps.v[k]);
+                    for (int k = 0; k < VEC; k += 2) {
+                        const F2 xk = f2(xv[s].v[k], xv[s].v[k + 1]);
+                        const F2 gk = mul2(f2(dv[s].v[k], dv[s].v[k + 1]),
+                                           f2(ps.v[k], ps.v[k + 1]));
+                        if constexpr (OP == OP_LN) {
+                            const F2 xh = mul2(sub2(xk, f2s(mu)), f2s(rs));
+                            s1p = add2(s1p, gk);
+                            s2p = fma2(gk, xh, s2p);
+                        } else {
+                            s1p = fma2(xk, xk, s1p);
+                            s2p = fma2(gk, xk, s2p);
+                        }
+                    }
+                } else {
+                    const float gk = __fmul_rn(dv[s].v[0], ps.v[0]);
                     if constexpr (OP == OP_LN) {
-                        const float xh = (xv[s].v[k] - mu) * rs;
+                        const float xh = (xv[s].v[0] - mu) * rs;
                         s1 += gk;
                         s2 = fmaf(gk, xh, s2);
                     } else {
-                        s1 = fmaf(xv[s].v[k], xv[s].v[k], s1);
-                        s2 = fmaf(gk, xv[s].v[k], s2);
+                        s1 = fmaf(xv[s].v[0], xv[s].v[0], s1);
+                        s2 = fmaf(gk, xv[s].v[0], s2);
                     }
                 }
             }
+        }
+        if constexpr (VEC > 1) {
+            float a, b;
+            f2_get(s1p, a, b);
+            s1 = a + b;
+            f2_get(s2p, a, b);
+            s2 = a + b;
         }
         s1 = warp_sum(s1);
         s2 = warp_sum(s2);
@@ -348,19 +372,46 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
                         if constexpr (OP == OP_LN) a1 = acc1[s];
                     }
                 }
+                if constexpr (VEC > 1) {
+                    // per element exactly the scalar sequence below, two
+                    // elements per packed instruction
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    const float gk = __fmul_rn(dv[s].v[k], ps.v[k]);
+                    for (int k = 0; k < VEC; k += 2) {
+                        const F2 xk = f2(xv[s].v[k], xv[s].v[k + 1]);
+                        const F2 dk = f2(dv[s].v[k], dv[s].v[k + 1]);
+                        const F2 gk = mul2(dk, f2(ps.v[k], ps.v[k + 1]));
+                        F2 ok;
+                        if constexpr (OP == OP_LN) {
+                            const F2 xh = mul2(sub2(xk, f2s(mu)), f2s(rs));
+                            ok = mul2(f2s(rs), fma2(xh, f2s(-c2), sub2(gk, f2s(c1))));
+                            if constexpr (PG) {
+                                const F2 u0 = add2(f2(a0.v[k], a0.v[k + 1]), dk);
+                                const F2 u1 = fma2(dk, xh, f2(a1.v[k], a1.v[k + 1]));
+                                f2_get(u0, a0.v[k], a0.v[k + 1]);
+                                f2_get(u1, a1.v[k], a1.v[k + 1]);
+                            }
+                        } else {
+                            ok = mul2(f2s(rs), fma2(xk, f2s(-c2), gk));
+                            if constexpr (PG) {
+                                const F2 u0 = fma2(dk, mul2(xk, f2s(rs)),
+                                                   f2(a0.v[k], a0.v[k + 1]));
+                                f2_get(u0, a0.v[k], a0.v[k + 1]);
+                            }
+                        }
+                        f2_get(ok, o.v[k], o.v[k + 1]);
+                    }
+                } else {
+                    const float gk = __fmul_rn(dv[s].v[0], ps.v[0]);
                     if constexpr (OP == OP_LN) {
-                        const float xh = (xv[s].v[k] - mu) * rs;
-                        o.v[k] = rs * (gk - c1 - xh * c2);
+                        const float xh = (xv[s].v[0] - mu) * rs;
+                        o.v[0] = rs * (gk - c1 - xh * c2);
                         if constexpr (PG) {
-                            a0.v[k] += dv[s].v[k];
-                            a1.v[k] = fmaf(dv[s].v[k], xh, a1.v[k]);
+                            a0.v[0] += dv[s].v[0];
+                            a1.v[0] = fmaf(dv[s].v[0], xh, a1.v[0]);
                         }
                     } else {
-                        o.v[k] = rs * (gk - xv[s].v[k] * c2);
-                        if constexpr (PG) a0.v[k] = fmaf(dv[s].v[k], xv[s].v[k] * rs, a0.v[k]);
+                        o.v[0] = rs * (gk - xv[s].v[0] * c2);
+                        if constexpr (PG) a0.v[0] = fmaf(dv[s].v[0], xv[s].v[0] * rs, a0.v[0]);
                     }
                 }
                 if constexpr (PG) {

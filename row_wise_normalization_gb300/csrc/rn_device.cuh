@@ -267,6 +267,46 @@ __device__ __forceinline__ bool aligned16(const T* p, int j) {
 }
 
 // ---------------------------------------------------------------------------
+// Two FP32 values in one 64-bit register. Blackwell's packed FP32 pipe does
+// add/sub/mul/fma on both halves in one instruction (.f32x2), each half
+// rounded exactly as the scalar instruction rounds it (.rn; no contraction
+// of an explicitly rounded mul or add into an fma), so element-wise work on
+// adjacent pairs takes half the instructions for identical results.
+// ---------------------------------------------------------------------------
+struct F2 {
+    unsigned long long r;
+};
+__device__ __forceinline__ F2 f2(float a, float b) {
+    F2 o;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(o.r) : "f"(a), "f"(b));
+    return o;
+}
+__device__ __forceinline__ F2 f2s(float a) { return f2(a, a); }
+__device__ __forceinline__ void f2_get(F2 v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v.r));
+}
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+    F2 o;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(o.r) : "l"(a.r), "l"(b.r));
+    return o;
+}
+__device__ __forceinline__ F2 sub2(F2 a, F2 b) {
+    F2 o;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(o.r) : "l"(a.r), "l"(b.r));
+    return o;
+}
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+    F2 o;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(o.r) : "l"(a.r), "l"(b.r));
+    return o;
+}
+// a * b + c, one rounding per half
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+    F2 o;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(o.r) : "l"(a.r), "l"(b.r), "l"(c.r));
+    return o;
+}
+
 // Reductions.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
