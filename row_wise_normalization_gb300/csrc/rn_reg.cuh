@@ -157,6 +157,41 @@ __device__ __forceinline__ void load_row(HeldRow<VEC, SLOTS, RES>& r, const T* x
     }
 }
 
+// 16-bit LayerNorm rows do more arithmetic per byte than FP32 ones; on rows
+// of a CTA their element-wise statistics and output run on adjacent pairs with the packed
+// FP32 instructions (each half rounded as the scalar instruction would be;
+// the sums become even/odd partial sums).
+template <int VEC, int SLOTS, bool RES>
+__device__ __forceinline__ float held_sum_pairs(const HeldRow<VEC, SLOTS, RES>& r) {
+    F2 a = f2s(0.f);
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+        for (int k = 0; k < VEC; k += 2) a = add2(a, f2(r.v[s].v[k], r.v[s].v[k + 1]));
+    float x0, x1;
+    f2_get(a, x0, x1);
+    return x0 + x1;
+}
+template <int VEC, int SLOTS, int TPR, bool RES>
+__device__ __forceinline__ float held_m2_pairs(const HeldRow<VEC, SLOTS, RES>& r, float c, int t,
+                                               int nv) {
+    F2 m = f2s(0.f);
+    const F2 c2 = f2s(c);
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        if (t + s * TPR < nv) {
+#pragma unroll
+            for (int k = 0; k < VEC; k += 2) {
+                const F2 d = sub2(f2(r.v[s].v[k], r.v[s].v[k + 1]), c2);
+                m = fma2(d, d, m);
+            }
+        }
+    }
+    float x0, x1;
+    f2_get(m, x0, x1);
+    return x0 + x1;
+}
+
 template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL,
           bool RES>
 __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES, AL))
@@ -192,6 +227,9 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     // mean). 16-bit storage carries 8-11 significant bits, far coarser.
     constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
     constexpr bool KLOAD = SHIFT && WPR > 1;
+    // (CTA-per-row rows only: warp-per-row rows keep the scalar order, which
+    // the batched kernel reproduces bit for bit)
+    constexpr bool PAIRS = OP == OP_LN && sizeof(T) == 2 && VEC == 8 && WPR > 1;
     const int64_t step = (int64_t)gridDim.x * RPC;
     int64_t row = (int64_t)blockIdx.x * RPC + g;
     if (row >= p.rows) return;                       // the whole group leaves together
@@ -302,11 +340,15 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                     }
                 }
             } else {
-                sum = cur.e;
+                if constexpr (PAIRS) {
+                    sum = cur.e + held_sum_pairs(cur);   // unused slots hold 0
+                } else {
+                    sum = cur.e;
 #pragma unroll
-                for (int s = 0; s < SLOTS; ++s)
+                    for (int s = 0; s < SLOTS; ++s)
 #pragma unroll
-                    for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
+                        for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
+                }
             }
 
             if constexpr (WPR == 1) {
@@ -315,13 +357,18 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                 // deviations in the shifted frame too: (x - K) - mu_s
                 const float ce = SHIFT ? (cur.e - K) - mu_s : cur.e - mu;
                 float m2 = has_e ? ce * ce : 0.f;
+                if constexpr (PAIRS) {
+                    m2 += held_m2_pairs<VEC, SLOTS, TPR, RES>(cur, mu, t, nv);
+                } else {
 #pragma unroll
-                for (int s = 0; s < SLOTS; ++s) {
-                    if (t + s * TPR < nv) {
+                    for (int s = 0; s < SLOTS; ++s) {
+                        if (t + s * TPR < nv) {
 #pragma unroll
-                        for (int k = 0; k < VEC; ++k) {
-                            const float c = SHIFT ? (cur.v[s].v[k] - K) - mu_s : cur.v[s].v[k] - mu;
-                            m2 = fmaf(c, c, m2);
+                            for (int k = 0; k < VEC; ++k) {
+                                const float c =
+                                    SHIFT ? (cur.v[s].v[k] - K) - mu_s : cur.v[s].v[k] - mu;
+                                m2 = fmaf(c, c, m2);
+                            }
                         }
                     }
                 }
@@ -338,14 +385,18 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                 // deviations from the warp mean, taken in the shifted frame
                 const float ce = SHIFT ? (cur.e - K) - wmean_s : cur.e - wmean_s;
                 float m2 = has_e ? ce * ce : 0.f;
+                if constexpr (PAIRS) {
+                    m2 += held_m2_pairs<VEC, SLOTS, TPR, RES>(cur, wmean_s, t, nv);
+                } else {
 #pragma unroll
-                for (int s = 0; s < SLOTS; ++s) {
-                    if (t + s * TPR < nv) {
+                    for (int s = 0; s < SLOTS; ++s) {
+                        if (t + s * TPR < nv) {
 #pragma unroll
-                        for (int k = 0; k < VEC; ++k) {
-                            const float c = SHIFT ? (cur.v[s].v[k] - K) - wmean_s
-                                                  : cur.v[s].v[k] - wmean_s;
-                            m2 = fmaf(c, c, m2);
+                            for (int k = 0; k < VEC; ++k) {
+                                const float c = SHIFT ? (cur.v[s].v[k] - K) - wmean_s
+                                                      : cur.v[s].v[k] - wmean_s;
+                                m2 = fmaf(c, c, m2);
+                            }
                         }
                     }
                 }
@@ -402,7 +453,15 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                     ldt_p(a, P0 + j, pa);
                     if constexpr (OP == OP_LN) ldt_p(b, P1 + j, pa);
                 }
-                if constexpr (OP == OP_LN) {
+                if constexpr (PAIRS) {
+#pragma unroll
+                    for (int k = 0; k < VEC; k += 2) {
+                        const F2 xo = mul2(sub2(f2(cur.v[s].v[k], cur.v[s].v[k + 1]), f2s(mu)),
+                                           f2s(rs));
+                        f2_get(fma2(xo, f2(a.v[k], a.v[k + 1]), f2(b.v[k], b.v[k + 1])), o.v[k],
+                               o.v[k + 1]);
+                    }
+                } else if constexpr (OP == OP_LN) {
 #pragma unroll
                     for (int k = 0; k < VEC; ++k)
                         o.v[k] = SHIFT ? fmaf(((cur.v[s].v[k] - K) - mu_s) * rs, a.v[k], b.v[k])
