@@ -661,6 +661,49 @@ struct BwdPlan {
     int64_t groups;      // workspace rows written (one per CTA)
 };
 
+// The current device's SM count and shared memory per SM, cached per thread.
+bool device_shape(int* dev, int* sms, int* smem_sm, cudaError_t* err) {
+    struct Cache {
+        int dev = -1, sms = 0, smem = 0;
+    };
+    static thread_local Cache cache[8];
+    if ((*err = cudaGetDevice(dev)) != cudaSuccess) return false;
+    Cache& c = cache[*dev & 7];
+    if (c.dev != *dev) {
+        if ((*err = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, *dev)) !=
+                cudaSuccess ||
+            (*err = cudaDeviceGetAttribute(&c.smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                           *dev)) != cudaSuccess)
+            return false;
+        c.dev = *dev;
+    }
+    *sms = c.sms;
+    *smem_sm = c.smem;
+    return true;
+}
+
+// Resident CTAs per SM of a backward kernel with `smem` bytes of dynamic
+// shared memory on device `dev` (raising its shared-memory limit first),
+// cached per thread so that a call does not repeat the occupancy query.
+int bwd_ctas_per_sm(const BwdEntry* e, int smem, int dev, cudaError_t* err) {
+    struct Cache {
+        const void* fn;
+        int dev, smem, n;
+    };
+    static thread_local Cache cache[32];
+    static thread_local int cache_next = 0;
+    for (auto& c : cache)
+        if (c.fn == e->fn && c.dev == dev && c.smem == smem && c.n > 0) return c.n;
+    if (e->prepare && (*err = e->prepare()) != cudaSuccess) return -1;
+    int per = 0;
+    if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, e->fn, e->threads, smem)) !=
+        cudaSuccess)
+        return -1;
+    cache[cache_next] = {e->fn, dev, smem, per};
+    cache_next = (cache_next + 1) % 32;
+    return per;
+}
+
 int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaError_t* err) {
     *err = cudaSuccess;
     const int vv = 16 / dtype_size(q.dtype);   // elements of one 128-bit vector
@@ -683,25 +726,15 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
     // x and dy in flight per CTA beyond what the registers hold.
     const BwdEntry* e = nullptr;
     int smem = 0, stages = 0;
-    int dev = 0, sms = 0, per = 0;
-    if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return RN_ERR_CUDA;
-    if ((*err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return RN_ERR_CUDA;
+    int dev = 0, sms = 0, smem_sm = 0;
+    if (!device_shape(&dev, &sms, &smem_sm, err)) return RN_ERR_CUDA;
     if (vec > 1 && (tpr == 256 || tpr == 512)) {
         const BwdEntry* se = bwd_staged_entry(q.op, q.dtype, slots, tpr, pg);
         if (se) {
             // as many stages (up to kBwdRingStages) as the SM's shared memory
             // gives each of the CTAs its registers allow
-            int regs_ctas = 0, smem_sm = 0;
-            if ((*err = se->prepare()) != cudaSuccess) return RN_ERR_CUDA;
-            if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&regs_ctas, se->fn,
-                                                                      se->threads, 0)) !=
-                cudaSuccess)
-                return RN_ERR_CUDA;
-            if ((*err = cudaDeviceGetAttribute(&smem_sm,
-                                               cudaDevAttrMaxSharedMemoryPerMultiprocessor,
-                                               dev)) != cudaSuccess)
-                return RN_ERR_CUDA;
+            const int regs_ctas = bwd_ctas_per_sm(se, 0, dev, err);
+            if (regs_ctas < 0) return RN_ERR_CUDA;
             const int64_t sb = bwd_stage_bytes(q.d, dtype_size(q.dtype));
             int64_t per_cta = smem_sm / (regs_ctas > 0 ? regs_ctas : 1) - 2048;
             if (per_cta > kBwdStagedSmemBudget) per_cta = kBwdStagedSmemBudget;
@@ -720,10 +753,8 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
         smem = e->smem_bytes;
     }
     // resident CTAs
-    if (e->prepare && (*err = e->prepare()) != cudaSuccess) return RN_ERR_CUDA;
-    if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, e->fn, e->threads, smem)) !=
-        cudaSuccess)
-        return RN_ERR_CUDA;
+    const int per = bwd_ctas_per_sm(e, smem, dev, err);
+    if (per < 0) return RN_ERR_CUDA;
     int64_t grid = (int64_t)(per > 0 ? per : 1) * sms;
     const int64_t rows_ctas = (q.rows + e->rows_per_cta - 1) / e->rows_per_cta;
     if (rows_ctas < grid) grid = rows_ctas;
