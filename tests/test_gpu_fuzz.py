@@ -205,3 +205,50 @@ def test_fuzz_backward(case):
         _, r = reference.rms_norm(x, g)
         terms = np.abs(dy.astype(np.float64) * x * r[:, None]).sum(axis=0)
         parity.check_colsum(dw, dwr, terms, chain, f"case {case} dw")
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_fuzz_backward_staged(case):
+    """Random backward calls in the staged range (rows of 256 or 512
+    threads on the vector layout: FP32 widths 3073-8192, 16-bit 2049-8192),
+    any storage type, row counts from one row to several ring cycles per CTA,
+    and a random workspace size (down to one partial row: one CTA whose ring
+    wraps once per row)."""
+    import test_gpu_backward as W
+    import test_gpu_backward_16bit as H
+
+    rng = np.random.default_rng([79, case])
+    dtype = ("f32", "bf16", "f16")[int(rng.integers(0, 3))]
+    vec = 4 if dtype == "f32" else 8
+    lo = 3073 if dtype == "f32" else 2049
+    d = int(rng.integers(lo // vec + 1, 8192 // vec + 1)) * vec
+    rows = int(rng.integers(1, min(2500, 3_000_000 // d) + 1))
+    op = LN if rng.random() < 0.5 else RMS
+    dist = DISTS[int(rng.integers(0, len(DISTS)))]
+    width = 2 * d if op == LN else d
+    full = capi.bwd_workspace_size(op, rows, d)
+    ws = int(rng.integers(1, max(2, full // (4 * width)) + 1)) * 4 * width
+    chain = max(4, -(-rows // 152)) + 16 if ws >= full else rows + 16
+    capi.device_error(clear=True)
+    if dtype == "f32":
+        wl = workloads.Workload("ln", rows, d, seed=9700 + case, x_dist=dist, x_std=_x_std(rng))
+        x = wl.x()
+        dy = workloads.Workload("ln", rows, d, seed=9800 + case).x()
+        g, _ = wl.params()
+        if op == LN:
+            m32, r32 = W._stats(x, g)
+            W._check_ln(x, dy, g, W._run_ln(x, dy, g, m32, r32, ws_bytes=ws), chain=chain)
+        else:
+            dx, dw = W._run_rms(x, dy, g, ws_bytes=ws)
+            dxr, dwr = reference.rms_norm_backward(dy, x, g)
+            parity.check_y(dx, dxr, what=f"case {case} dx")
+            _, r = reference.rms_norm(x, g)
+            terms = np.abs(dy.astype(np.float64) * x * r[:, None]).sum(axis=0)
+            parity.check_colsum(dw, dwr, terms, chain, f"case {case} dw")
+    else:
+        xb, xw, dyb, dyw, gb, gw, bw = H._inputs(rows, d, dtype, 9900 + case,
+                                                 "offset" if dist == "offset" else "normal")
+        m32, r32 = H._stats(xw, gw, bw)
+        out = H._run(op, dtype, xb, dyb, gb, m32, r32, ws_bytes=ws)
+        H._check(op, dtype, xw, dyw, gw, bw, out, chain=chain)
+    assert capi.device_error() == 0
