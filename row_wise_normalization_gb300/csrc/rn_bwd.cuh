@@ -591,11 +591,17 @@ const BwdEntry BwdStagedInst<OP, T, SLOTS, TPR, PG>::entry = {
 template <int OP, typename T, bool PG>
 const BwdEntry* bwd_staged_pick(int slots, int tpr) {
     if constexpr (sizeof(T) == 4) {
+        if (tpr == 64 && slots == 3) return &BwdStagedInst<OP, T, 3, 64, PG>::entry;
+        if (tpr == 64 && slots == 4) return &BwdStagedInst<OP, T, 4, 64, PG>::entry;
+        if (tpr == 128 && slots == 3) return &BwdStagedInst<OP, T, 3, 128, PG>::entry;
+        if (tpr == 128 && slots == 4) return &BwdStagedInst<OP, T, 4, 128, PG>::entry;
         if (tpr == 256 && slots == 3) return &BwdStagedInst<OP, T, 3, 256, PG>::entry;
         if (tpr == 256 && slots == 4) return &BwdStagedInst<OP, T, 4, 256, PG>::entry;
         if (tpr == 512 && slots == 3) return &BwdStagedInst<OP, T, 3, 512, PG>::entry;
         if (tpr == 512 && slots == 4) return &BwdStagedInst<OP, T, 4, 512, PG>::entry;
     } else {
+        if (tpr == 64 && slots == 2) return &BwdStagedInst<OP, T, 2, 64, PG>::entry;
+        if (tpr == 128 && slots == 2) return &BwdStagedInst<OP, T, 2, 128, PG>::entry;
         if (tpr == 256 && slots == 2) return &BwdStagedInst<OP, T, 2, 256, PG>::entry;
         if (tpr == 512 && slots == 2) return &BwdStagedInst<OP, T, 2, 512, PG>::entry;
     }

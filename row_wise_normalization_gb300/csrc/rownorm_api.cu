@@ -704,6 +704,9 @@ int bwd_ctas_per_sm(const BwdEntry* e, int smem, int dev, cudaError_t* err) {
     return per;
 }
 
+// Rows per CTA below which 64-128-thread backward rows stay on registers.
+constexpr int kBwdStagedMinRows = 8;
+
 int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaError_t* err) {
     *err = cudaSuccess;
     const int vv = 16 / dtype_size(q.dtype);   // elements of one 128-bit vector
@@ -722,13 +725,21 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
     const int need = (int)((units + tpr - 1) / tpr);
     slots = need <= 4 ? need : 8;
     // Rows of 256 or 512 threads on the vector layout run the staged form
-    // when its ring fits: the bulk-copy engine keeps kBwdStages - 1 rows of
-    // x and dy in flight per CTA beyond what the registers hold.
+    // when its ring fits: the bulk-copy engine keeps up to kBwdRingStages - 1
+    // rows of x and dy in flight per CTA beyond what the registers hold. Rows
+    // of 64 or 128 threads do so only with 16-bit storage and when every CTA
+    // walks at least 8 rows: the staged form gives each such row its own
+    // CTA, so it writes several times more partial rows for the column
+    // reduction, which FP32 rows (already near the bandwidth on registers)
+    // and short calls do not win back. Measured on GB300, cold L2: BF16
+    // LayerNorm 16384 x 2048 64.9 -> 49.7 us, 32768 x 1024 57.6 -> 51.6 us;
+    // FP32 32768 x 1024 72.2 -> 74.0 us and BF16 4096 x 768 16.8 -> 19.2 us
+    // had it run staged.
     const BwdEntry* e = nullptr;
     int smem = 0, stages = 0;
     int dev = 0, sms = 0, smem_sm = 0;
     if (!device_shape(&dev, &sms, &smem_sm, err)) return RN_ERR_CUDA;
-    if (vec > 1 && (tpr == 256 || tpr == 512)) {
+    if (vec > 1 && tpr >= 64 && tpr <= 512 && (tpr >= 256 || q.dtype != DT_F32)) {
         const BwdEntry* se = bwd_staged_entry(q.op, q.dtype, slots, tpr, pg);
         if (se) {
             // as many stages (up to kBwdRingStages) as the SM's shared memory
@@ -740,7 +751,13 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
             if (per_cta > kBwdStagedSmemBudget) per_cta = kBwdStagedSmemBudget;
             int64_t n = per_cta / sb;
             if (n > kBwdRingStages) n = kBwdRingStages;
-            if (n >= 2) {
+            bool take = n >= 2;
+            if (take && tpr < 256) {
+                const int per_s = bwd_ctas_per_sm(se, (int)(n * sb), dev, err);
+                if (per_s < 0) return RN_ERR_CUDA;
+                take = q.rows >= (int64_t)kBwdStagedMinRows * per_s * sms;
+            }
+            if (take) {
                 e = se;
                 stages = (int)n;
                 smem = (int)(n * sb);

@@ -195,3 +195,18 @@ def test_backward_16bit_staged_one_cta_and_no_grads(op, d):
     out = _run(op, "bf16", xb, dyb, gb, m32, r32, grads=False)
     _check(op, "bf16", xw, dyw, gw, bw, out, chain=0)
     assert capi.device_error() == 0
+
+
+# 16-bit rows of 64 or 128 threads run the staged backward when every CTA
+# walks at least 8 rows (one CTA per row group there): calls large enough
+# to take that path, LayerNorm and RMSNorm, both thread counts.
+@pytest.mark.parametrize("dtype,op,d,rows", [("bf16", LN, 1536, 5000), ("bf16", LN, 1024, 10000),
+                                             ("f16", RMS, 1536, 10000),
+                                             ("bf16", RMS, 520, 20000)])
+def test_backward_16bit_staged_narrow_rows(dtype, op, d, rows):
+    xb, xw, dyb, dyw, gb, gw, bw = _inputs(rows, d, dtype, 821, "offset")
+    m32, r32 = _stats(xw, gw, bw)
+    capi.device_error(clear=True)
+    out = _run(op, dtype, xb, dyb, gb, m32, r32)
+    _check(op, dtype, xw, dyw, gw, bw, out, chain=max(4, -(-rows // 152)) + 16)
+    assert capi.device_error() == 0
