@@ -203,6 +203,18 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
         }
     }
 
+    // staged 16-bit LayerNorm: the saved statistics of the group's next row
+    // are loaded one row ahead, so that a row whose stage is ready does not
+    // wait for them (BF16 8192 x 8192 94.3 -> 82.5 us; FP32 rows, whose
+    // stages take twice as long to land, were 1-2% slower with it)
+    constexpr bool SPF = STG && OP == OP_LN && sizeof(T) == 2;
+    float mu_next = 0.f, rs_next = 0.f;
+    if constexpr (SPF) {
+        if (group < p.rows) {
+            mu_next = ld_p1(p.mean + group);
+            rs_next = ld_p1(p.rstd + group);
+        }
+    }
     int it = 0;
     for (int64_t row = group; row < p.rows; row += ngroups, ++it) {
         // SMS: re-read the state every row rather than let it be hoisted
@@ -214,7 +226,14 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
         float mu = 0.f, rs = 0.f;
         bool ok = true;   // staged: this thread's wait for the row completed
         if constexpr (STG) {
-            if constexpr (OP == OP_LN) {
+            if constexpr (SPF) {
+                mu = mu_next;
+                rs = rs_next;
+                if (row + ngroups < p.rows) {
+                    mu_next = ld_p1(p.mean + row + ngroups);
+                    rs_next = ld_p1(p.rstd + row + ngroups);
+                }
+            } else if constexpr (OP == OP_LN) {
                 mu = ld_p1(p.mean + row);
                 rs = ld_p1(p.rstd + row);
             }
