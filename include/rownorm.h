@@ -227,7 +227,12 @@ int rms_fwd_batched(int dtype, const rn_problem *problems, int count, float eps,
  * d*4 for RMS) runs fewer CTAs, and one below that returns RN_ERR_SIZE.
  * Results are bitwise repeatable for a given device and workspace size.
  * Calls on one stream may share a workspace; calls that may run at the same
- * time on the GPU need workspaces of their own. Widths up to 16384
+ * time on the GPU need workspaces of their own. Rows wide enough for 256 or
+ * 512 threads (and 16-bit rows of 64-128 threads in long calls) are brought
+ * into shared memory by bulk copies; their waits are bounded as the staged
+ * forward's are (RN_DEVERR_STAGED_TIMEOUT in rn_device_error). The calls
+ * launch only on `stream`, so after one ordinary call of a configuration
+ * they can be captured into a CUDA graph. Widths up to 16384
  * (aligned arrays, d % 4 == 0) or 8192 (otherwise); wider rows return
  * RN_ERR_SIZE. Two kernel launches when parameter gradients are wanted, one
  * otherwise; rows == 0 zeroes the requested parameter gradients.
@@ -381,7 +386,7 @@ int rn_plan_for_residual(int op, int variant, int64_t d, const void *x, const vo
                          rn_plan *plan);
 
 /* Device error word of the current device: bit 0 (RN_DEVERR_STAGED_TIMEOUT)
- * is set if a staged kernel's wait for a bulk copy ran out (about one
+ * is set if a staged kernel's (forward or backward) wait for a bulk copy ran out (about one
  * second; the kernel then stops early and its outputs are incomplete). The
  * word is sticky until cleared: `clear` != 0 resets it after reading.
  * Synchronous (a device-to-host copy). Returns RN_OK, RN_ERR_NULL or
