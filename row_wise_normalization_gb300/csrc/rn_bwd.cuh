@@ -117,8 +117,8 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
     bwd_kernel(const BwdParams p) {
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
     static_assert(VEC == 1 || VEC == Elem<T>::kVec, "a vector is one 128-bit access");
-    static_assert(!STG || (RPC == 1 && VEC > 1 && TPR >= 64 && !bwd_sms(TPR)),
-                  "staged: one row group per CTA, vector layout, state in registers");
+    static_assert(!STG || (RPC == 1 && VEC > 1 && TPR >= 64 && (!bwd_sms(TPR) || OP == OP_RMS)),
+                  "staged: one row group per CTA, vector layout, accumulators in registers");
     const T* X = reinterpret_cast<const T*>(p.x);
     const T* DY = reinterpret_cast<const T*>(p.dy);
     const T* P0 = reinterpret_cast<const T*>(p.p0);
@@ -143,7 +143,9 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
     const int nst = STG ? p.stages : 1;
     const int64_t rowbytes = (int64_t)d * (int64_t)sizeof(T);
     const int64_t rpad = (rowbytes + 127) / 128 * 128;
-    unsigned char* const ring = reinterpret_cast<unsigned char*>(bwd_state);
+    // (after the parameter plane when the parameters live in shared memory)
+    unsigned char* const ring = reinterpret_cast<unsigned char*>(bwd_state) +
+                                (STG && bwd_sms(TPR * RPC) ? SLOTS * VEC * TPR * 4 : 0);
     auto issue = [&](int k) {
         const int64_t r = group + (int64_t)k * ngroups;
         if (r >= p.rows) return;
@@ -165,12 +167,18 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
 
     // parameters of my columns, held for every row (in registers, or SMS:
     // in shared memory, as are the accumulators)
-    constexpr bool SMS = bwd_sms(TPR * RPC);
-    constexpr int NR = SMS ? 1 : SLOTS;   // vectors of state held in registers
+    // PSM: the parameters in shared memory (1024-thread groups); SMS: the
+    // accumulators too (the register form; the staged 1024-thread RMSNorm
+    // keeps its single accumulator in registers and gives the rest of the
+    // shared memory to its ring)
+    constexpr bool PSM = bwd_sms(TPR * RPC);
+    constexpr bool SMS = PSM && !STG;
+    constexpr int NRP = PSM ? 1 : SLOTS;  // parameter vectors held in registers
+    constexpr int NR = SMS ? 1 : SLOTS;   // accumulator vectors held in registers
     float* const s_par = bwd_state;
     float* const s_acc0 = bwd_state + SLOTS * VEC * TPR;
     float* const s_acc1 = s_acc0 + SLOTS * VEC * TPR;
-    Vec<VEC> par[NR];
+    Vec<VEC> par[NRP];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
         const int q = t + s * TPR;
@@ -181,7 +189,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
 #pragma unroll
             for (int k = 0; k < VEC; ++k) v.v[k] = 0.f;
         }
-        if constexpr (SMS)
+        if constexpr (PSM)
             sms_st<VEC, TPR>(s_par, s, t, v);
         else
             par[s] = v;
@@ -219,7 +227,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
     for (int64_t row = group; row < p.rows; row += ngroups, ++it) {
         // SMS: re-read the state every row rather than let it be hoisted
         // into registers that the held row needs
-        if constexpr (SMS) asm volatile("" ::: "memory");
+        if constexpr (PSM) asm volatile("" ::: "memory");
         const T* xr = X + row * p.d;
         const T* dyr = DY + row * p.d;
         Vec<VEC> xv[SLOTS], dv[SLOTS];
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
         for (int s = 0; s < SLOTS; ++s) {
             if (t + s * TPR < nv) {
                 Vec<VEC> ps;
-                if constexpr (SMS)
+                if constexpr (PSM)
                     sms_ld<VEC, TPR>(ps, s_par, s, t);
                 else
                     ps = par[s];
@@ -385,7 +393,10 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
                         if constexpr (OP == OP_LN) sms_ld<VEC, TPR>(a1, s_acc1, s, t);
                     }
                 } else {
-                    ps = par[s];
+                    if constexpr (PSM)
+                        sms_ld<VEC, TPR>(ps, s_par, s, t);
+                    else
+                        ps = par[s];
                     if constexpr (PG) {
                         a0 = acc0[s];
                         if constexpr (OP == OP_LN) a1 = acc1[s];
@@ -585,8 +596,10 @@ const BwdEntry BwdInst<OP, T, VEC, SLOTS, TPR, PG>::entry = {
 template <int OP, typename T, int SLOTS, int TPR, bool PG>
 struct BwdStagedInst {
     static constexpr int VEC = Elem<T>::kVec;
+    // the parameter plane of 1024-thread groups, ahead of the ring
+    static constexpr int PAR = bwd_sms(TPR) ? SLOTS * VEC * TPR * 4 : 0;
     static cudaError_t launch(const BwdParams& p, int grid, cudaStream_t s) {
-        const int smem = (int)(p.stages * bwd_stage_bytes(p.d, (int)sizeof(T)));
+        const int smem = PAR + (int)(p.stages * bwd_stage_bytes(p.d, (int)sizeof(T)));
         bwd_kernel<OP, T, VEC, SLOTS, TPR, 1, PG, true><<<grid, TPR, smem, s>>>(p);
         return cudaGetLastError();
     }
@@ -600,9 +613,9 @@ struct BwdStagedInst {
 
 template <int OP, typename T, int SLOTS, int TPR, bool PG>
 const BwdEntry BwdStagedInst<OP, T, SLOTS, TPR, PG>::entry = {
-    (const void*)&bwd_kernel<OP, T, Elem<T>::kVec, SLOTS, TPR, 1, PG, true>, TPR, 1, 0,
-    &BwdStagedInst<OP, T, SLOTS, TPR, PG>::launch, &BwdStagedInst<OP, T, SLOTS, TPR, PG>::prepare,
-    1};
+    (const void*)&bwd_kernel<OP, T, Elem<T>::kVec, SLOTS, TPR, 1, PG, true>, TPR, 1,
+    BwdStagedInst<OP, T, SLOTS, TPR, PG>::PAR, &BwdStagedInst<OP, T, SLOTS, TPR, PG>::launch,
+    &BwdStagedInst<OP, T, SLOTS, TPR, PG>::prepare, 1};
 
 // The staged shapes the planner reaches: 256 or 512 threads per row and,
 // since it takes the fewest threads that hold the row, more than half the
@@ -623,6 +636,8 @@ const BwdEntry* bwd_staged_pick(int slots, int tpr) {
         if (tpr == 128 && slots == 2) return &BwdStagedInst<OP, T, 2, 128, PG>::entry;
         if (tpr == 256 && slots == 2) return &BwdStagedInst<OP, T, 2, 256, PG>::entry;
         if (tpr == 512 && slots == 2) return &BwdStagedInst<OP, T, 2, 512, PG>::entry;
+        if constexpr (OP == OP_RMS)
+            if (tpr == 1024 && slots == 2) return &BwdStagedInst<OP, T, 2, 1024, PG>::entry;
     }
     return nullptr;
 }

@@ -739,7 +739,8 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
     int smem = 0, stages = 0;
     int dev = 0, sms = 0, smem_sm = 0;
     if (!device_shape(&dev, &sms, &smem_sm, err)) return RN_ERR_CUDA;
-    if (vec > 1 && tpr >= 64 && tpr <= 512 && (tpr >= 256 || q.dtype != DT_F32)) {
+    if (vec > 1 && tpr >= 64 && (tpr >= 256 || q.dtype != DT_F32) &&
+        (tpr <= 512 || (q.op == OP_RMS && q.dtype != DT_F32))) {
         const BwdEntry* se = bwd_staged_entry(q.op, q.dtype, slots, tpr, pg);
         if (se) {
             // as many stages (up to kBwdRingStages) as the SM's shared memory
@@ -749,7 +750,7 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
             const int64_t sb = bwd_stage_bytes(q.d, dtype_size(q.dtype));
             int64_t per_cta = smem_sm / (regs_ctas > 0 ? regs_ctas : 1) - 2048;
             if (per_cta > kBwdStagedSmemBudget) per_cta = kBwdStagedSmemBudget;
-            int64_t n = per_cta / sb;
+            int64_t n = (per_cta - se->smem_bytes) / sb;   // after a parameter plane
             if (n > kBwdRingStages) n = kBwdRingStages;
             bool take = n >= 2;
             if (take && tpr < 256) {
@@ -760,7 +761,7 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
             if (take) {
                 e = se;
                 stages = (int)n;
-                smem = (int)(n * sb);
+                smem = se->smem_bytes + (int)(n * sb);
             }
         }
     }

@@ -210,3 +210,20 @@ def test_backward_16bit_staged_narrow_rows(dtype, op, d, rows):
     out = _run(op, dtype, xb, dyb, gb, m32, r32)
     _check(op, dtype, xw, dyw, gw, bw, out, chain=max(4, -(-rows // 152)) + 16)
     assert capi.device_error() == 0
+
+
+# 16-bit RMSNorm rows of 1024 threads (8193-16384 wide) run staged too, with
+# the parameters in shared memory ahead of a 2-4 stage ring: several rows per
+# CTA, and a one-CTA grid whose ring wraps once per row.
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [12288, 16384])
+def test_backward_16bit_staged_wide_rms(dtype, d):
+    rows = 500
+    xb, xw, dyb, dyw, gb, gw, bw = _inputs(rows, d, dtype, 823, "offset")
+    m32, r32 = _stats(xw, gw, bw)
+    capi.device_error(clear=True)
+    out = _run(RMS, dtype, xb, dyb, gb, m32, r32)
+    _check(RMS, dtype, xw, dyw, gw, bw, out, chain=max(4, -(-rows // 152)) + 16)
+    out = _run(RMS, dtype, xb, dyb, gb, m32, r32, ws_bytes=d * 4)   # one CTA
+    _check(RMS, dtype, xw, dyw, gw, bw, out, chain=rows + 16)
+    assert capi.device_error() == 0
