@@ -440,6 +440,30 @@ def gbs(nbytes, ms):
     return nbytes / (ms * 1e-3) / 1e9
 
 
+def parity_gate(case_wl, out, gpu_result):
+    """The oracle's output for the batch against the GPU's: "pass" or the
+    first failure."""
+    import parity as P
+
+    x = case_wl.x()
+    try:
+        P.check_y(gpu_result[0], out[0])
+        if case_wl.op == "ln":
+            P.check_mean(gpu_result[1], out[1], x)
+            P.check_rstd(gpu_result[2], out[2])
+        return "pass"
+    except AssertionError as e:
+        return f"FAIL: {e}"
+
+
+def oracle_once(case_wl):
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import c_oracle
+
+    fn = c_oracle.layer_norm if case_wl.op == "ln" else c_oracle.rms_norm
+    return fn(case_wl.x(), *case_wl.params(), case_wl.eps)
+
+
 def cpu_baseline_leg(case_wl, gpu_result=None, seconds=10.0):
     """Time the C oracle (as it stands) on the host: whole passes over the
     headline batch, once on one thread (about `seconds`) and once on every
@@ -488,18 +512,7 @@ def cpu_baseline_leg(case_wl, gpu_result=None, seconds=10.0):
     all_cores = {"value": nbytes * n_all / el_all / 1e9, "unit": UNIT, "cores": len(parts),
                  "sample": f"{n_all} whole passes over {case_wl.rows}x{case_wl.d}, rows split "
                            f"over {len(parts)} threads, {el_all:.1f} s"}
-    parity = None
-    if gpu_result is not None:
-        import parity as P
-
-        try:
-            P.check_y(gpu_result[0], out[0])
-            if case_wl.op == "ln":
-                P.check_mean(gpu_result[1], out[1], x)
-                P.check_rstd(gpu_result[2], out[2])
-            parity = "pass"
-        except AssertionError as e:
-            parity = f"FAIL: {e}"
+    parity = parity_gate(case_wl, out, gpu_result) if gpu_result is not None else None
     single = {"value": nbytes * n / el / 1e9, "unit": UNIT, "cores": 1,
               "sample": f"{n} whole passes over {case_wl.rows}x{case_wl.d}, one thread, "
                         f"{el:.1f} s"}
@@ -561,6 +574,11 @@ def run_ours(args, rank, world, local_rank):
     dist = None
     if world > 1:
         import torch.distributed as dist
+
+        # the shape sweep and the other context numbers are one-GPU figures;
+        # under several ranks they would hold every GPU while rank 0 alone
+        # measures them
+        args.no_sweep = True
     peak, peak_src = hbm_peak()
 
     def barrier():
@@ -900,7 +918,12 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- CPU baseline + parity gate (oracle on the host cores) --------------
     gpu_out = (case.y.cpu().numpy(), case.mean.cpu().numpy(), case.rstd.cpu().numpy())
-    cpu, parity = cpu_baseline_leg(wl, gpu_out, seconds=args.cpu_seconds)
+    if world == 1:
+        cpu, parity = cpu_baseline_leg(wl, gpu_out, seconds=args.cpu_seconds)
+    else:
+        # the CPU baseline is a one-GPU figure; with several ranks rank 0
+        # only checks its batch against the oracle (one pass)
+        cpu, parity = None, parity_gate(wl, oracle_once(wl), gpu_out)
     if parity != "pass":
         print(f"parity gate failed: {parity}", file=sys.stderr)
 
