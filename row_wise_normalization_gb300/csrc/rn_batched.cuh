@@ -49,13 +49,12 @@ __device__ __forceinline__ void batched_params(Vec<VEC> (&a)[SLOTS],
 // the same order, so the results match a single call's bit for bit). AL: the
 // problem's arrays are 16-byte aligned and d is a multiple of the vector.
 template <int OP, typename T, int SLOTS, bool AL>
-__device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, const T* P1,
-                                            float* mean, float* rstd, int64_t row, int d,
-                                            float eps, int lane) {
+__device__ __forceinline__ void batched_row_held(const HeldRow<Elem<T>::kVec, SLOTS, false>& cur,
+                                                 T* yr, const T* P0, const T* P1, float* mean,
+                                                 float* rstd, int64_t row, int d, float eps,
+                                                 int lane) {
     constexpr int VEC = Elem<T>::kVec;
     const float fd = (float)d;
-    HeldRow<VEC, SLOTS, false> cur;
-    load_row<T, VEC, SLOTS, 32, AL, false>(cur, xr, nullptr, d, lane);
     const int h = cur.h, nv = cur.nv, tl = cur.tl;
     const bool has_e = !AL && lane < h + tl;
     const int ei = (lane < h) ? lane : h + VEC * nv + (lane - h);
@@ -169,11 +168,42 @@ __device__ __forceinline__ void batched_row(const T* xr, T* yr, const T* P0, con
     }
 }
 
+// Rows [r0, r1) of one problem. Narrow FP32 slices (at most 16 floats a
+// lane) issue the loads of the next row before the current one is reduced
+// and written, as the warp-per-row kernel's prefetch does (FP32 128 problems
+// of 2048 x 64 70.1 -> 60.1 us, 64 x 512 x 128 17.0 -> 16.4 us; 16-bit rows,
+// at fewer resident CTAs, were slower with it: 64 x 512 x 128 19.0 -> 22.6 us).
+template <int OP, typename T, int SLOTS, bool AL>
+__device__ __forceinline__ void batched_rows(const T* X, T* Y, const T* P0, const T* P1,
+                                             float* mean, float* rstd, int64_t r0, int64_t r1,
+                                             int d, float eps, int lane) {
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr bool BPF = sizeof(T) == 4 && SLOTS * VEC <= 16;
+    HeldRow<VEC, SLOTS, false> cur;
+    load_row<T, VEC, SLOTS, 32, AL, false>(cur, X + r0 * d, nullptr, d, lane);
+    for (int64_t row = r0; row < r1; ++row) {
+        HeldRow<VEC, SLOTS, false> nxt;
+        if constexpr (BPF) {
+            if (row + 1 < r1)
+                load_row<T, VEC, SLOTS, 32, AL, false>(nxt, X + (row + 1) * d, nullptr, d, lane);
+        }
+        batched_row_held<OP, T, SLOTS, AL>(cur, Y + row * d, P0, P1, mean, rstd, row, d, eps,
+                                           lane);
+        if constexpr (BPF) {
+            cur = nxt;
+        } else if (row + 1 < r1) {
+            load_row<T, VEC, SLOTS, 32, AL, false>(cur, X + (row + 1) * d, nullptr, d, lane);
+        }
+    }
+}
+
 // Register budget per SLOTS: about 12 per held float and 52 fixed (the
 // problem's fields, the row's head/tail and alignment state), plus the
-// early-loaded parameters of slices of at most 8 floats.
+// early-loaded parameters of slices of at most 8 floats and the prefetched
+// row of FP32 slices of at most 16.
 constexpr int batch_min_ctas(int slots, int vec) {
-    const int regs = 52 + 12 * slots * vec / 4 + (slots * vec <= 8 ? 2 * slots * vec : 0);
+    const int regs = 52 + 12 * slots * vec / 4 + (slots * vec <= 8 ? 2 * slots * vec : 0) +
+                     (vec == 4 && slots * vec <= 16 ? 2 * slots * vec : 0);   // prefetched row
     const int n = 65536 / (((regs + 7) / 8) * 8 * kBatchThreads);
     return n < 1 ? 1 : (n > 16 ? 16 : n);
 }
@@ -211,19 +241,13 @@ __global__ void __launch_bounds__(kBatchThreads, batch_min_ctas(SLOTS, Elem<T>::
         float* mean = pr.mean;
         float* rstd = pr.rstd;
         const float eps = p.eps;
-        if (pr.al) {
-            for (; r < last; ++r) {
-                const int64_t row = r - first;
-                batched_row<OP, T, SLOTS, true>(X + row * d, Y + row * d, P0, P1, mean, rstd,
-                                                row, d, eps, lane);
-            }
-        } else {
-            for (; r < last; ++r) {
-                const int64_t row = r - first;
-                batched_row<OP, T, SLOTS, false>(X + row * d, Y + row * d, P0, P1, mean, rstd,
-                                                 row, d, eps, lane);
-            }
-        }
+        if (pr.al)
+            batched_rows<OP, T, SLOTS, true>(X, Y, P0, P1, mean, rstd, r - first, last - first, d,
+                                             eps, lane);
+        else
+            batched_rows<OP, T, SLOTS, false>(X, Y, P0, P1, mean, rstd, r - first, last - first,
+                                              d, eps, lane);
+        r = last;
         if (r >= r_end) break;
         ++k;   // problems in the table all have rows > 0
     }
