@@ -89,3 +89,21 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
 
     assert bench.run_reference(Args, 1, 2) is None
     assert capsys.readouterr().out == ""
+
+
+def test_parity_gate_of_several_ranks():
+    """With several ranks rank 0 checks its batch against one oracle pass
+    instead of timing the oracle: the gate passes on the oracle's own output
+    (rounded to FP32, as a GPU writes it) and names the first failure when
+    one output is off by more than the tolerance."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    wl = bench.pick_workload("ln_512x128")
+    out = bench.oracle_once(wl)
+    got = tuple(a.astype("float32") for a in out)
+    assert bench.parity_gate(wl, out, got) == "pass"
+    bad = got[0].copy()
+    bad[7, 3] += 1e-2
+    verdict = bench.parity_gate(wl, out, (bad, got[1], got[2]))
+    assert verdict.startswith("FAIL")
