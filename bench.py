@@ -593,6 +593,18 @@ def run_ours(args, rank, world, local_rank):
     if sampler:
         sampler.start()
 
+    # correctness gate before any timing: one call, checked against the
+    # oracle on this rank's batch; a failing call is not timed
+    case.launch()
+    torch.cuda.synchronize()
+    gate = parity_gate(wl, oracle_once(wl), (case.y.cpu().numpy(), case.mean.cpu().numpy(),
+                                             case.rstd.cpu().numpy()))
+    if gate != "pass":
+        print(f"parity gate failed before timing (rank {rank}): {gate}", file=sys.stderr)
+        if sampler:
+            sampler.stop()
+        raise SystemExit(3)
+
     # warm-up
     for _ in range(args.warmup):
         flush()
