@@ -119,9 +119,11 @@ int rms_fwd(const float *x, const float *w, float *y,
  *   y, mean_out, rstd_out, gamma, beta, w: as in ln_fwd / rms_fwd, of h.
  * The pages name this fusion as absent from their kernels ("RMSNorm on an
  * RTX 5070 ...", section "The operator and the change"). One kernel launch;
- * AUTO uses the register-held kernels up to d = 32768 floats and the
- * streaming kernel beyond (the staged and cluster variants have no residual
- * form: RN_ERR_VARIANT).
+ * AUTO uses the register-held kernels on rows of up to 512 threads (d up to
+ * 16384 floats with 16-byte aligned rows, 4096 with scalar accesses) and
+ * the streaming kernel beyond. A forced RN_VARIANT_BLOCK on a wider row
+ * (1024 threads), and the staged and cluster variants, have no residual
+ * form: RN_ERR_VARIANT.
  */
 int ln_fwd_residual(const float *x, const float *res, const float *gamma, const float *beta,
                     float *h_out, float *y, float *mean_out, float *rstd_out,

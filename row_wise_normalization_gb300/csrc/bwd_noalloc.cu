@@ -10,19 +10,20 @@
 // as ln_bwd and uses, as its workspace, one file-scope array that every GPU
 // loading the library holds until the process exits.
 //
-// Set-up: the first call on each device (with that device current) looks up
-// the array's device address with cudaGetSymbolAddress and keeps it; make
-// that first call before any stream capture on the device. No call here
-// allocates: no cudaMalloc, no cudaFree, no allocating library routine.
+// Set-up: the first call that needs the array in a CUDA context (with that
+// context's device current) looks up the array's device address with
+// cudaGetSymbolAddress, checks the result and keeps the address for that
+// context; make that first call before any stream capture on the device. A
+// context created anew for the device (after cudaDeviceReset, say) gets a
+// lookup of its own, since the address is kept per context, not per device
+// number. No call here allocates: no cudaMalloc, no cudaFree, no allocating
+// library routine.
 //
 // Every call shares the one array, which keeps whatever the last call left
 // there. Nothing in it needs to start at zero: the row kernel writes every
 // partial row that the column reduction then reads. Calls whose kernels can
 // overlap on the GPU (different streams, or different host threads, on the
 // same device) race on the array; serialise them, e.g. on one stream.
-#include <atomic>
-#include <mutex>
-
 #include "rn_params.h"
 #include "rownorm.h"
 
@@ -30,29 +31,13 @@ namespace {
 
 static __device__ __align__(256) float g_noalloc_scratch[RN_NOALLOC_SCRATCH_BYTES / 4];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_ptr[kMaxDevices];
-std::mutex g_setup_mu;
-
-// The array's address on the current device, looked up once per device.
+// The array's address in the current context (looked up once per context).
 int scratch_on_current_device(void** out) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return rn::record_cuda_error(err);
-    if (dev < 0 || dev >= kMaxDevices) return rn::record_cuda_error(cudaErrorInvalidDevice);
-    void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        std::lock_guard<std::mutex> lk(g_setup_mu);
-        p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
-        if (!p) {
-            err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-            if (err != cudaSuccess || !p)
-                return rn::record_cuda_error(err != cudaSuccess ? err : cudaErrorInvalidSymbol);
-            g_scratch_ptr[dev].store(p, std::memory_order_release);
-        }
-    }
-    *out = p;
-    return RN_OK;
+    static rn::SymbolAddressCache cache;
+    const cudaError_t err = cache.get(out, [](void** p) {
+        return cudaGetSymbolAddress(p, g_noalloc_scratch);
+    });
+    return err == cudaSuccess ? RN_OK : rn::record_cuda_error(err);
 }
 
 }  // namespace
@@ -60,10 +45,18 @@ int scratch_on_current_device(void** out) {
 extern "C" int ln_bwd_noalloc(const float* dy, const float* x, const float* gamma,
                               const float* mean, const float* rstd, float* dx, float* dgamma,
                               float* dbeta, int64_t rows, int64_t d, void* stream) {
+    // the checks every backward call makes come first, so that errors (and
+    // rows == 0, which only zeroes the requested gradients) are reported as
+    // ln_bwd reports them
+    const int st = rn::ln_bwd_check_args(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d);
+    if (st != RN_OK) return st;
+    const bool pg = dgamma || dbeta;
+    if (rows == 0 || !pg)   // no partials: the scratch is not needed
+        return ln_bwd(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, nullptr, 0, stream);
     if (d > RN_NOALLOC_MAX_D) return RN_ERR_SCRATCH;
     void* scratch = nullptr;
-    const int st = scratch_on_current_device(&scratch);
-    if (st != RN_OK) return st;
+    const int sst = scratch_on_current_device(&scratch);
+    if (sst != RN_OK) return sst;
     return ln_bwd(dy, x, gamma, mean, rstd, dx, dgamma, dbeta, rows, d, scratch,
                   (size_t)RN_NOALLOC_SCRATCH_BYTES, stream);
 }

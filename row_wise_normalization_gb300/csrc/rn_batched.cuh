@@ -220,7 +220,9 @@ __global__ void __launch_bounds__(kBatchThreads, batch_min_ctas(SLOTS, Elem<T>::
     const int64_t chunk = (total + nwarps - 1) / nwarps;
     int64_t r = warp * chunk;
     const int64_t r_end = r + chunk < total ? r + chunk : total;
+    pdl_launch_dependents();
     if (r >= r_end) return;
+    pdl_wait();   // no global access before this (the table is a kernel parameter)
     int k = 0, hi = p.n - 1;   // the last k with start[k] <= r
     while (k < hi) {
         const int mid = (k + hi + 1) >> 1;
@@ -256,8 +258,7 @@ __global__ void __launch_bounds__(kBatchThreads, batch_min_ctas(SLOTS, Elem<T>::
 template <int OP, typename T, int SLOTS>
 struct BatchInst {
     static cudaError_t launch(const BatchParams& p, int grid, cudaStream_t s) {
-        batched_kernel<OP, T, SLOTS><<<grid, kBatchThreads, 0, s>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(batched_kernel<OP, T, SLOTS>, (unsigned)grid, kBatchThreads, 0, s, p);
     }
     static const BatchEntry entry;
 };

@@ -658,15 +658,35 @@ constexpr int bwd_max_slots() {
     return VEC == 1 ? 8 : 16 / VEC;
 }
 
+// The shapes the planner reaches: it takes the fewest threads that hold the
+// row, so rows of 64 or more threads hold more than half of a thread's
+// vectors (FP32: 3 or 4 quads; 16-bit: 2 vectors of 8), and scalar rows of
+// 64 or more threads are given 8 slots; rows of one warp take any count.
+// Nothing else is compiled.
+template <int VEC, int S, int TPR>
+constexpr bool bwd_reachable() {
+    constexpr int M = bwd_max_slots<VEC>();
+    if (S > M) return false;
+    if (TPR == 32) return true;
+    return VEC == 1 ? S == 8 : 2 * S > M;
+}
+
+template <int OP, typename T, int VEC, int S, int TPR, bool PG>
+const BwdEntry* bwd_inst_entry() {
+    if constexpr (bwd_reachable<VEC, S, TPR>())
+        return &BwdInst<OP, T, VEC, S, TPR, PG>::entry;
+    else
+        return nullptr;
+}
+
 template <int OP, typename T, int VEC, int TPR, bool PG>
 const BwdEntry* bwd_pick_slots(int slots) {
-    constexpr int M = bwd_max_slots<VEC>();
     switch (slots) {
-        case 1: return &BwdInst<OP, T, VEC, 1, TPR, PG>::entry;
-        case 2: return &BwdInst<OP, T, VEC, 2, TPR, PG>::entry;
-        case 3: if constexpr (M >= 3) return &BwdInst<OP, T, VEC, 3, TPR, PG>::entry; else return nullptr;
-        case 4: if constexpr (M >= 4) return &BwdInst<OP, T, VEC, 4, TPR, PG>::entry; else return nullptr;
-        case 8: if constexpr (M >= 8) return &BwdInst<OP, T, VEC, 8, TPR, PG>::entry; else return nullptr;
+        case 1: return bwd_inst_entry<OP, T, VEC, 1, TPR, PG>();
+        case 2: return bwd_inst_entry<OP, T, VEC, 2, TPR, PG>();
+        case 3: return bwd_inst_entry<OP, T, VEC, 3, TPR, PG>();
+        case 4: return bwd_inst_entry<OP, T, VEC, 4, TPR, PG>();
+        case 8: return bwd_inst_entry<OP, T, VEC, 8, TPR, PG>();
         default: return nullptr;
     }
 }

@@ -7,11 +7,31 @@
 // row is read from HBM once and written from the registers, exactly as in the
 // CTA-per-row kernel; only the statistics cross SMs. Each warp reduces its
 // share to (count, sum, mean, centred M2) about its own mean, and lanes
-// 0..CL-1 store that float4 straight into slot (c, warp) of every CTA of the
-// cluster through distributed shared memory (mapa + st.shared::cluster). One
-// cluster barrier (release/acquire) later every thread merges the CL*WPR
-// partials with the parallel-axis rule. Slots are double-buffered by row
-// parity, so one cluster barrier per row is the only synchronisation.
+// 0..CL-1 send that float4 straight into slot (c, warp) of every CTA of the
+// cluster with an asynchronous distributed-shared-memory store
+// (st.async ... mbarrier::complete_tx) that also counts its 16 bytes on the
+// receiving CTA's mbarrier for that slot buffer. A CTA waits on its own
+// mbarrier until all CL * WPR partials of the row have landed, then every
+// thread merges them with the parallel-axis rule.
+//
+// No cluster barrier and no memory fence sits on the per-row path: a
+// barrier.cluster.arrive.release orders every earlier memory access of the
+// thread, the prefetched next row's global loads included, so each row used
+// to wait for the next row's loads before its statistics could meet.
+//
+// Slot buffers and their mbarriers are double-buffered by row parity. Reuse
+// needs no release signal: a CTA writes row i + 2's partials into buffer
+// (i & 1) of a peer only after it has received every partial of row i + 1,
+// and each warp of that peer sends its row i + 1 partial only after it has
+// read buffer (i & 1) for row i. Thread 0 of each CTA arms the next phase of
+// a buffer (arrive + expect_tx of CL * WPR * 16 bytes) right after its own
+// wait on that buffer, before its warp sends the next row's partial.
+//
+// Waits are bounded (1 s of %globaltimer): a wait that runs out sets
+// RN_DEVERR_CLUSTER_TIMEOUT in the device error word it was given and its
+// warp stops processing rows; every warp still meets the cluster barrier at
+// the end, so that no CTA leaves while a peer could address its shared
+// memory.
 //
 // The partials are formed on x - K, K the row's first element: a merge adds
 // the product of a partial mean's rounding error (~u |mean|) and the spread
@@ -24,7 +44,7 @@
 // slice when PF is set.
 #pragma once
 
-#include "rn_device.cuh"
+#include "rn_async.cuh"
 
 namespace rn {
 
@@ -39,14 +59,48 @@ __device__ __forceinline__ void cluster_sync_all() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Store a float4 into CTA `rank`'s shared memory at the address that `local`
-// has in this CTA.
-__device__ __forceinline__ void dsmem_store4(const void* local, unsigned rank, float4 v) {
+// The address that the shared-memory location `local` of this CTA has in
+// CTA `rank` of the cluster.
+__device__ __forceinline__ unsigned dsmem_map(const void* local, unsigned rank) {
     unsigned la = (unsigned)__cvta_generic_to_shared(local), ra;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(v.x),
-                 "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
+    return ra;
+}
+
+// Asynchronous store of a float4 into CTA `rank`'s shared memory at the
+// address `local` has in this CTA, completing 16 bytes of transaction count
+// on that CTA's mbarrier at the address `bar` has in this CTA.
+__device__ __forceinline__ void dsmem_send4(const void* local, const void* bar, unsigned rank,
+                                            float4 v) {
+    const unsigned ra = dsmem_map(local, rank), rb = dsmem_map(bar, rank);
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(ra),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rb)
+        : "memory");
+}
+
+// Wait (acquire at cluster scope: the data came from other CTAs' st.async)
+// for the phase of `bar` with the given parity; gives up after limit_ns.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
+                                                          unsigned long long limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+    return true;
 }
 
 template <int OP, int SLOTS, int TPB, int CL, bool PF, bool AL>
@@ -63,6 +117,7 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
     constexpr int WPR = C::WPR;
     constexpr int NE = C::NE;
     __shared__ __align__(16) float4 slots[2][NE];
+    __shared__ __align__(8) unsigned long long full[2];   // one mbarrier per slot buffer
 
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     const unsigned c = cluster_ctarank();
@@ -70,9 +125,24 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
     const int64_t nclusters = gridDim.x / CL;
     const int d = (int)p.d;
     const float fd = (float)d;
+    constexpr uint32_t kRowBytes = NE * 16;                // partials one row brings to a CTA
 
-    // every CTA of the cluster is running before anyone writes into a peer
+    pdl_launch_dependents();
+    // rows of this cluster: cluster_id, cluster_id + nclusters, ...
+    const int64_t nmine =
+        cluster_id < p.rows ? (p.rows - 1 - cluster_id) / nclusters + 1 : 0;
+    if (t == 0) {
+        mbar_init(smem_addr(&full[0]), 1);
+        mbar_init(smem_addr(&full[1]), 1);
+        // arm the phases of the first two rows
+        if (nmine > 0) mbar_arrive_expect_tx(smem_addr(&full[0]), kRowBytes);
+        if (nmine > 1) mbar_arrive_expect_tx(smem_addr(&full[1]), kRowBytes);
+        mbar_fence_init();
+    }
+    // every CTA of the cluster is running, with its mbarriers initialised,
+    // before anyone sends into a peer
     cluster_sync_all();
+    pdl_wait();   // no global access before this
 
     struct Slice {
         Vec<4> v[SLOTS];
@@ -112,8 +182,7 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
     int64_t row = cluster_id;
     Slice cur;
     if (row < p.rows) load(cur, row);
-    int it = 0;
-    for (; row < p.rows; row += nclusters, ++it) {
+    for (int64_t it = 0; it < nmine; ++it, row += nclusters) {
         const int64_t nrow = row + nclusters;
         Slice nxt;
         if constexpr (PF) {
@@ -174,10 +243,24 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
                 part = make_float4(0.f, warp_sum(ss), 0.f, 0.f);
             }
         }
-        // lane r publishes this warp's partial into CTA r's slot (c, w)
-        float4* buf = slots[it & 1];
-        if (lane < CL) dsmem_store4(&buf[c * WPR + w], (unsigned)lane, part);
-        cluster_sync_all();
+        // lane r sends this warp's partial into CTA r's slot (c, w) and
+        // counts its bytes on CTA r's mbarrier of this buffer
+        const int b = (int)(it & 1);
+        float4* buf = slots[b];
+        if (lane < CL) dsmem_send4(&buf[c * WPR + w], &full[b], (unsigned)lane, part);
+        const uint32_t bar = smem_addr(&full[b]);
+        const bool ok = mbar_wait_cluster_bounded(bar, (uint32_t)((it >> 1) & 1), kWaitLimitNs);
+        // thread 0 arms this buffer's next phase (row it + 2) before its warp
+        // sends row it + 1's partial; other CTAs' sends for row it + 2 come
+        // after they have received that partial
+        if (t == 0 && it + 2 < nmine) mbar_arrive_expect_tx(bar, kRowBytes);
+        // a wait that ran out stops the whole warp (the loop holds no CTA
+        // barrier, so warps may stop at different rows: each later wait of a
+        // warp still running also runs out)
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0 && p.err) atomicOr(p.err, kErrClusterTimeout);
+            break;
+        }
 
         // ---- merge the CL * WPR partials (every thread) -----------------
         float mu = 0.f, rs, mus = 0.f;   // mus = mu - K; the output is formed as (x - K) - mus
@@ -214,13 +297,13 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
             const int q = t + k * TPB;
             if (q < nq) {
                 const int j = h + 4 * (q0 + q);
-                Vec<4> a, b, o;
+                Vec<4> a, bb, o;
                 ld_p(a, p.p0 + j, pa);
                 if constexpr (OP == OP_LN) {
-                    ld_p(b, p.p1 + j, pa);
+                    ld_p(bb, p.p1 + j, pa);
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        o.v[u] = fmaf(((cur.v[k].v[u] - cur.K) - mus) * rs, a.v[u], b.v[u]);
+                        o.v[u] = fmaf(((cur.v[k].v[u] - cur.K) - mus) * rs, a.v[u], bb.v[u]);
                 } else {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) o.v[u] = cur.v[k].v[u] * rs * a.v[u];
@@ -262,13 +345,15 @@ struct ClusterInst {
         cfg.blockDim = dim3(TPB, 1, 1);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = s;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = CL;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         return cudaLaunchKernelEx(&cfg, cluster_kernel<OP, SLOTS, TPB, CL, PF, AL>, p);
     }
     static cudaError_t prepare(int) {

@@ -19,6 +19,22 @@ namespace rn {
 // they go through the read-only path with L1 allocation. y is written once and
 // never re-read by the kernel, so it is stored with the streaming (.cs) hint.
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. The forward kernels are launched with
+// programmatic stream serialization (launch_pdl in rn_params.h): the GPU may
+// schedule such a kernel while the kernel ahead of it on the stream is still
+// running, so its launch and CTA set-up overlap that kernel's tail. Each
+// forward kernel therefore (1) lets the kernel behind it be scheduled as soon
+// as all of its own CTAs are resident (every CTA signals at its start; a
+// persistent grid is one wave, so no CTA of it waits for a slot the next
+// kernel took), and (2) touches no global memory before pdl_wait() returns,
+// which is when the kernel ahead has completed and its writes are visible.
+// Without a kernel ahead (first launch, a copy or an event before it) the
+// wait returns at once.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Asks the bulk-copy engine to bring `bytes` (a multiple of 16) from a
 // 16-byte-aligned global address into L2, without waiting for them.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 namespace rn {
@@ -30,7 +32,28 @@ struct Params {
     int64_t ldx, ldy;  // row strides of x and y, in elements (>= d; d when contiguous)
     int64_t ldr, ldh;  // row strides of r and h
     float eps;
+    unsigned int* err = nullptr;   // device error word (the cluster kernel's bounded waits)
 };
+
+// Launches a forward kernel with programmatic stream serialization (see
+// pdl_wait in rn_device.cuh): stream order is kept, since the kernel waits
+// for the one ahead of it before its first global access, but its launch
+// overlaps that kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned threads, size_t smem,
+                       cudaStream_t s, const Args&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // One compiled kernel configuration.
 struct KernelEntry {
@@ -188,6 +211,12 @@ constexpr int kBwdMinRowsPerGroup = 4;   // rows a backward row group takes at l
 // Records err as this thread's last CUDA error; returns RN_ERR_CUDA.
 int record_cuda_error(cudaError_t err);
 
+// ln_bwd's argument checks (sizes, null pointers, alignment, aliasing) for an
+// FP32 call, without those of the workspace; returns an rn_status.
+int ln_bwd_check_args(const float* dy, const float* x, const float* gamma, const float* mean,
+                      const float* rstd, float* dx, float* dgamma, float* dbeta, int64_t rows,
+                      int64_t d);
+
 // Launches the bounded-wait self-test (one CTA, a wait nothing completes).
 cudaError_t bounded_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
 
@@ -196,6 +225,54 @@ cudaError_t device_error_word(unsigned int* out, bool clear);
 // The device address of that word on the current device (for kernels built in
 // other translation units, which receive it as a parameter).
 cudaError_t device_error_address(unsigned int** out);
+
+// A process-unique identifier of the CUDA context current on this thread (0
+// if none is). A device's primary context gets a new identifier when it is
+// created again (after cudaDeviceReset, say), so caches of device addresses
+// are keyed on it rather than on the device number.
+cudaError_t current_context_id(unsigned long long* id);
+
+// A __device__ variable's address in the current context: `lookup` (which
+// calls cudaGetSymbolAddress in the translation unit that defines the
+// variable, with the device current) runs the first time the address is
+// needed in each context, and the address is kept for later calls, so that
+// a call inside a stream capture makes no lookup once one call in that
+// context has run outside it.
+class SymbolAddressCache {
+  public:
+    cudaError_t get(void** out, cudaError_t (*lookup)(void**)) {
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        if (dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+        unsigned long long ctx = 0;
+        if ((err = current_context_id(&ctx)) != cudaSuccess) return err;
+        std::lock_guard<std::mutex> lk(mu_);
+        Entry& en = e_[dev];
+        if (ctx != 0 && en.ctx == ctx && en.ptr) {
+            *out = en.ptr;
+            return cudaSuccess;
+        }
+        void* p = nullptr;
+        if ((err = lookup(&p)) != cudaSuccess) return err;
+        if (!p) return cudaErrorInvalidSymbol;
+        // the lookup made the device's primary context current if none was
+        if ((err = current_context_id(&ctx)) != cudaSuccess) return err;
+        en.ctx = ctx;
+        en.ptr = p;
+        *out = p;
+        return cudaSuccess;
+    }
+
+  private:
+    static constexpr int kDevices = 64;
+    struct Entry {
+        unsigned long long ctx = 0;
+        void* ptr = nullptr;
+    };
+    std::mutex mu_;
+    Entry e_[kDevices];
+};
 
 // Compiled configuration space of the register-held kernels.
 constexpr int kMaxSlots = 8;

@@ -232,7 +232,9 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     constexpr bool PAIRS = OP == OP_LN && sizeof(T) == 2 && VEC == 8 && WPR > 1;
     const int64_t step = (int64_t)gridDim.x * RPC;
     int64_t row = (int64_t)blockIdx.x * RPC + g;
+    pdl_launch_dependents();
     if (row >= p.rows) return;                       // the whole group leaves together
+    pdl_wait();                                      // no global access before this
 
     HeldRow<VEC, SLOTS, RES> cur;
     load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
@@ -521,8 +523,8 @@ struct RegInst {
     static constexpr int RPC = (TPR == 32) ? kWarpRowsPerCta : 1;
     static constexpr bool PF = NOPF ? false : reg_prefetch(VEC, SLOTS, TPR, RES);
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
-        reg_kernel<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES><<<grid, TPR * RPC, 0, s>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(reg_kernel<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES>, (unsigned)grid,
+                          TPR * RPC, 0, s, p);
     }
     static const KernelEntry entry;
 };
@@ -551,9 +553,24 @@ constexpr int reg_max_slots() {
     }
 }
 
+// Configurations the planner can select. The CTA-per-row shape takes the
+// fewest threads that hold the row, so a row of 128 or more threads holds
+// more than half of a thread's slots (a row that fits in half of them takes
+// half the threads); rows of 32 or 64 threads take any slot count (the warp
+// range, and the CTA variant forced on narrow rows). Residual rows of 1024
+// threads are refused by the planner (x and the residual do not fit the 64
+// registers a thread of a 1024-thread CTA has). Nothing else is compiled.
+template <int VEC, int S, int TPR, bool RES>
+constexpr bool reg_reachable() {
+    constexpr int maxs = VEC == 1 ? kMaxSlots : 32 / VEC;
+    return !(RES && TPR == 1024) && (TPR <= 64 || 2 * S > maxs);
+}
+
 template <int OP, typename T, int VEC, int S, int TPR, bool PP, bool AL, bool RES, bool NOPF>
 const KernelEntry* reg_inst_entry() {
-    if constexpr (NOPF && !reg_prefetch(VEC, S, TPR, RES))
+    if constexpr (!reg_reachable<VEC, S, TPR, RES>())
+        return nullptr;
+    else if constexpr (NOPF && !reg_prefetch(VEC, S, TPR, RES))
         return nullptr;   // the default instance already runs without prefetch
     else
         return &RegInst<OP, T, VEC, S, TPR, PP, AL, RES, NOPF>::entry;

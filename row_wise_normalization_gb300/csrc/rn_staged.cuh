@@ -86,12 +86,14 @@ __global__ void __launch_bounds__(TPB, 1) staged_kernel(const Params p) {
     const int64_t stride = gridDim.x;
     const int64_t nmine = first < p.rows ? (p.rows - 1 - first) / stride + 1 : 0;
 
+    pdl_launch_dependents();
     if (t == 0) {
         abort_flag = 0;
         for (int s = 0; s < STAGES; ++s) mbar_init(smem_addr(&bars[s]), 1);
         mbar_fence_init();
     }
     __syncthreads();
+    pdl_wait();   // no global access (bulk copies included) before this
 
     // Issue the copy of my i-th row into stage i % STAGES (thread 0 only).
     auto issue = [&](int64_t i) {
@@ -236,8 +238,7 @@ template <int OP, int TPB, int STAGES>
 struct StagedInst {
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
         const int smem = STAGES * staged_stage_bytes(p.d);
-        staged_kernel<OP, TPB, STAGES><<<grid, TPB, smem, s>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(staged_kernel<OP, TPB, STAGES>, (unsigned)grid, TPB, (size_t)smem, s, p);
     }
     // The limit is per function and process-wide, so it is raised once to the
     // whole budget (never lowered to one launch's need, which would break a

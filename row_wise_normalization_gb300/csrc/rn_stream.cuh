@@ -65,6 +65,9 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
     const int64_t d = p.d;
     const float fd = (float)d;
 
+    pdl_launch_dependents();
+    if ((int64_t)blockIdx.x >= p.rows) return;
+    pdl_wait();   // no global access before this
     int it = 0;
     for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x, ++it) {
         const T* xr = X + row * p.ldx;
@@ -188,8 +191,8 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
 template <int OP, typename T, int VEC, bool RES>
 struct StreamInst {
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
-        stream_kernel<OP, T, VEC, kStreamThreads, RES><<<grid, kStreamThreads, 0, s>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(stream_kernel<OP, T, VEC, kStreamThreads, RES>, (unsigned)grid,
+                          kStreamThreads, 0, s, p);
     }
     static const KernelEntry entry;
 };

@@ -9,6 +9,7 @@
 #include <utility>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "rownorm.h"
@@ -231,6 +232,9 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
         case RN_VARIANT_BLOCK: {
             int tpr, slots;
             if (!block_shape(units, maxs, &tpr, &slots)) return RN_ERR_VARIANT;
+            // a residual row of 1024 threads would hold x and the residual in
+            // the 64 registers such a thread has, and spill: not compiled
+            if (q.res && tpr == 1024) return RN_ERR_VARIANT;
             pl->slots = slots;
             pl->threads_per_row = tpr;
             pl->rows_per_cta = 1;
@@ -916,6 +920,71 @@ int bwd_workspace(int op, int64_t rows, int64_t d, size_t* bytes) {
 
 namespace rn {
 int record_cuda_error(cudaError_t err) { return fail_cuda(err); }
+
+int ln_bwd_check_args(const float* dy, const float* x, const float* gamma, const float* mean,
+                      const float* rstd, float* dx, float* dgamma, float* dbeta, int64_t rows,
+                      int64_t d) {
+    BwdRequest q{};
+    q.op = OP_LN;
+    q.dy = dy;
+    q.x = x;
+    q.p0 = gamma;
+    q.mean = mean;
+    q.rstd = rstd;
+    q.dx = dx;
+    q.dp0 = dgamma;
+    q.dp1 = dbeta;
+    q.rows = rows;
+    q.d = d;
+    return bwd_validate(q, false);   // every check except those of the workspace
+}
+
+namespace ctxq {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+struct CtxFns {
+    CtxGetCurrentFn current = nullptr;
+    CtxGetIdFn id = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+// The two driver calls, found once through the runtime (no link to the
+// driver library is needed).
+const CtxFns& ctx_fns() {
+    static const CtxFns fns = [] {
+        CtxFns f;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        f.err = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                                 &q);
+        if (f.err != cudaSuccess) return f;
+        if (q != cudaDriverEntryPointSuccess || !p) {
+            f.err = cudaErrorNotSupported;
+            return f;
+        }
+        f.current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        f.err = cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q);
+        if (f.err != cudaSuccess) return f;
+        if (q != cudaDriverEntryPointSuccess || !p) {
+            f.err = cudaErrorNotSupported;
+            return f;
+        }
+        f.id = reinterpret_cast<CtxGetIdFn>(p);
+        return f;
+    }();
+    return fns;
+}
+}  // namespace ctxq
+
+cudaError_t current_context_id(unsigned long long* id) {
+    const ctxq::CtxFns& f = ctxq::ctx_fns();
+    if (!f.current || !f.id) return f.err != cudaSuccess ? f.err : cudaErrorNotSupported;
+    CUcontext c = nullptr;
+    if (f.current(&c) != CUDA_SUCCESS) return cudaErrorUnknown;
+    *id = 0;
+    if (c && f.id(c, id) != CUDA_SUCCESS) return cudaErrorUnknown;
+    return cudaSuccess;
+}
 }  // namespace rn
 
 extern "C" {

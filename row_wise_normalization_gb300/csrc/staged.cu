@@ -1,6 +1,4 @@
 // Shared-memory-staged (bulk-copy) kernels and the device error word.
-#include <atomic>
-
 #include "rn_staged.cuh"
 
 namespace rn {
@@ -32,20 +30,16 @@ cudaError_t device_error_word(unsigned int* out, bool clear) {
     return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
 }
 
-// Looked up once per device and kept, so that later calls (a stream capture
-// among them) make no runtime query.
+// Looked up once per CUDA context and kept, so that later calls (a stream
+// capture among them) make no runtime query; a context created anew (after a
+// device reset) gets a fresh lookup.
 cudaError_t device_error_address(unsigned int** out) {
-    static std::atomic<void*> cache[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static SymbolAddressCache cache;
+    void* p = nullptr;
+    const cudaError_t e = cache.get(&p, [](void** q) {
+        return cudaGetSymbolAddress(q, g_device_error);
+    });
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    void* p = cache[dev].load(std::memory_order_acquire);
-    if (!p) {
-        e = cudaGetSymbolAddress(&p, g_device_error);
-        if (e != cudaSuccess) return e;
-        cache[dev].store(p, std::memory_order_release);
-    }
     *out = static_cast<unsigned int*>(p);
     return cudaSuccess;
 }

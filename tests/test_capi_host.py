@@ -317,3 +317,84 @@ def test_batched_validation_without_launch(lib):
 def test_bounded_wait_selftest_rejects_out_of_range_limits(lib):
     assert capi.selftest_bounded_wait(0, 0) == capi.RN_ERR_SIZE
     assert capi.selftest_bounded_wait(2000000, 0) == capi.RN_ERR_SIZE
+
+
+def test_no_alloc_checks_arguments_before_its_width_limit(lib):
+    """ln_bwd_noalloc reports what ln_bwd would report before its own width
+    limit: rows == 0 is a no-op at any width, a NULL input is RN_ERR_NULL, and
+    only a call that needs the static partials (parameter gradients wanted,
+    rows > 0) is refused for d > RN_NOALLOC_MAX_D. None of these calls reaches
+    CUDA."""
+    d = capi.RN_NOALLOC_MAX_D + 904
+    rows = 5
+    nd, nr = rows * d * 4, rows * 4
+    base = A
+    ptrs = {}
+    for name, n in (("dy", nd), ("x", nd), ("gamma", 4 * d), ("mean", nr), ("rstd", nr),
+                    ("dx", nd), ("dgamma", 4 * d), ("dbeta", 4 * d)):
+        ptrs[name] = base
+        base += (n + 0xFFFF) & ~0xFFFF
+    order = ("dy", "x", "gamma", "mean", "rstd", "dx", "dgamma", "dbeta")
+
+    def call(rows_, **kw):
+        p = dict(ptrs)
+        p.update(kw)
+        return capi.ln_bwd_noalloc(*[p[k] for k in order], rows_, d, 0)
+
+    assert call(0, **{k: 0 for k in order}) == capi.RN_OK
+    assert call(rows, dy=0) == capi.RN_ERR_NULL
+    assert call(rows, dx=ptrs["x"]) == capi.RN_ERR_ALIAS
+    assert call(rows, dgamma=ptrs["dgamma"] + 2) == capi.RN_ERR_ALIGN
+    assert call(-1) == capi.RN_ERR_SIZE
+    assert call(rows) == capi.RN_ERR_SCRATCH
+    assert call(rows, dgamma=0) == capi.RN_ERR_SCRATCH
+
+
+def _widths():
+    ws = set(range(1, 300)) | {w + k for w in (384, 512, 768, 1024, 1536, 2048, 3072, 4096,
+                                                6144, 8192, 12288, 16384, 24576, 32768)
+                               for k in range(-9, 10)}
+    return sorted(w for w in ws if w > 0)
+
+
+@pytest.mark.parametrize("dtype", [capi.RN_DTYPE_F32, capi.RN_DTYPE_BF16, capi.RN_DTYPE_F16])
+def test_every_planned_register_configuration_is_compiled(lib, dtype):
+    """Only the configurations the planner can choose are compiled. A call
+    whose plan is a register-held kernel must get as far as the launch: on a
+    machine without a GPU that is RN_ERR_CUDA (the first CUDA call fails),
+    while a configuration missing from the library returns RN_ERR_VARIANT
+    before any CUDA call."""
+    es = 4 if dtype == capi.RN_DTYPE_F32 else 2
+    X, Y, P = A, A + (1 << 28), A + (1 << 29)
+    for d in _widths():
+        for xo, yo, po in ((0, 0, 0), (1, 1, 0), (3, 3, 2), (0, 1, 0)):
+            x, y, g = X + es * xo, Y + es * yo, P + es * po
+            b = g + (1 << 20)
+            for v in (capi.RN_VARIANT_AUTO, capi.RN_VARIANT_WARP, capi.RN_VARIANT_BLOCK):
+                for op in (capi.RN_OP_LN, capi.RN_OP_RMS):
+                    p1 = b if op == capi.RN_OP_LN else 0
+                    try:
+                        pl = capi.plan_typed(dtype, op, v, d, x, y, g, p1)
+                    except capi.RowNormError:
+                        continue
+                    if pl.variant not in (capi.RN_VARIANT_WARP, capi.RN_VARIANT_BLOCK):
+                        continue
+                    if op == capi.RN_OP_LN:
+                        st = capi.ln_fwd_typed(dtype, v, x, g, b, y, 0, 0, 3, d, 1e-5, 0)
+                    else:
+                        st = capi.rms_fwd_typed(dtype, v, x, g, y, 3, d, 1e-5, 0)
+                    assert st == capi.RN_ERR_CUDA, (dtype, op, v, d, xo, yo, po, st)
+                    if dtype != capi.RN_DTYPE_F32:
+                        continue
+                    # the residual forms of the same rows
+                    r = A + (1 << 30) + 4 * xo
+                    try:
+                        capi.plan_residual(op, v, d, x, r, 0, y, g, p1)
+                    except capi.RowNormError:
+                        continue
+                    if op == capi.RN_OP_LN:
+                        st = capi.ln_fwd_residual_variant(v, x, r, g, b, 0, y, 0, 0, 3, d,
+                                                          1e-5, 0)
+                    else:
+                        st = capi.rms_fwd_residual_variant(v, x, r, g, 0, y, 3, d, 1e-5, 0)
+                    assert st == capi.RN_ERR_CUDA, ("res", op, v, d, xo, yo, po, st)
