@@ -1204,12 +1204,16 @@ VARIANTS = ("auto", "warp", "block", "staged", "stream", "cluster")
 
 
 def run_case(args):
-    """One forward call, variant forced, timed alone: W warm-up launches, K
-    launches each after the L2 flush (cold), then K launches back to back on
-    the same buffers behind a GPU spin (warm). Prints one JSON line. The
-    launch order is fixed so that an ncu capture can select a cold launch
-    (any launch under --cache-control all) or a warm one (launch W + K + 2
-    under --cache-control none: a warm launch that follows another)."""
+    """One forward call, variant forced: W warm-up launches, K launches each
+    after the L2 flush (cold), K launches back to back on the same buffers
+    behind a GPU spin (warm), then (forward calls) n launches over n
+    distinct copies of x and y, more than twice the L2 in all, and K more
+    back to back over them, one event pair around the K (back_to_back).
+    Prints one JSON line. The launch order is fixed so that an ncu capture
+    can select a cold launch (any launch under --cache-control all), a warm
+    one (launch W + K + 2 under --cache-control none: a warm launch that
+    follows another) or a back-to-back one (W + 2K + n + 2 and on, under
+    --cache-control none)."""
     import torch
 
     import row_wise_normalization_gb300 as rn
@@ -1273,6 +1277,34 @@ def run_case(args):
     flush = Flusher(torch, device)
     cold = time_launches(torch, f, args.steps, flush)
     warm = time_launches(torch, f, args.steps)
+    b2b = None
+    if not (args.backward or args.residual):
+        # back to back over distinct copies of x (and y), more than twice the
+        # L2 in all, one event pair around K calls
+        l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (128 << 20)
+        n = max(2, -(-2 * l2 // (2 * x.numel() * x.element_size())) + 1)
+        xs = [(x.clone(), torch.empty_like(y)) for _ in range(n)]
+
+        def fi(i):
+            xi, yi = xs[i % n]
+            if op == "ln":
+                rn.ln_fwd(xi, ps[0], ps[1], wl.eps, y=yi, mean=mean, rstd=rstd, variant=variant)
+            else:
+                rn.rms_fwd(xi, ps[0], wl.eps, y=yi, variant=variant)
+
+        for i in range(n):
+            fi(i)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(HOST_LEAD_CYCLES_PER_STEP * args.steps)
+        a.record()
+        for i in range(args.steps):
+            fi(i)
+        b.record()
+        torch.cuda.synchronize()
+        b2b = [a.elapsed_time(b) / args.steps]
+        del xs
     opc = capi.RN_OP_LN if op == "ln" else capi.RN_OP_RMS
     if args.residual:
         pl = capi.plan_residual(opc, variant, d, x.data_ptr(), r.data_ptr(), h.data_ptr(),
@@ -1286,7 +1318,9 @@ def run_case(args):
            "planned": ("backward row kernel + column reduction" if args.backward
                        else capi.variant_name(pl.variant)),
            "bytes": nbytes}
-    for name, ts in (("cold", cold), ("warm", warm)):
+    for name, ts in (("cold", cold), ("warm", warm), ("back_to_back", b2b)):
+        if ts is None:
+            continue
         med = statistics.median(ts)
         out[name] = {"ms_median": med, "GBps": gbs(nbytes, med),
                      "frac_of_measured_hbm": gbs(nbytes, med) / peak}

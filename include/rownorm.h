@@ -39,6 +39,16 @@
  *   Stream      `stream` is a cudaStream_t passed as void*; NULL means the
  *               legacy default stream. Work is enqueued asynchronously; the
  *               results are valid once the stream has reached that point.
+ *               The forward kernels are launched with programmatic stream
+ *               serialization (programmatic dependent launch): the GPU may
+ *               start one while the kernel ahead of it on the stream is
+ *               still running, and it reads and writes nothing before that
+ *               kernel has completed, so stream order holds as for any
+ *               launch. Work the caller enqueues afterwards sees the
+ *               results as usual; only a kernel of the caller's that is
+ *               itself launched with programmatic serialization right after
+ *               one of these calls must wait (cudaGridDependencySynchronize)
+ *               before it reads the outputs, as for any programmatic launch.
  *   Sizes       rows == 0 is a no-op returning RN_OK (pointers may then be
  *               NULL). rows < 0, d <= 0, or rows*d beyond 2^61 elements
  *               returns RN_ERR_SIZE.
@@ -278,15 +288,21 @@ int rms_bwd_typed(int dtype, const void *dy, const void *x, const void *w, void 
  * synchronisation, or C code with no allocator. Arguments, layouts, results
  * and errors are those of ln_bwd, without the workspace: the parameter-
  * gradient partials go to one static device array of RN_NOALLOC_SCRATCH_BYTES
- * (8 MiB), which every GPU that loads the library holds until exit.
- * d > RN_NOALLOC_MAX_D (4096) returns RN_ERR_SCRATCH and launches nothing; at
+ * (8 MiB), which every GPU that loads the library holds until exit. At
  * d <= 4096 the array holds at least 256 partial rows, so the grid matches
  * ln_bwd's with a workspace of that size, and the results are the same bits.
- * The first call on each device looks the array up (cudaGetSymbolAddress,
- * with that device current); make that call before any stream capture on the
- * device. Nothing here calls cudaMalloc, cudaFree or another allocating
- * routine. All calls share the array and nothing in it has to start at zero;
- * calls that can overlap on the GPU (two streams, two threads) race on it.
+ * The first call on a device that needs the array looks it up
+ * (cudaGetSymbolAddress, with that device current) and keeps the address for
+ * the device's CUDA context; make that call before any stream capture on the
+ * device. A new context for the device (after cudaDeviceReset) is looked up
+ * again on its first call. Nothing here calls cudaMalloc, cudaFree or
+ * another allocating routine. All calls share the array and nothing in it
+ * has to start at zero; calls that can overlap on the GPU (two streams, two
+ * threads) race on it. The arguments are checked as ln_bwd checks them
+ * first; then a call that needs the partials (rows > 0 and dgamma or dbeta
+ * not NULL) with d > RN_NOALLOC_MAX_D (4096) returns RN_ERR_SCRATCH and
+ * launches nothing. Without parameter gradients no partials are needed and
+ * every width ln_bwd takes runs.
  */
 #define RN_NOALLOC_SCRATCH_BYTES (8u << 20)
 #define RN_NOALLOC_MAX_D 4096
@@ -388,12 +404,16 @@ int rn_plan_for_residual(int op, int variant, int64_t d, const void *x, const vo
                          rn_plan *plan);
 
 /* Device error word of the current device: bit 0 (RN_DEVERR_STAGED_TIMEOUT)
- * is set if a staged kernel's (forward or backward) wait for a bulk copy ran out (about one
- * second; the kernel then stops early and its outputs are incomplete). The
- * word is sticky until cleared: `clear` != 0 resets it after reading.
- * Synchronous (a device-to-host copy). Returns RN_OK, RN_ERR_NULL or
- * RN_ERR_CUDA. */
-enum { RN_DEVERR_STAGED_TIMEOUT = 1 };
+ * is set if a staged kernel's (forward or backward) wait for a bulk copy ran
+ * out, bit 1 (RN_DEVERR_CLUSTER_TIMEOUT) if a cluster kernel's wait for its
+ * peer CTAs' partial statistics did (about one second each; the kernel then
+ * stops early and its outputs are incomplete). The word is sticky until
+ * cleared: `clear` != 0 resets it after reading. Synchronous (a
+ * device-to-host copy). Returns RN_OK, RN_ERR_NULL or RN_ERR_CUDA. The
+ * kernels find the word's device address once per CUDA context (a device
+ * reset gives the device a new context and a new lookup); make one call of
+ * each configuration before capturing calls into a CUDA graph. */
+enum { RN_DEVERR_STAGED_TIMEOUT = 1, RN_DEVERR_CLUSTER_TIMEOUT = 2 };
 int rn_device_error(unsigned int *flags, int clear);
 
 /* Self-test of the failure path above (library infrastructure; the paper has

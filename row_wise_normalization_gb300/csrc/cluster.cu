@@ -7,9 +7,11 @@ namespace rn {
 template <int OP, bool AL>
 const ClusterEntry* cluster_pick(int slots, int threads, int cl) {
     if (threads == 256) {
+        // 4 quads a thread only on 2 CTAs: a wider cluster of 4 quads holds
+        // what half as many CTAs of 8 quads hold, and the planner takes those
+        if (cl == 2 && slots == 4) return &ClusterInst<OP, 4, 256, 2, AL>::entry;
 #define RN_CL(CLV) \
     if (cl == CLV) {                                                            \
-        if (slots == 4) return &ClusterInst<OP, 4, 256, CLV, AL>::entry;       \
         if (slots == 6) return &ClusterInst<OP, 6, 256, CLV, AL>::entry;       \
         if (slots == 8) return &ClusterInst<OP, 8, 256, CLV, AL>::entry;       \
     }

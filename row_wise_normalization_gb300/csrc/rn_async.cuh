@@ -77,24 +77,4 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// One 128-bit vector of T (4 FP32 or 8 16-bit elements) from shared memory,
-// widened to FP32. A plain load: the compiler keeps it after the preceding
-// mbarrier wait (an asm statement that clobbers memory).
-template <typename T, int VEC>
-__device__ __forceinline__ void lds_vec(Vec<VEC>& r, const T* p) {
-    static_assert(VEC * sizeof(T) == 16, "one 128-bit vector");
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    if constexpr (sizeof(T) == 4) {
-        r.v[0] = __uint_as_float(u.x);
-        r.v[1] = __uint_as_float(u.y);
-        r.v[2] = __uint_as_float(u.z);
-        r.v[3] = __uint_as_float(u.w);
-    } else {
-        unpack2(u.x, r.v[0], r.v[1], (T*)nullptr);
-        unpack2(u.y, r.v[2], r.v[3], (T*)nullptr);
-        unpack2(u.z, r.v[4], r.v[5], (T*)nullptr);
-        unpack2(u.w, r.v[6], r.v[7], (T*)nullptr);
-    }
-}
-
 }  // namespace rn

@@ -587,8 +587,10 @@ const BwdEntry BwdInst<OP, T, VEC, SLOTS, TPR, PG>::entry = {
     (const void*)&bwd_kernel<OP, T, VEC, SLOTS, TPR, BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC, PG>,
     TPR * BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC, BwdInst<OP, T, VEC, SLOTS, TPR, PG>::RPC,
     BwdInst<OP, T, VEC, SLOTS, TPR, PG>::SMEM, &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::launch,
-    BwdInst<OP, T, VEC, SLOTS, TPR, PG>::SMEM > 48 * 1024 ? &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::prepare
-                                                          : nullptr};
+    // (any dynamic shared memory raises the limit: the default 48 KB counts
+    // the static shared memory too)
+    BwdInst<OP, T, VEC, SLOTS, TPR, PG>::SMEM > 0 ? &BwdInst<OP, T, VEC, SLOTS, TPR, PG>::prepare
+                                                  : nullptr};
 
 // Staged instances: the ring's size follows d and p.stages, so the dynamic
 // shared memory is set per launch and its limit raised once to the whole

@@ -108,6 +108,14 @@ struct ClusterCfg {
     static constexpr int WPR = TPB / 32;
     static constexpr int NE = CL * WPR;          // partials merged per row
     static constexpr int MINB = PF ? (TPB <= 256 ? 2 : 1) : (TPB >= 1024 ? 1 : (TPB == 512 ? 2 : 768 / TPB));
+    // PSM: aligned rows of 256-thread CTAs keep the CTA's slice of gamma/beta
+    // (w) in dynamic shared memory, loaded once: every thread its own quads,
+    // in planes of TPB float4 per slot (64 KB per CTA for LayerNorm at 8 quads
+    // a thread). Unaligned rows move their head peel, and with it the
+    // columns a thread owns, from row to row; wider CTAs would need more
+    // shared memory than an SM has for two of them.
+    static constexpr bool PSM = AL && TPB == 256;
+    static constexpr int SMEM = PSM ? (OP == OP_LN ? 2 : 1) * SLOTS * TPB * 16 : 0;
 };
 
 template <int OP, int SLOTS, int TPB, int CL, bool PF, bool AL>
@@ -143,6 +151,25 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
     // before anyone sends into a peer
     cluster_sync_all();
     pdl_wait();   // no global access before this
+
+    // the CTA's parameter slice, staged once (PSM); thread t reads back only
+    // the entries it wrote, so no barrier is needed
+    extern __shared__ __align__(16) float4 cl_par[];
+    if constexpr (C::PSM) {
+        const int nv = d >> 2;
+        const int Q = (nv + CL - 1) / CL;
+        const int q0 = (int)c * Q;
+        const int nq = nv - q0 < Q ? nv - q0 : Q;
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) {
+            const int q = t + k * TPB;
+            if (q < nq) {
+                cl_par[k * TPB + t] = ld_p4(p.p0 + 4 * (q0 + q));
+                if constexpr (OP == OP_LN)
+                    cl_par[(SLOTS + k) * TPB + t] = ld_p4(p.p1 + 4 * (q0 + q));
+            }
+        }
+    }
 
     struct Slice {
         Vec<4> v[SLOTS];
@@ -298,9 +325,18 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
             if (q < nq) {
                 const int j = h + 4 * (q0 + q);
                 Vec<4> a, bb, o;
-                ld_p(a, p.p0 + j, pa);
+                if constexpr (C::PSM) {
+                    const float4 a4 = cl_par[k * TPB + t];
+                    a.v[0] = a4.x; a.v[1] = a4.y; a.v[2] = a4.z; a.v[3] = a4.w;
+                    if constexpr (OP == OP_LN) {
+                        const float4 b4 = cl_par[(SLOTS + k) * TPB + t];
+                        bb.v[0] = b4.x; bb.v[1] = b4.y; bb.v[2] = b4.z; bb.v[3] = b4.w;
+                    }
+                } else {
+                    ld_p(a, p.p0 + j, pa);
+                    if constexpr (OP == OP_LN) ld_p(bb, p.p1 + j, pa);
+                }
                 if constexpr (OP == OP_LN) {
-                    ld_p(bb, p.p1 + j, pa);
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         o.v[u] = fmaf(((cur.v[k].v[u] - cur.K) - mus) * rs, a.v[u], bb.v[u]);
@@ -339,11 +375,12 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
 template <int OP, int SLOTS, int TPB, int CL, bool AL>
 struct ClusterInst {
     static constexpr bool PF = TPB <= 256;
+    static constexpr int SMEM = ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::SMEM;
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid, 1, 1);
         cfg.blockDim = dim3(TPB, 1, 1);
-        cfg.dynamicSmemBytes = 0;
+        cfg.dynamicSmemBytes = SMEM;
         cfg.stream = s;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -357,16 +394,23 @@ struct ClusterInst {
         return cudaLaunchKernelEx(&cfg, cluster_kernel<OP, SLOTS, TPB, CL, PF, AL>, p);
     }
     static cudaError_t prepare(int) {
+        cudaError_t e = cudaSuccess;
         if (CL > 8)
-            return cudaFuncSetAttribute(cluster_kernel<OP, SLOTS, TPB, CL, PF, AL>,
-                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        return cudaSuccess;
+            e = cudaFuncSetAttribute(cluster_kernel<OP, SLOTS, TPB, CL, PF, AL>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        // any dynamic shared memory: the default limit covers static and
+        // dynamic together (48 KB), which the static part already uses some of
+        if (e == cudaSuccess && SMEM > 0)
+            e = cudaFuncSetAttribute(cluster_kernel<OP, SLOTS, TPB, CL, PF, AL>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        return e;
     }
     // Clusters that can be resident at once.
     static cudaError_t max_clusters(int* n) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(CL, 1, 1);
         cfg.blockDim = dim3(TPB, 1, 1);
+        cfg.dynamicSmemBytes = SMEM;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = CL;

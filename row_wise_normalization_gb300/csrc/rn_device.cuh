@@ -386,4 +386,39 @@ __device__ __forceinline__ int head_peel(const float* p, int64_t d) {
     return h > d ? (int)d : h;
 }
 
+// 16 raw bytes of a parameter vector (read-only path, L1 allocated), and a
+// 16-byte store to shared memory: the parameters staged per CTA.
+template <typename T>
+__device__ __forceinline__ uint4 ld_p_raw16(const T* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+template <typename T>
+__device__ __forceinline__ void st_shared_v4(T* p, uint4 v) {
+    *reinterpret_cast<uint4*>(p) = v;
+}
+
+// One 128-bit vector of T (4 FP32 or 8 16-bit elements) from shared memory,
+// widened to FP32. A plain load: the compiler keeps it after the preceding
+// mbarrier wait (an asm statement that clobbers memory).
+template <typename T, int VEC>
+__device__ __forceinline__ void lds_vec(Vec<VEC>& r, const T* p) {
+    static_assert(VEC * sizeof(T) == 16, "one 128-bit vector");
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    if constexpr (sizeof(T) == 4) {
+        r.v[0] = __uint_as_float(u.x);
+        r.v[1] = __uint_as_float(u.y);
+        r.v[2] = __uint_as_float(u.z);
+        r.v[3] = __uint_as_float(u.w);
+    } else {
+        unpack2(u.x, r.v[0], r.v[1], (T*)nullptr);
+        unpack2(u.y, r.v[2], r.v[3], (T*)nullptr);
+        unpack2(u.z, r.v[4], r.v[5], (T*)nullptr);
+        unpack2(u.w, r.v[6], r.v[7], (T*)nullptr);
+    }
+}
+
 }  // namespace rn

@@ -58,7 +58,16 @@ constexpr int reg_budget(int op, int vec, int slots, bool pf, bool pp, bool res 
 // SM, LayerNorm rows of 256 threads at 768. Narrower slices fill the SM as
 // far as the budget allows.
 constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, bool pp,
-                           bool res = false, bool al = true) {
+                           bool res = false, bool al = true, bool ps = false) {
+    if (ps) {
+        // parameters in shared memory (warp-per-row instances): as many CTAs
+        // as the held row (two with prefetch) and a fixed allowance let fit,
+        // so that without prefetch every row of a call up to that size is in
+        // flight at once (LayerNorm FP32 d = 768: 72 registers, 7 CTAs of 128)
+        const int per = ((48 + slots * vec * (pf ? 2 : 1) + 7) / 8) * 8;
+        const int n = 65536 / (per * threads);
+        return n < 1 ? 1 : (n > 16 ? 16 : n);
+    }
     if (vec == 8 && slots * vec >= 24 && !pf && threads >= 128) {
         const int target = (op == 0 && threads == 256) ? 768 : 1024;
         return target / threads > 0 ? target / threads : 1;
@@ -193,10 +202,12 @@ __device__ __forceinline__ float held_m2_pairs(const HeldRow<VEC, SLOTS, RES>& r
 }
 
 template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL,
-          bool RES>
-__global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES, AL))
+          bool RES, bool PS = false>
+__global__ void __launch_bounds__(TPR * RPC,
+                                  reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES, AL, PS))
     reg_kernel(const Params p) {
     static_assert(TPR % 32 == 0 && TPR * RPC <= 1024, "bad CTA shape");
+    static_assert(!PS || (AL && !PP && !RES && TPR == 32), "shared parameters: aligned warp rows");
     static_assert(VEC == 1 || VEC == Elem<T>::kVec, "a vector is one 128-bit access");
     static_assert(!PP || VEC > 1, "parameters are held only on the vector path");
     static_assert(!AL || VEC > 1, "the aligned layout is a vector layout");
@@ -233,12 +244,32 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
     const int64_t step = (int64_t)gridDim.x * RPC;
     int64_t row = (int64_t)blockIdx.x * RPC + g;
     pdl_launch_dependents();
-    if (row >= p.rows) return;                       // the whole group leaves together
-    pdl_wait();                                      // no global access before this
-
     HeldRow<VEC, SLOTS, RES> cur;
-    load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
-                                                 RES ? R + row * p.ldr : nullptr, d, t);
+    // PS (parameters staged in shared memory): the CTA copies gamma/beta (w)
+    // into shared memory once, after issuing its rows' loads and while they
+    // are in flight, and every row reads them from there -- no registers held
+    // for them across rows, and no global load of them after a row's
+    // reduction. Groups without a row take part in the copy, then leave.
+    constexpr int NPS = OP == OP_LN ? 2 : 1;
+    __shared__ __align__(16) T sp[PS ? NPS : 1][PS ? SLOTS * TPR * VEC : 1];
+    if constexpr (PS) {
+        pdl_wait();                                  // no global access before this
+        const bool active = row < p.rows;
+        if (active)
+            load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx, nullptr, d, t);
+        const int nvp = d / VEC;
+        for (int q = threadIdx.x; q < nvp; q += TPR * RPC) {
+            st_shared_v4(&sp[0][q * VEC], ld_p_raw16(P0 + q * VEC));
+            if constexpr (OP == OP_LN) st_shared_v4(&sp[1][q * VEC], ld_p_raw16(P1 + q * VEC));
+        }
+        __syncthreads();
+        if (!active) return;                         // the whole group leaves together
+    } else {
+        if (row >= p.rows) return;                   // the whole group leaves together
+        pdl_wait();                                  // no global access before this
+        load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
+                                                     RES ? R + row * p.ldr : nullptr, d, t);
+    }
 
     // Parameters held across rows (PP, only with AL): every row is aligned.
     Vec<VEC> pg[PP ? SLOTS : 1], pb[(PP && OP == OP_LN) ? SLOTS : 1];
@@ -297,7 +328,7 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
         // parameters load this row's gamma/beta (w) now, so that the loads
         // overlap the reduction instead of following it -- on the short,
         // launch-bound rows the dependent chain is the whole kernel
-        constexpr bool EP = !PP && SLOTS * VEC <= 8;
+        constexpr bool EP = !PP && !PS && SLOTS * VEC <= 8;
         Vec<VEC> ea[EP ? SLOTS : 1], eb[(EP && OP == OP_LN) ? SLOTS : 1];
         float eae = 0.f, ebe = 0.f;
         if constexpr (EP) {
@@ -448,6 +479,9 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
                 if constexpr (PP) {
                     a = pg[s];
                     if constexpr (OP == OP_LN) b = pb[s];
+                } else if constexpr (PS) {
+                    lds_vec<T, VEC>(a, &sp[0][j]);
+                    if constexpr (OP == OP_LN) lds_vec<T, VEC>(b, &sp[1][j]);
                 } else if constexpr (EP) {
                     a = ea[s];
                     if constexpr (OP == OP_LN) b = eb[s];
@@ -517,26 +551,48 @@ __global__ void __launch_bounds__(TPR * RPC, reg_min_ctas(TPR * RPC, OP, VEC, SL
 // NOPF: the same configuration compiled without prefetch at the no-prefetch
 // occupancy, for calls whose rows all fit in one wave of it (nothing to
 // overlap a prefetch with); only where the default instance prefetches.
+// PS: parameters staged in shared memory (warp-per-row, aligned, no prefetch).
 template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES,
-          bool NOPF = false>
+          bool NOPF = false, bool PS = false>
 struct RegInst {
     static constexpr int RPC = (TPR == 32) ? kWarpRowsPerCta : 1;
     static constexpr bool PF = NOPF ? false : reg_prefetch(VEC, SLOTS, TPR, RES);
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
-        return launch_pdl(reg_kernel<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES>, (unsigned)grid,
-                          TPR * RPC, 0, s, p);
+        return launch_pdl(reg_kernel<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES, PS>,
+                          (unsigned)grid, TPR * RPC, 0, s, p);
     }
     static const KernelEntry entry;
 };
 
-template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES, bool NOPF>
-const KernelEntry RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::entry = {
+template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES, bool NOPF,
+          bool PS>
+const KernelEntry RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::entry = {
     (const void*)&reg_kernel<OP, T, VEC, SLOTS, TPR,
-                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::RPC,
-                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::PF, PP, AL, RES>,
-    TPR * RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::RPC,
-    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::RPC, 0,
-    &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF>::launch, nullptr};
+                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::RPC,
+                             RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::PF, PP, AL,
+                             RES, PS>,
+    TPR * RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::RPC,
+    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::RPC, 0,
+    &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::launch, nullptr};
+
+// The warp-per-row instances with their parameters in shared memory: every
+// slot count a row of up to 32 * 8 FP32 (32 * 4 16-bit) vectors needs, with
+// (NOPF false) or without prefetch.
+template <int OP, typename T, int VEC, bool NOPF = true>
+const KernelEntry* reg_pick_ps(int slots) {
+    constexpr int M = 32 / VEC;
+    switch (slots) {
+        case 1: return &RegInst<OP, T, VEC, 1, 32, false, true, false, NOPF, true>::entry;
+        case 2: return &RegInst<OP, T, VEC, 2, 32, false, true, false, NOPF, true>::entry;
+        case 3: return &RegInst<OP, T, VEC, 3, 32, false, true, false, NOPF, true>::entry;
+        case 4: return &RegInst<OP, T, VEC, 4, 32, false, true, false, NOPF, true>::entry;
+        case 5: if constexpr (M >= 5) return &RegInst<OP, T, VEC, 5, 32, false, true, false, NOPF, true>::entry; else return nullptr;
+        case 6: if constexpr (M >= 6) return &RegInst<OP, T, VEC, 6, 32, false, true, false, NOPF, true>::entry; else return nullptr;
+        case 7: if constexpr (M >= 7) return &RegInst<OP, T, VEC, 7, 32, false, true, false, NOPF, true>::entry; else return nullptr;
+        case 8: if constexpr (M >= 8) return &RegInst<OP, T, VEC, 8, 32, false, true, false, NOPF, true>::entry; else return nullptr;
+        default: return nullptr;
+    }
+}
 
 // Slots per thread a family is compiled for: up to 8 FP32 vectors (32 floats),
 // 4 16-bit vectors (32 floats) or 8 scalars; held parameters allow 24 floats,

@@ -133,6 +133,16 @@ def test_backward_small_workspace_and_no_param_grads():
     _check_ln(x, dy, g, out, chain=rows)
 
 
+@pytest.mark.parametrize("d", [8196, 12288, 16384])
+def test_wide_backward_without_param_grads(d):
+    """1024-thread rows without parameter gradients: the parameters alone
+    take the dynamic shared memory (exactly 48 KB at 12288 floats)."""
+    rows = 64
+    x, dy, g, _ = _case(rows, d, seed=89)
+    m32, r32 = _stats(x, g)
+    _check_ln(x, dy, g, _run_ln(x, dy, g, m32, r32, param_grads=False), chain=0)
+
+
 def test_backward_torch_binding_and_autograd_match():
     torch = G.torch_cuda()
     import row_wise_normalization_gb300 as rn

@@ -87,8 +87,8 @@ def test_sweep_offset_rows(wl):
 # ---------------------------------------------------------------------------
 # ragged widths and every 16-byte phase of x, y and the parameters
 # ---------------------------------------------------------------------------
-PHASE_WIDTHS = [1, 2, 3, 5, 7, 31, 33, 127, 130, 769, 1027, 1029, 4099, 8193, 9000, 32771,
-                33001]
+PHASE_WIDTHS = [1, 2, 3, 5, 7, 31, 33, 127, 130, 769, 1027, 1029, 4099, 8193, 9000, 16387,
+                20000, 20003, 24576, 24579, 32768, 32771, 33001]
 
 
 @pytest.mark.parametrize("d", PHASE_WIDTHS)
@@ -134,6 +134,36 @@ def test_very_wide_rows(rows, d):
             _check_ln(x, g, b, G.run_ln(x, g, b, variant=v, x_off=x_off, y_off=y_off, p_off=2))
         for v in G.variants_for(RMS, d, x_off, y_off):
             _check_rms(x, g, G.run_rms(x, g, variant=v, x_off=x_off, y_off=y_off))
+
+
+def _cluster_shapes():
+    # every compiled cluster shape at the widest row it takes: 256-thread CTAs
+    # of 4 (2 CTAs only), 6 or 8 quads a thread over 2-16 CTAs, then 16 CTAs
+    # of 512 and 1024 threads
+    out = [(2, 256, 4)] + [(c, 256, s) for c in (2, 4, 8, 16) for s in (6, 8)]
+    return out + [(16, 512, 8), (16, 1024, 8)]
+
+
+@pytest.mark.parametrize("cl,threads,slots", _cluster_shapes())
+def test_every_cluster_shape(cl, threads, slots):
+    """The cluster kernel at every compiled shape (parameters in shared
+    memory on aligned 256-thread shapes, 16-96 KB of it), LayerNorm and
+    RMSNorm, aligned and at another 16-byte phase, at the widest row of the
+    shape, through the forced variant."""
+    rows = 3
+    d_al = 4 * cl * threads * slots                    # the widest aligned row
+    for d, x_off, y_off in ((d_al, 0, 0), (d_al - 4 * (cl - 1) - 2, 1, 1)):
+        wl = workloads.Workload("ln", rows, d, seed=43, x_dist="offset", x_std=2.0)
+        x = wl.x()
+        g, b = wl.params()
+        pl = capi.plan(LN, capi.RN_VARIANT_CLUSTER, d, (1 << 20) + 4 * x_off,
+                       (1 << 30) + 4 * y_off)
+        assert (pl.cluster, pl.threads_per_cta, pl.slots) == (cl, threads, slots)
+        assert pl.aligned == (1 if x_off == 0 else 0)
+        _check_ln(x, g, b, G.run_ln(x, g, b, variant=capi.RN_VARIANT_CLUSTER, x_off=x_off,
+                                    y_off=y_off, p_off=2 * x_off))
+        _check_rms(x, g, G.run_rms(x, g, variant=capi.RN_VARIANT_CLUSTER, x_off=x_off,
+                                   y_off=y_off, p_off=2 * x_off))
 
 
 @pytest.mark.parametrize("rows,d", [(40000, 16384), (5000, 65536)])
