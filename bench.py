@@ -85,7 +85,7 @@ def hbm_peak():
 # family): a change to any of them invalidates recorded ncu counters.
 KERNEL_SOURCES = ("rn_reg.cuh", "rn_device.cuh", "rn_params.h", "reg_ln_v4.cu", "reg_ln_v4_al.cu",
                   "reg_ln_v4_pp.cu", "reg_ln_v1.cu", "reg_rms_v4.cu", "reg_rms_v4_al.cu",
-                  "reg_rms_v4_pp.cu", "reg_rms_v1.cu")
+                  "reg_rms_v4_pp.cu", "reg_rms_v1.cu", "reg_ps_f32.cu")
 
 
 CLOCK_WINDOW_S = 0.3
@@ -1129,7 +1129,9 @@ def run_ours(args, rank, world, local_rank):
                                                 "distinct batches"},
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6800 GB/s",
-                     "kernel": f"reg_kernel ({pl['variant']}), one launch per step",
+                     "kernel": f"reg_kernel ({pl['variant']} per row; at 4096 x 768 the "
+                               "instance with gamma/beta staged in shared memory, every row "
+                               "in flight in one wave), one launch per step",
                      "plan": pl},
         "cpu_baseline": cpu,
         "parity": parity,

@@ -363,12 +363,21 @@ __global__ void __launch_bounds__(TPR * RPC, bwd_min_ctas(TPR * RPC, SLOTS * VEC
             } else {
                 named_sync(1 + g, TPR);
             }
-            s1 = 0.f;
-            s2 = 0.f;
+            if constexpr (WPR >= 16) {
+                // 16 or 32 partials: a shuffle reduction (every lane ends
+                // with the same sums) rather than a serial chain of that
+                // many shared-memory loads, which the 64 registers of a
+                // 1024-thread CTA could not hold without spilling
+                s1 = warp_sum(lane < WPR ? slot[lane][0] : 0.f);
+                s2 = warp_sum(lane < WPR ? slot[lane][1] : 0.f);
+            } else {
+                s1 = 0.f;
+                s2 = 0.f;
 #pragma unroll
-            for (int k = 0; k < WPR; ++k) {
-                s1 += slot[k][0];
-                s2 += slot[k][1];
+                for (int k = 0; k < WPR; ++k) {
+                    s1 += slot[k][0];
+                    s2 += slot[k][1];
+                }
             }
         }
         float c1, c2;

@@ -78,6 +78,12 @@ constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, boo
         // (the one-wave instances) 512, which leaves 128 registers (a wide
         // LayerNorm slice needs about 100) and no spills
         if (threads < 256) return 512 / threads;
+        // the one-wave LayerNorm instances of 256 threads and 6-7 vectors
+        // (their default instance prefetches): two CTAs, 128 registers and
+        // no spill; at three CTAs they spilled 8-12 bytes and ran 12-13%
+        // slower back to back (300 x 6144 5.50 -> 4.79 us, 300 x 7168
+        // 6.11 -> 5.36 us; equal with the L2 flushed before each launch)
+        if (threads == 256 && op == 0 && al && (slots == 6 || slots == 7)) return 2;
         return threads >= 1024 ? 1 : (threads == 512 ? 2 : 768 / threads);
     }
     // the general (unaligned) vector layout also carries the row's head
@@ -626,6 +632,8 @@ template <int OP, typename T, int VEC, int S, int TPR, bool PP, bool AL, bool RE
 const KernelEntry* reg_inst_entry() {
     if constexpr (!reg_reachable<VEC, S, TPR, RES>())
         return nullptr;
+    else if constexpr (AL && !PP && reg_may_hold_params(VEC, S, TPR))
+        return nullptr;   // aligned rows of this shape hold their parameters (the PP sibling)
     else if constexpr (NOPF && !reg_prefetch(VEC, S, TPR, RES))
         return nullptr;   // the default instance already runs without prefetch
     else

@@ -209,8 +209,19 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
         // give up or pay for in shared-memory passes.
         // With a residual, 1024-thread rows would hold x and the residual in
         // 64 registers and spill; those rows stream instead.
+        // Aligned FP32 LayerNorm rows too wide for 512 threads go to the
+        // cluster (now that its statistics meet without a cluster barrier and
+        // its parameters stay in shared memory) rather than to one
+        // 1024-thread CTA: measured on GB300, A/B in two runs, LayerNorm
+        // 4096 x 20000 123 -> 109 us and 512 x 32768 34.2 -> 28.9 us (cold),
+        // 1024 x 24576 35.9 -> 34.1 us (back to back), about even at
+        // 2048 x 24576; RMSNorm 1024 x 20000 stays faster on one CTA
+        // (27.6 against 29.6 us back to back).
         if (units <= 32 * maxs)
             v = RN_VARIANT_WARP;
+        else if (q.op == OP_LN && f32 && !q.res && al && units > 512 * maxs &&
+                 units <= 1024 * maxs && cluster_shape(units, &ct, &cc, &cs))
+            v = RN_VARIANT_CLUSTER;
         else if (units <= (q.res ? 512 : 1024) * maxs)
             v = RN_VARIANT_BLOCK;
         else if (f32 && !q.res && vec == 4 && cluster_shape(units, &ct, &cc, &cs))

@@ -114,6 +114,22 @@ def test_plan_by_width(lib, d, variant, tpr, slots):
     assert (p.variant, p.vec, p.threads_per_row, p.slots) == (variant, 4, tpr, slots)
 
 
+@pytest.mark.parametrize("d,op,variant,cl", [
+    (16384, capi.RN_OP_LN, capi.RN_VARIANT_BLOCK, 1),      # 512 threads
+    (16388, capi.RN_OP_LN, capi.RN_VARIANT_CLUSTER, 4),    # past 512 threads: cluster
+    (20000, capi.RN_OP_LN, capi.RN_VARIANT_CLUSTER, 4),
+    (32768, capi.RN_OP_LN, capi.RN_VARIANT_CLUSTER, 4),
+    (20000, capi.RN_OP_RMS, capi.RN_VARIANT_BLOCK, 1),     # RMSNorm: one CTA per row
+    (32768, capi.RN_OP_RMS, capi.RN_VARIANT_BLOCK, 1),
+])
+def test_aligned_layernorm_rows_past_512_threads_take_the_cluster(lib, d, op, variant, cl):
+    p = capi.plan(op, capi.RN_VARIANT_AUTO, d, A, A + 0x1000000, A + 0x2000000, A + 0x3000000)
+    assert (p.variant, p.cluster) == (variant, cl)
+    # rows whose accesses are not all aligned stay on one CTA per row
+    p = capi.plan(op, capi.RN_VARIANT_AUTO, d, A, A + 0x1000000, A + 0x2000004, 0)
+    assert p.variant == capi.RN_VARIANT_BLOCK
+
+
 @pytest.mark.parametrize("d,stages", [(1, 4), (3, 4), (4, 4), (8192, 4), (14464, 4),
                                       (14468, 3), (19264, 3), (19268, 2), (28928, 2),
                                       (28932, 1), (57856, 1)])
