@@ -584,18 +584,27 @@ const KernelEntry RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::entry 
 // The warp-per-row instances with their parameters in shared memory: every
 // slot count a row of up to 32 * 8 FP32 (32 * 4 16-bit) vectors needs, with
 // (NOPF false) or without prefetch.
+template <int OP, typename T, int VEC, int S, bool NOPF>
+const KernelEntry* reg_ps_entry() {
+    // with prefetch only the rows that would otherwise hold their parameters
+    // in registers take it
+    if constexpr (S <= 32 / VEC && (NOPF || reg_may_hold_params(VEC, S, 32)))
+        return &RegInst<OP, T, VEC, S, 32, false, true, false, NOPF, true>::entry;
+    else
+        return nullptr;
+}
+
 template <int OP, typename T, int VEC, bool NOPF = true>
 const KernelEntry* reg_pick_ps(int slots) {
-    constexpr int M = 32 / VEC;
     switch (slots) {
-        case 1: return &RegInst<OP, T, VEC, 1, 32, false, true, false, NOPF, true>::entry;
-        case 2: return &RegInst<OP, T, VEC, 2, 32, false, true, false, NOPF, true>::entry;
-        case 3: return &RegInst<OP, T, VEC, 3, 32, false, true, false, NOPF, true>::entry;
-        case 4: return &RegInst<OP, T, VEC, 4, 32, false, true, false, NOPF, true>::entry;
-        case 5: if constexpr (M >= 5) return &RegInst<OP, T, VEC, 5, 32, false, true, false, NOPF, true>::entry; else return nullptr;
-        case 6: if constexpr (M >= 6) return &RegInst<OP, T, VEC, 6, 32, false, true, false, NOPF, true>::entry; else return nullptr;
-        case 7: if constexpr (M >= 7) return &RegInst<OP, T, VEC, 7, 32, false, true, false, NOPF, true>::entry; else return nullptr;
-        case 8: if constexpr (M >= 8) return &RegInst<OP, T, VEC, 8, 32, false, true, false, NOPF, true>::entry; else return nullptr;
+        case 1: return reg_ps_entry<OP, T, VEC, 1, NOPF>();
+        case 2: return reg_ps_entry<OP, T, VEC, 2, NOPF>();
+        case 3: return reg_ps_entry<OP, T, VEC, 3, NOPF>();
+        case 4: return reg_ps_entry<OP, T, VEC, 4, NOPF>();
+        case 5: return reg_ps_entry<OP, T, VEC, 5, NOPF>();
+        case 6: return reg_ps_entry<OP, T, VEC, 6, NOPF>();
+        case 7: return reg_ps_entry<OP, T, VEC, 7, NOPF>();
+        case 8: return reg_ps_entry<OP, T, VEC, 8, NOPF>();
         default: return nullptr;
     }
 }

@@ -29,6 +29,7 @@ RN_DECL_FAMILY(ln)
 RN_DECL_FAMILY(rms)
 #undef RN_DECL_FAMILY
 const KernelEntry* reg_entry_ps_f32(int, int);
+const KernelEntry* reg_entry_pfps_f32(int, int);
 const KernelEntry* reg_entry_ps_bf16(int, int);
 const KernelEntry* reg_entry_ps_f16(int, int);
 const KernelEntry* reg_entry_ln_v4_al_nopf(int, int);
@@ -511,6 +512,25 @@ int run(const Request& q, int variant, void* stream) {
             if (want <= rp) {
                 e = ep;
                 resident = rp;
+            } else if (q.dtype == DT_F32 && q.op == OP_LN && pl.params_held && pl.slots >= 5) {
+                // more rows than one wave of it: FP32 LayerNorm rows of 5-6
+                // quads a lane, whose gamma and beta would take 40-48
+                // registers, prefetch with the parameters in shared memory
+                // instead (5 CTAs of 128 per SM at d = 768 rather than 3),
+                // for up to 8 waves of rows. Measured on GB300, A/B in two
+                // runs, back to back: 8192 x 768 10.11 -> 9.58 us, 5000 x
+                // 768 7.05 -> 6.86 us, 16384 x 768 17.64 -> 17.45 us; but
+                // 65536 x 768 63.9 -> 64.9 us, 12000 x 256 (2 quads)
+                // 5.98 -> 6.21 us, RMSNorm 8192 x 768 9.37 -> 9.52 us.
+                const KernelEntry* ef = reg_entry_pfps_f32(q.op, pl.slots);
+                if (ef) {
+                    const int rf = resident_ctas(ef, 0, &err);
+                    if (err != cudaSuccess) return fail_cuda(err);
+                    if (want <= 8 * (int64_t)rf) {
+                        e = ef;
+                        resident = rf;
+                    }
+                }
             }
         }
     }
