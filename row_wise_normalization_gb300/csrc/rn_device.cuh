@@ -29,7 +29,11 @@ namespace rn {
 // kernel took), and (2) touches no global memory before pdl_wait() returns,
 // which is when the kernel ahead has completed and its writes are visible.
 // Without a kernel ahead (first launch, a copy or an event before it) the
-// wait returns at once.
+// wait returns at once. That includes L2 prefetches: with one bulk L2
+// prefetch of each row issued before the wait, a chain of calls on GB300 in
+// which every call overwrote the buffer the previous call read, and read the
+// one it wrote, returned stale values for about 1 % of the elements.
+// Prefetches after the wait are safe.
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
