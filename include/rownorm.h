@@ -406,14 +406,16 @@ int rn_plan_for_residual(int op, int variant, int64_t d, const void *x, const vo
 /* Device error word of the current device: bit 0 (RN_DEVERR_STAGED_TIMEOUT)
  * is set if a staged kernel's (forward or backward) wait for a bulk copy ran
  * out, bit 1 (RN_DEVERR_CLUSTER_TIMEOUT) if a cluster kernel's wait for its
- * peer CTAs' partial statistics did (about one second each; the kernel then
- * stops early and its outputs are incomplete). The word is sticky until
+ * peer CTAs' partial statistics did, bit 2 (RN_DEVERR_PARAMS_TIMEOUT) if a
+ * register-held kernel's wait for the bulk copy of gamma/beta (w) into
+ * shared memory did (about one second each; the kernel then stops early,
+ * or, for bit 2, writes outputs that are not valid). The word is sticky until
  * cleared: `clear` != 0 resets it after reading. Synchronous (a
  * device-to-host copy). Returns RN_OK, RN_ERR_NULL or RN_ERR_CUDA. The
  * kernels find the word's device address once per CUDA context (a device
  * reset gives the device a new context and a new lookup); make one call of
  * each configuration before capturing calls into a CUDA graph. */
-enum { RN_DEVERR_STAGED_TIMEOUT = 1, RN_DEVERR_CLUSTER_TIMEOUT = 2 };
+enum { RN_DEVERR_STAGED_TIMEOUT = 1, RN_DEVERR_CLUSTER_TIMEOUT = 2, RN_DEVERR_PARAMS_TIMEOUT = 4 };
 int rn_device_error(unsigned int *flags, int clear);
 
 /* Self-test of the failure path above (library infrastructure; the paper has

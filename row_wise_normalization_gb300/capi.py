@@ -29,6 +29,7 @@ RN_ERR_SCRATCH = 9
 # device error word bits
 RN_DEVERR_STAGED_TIMEOUT = 1
 RN_DEVERR_CLUSTER_TIMEOUT = 2
+RN_DEVERR_PARAMS_TIMEOUT = 4
 
 # static scratch of ln_bwd_noalloc
 RN_NOALLOC_SCRATCH_BYTES = 8 << 20

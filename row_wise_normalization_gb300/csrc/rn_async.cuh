@@ -11,6 +11,7 @@ namespace rn {
 
 constexpr unsigned kErrStagedTimeout = 1u;
 constexpr unsigned kErrClusterTimeout = 2u;
+constexpr unsigned kErrParamsTimeout = 4u;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
 
 __device__ __forceinline__ unsigned long long global_ns() {

@@ -24,32 +24,11 @@
 
 namespace rn {
 
-// The parameters of one row's vectors and head/tail scalar.
-template <int OP, typename T, int VEC, int SLOTS>
-__device__ __forceinline__ void batched_params(Vec<VEC> (&a)[SLOTS],
-                                               Vec<VEC> (&b)[OP == OP_LN ? SLOTS : 1],
-                                               float& ae, float& be, const T* P0, const T* P1,
-                                               int h, int nv, bool has_e, int ei, bool aligned,
-                                               int lane) {
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-        const int q = lane + s * 32;
-        if (q < nv) {
-            ldt_p(a[s], P0 + h + q * VEC, aligned);
-            if constexpr (OP == OP_LN) ldt_p(b[s], P1 + h + q * VEC, aligned);
-        }
-    }
-    if (has_e) {
-        ae = ldt_p1(P0 + ei);
-        if constexpr (OP == OP_LN) be = ldt_p1(P1 + ei);
-    }
-}
-
 // One row, as the warp-per-row kernel computes it (the same operations in
 // the same order, so the results match a single call's bit for bit). AL: the
 // problem's arrays are 16-byte aligned and d is a multiple of the vector.
 template <int OP, typename T, int SLOTS, bool AL>
-__device__ __forceinline__ void batched_row_held(const HeldRow<Elem<T>::kVec, SLOTS, false>& cur,
+__device__ __forceinline__ void batched_row_held(HeldRow<Elem<T>::kVec, SLOTS, false>& cur,
                                                  T* yr, const T* P0, const T* P1, float* mean,
                                                  float* rstd, int64_t row, int d, float eps,
                                                  int lane) {
@@ -70,56 +49,15 @@ __device__ __forceinline__ void batched_row_held(const HeldRow<Elem<T>::kVec, SL
     Vec<VEC> pa0[SLOTS], pa1[OP == OP_LN ? SLOTS : 1];
     float pe0 = 0.f, pe1 = 0.f;
     if constexpr (EP)
-        batched_params<OP, T, VEC, SLOTS>(pa0, pa1, pe0, pe1, P0, P1, h, nv, has_e, ei, pa, lane);
+        load_row_params<OP, T, VEC, SLOTS, 32>(pa0, pa1, pe0, pe1, P0, P1, h, nv, has_e, ei, pa,
+                                               lane);
 
-    // FP32 LayerNorm rows work in the frame shifted by the row's first
-    // element K, as the warp-per-row kernel does
+    // the statistics as the warp-per-row kernel takes them (FP32 vector rows
+    // leave centred in place: (x - K) - mu_s)
     constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
+    constexpr bool PK = sizeof(T) == 4 && VEC == 4;
     float mu = 0.f, rs, K = 0.f, mu_s = 0.f;
-    if constexpr (OP == OP_LN) {
-        float sum;
-        if constexpr (SHIFT) {
-            const float first = (h > 0 || nv == 0) ? cur.e : cur.v[0].v[0];
-            K = __shfl_sync(0xffffffffu, first, 0);
-            sum = has_e ? cur.e - K : 0.f;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                if (lane + s * 32 < nv) {
-#pragma unroll
-                    for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k] - K;
-                }
-            }
-            mu_s = warp_sum(sum) / fd;
-            mu = K + mu_s;
-        } else {
-            sum = cur.e;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s)
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
-            mu = warp_sum(sum) / fd;
-        }
-        const float ce = SHIFT ? (cur.e - K) - mu_s : cur.e - mu;
-        float m2 = has_e ? ce * ce : 0.f;
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s) {
-            if (lane + s * 32 < nv) {
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) {
-                    const float c = SHIFT ? (cur.v[s].v[k] - K) - mu_s : cur.v[s].v[k] - mu;
-                    m2 = fmaf(c, c, m2);
-                }
-            }
-        }
-        rs = rsqrtf(warp_sum(m2) / fd + eps);
-    } else {
-        float ss = cur.e * cur.e;
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s)
-#pragma unroll
-            for (int k = 0; k < VEC; ++k) ss = fmaf(cur.v[s].v[k], cur.v[s].v[k], ss);
-        rs = rsqrtf(warp_sum(ss) / fd + eps);
-    }
+    warp_row_stats<OP, T, VEC, SLOTS, false>(cur, lane, has_e, fd, eps, K, mu_s, mu, rs);
 
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) {
@@ -134,7 +72,9 @@ __device__ __forceinline__ void batched_row_held(const HeldRow<Elem<T>::kVec, SL
                 ldt_p(a, P0 + j, pa);
                 if constexpr (OP == OP_LN) ldt_p(b, P1 + j, pa);
             }
-            if constexpr (OP == OP_LN) {
+            if constexpr (PK) {
+                o = out_pairs<OP, false>(cur.v[s], a, b, 0.f, rs);
+            } else if constexpr (OP == OP_LN) {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
                     o.v[k] = SHIFT ? fmaf(((cur.v[s].v[k] - K) - mu_s) * rs, a.v[k], b.v[k])

@@ -16,8 +16,15 @@ namespace rn {
 //
 // x is streamed: read exactly once, so it bypasses L1 (no_allocate) and asks
 // L2 to fetch whole 256-byte blocks. gamma/beta/w are re-read by every row, so
-// they go through the read-only path with L1 allocation. y is written once and
-// never re-read by the kernel, so it is stored with the streaming (.cs) hint.
+// they are cached in L1. y is written once and never re-read by the kernel, so
+// it is stored with the streaming (.cs) hint.
+// No load takes the non-coherent (.nc) path, which needs its data read-only
+// for the whole life of the kernel: under programmatic dependent launch
+// (below) a kernel's life starts while the kernel ahead of it may still be
+// writing what this one reads. With .nc loads of x, ping-pong chains of calls
+// on GB300 (each call reading the buffer the previous call wrote) read stale
+// values in about 0.4 % of 2400 chains of the warp-per-row LayerNorm; with
+// coherent loads, none in 8000.
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch. The forward kernels are launched with
 // programmatic stream serialization (launch_pdl in rn_params.h): the GPU may
@@ -47,7 +54,7 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
 
 __device__ __forceinline__ float4 ld_x4(const float* p) {
     float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(p));
     return v;
@@ -55,13 +62,13 @@ __device__ __forceinline__ float4 ld_x4(const float* p) {
 
 __device__ __forceinline__ float ld_x1(const float* p) {
     float v;
-    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    asm volatile("ld.global.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
     return v;
 }
 
 __device__ __forceinline__ float4 ld_p4(const float* p) {
     float4 v;
-    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.v4.f32 {%0,%1,%2,%3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(p));
     return v;
@@ -69,7 +76,7 @@ __device__ __forceinline__ float4 ld_p4(const float* p) {
 
 __device__ __forceinline__ float ld_p1(const float* p) {
     float v;
-    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
     return v;
 }
 
@@ -170,7 +177,7 @@ __device__ __forceinline__ uint16_t f_to_half(float f, __half*) {
 template <typename T>
 __device__ __forceinline__ void ld_x8(float* o, const T* p) {
     uint32_t a, b, c, d;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
                  : "l"(p));
     unpack2(a, o[0], o[1], (T*)nullptr);
@@ -181,7 +188,7 @@ __device__ __forceinline__ void ld_x8(float* o, const T* p) {
 template <typename T>
 __device__ __forceinline__ void ld_p8(float* o, const T* p) {
     uint32_t a, b, c, d;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
                  : "l"(p));
     unpack2(a, o[0], o[1], (T*)nullptr);
@@ -193,9 +200,9 @@ template <typename T>
 __device__ __forceinline__ float ld_h1(const T* p, bool stream) {
     uint16_t u;
     if (stream)
-        asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(u) : "l"(p));
+        asm volatile("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(u) : "l"(p));
     else
-        asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(u) : "l"(p));
+        asm volatile("ld.global.u16 %0, [%1];" : "=h"(u) : "l"(p));
     return half_to_f(u, (T*)nullptr);
 }
 template <typename T>
@@ -390,12 +397,12 @@ __device__ __forceinline__ int head_peel(const float* p, int64_t d) {
     return h > d ? (int)d : h;
 }
 
-// 16 raw bytes of a parameter vector (read-only path, L1 allocated), and a
+// 16 raw bytes of a parameter vector (L1 allocated), and a
 // 16-byte store to shared memory: the parameters staged per CTA.
 template <typename T>
 __device__ __forceinline__ uint4 ld_p_raw16(const T* p) {
     uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
@@ -423,6 +430,29 @@ __device__ __forceinline__ void lds_vec(Vec<VEC>& r, const T* p) {
         unpack2(u.z, r.v[4], r.v[5], (T*)nullptr);
         unpack2(u.w, r.v[6], r.v[7], (T*)nullptr);
     }
+}
+
+// One element of a staged parameter array as FP32.
+template <typename T>
+__device__ __forceinline__ float lds_f(const T* p) {
+    if constexpr (sizeof(T) == 4)
+        return *reinterpret_cast<const float*>(p);
+    else
+        return half_to_f(*reinterpret_cast<const uint16_t*>(p), (T*)nullptr);
+}
+
+// VEC consecutive staged parameters from p, which is 16-byte aligned when
+// `al` (one 128-bit load), else element by element.
+template <typename T, int VEC>
+__device__ __forceinline__ void lds_vec_at(Vec<VEC>& r, const T* p, bool al) {
+    if constexpr (VEC * sizeof(T) == 16) {
+        if (al) {
+            lds_vec<T, VEC>(r, p);
+            return;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) r.v[k] = lds_f(p + k);
 }
 
 }  // namespace rn

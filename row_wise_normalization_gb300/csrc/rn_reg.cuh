@@ -2,7 +2,7 @@
 //
 // Shape of the computation, for one row of width d:
 //   1. every thread issues all of its loads of the row up front: SLOTS
-//      vectors of VEC floats (128-bit ld.global.nc when VEC == 4), plus at
+//      vectors of VEC floats (128-bit loads when VEC == 4), plus at
 //      most one scalar of the unaligned head or tail; the row is read from
 //      HBM exactly once and stays in registers until it is written back
 //      (the single-pass, row-in-registers structure of "The load in flight,
@@ -18,6 +18,9 @@
 //      RMSNorm needs only the sum of squares;
 //   3. rstd = rsqrtf(var + eps) and the row is written from the registers
 //      with streaming 128-bit stores.
+// FP32 vector rows do their element-wise arithmetic on pairs of elements
+// with the packed .f32x2 instructions (shift_sum_pairs and the helpers
+// beside it), which halves the instructions a row takes.
 //
 // The grid is persistent (at most the resident CTA count); a row group walks
 // rows g, g + step, ... With PF the loads of the next row are issued before
@@ -34,7 +37,7 @@
 // threads 0..h+tl-1. Rows whose x and y differ in 16-byte phase use VEC = 1.
 #pragma once
 
-#include "rn_device.cuh"
+#include "rn_async.cuh"
 
 namespace rn {
 
@@ -207,6 +210,216 @@ __device__ __forceinline__ float held_m2_pairs(const HeldRow<VEC, SLOTS, RES>& r
     return x0 + x1;
 }
 
+// FP32 rows held as 128-bit vectors (PK: VEC 4, no residual) run the same
+// way, and apply the LayerNorm shift by the row's first element K to the
+// held vectors in place, once; with one warp per row the centring by the
+// row's shifted mean mu_s too. The output is then one packed multiply and
+// one packed fused multiply-add per pair: the same roundings, in the same
+// order, as the scalar ((x - K) - mu_s) * rs * gamma + beta, at half the
+// instructions.
+template <int VEC, int SLOTS, int TPR, bool RES>
+__device__ __forceinline__ float shift_sum_pairs(HeldRow<VEC, SLOTS, RES>& r, float K, int t,
+                                                 int nv) {
+    const F2 k2 = f2s(K);
+    F2 a = f2s(0.f);
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        if (t + s * TPR < nv) {
+#pragma unroll
+            for (int k = 0; k < VEC; k += 2) {
+                const F2 d = sub2(f2(r.v[s].v[k], r.v[s].v[k + 1]), k2);
+                f2_get(d, r.v[s].v[k], r.v[s].v[k + 1]);
+                a = add2(a, d);
+            }
+        }
+    }
+    float x0, x1;
+    f2_get(a, x0, x1);
+    return x0 + x1;
+}
+template <int VEC, int SLOTS, int TPR, bool RES>
+__device__ __forceinline__ float centre_m2_pairs(HeldRow<VEC, SLOTS, RES>& r, float c, int t,
+                                                 int nv) {
+    const F2 c2 = f2s(c);
+    F2 m = f2s(0.f);
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        if (t + s * TPR < nv) {
+#pragma unroll
+            for (int k = 0; k < VEC; k += 2) {
+                const F2 d = sub2(f2(r.v[s].v[k], r.v[s].v[k + 1]), c2);
+                f2_get(d, r.v[s].v[k], r.v[s].v[k + 1]);
+                m = fma2(d, d, m);
+            }
+        }
+    }
+    float x0, x1;
+    f2_get(m, x0, x1);
+    return x0 + x1;
+}
+template <int VEC, int SLOTS, bool RES>
+__device__ __forceinline__ float held_ss_pairs(const HeldRow<VEC, SLOTS, RES>& r) {
+    F2 a = f2s(0.f);
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+        for (int k = 0; k < VEC; k += 2) {   // unused slots hold 0
+            const F2 x = f2(r.v[s].v[k], r.v[s].v[k + 1]);
+            a = fma2(x, x, a);
+        }
+    float x0, x1;
+    f2_get(a, x0, x1);
+    return x0 + x1;
+}
+// One output vector from held FP32 values x: LayerNorm (x - m) * rs * a + b
+// (SUB) or x * rs * a + b, RMSNorm x * rs * a.
+template <int OP, bool SUB>
+__device__ __forceinline__ Vec<4> out_pairs(const Vec<4>& x, const Vec<4>& a, const Vec<4>& b,
+                                            float m, float rs) {
+    Vec<4> o;
+    const F2 r2 = f2s(rs), m2 = f2s(m);
+#pragma unroll
+    for (int k = 0; k < 4; k += 2) {
+        F2 c = f2(x.v[k], x.v[k + 1]);
+        if constexpr (SUB) c = sub2(c, m2);
+        if constexpr (OP == OP_LN)
+            f2_get(fma2(mul2(c, r2), f2(a.v[k], a.v[k + 1]), f2(b.v[k], b.v[k + 1])), o.v[k],
+                   o.v[k + 1]);
+        else
+            f2_get(mul2(mul2(c, r2), f2(a.v[k], a.v[k + 1])), o.v[k], o.v[k + 1]);
+    }
+    return o;
+}
+
+// The parameters (gamma/beta or w) of one held row's vectors and its
+// head/tail scalar, for thread t of a row group of TPR threads.
+template <int OP, typename T, int VEC, int SLOTS, int TPR>
+__device__ __forceinline__ void load_row_params(Vec<VEC> (&a)[SLOTS],
+                                                Vec<VEC> (&b)[OP == OP_LN ? SLOTS : 1],
+                                                float& ae, float& be, const T* P0, const T* P1,
+                                                int h, int nv, bool has_e, int ei, bool aligned,
+                                                int t) {
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+        const int q = t + s * TPR;
+        if (q < nv) {
+            ldt_p(a[s], P0 + h + q * VEC, aligned);
+            if constexpr (OP == OP_LN) ldt_p(b[s], P1 + h + q * VEC, aligned);
+        }
+    }
+    if (has_e) {
+        ae = ldt_p1(P0 + ei);
+        if constexpr (OP == OP_LN) be = ldt_p1(P1 + ei);
+    }
+}
+
+// Statistics of a row that one warp holds (lane t): the shift K, the shifted
+// mean mu_s, the mean and rs, as the warp-per-row and batched kernels both
+// take them, so that the two agree bit for bit. FP32 LayerNorm works in the
+// frame shifted by K (see reg_kernel); with PK its held vectors leave
+// centred in place, (x - K) - mu_s.
+template <int OP, typename T, int VEC, int SLOTS, bool RES>
+__device__ __forceinline__ void warp_row_stats(HeldRow<VEC, SLOTS, RES>& cur, int t, bool has_e,
+                                               float fd, float eps, float& K, float& mu_s,
+                                               float& mu, float& rs) {
+    constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
+    constexpr bool PK = sizeof(T) == 4 && VEC == 4 && !RES;
+    const int h = cur.h, nv = cur.nv;
+    if constexpr (OP == OP_LN) {
+        float sum;
+        if constexpr (SHIFT) {
+            // lane 0 holds the row's first element: its head scalar, else its
+            // first vector, else (no vectors) its tail scalar
+            const float first = (h > 0 || nv == 0) ? cur.e : cur.v[0].v[0];
+            K = __shfl_sync(0xffffffffu, first, 0);
+            sum = has_e ? cur.e - K : 0.f;
+            if constexpr (PK) {
+                sum += shift_sum_pairs<VEC, SLOTS, 32, RES>(cur, K, t, nv);
+            } else {
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s) {
+                    if (t + s * 32 < nv) {
+#pragma unroll
+                        for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k] - K;
+                    }
+                }
+            }
+        } else {
+            sum = cur.e;
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k];   // unused slots hold 0
+        }
+        mu_s = warp_sum(sum) / fd;
+        mu = SHIFT ? K + mu_s : mu_s;
+        // deviations in the shifted frame too: (x - K) - mu_s
+        const float ce = SHIFT ? (cur.e - K) - mu_s : cur.e - mu;
+        float m2 = has_e ? ce * ce : 0.f;
+        if constexpr (PK) {
+            m2 += centre_m2_pairs<VEC, SLOTS, 32, RES>(cur, mu_s, t, nv);
+        } else {
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+                if (t + s * 32 < nv) {
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) {
+                        const float c = SHIFT ? (cur.v[s].v[k] - K) - mu_s : cur.v[s].v[k] - mu;
+                        m2 = fmaf(c, c, m2);
+                    }
+                }
+            }
+        }
+        rs = rsqrtf(warp_sum(m2) / fd + eps);
+    } else {
+        float ss = cur.e * cur.e;
+        if constexpr (PK) {
+            ss += held_ss_pairs(cur);
+        } else {
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) ss = fmaf(cur.v[s].v[k], cur.v[s].v[k], ss);
+        }
+        rs = rsqrtf(warp_sum(ss) / fd + eps);
+    }
+}
+
+// Whether an instance loads each row's parameters together with the row
+// (EP), so that their latency overlaps the row's own loads: slices of at
+// most 8 floats without held or staged parameters.
+template <int OP, int VEC, int SLOTS, bool PP, bool PS>
+constexpr bool reg_early_params() {
+    return !PP && !PS && SLOTS * VEC <= 8;
+}
+
+// Bytes of shared memory an instance stages its parameters in (0: none).
+// PS instances always do; otherwise every instance that neither holds its
+// parameters in registers (PP) nor loads them with the row (EP), as long as
+// the copies of its resident CTAs take at most 128 KB of an SM. Those instances would otherwise load the parameters
+// from global memory after each row's reduction, where the dependent chain
+// waits for them. Measured on GB300: LayerNorm 2048 x 4096 13.2 -> 12.5 us
+// back to back (3 CTAs of 32 KB); but with 192 KB of an SM staged (LayerNorm
+// 256 x 8 vectors, 3 CTAs of 64 KB) 320 -> 386 us at 32768 x 8192, as the
+// L1 left beside it no longer held the loads in flight.
+// Elements per staged array: the held vectors' span plus room for an
+// unaligned row's head and tail scalars (at most 6), a whole number of
+// 16-byte units so that the second array stays aligned.
+template <int VEC, int SLOTS, int TPR>
+constexpr int reg_sp_elems() {
+    return SLOTS * TPR * VEC + 2 * VEC;
+}
+
+template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL,
+          bool RES, bool PS>
+constexpr int reg_sp_bytes() {
+    const int bytes = (OP == OP_LN ? 2 : 1) * reg_sp_elems<VEC, SLOTS, TPR>() * (int)sizeof(T);
+    if (PS) return bytes;
+    if (PP || reg_early_params<OP, VEC, SLOTS, PP, PS>()) return 0;
+    const int ctas = reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES, AL, PS);
+    return ctas * bytes <= 128 * 1024 ? bytes : 0;
+}
+
 template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL,
           bool RES, bool PS = false>
 __global__ void __launch_bounds__(TPR * RPC,
@@ -244,32 +457,69 @@ __global__ void __launch_bounds__(TPR * RPC,
     // mean). 16-bit storage carries 8-11 significant bits, far coarser.
     constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
     constexpr bool KLOAD = SHIFT && WPR > 1;
-    // (CTA-per-row rows only: warp-per-row rows keep the scalar order, which
-    // the batched kernel reproduces bit for bit)
+    // (16-bit pairs on CTA-per-row rows only: warp-per-row rows take their
+    // statistics from warp_row_stats, which the batched kernel shares)
     constexpr bool PAIRS = OP == OP_LN && sizeof(T) == 2 && VEC == 8 && WPR > 1;
+    // FP32 vector rows without a residual: packed pairs, the LayerNorm shift
+    // (and, for warp rows, the centring) applied to the held vectors in place
+    constexpr bool PK = sizeof(T) == 4 && VEC == 4 && !RES;
     const int64_t step = (int64_t)gridDim.x * RPC;
     int64_t row = (int64_t)blockIdx.x * RPC + g;
     pdl_launch_dependents();
     HeldRow<VEC, SLOTS, RES> cur;
-    // PS (parameters staged in shared memory): the CTA copies gamma/beta (w)
-    // into shared memory once, after issuing its rows' loads and while they
-    // are in flight, and every row reads them from there -- no registers held
+    // SP (parameters staged in shared memory, reg_sp_bytes): gamma/beta (w)
+    // are copied into dynamic shared memory once, while the rows' loads are
+    // in flight, and every row reads them from there -- no registers held
     // for them across rows, and no global load of them after a row's
-    // reduction. Groups without a row take part in the copy, then leave.
-    constexpr int NPS = OP == OP_LN ? 2 : 1;
-    __shared__ __align__(16) T sp[PS ? NPS : 1][PS ? SLOTS * TPR * VEC : 1];
-    if constexpr (PS) {
+    // reduction. Aligned rows (SPB): thread 0 has the bulk-copy engine make
+    // the copy, and the first row waits (bounded) for it before its output;
+    // thread 0's group always has a row (the grid is at most one CTA per row
+    // group), so the CTA outlives the copy. Other rows: every thread copies
+    // its share, then the CTA meets once, before any group leaves.
+    constexpr bool SP = reg_sp_bytes<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES, PS>() > 0;
+    constexpr bool SPB = SP && AL;
+    extern __shared__ __align__(16) unsigned char reg_dyn_smem[];
+    __shared__ __align__(8) unsigned long long sp_bar;
+    T* const sp0 = reinterpret_cast<T*>(reg_dyn_smem);
+    T* const sp1 = sp0 + reg_sp_elems<VEC, SLOTS, TPR>();
+    if constexpr (SP && !SPB) {
         pdl_wait();                                  // no global access before this
         const bool active = row < p.rows;
         if (active)
-            load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx, nullptr, d, t);
-        const int nvp = d / VEC;
-        for (int q = threadIdx.x; q < nvp; q += TPR * RPC) {
-            st_shared_v4(&sp[0][q * VEC], ld_p_raw16(P0 + q * VEC));
-            if constexpr (OP == OP_LN) st_shared_v4(&sp[1][q * VEC], ld_p_raw16(P1 + q * VEC));
+            load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
+                                                         RES ? R + row * p.ldr : nullptr, d, t);
+        constexpr int E16 = 16 / (int)sizeof(T);     // elements in 16 bytes
+        int body = 0;
+        if (aligned16(P0, 0) && (OP != OP_LN || aligned16(P1, 0))) {
+            body = d - d % E16;
+            for (int q = threadIdx.x; q < body / E16; q += TPR * RPC) {
+                st_shared_v4(sp0 + q * E16, ld_p_raw16(P0 + q * E16));
+                if constexpr (OP == OP_LN) st_shared_v4(sp1 + q * E16, ld_p_raw16(P1 + q * E16));
+            }
+        }
+        for (int j = body + threadIdx.x; j < d; j += TPR * RPC) {
+            sp0[j] = P0[j];
+            if constexpr (OP == OP_LN) sp1[j] = P1[j];
         }
         __syncthreads();
         if (!active) return;                         // the whole group leaves together
+    } else if constexpr (SPB) {
+        if (threadIdx.x == 0) {
+            mbar_init(smem_addr(&sp_bar), 1);
+            mbar_fence_init();
+        }
+        __syncthreads();
+        pdl_wait();                                  // no global access before this
+        if (row >= p.rows) return;                   // the whole group leaves together
+        load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
+                                                     RES ? R + row * p.ldr : nullptr, d, t);
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = (uint32_t)d * (uint32_t)sizeof(T);   // aligned: 16 | bytes
+            const uint32_t bar = smem_addr(&sp_bar);
+            mbar_arrive_expect_tx(bar, (OP == OP_LN ? 2u : 1u) * bytes);
+            bulk_g2s(smem_addr(sp0), P0, bytes, bar);
+            if constexpr (OP == OP_LN) bulk_g2s(smem_addr(sp1), P1, bytes, bar);
+        }
     } else {
         if (row >= p.rows) return;                   // the whole group leaves together
         pdl_wait();                                  // no global access before this
@@ -334,48 +584,37 @@ __global__ void __launch_bounds__(TPR * RPC,
         // parameters load this row's gamma/beta (w) now, so that the loads
         // overlap the reduction instead of following it -- on the short,
         // launch-bound rows the dependent chain is the whole kernel
-        constexpr bool EP = !PP && !PS && SLOTS * VEC <= 8;
-        Vec<VEC> ea[EP ? SLOTS : 1], eb[(EP && OP == OP_LN) ? SLOTS : 1];
+        constexpr bool EP = reg_early_params<OP, VEC, SLOTS, PP, PS>();
+        constexpr int NPA = EP ? SLOTS : 1;
+        Vec<VEC> ea[NPA], eb[OP == OP_LN ? NPA : 1];
         float eae = 0.f, ebe = 0.f;
-        if constexpr (EP) {
-            bool epa = true;
-            if constexpr (VEC > 1 && !AL) {
-                epa = aligned16(P0, h);
-                if constexpr (OP == OP_LN) epa = epa && aligned16(P1, h);
-            }
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s) {
-                const int q = t + s * TPR;
-                if (q < nv) {
-                    ldt_p(ea[s], P0 + h + q * VEC, epa);
-                    if constexpr (OP == OP_LN) ldt_p(eb[s], P1 + h + q * VEC, epa);
-                }
-            }
-            if (has_e) {
-                eae = ldt_p1(P0 + ei);
-                if constexpr (OP == OP_LN) ebe = ldt_p1(P1 + ei);
-            }
+        bool pa = true;   // parameter vectors 16-byte aligned at this row's phase
+        if constexpr (VEC > 1 && !PP && !AL) {
+            pa = aligned16(P0, h);
+            if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
         }
+        if constexpr (EP)
+            load_row_params<OP, T, VEC, NPA, TPR>(ea, eb, eae, ebe, P0, P1, h, nv, has_e, ei, pa,
+                                                  t);
 
         // ---- statistics ------------------------------------------------
         float mu = 0.f, rs, K = 0.f, mu_s = 0.f;   // mu_s = mu - K (SHIFT)
-        if constexpr (OP == OP_LN) {
+        if constexpr (WPR == 1) {
+            warp_row_stats<OP, T, VEC, SLOTS, RES>(cur, t, has_e, fd, p.eps, K, mu_s, mu, rs);
+        } else if constexpr (OP == OP_LN) {
             float sum;
             if constexpr (SHIFT) {
-                if constexpr (WPR == 1) {
-                    // lane 0 holds the row's first element: its head scalar,
-                    // else its first vector, else (no vectors) its tail scalar
-                    const float first = (h > 0 || nv == 0) ? cur.e : cur.v[0].v[0];
-                    K = __shfl_sync(0xffffffffu, first, 0);
-                } else {
-                    K = cur.k;
-                }
+                K = cur.k;
                 sum = has_e ? cur.e - K : 0.f;
+                if constexpr (PK) {
+                    sum += shift_sum_pairs<VEC, SLOTS, TPR, RES>(cur, K, t, nv);   // x -> x - K
+                } else {
 #pragma unroll
-                for (int s = 0; s < SLOTS; ++s) {
-                    if (t + s * TPR < nv) {
+                    for (int s = 0; s < SLOTS; ++s) {
+                        if (t + s * TPR < nv) {
 #pragma unroll
-                        for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k] - K;
+                            for (int k = 0; k < VEC; ++k) sum += cur.v[s].v[k] - K;
+                        }
                     }
                 }
             } else {
@@ -390,29 +629,7 @@ __global__ void __launch_bounds__(TPR * RPC,
                 }
             }
 
-            if constexpr (WPR == 1) {
-                mu_s = warp_sum(sum) / fd;
-                mu = SHIFT ? K + mu_s : mu_s;
-                // deviations in the shifted frame too: (x - K) - mu_s
-                const float ce = SHIFT ? (cur.e - K) - mu_s : cur.e - mu;
-                float m2 = has_e ? ce * ce : 0.f;
-                if constexpr (PAIRS) {
-                    m2 += held_m2_pairs<VEC, SLOTS, TPR, RES>(cur, mu, t, nv);
-                } else {
-#pragma unroll
-                    for (int s = 0; s < SLOTS; ++s) {
-                        if (t + s * TPR < nv) {
-#pragma unroll
-                            for (int k = 0; k < VEC; ++k) {
-                                const float c =
-                                    SHIFT ? (cur.v[s].v[k] - K) - mu_s : cur.v[s].v[k] - mu;
-                                m2 = fmaf(c, c, m2);
-                            }
-                        }
-                    }
-                }
-                rs = rsqrtf(warp_sum(m2) / fd + p.eps);
-            } else {
+            {
                 const float wsum = warp_sum(sum);
                 int nw = (w == 0) ? (h + tl) : 0;          // elements this warp holds
 #pragma unroll
@@ -424,7 +641,7 @@ __global__ void __launch_bounds__(TPR * RPC,
                 // deviations from the warp mean, taken in the shifted frame
                 const float ce = SHIFT ? (cur.e - K) - wmean_s : cur.e - wmean_s;
                 float m2 = has_e ? ce * ce : 0.f;
-                if constexpr (PAIRS) {
+                if constexpr (PAIRS || PK) {   // PK: the held vectors are x - K
                     m2 += held_m2_pairs<VEC, SLOTS, TPR, RES>(cur, wmean_s, t, nv);
                 } else {
 #pragma unroll
@@ -452,30 +669,29 @@ __global__ void __launch_bounds__(TPR * RPC,
             }
         } else {
             float ss = cur.e * cur.e;
-#pragma unroll
-            for (int s = 0; s < SLOTS; ++s)
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) ss = fmaf(cur.v[s].v[k], cur.v[s].v[k], ss);
-            if constexpr (WPR == 1) {
-                ss = warp_sum(ss);
+            if constexpr (PK) {
+                ss += held_ss_pairs(cur);
             } else {
-                const float wss = warp_sum(ss);
-                float(*slot)[NST] = xch[it & (NBUF - 1)][g];
-                if (lane == 0) slot[w][0] = wss;
-                named_sync(1 + g, TPR);
-                ss = merge_sum_warps<WPR, NST>(slot, lane);
+#pragma unroll
+                for (int s = 0; s < SLOTS; ++s)
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) ss = fmaf(cur.v[s].v[k], cur.v[s].v[k], ss);
             }
+            const float wss = warp_sum(ss);
+            float(*slot)[NST] = xch[it & (NBUF - 1)][g];
+            if (lane == 0) slot[w][0] = wss;
+            named_sync(1 + g, TPR);
+            ss = merge_sum_warps<WPR, NST>(slot, lane);
             rs = rsqrtf(ss / fd + p.eps);
         }
 
         // ---- normalize and store from the held registers ----------------
+        if constexpr (SPB) {
+            if (it == 0 && !mbar_wait_bounded(smem_addr(&sp_bar), 0) && p.err)
+                atomicOr(p.err, kErrParamsTimeout);   // the outputs are then not valid
+        }
         T* yr = Y + row * p.ldy;
         T* hr = RES && p.h ? H + row * p.ldh : nullptr;
-        bool pa = true;   // parameter vectors 16-byte aligned at this row's phase
-        if constexpr (VEC > 1 && !PP && !EP && !AL) {
-            pa = aligned16(P0, h);
-            if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
-        }
 #pragma unroll
         for (int s = 0; s < SLOTS; ++s) {
             const int q = t + s * TPR;
@@ -485,9 +701,12 @@ __global__ void __launch_bounds__(TPR * RPC,
                 if constexpr (PP) {
                     a = pg[s];
                     if constexpr (OP == OP_LN) b = pb[s];
-                } else if constexpr (PS) {
-                    lds_vec<T, VEC>(a, &sp[0][j]);
-                    if constexpr (OP == OP_LN) lds_vec<T, VEC>(b, &sp[1][j]);
+                } else if constexpr (SP) {
+                    // 16-byte aligned in shared memory when the row's head
+                    // peel is whole vectors (always, for aligned rows)
+                    const bool sa = AL || h % VEC == 0;
+                    lds_vec_at<T, VEC>(a, sp0 + j, sa);
+                    if constexpr (OP == OP_LN) lds_vec_at<T, VEC>(b, sp1 + j, sa);
                 } else if constexpr (EP) {
                     a = ea[s];
                     if constexpr (OP == OP_LN) b = eb[s];
@@ -495,7 +714,10 @@ __global__ void __launch_bounds__(TPR * RPC,
                     ldt_p(a, P0 + j, pa);
                     if constexpr (OP == OP_LN) ldt_p(b, P1 + j, pa);
                 }
-                if constexpr (PAIRS) {
+                if constexpr (PK) {
+                    // warp rows hold (x - K) - mu_s, CTA rows x - K (LayerNorm)
+                    o = out_pairs<OP, (OP == OP_LN && WPR > 1)>(cur.v[s], a, b, mu_s, rs);
+                } else if constexpr (PAIRS) {
 #pragma unroll
                     for (int k = 0; k < VEC; k += 2) {
                         const F2 xo = mul2(sub2(f2(cur.v[s].v[k], cur.v[s].v[k + 1]), f2s(mu)),
@@ -520,11 +742,12 @@ __global__ void __launch_bounds__(TPR * RPC,
         }
         if (RES && has_e && hr) stt_y1(hr + ei, cur.e);
         if (has_e) {
-            const float a = PP ? pge : (EP ? eae : ldt_p1(P0 + ei));
+            const float a =
+                PP ? pge : (EP ? eae : (SP ? lds_f(sp0 + ei) : ldt_p1(P0 + ei)));
             float o;
             if constexpr (OP == OP_LN)
                 o = fmaf((SHIFT ? (cur.e - K) - mu_s : cur.e - mu) * rs, a,
-                         PP ? pbe : (EP ? ebe : ldt_p1(P1 + ei)));
+                         PP ? pbe : (EP ? ebe : (SP ? lds_f(sp1 + ei) : ldt_p1(P1 + ei))));
             else
                 o = cur.e * rs * a;
             stt_y1(yr + ei, o);
@@ -557,15 +780,22 @@ __global__ void __launch_bounds__(TPR * RPC,
 // NOPF: the same configuration compiled without prefetch at the no-prefetch
 // occupancy, for calls whose rows all fit in one wave of it (nothing to
 // overlap a prefetch with); only where the default instance prefetches.
-// PS: parameters staged in shared memory (warp-per-row, aligned, no prefetch).
+// PS: the one-wave warp-per-row instances with the parameters staged in
+// shared memory (reg_sp_bytes stages them in others too).
 template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES,
           bool NOPF = false, bool PS = false>
 struct RegInst {
     static constexpr int RPC = (TPR == 32) ? kWarpRowsPerCta : 1;
     static constexpr bool PF = NOPF ? false : reg_prefetch(VEC, SLOTS, TPR, RES);
+    static constexpr int SMEM = reg_sp_bytes<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES, PS>();
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {
         return launch_pdl(reg_kernel<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES, PS>,
-                          (unsigned)grid, TPR * RPC, 0, s, p);
+                          (unsigned)grid, TPR * RPC, SMEM, s, p);
+    }
+    // the limit is per function and process-wide; raising it again is harmless
+    static cudaError_t prepare(int) {
+        return cudaFuncSetAttribute(reg_kernel<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES, PS>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     }
     static const KernelEntry entry;
 };
@@ -578,8 +808,14 @@ const KernelEntry RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::entry 
                              RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::PF, PP, AL,
                              RES, PS>,
     TPR * RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::RPC,
-    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::RPC, 0,
-    &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::launch, nullptr};
+    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::RPC,
+    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::SMEM,
+    &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::launch,
+    // (any dynamic shared memory raises the limit: the default 48 KB counts
+    // the static shared memory too)
+    RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::SMEM > 0
+        ? &RegInst<OP, T, VEC, SLOTS, TPR, PP, AL, RES, NOPF, PS>::prepare
+        : nullptr};
 
 // The warp-per-row instances with their parameters in shared memory: every
 // slot count a row of up to 32 * 8 FP32 (32 * 4 16-bit) vectors needs, with

@@ -349,6 +349,7 @@ unsigned long long ctx_now() {
 // current device at once (0 on error). Raises the kernel's dynamic shared
 // memory limit first when it needs more than the default.
 int resident_ctas(const KernelEntry* e, int smem, cudaError_t* err) {
+    if (smem == 0) smem = e->smem_bytes;   // instances that stage their parameters
     struct Cache {
         const void* fn;
         unsigned long long ctx;
@@ -442,6 +443,12 @@ int run(const Request& q, int variant, void* stream) {
     prm.ldh = q.d;
     prm.eps = q.eps;
     const cudaStream_t s = (cudaStream_t)stream;
+    // where the kernels' bounded waits (cluster exchange, staged parameters)
+    // report a timeout
+    {
+        const cudaError_t e0 = device_error_address(&prm.err);
+        if (e0 != cudaSuccess) return fail_cuda(e0);
+    }
 
     if (pl.variant == RN_VARIANT_CLUSTER) {
         const ClusterEntry* ce =

@@ -11,7 +11,12 @@ global access. These tests give that wait something to protect:
 * a ping-pong chain in which every call also overwrites the buffer the call
   before it read (a write-after-read across launches), checked at the end
   against the oracle chain;
-* both chains captured once into a CUDA graph and replayed on new inputs.
+* both chains captured once into a CUDA graph and replayed on new inputs;
+* ping-pong chains (FP32, 16-bit, with a residual) run back to back hundreds
+  of times, directly and from a CUDA graph, each result compared bit for bit
+  with the same chain run with a device synchronisation after every call
+  (the kernels are deterministic, so any difference is a read that the
+  dependency wait did not order).
 
 Every output buffer starts as sentinel values, so a call that read its input
 before the previous call had written it would see sentinels, not data.
@@ -184,3 +189,143 @@ def test_batched_calls_chained():
             yr, _, _ = _oracle_step(k, x, gh, bh)
             parity.check_y(y, yr, what=f"problem {i} step {k}")
             x = y
+
+
+# ---------------------------------------------------------------------------
+# back to back against synchronised, bit for bit
+# ---------------------------------------------------------------------------
+RACE_STEPS = 8
+RACE_DIRECT = 200    # chains enqueued behind a device sleep, so they run back to back
+RACE_GRAPH = 600     # replays of one captured chain
+
+
+def _race(torch, reset, chain, outs):
+    """Runs reset + chain with a sync after every call (twice: the kernels
+    must be deterministic), then back to back RACE_DIRECT times and from a
+    CUDA graph RACE_GRAPH times; returns how many of those results differ
+    from the synchronised one in any bit of any tensor of ``outs``."""
+    reset()
+    chain(True)
+    ref = [o.clone() for o in outs]
+    reset()
+    chain(True)
+    assert all(torch.equal(o, r) for o, r in zip(outs, ref)), \
+        "the synchronised chain is not deterministic"
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+
+    def count():
+        diff = torch.zeros((), dtype=torch.bool, device="cuda")
+        for o, r in zip(outs, ref):
+            diff |= (o != r).any()
+        bad.add_(diff.to(torch.int64))
+
+    for _ in range(RACE_DIRECT):
+        torch.cuda._sleep(2_000_000)   # the host enqueues the chain meanwhile
+        reset()
+        chain(False)
+        count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        reset()
+        chain(False)
+    for _ in range(RACE_GRAPH):
+        graph.replay()
+        count()
+    torch.cuda.synchronize()
+    return int(bad.item())
+
+
+def _race_buffers(torch, rows, d, dtype, seed):
+    x0 = workloads.Workload("ln", rows, d, seed=seed, x_dist="offset", x_std=2.0).x()
+    gh, bh = _params(d, seed=seed + 1)
+    t = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    x0 = torch.from_numpy(x0.reshape(-1)).to("cuda", t)
+    g = torch.from_numpy(gh).to("cuda", t)
+    b = torch.from_numpy(bh).to("cuda", t)
+    mean = torch.empty(rows, dtype=torch.float32, device="cuda")
+    rstd = torch.empty_like(mean)
+    return x0, g, b, mean, rstd
+
+
+@pytest.mark.parametrize("dtype,variant,rows,d", [
+    ("f32", v, r, d) for (v, r, d) in CASES[:7]] + [
+    ("f32", capi.RN_VARIANT_AUTO, 4096, 768),
+    ("f32", capi.RN_VARIANT_AUTO, 8192, 768),
+    ("f32", capi.RN_VARIANT_AUTO, 2048, 4096),
+    ("bf16", capi.RN_VARIANT_AUTO, 4096, 768),
+    ("bf16", capi.RN_VARIANT_AUTO, 1024, 4096),
+    ("f16", capi.RN_VARIANT_AUTO, 2048, 2048),
+    ("bf16", capi.RN_VARIANT_AUTO, 32, 40000),
+])
+def test_back_to_back_chains_match_synchronised_ones(dtype, variant, rows, d):
+    """A <- op(B) <- op(A) ..., LayerNorm and RMSNorm alternating: every call
+    reads what the call before it wrote and overwrites what it read."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn  # noqa: F401  (loads the library)
+
+    code = {"f32": capi.RN_DTYPE_F32, "bf16": capi.RN_DTYPE_BF16, "f16": capi.RN_DTYPE_F16}[dtype]
+    x0, g, b, mean, rstd = _race_buffers(torch, rows, d, dtype, seed=941)
+    bufs = (torch.empty_like(x0), torch.empty_like(x0))
+
+    def reset():
+        bufs[0].copy_(x0)
+        bufs[1].fill_(float("nan"))
+
+    def chain(sync):
+        s = torch.cuda.current_stream().cuda_stream
+        for k in range(RACE_STEPS):
+            src, dst = bufs[k % 2], bufs[(k + 1) % 2]
+            if k % 2 == 0:
+                st = capi.ln_fwd_typed(code, variant, src.data_ptr(), g.data_ptr(), b.data_ptr(),
+                                       dst.data_ptr(), mean.data_ptr(), rstd.data_ptr(), rows, d,
+                                       EPS, s)
+            else:
+                st = capi.rms_fwd_typed(code, variant, src.data_ptr(), g.data_ptr(),
+                                        dst.data_ptr(), rows, d, EPS, s)
+            capi.check(st)
+            if sync:
+                torch.cuda.synchronize()
+
+    assert _race(torch, reset, chain, (bufs[RACE_STEPS % 2],)) == 0
+
+
+@pytest.mark.parametrize("variant,rows,d", [
+    (capi.RN_VARIANT_AUTO, 4096, 768),
+    (capi.RN_VARIANT_BLOCK, 1024, 4096),
+    (capi.RN_VARIANT_AUTO, 64, 20000),
+])
+def test_back_to_back_residual_chains_match_synchronised_ones(variant, rows, d):
+    """Residual calls: each reads the previous call's y as x and its h as the
+    residual, and writes h and y over the two buffers the previous call read."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn  # noqa: F401
+
+    x0, g, b, mean, rstd = _race_buffers(torch, rows, d, "f32", seed=951)
+    r0 = torch.flip(x0, (0,)).contiguous()
+    pair = ((torch.empty_like(x0), torch.empty_like(x0)),
+            (torch.empty_like(x0), torch.empty_like(x0)))   # (x or y, residual or h)
+
+    def reset():
+        pair[0][0].copy_(x0)
+        pair[0][1].copy_(r0)
+        pair[1][0].fill_(float("nan"))
+        pair[1][1].fill_(float("nan"))
+
+    def chain(sync):
+        s = torch.cuda.current_stream().cuda_stream
+        for k in range(RACE_STEPS):
+            (xi, ri), (yo, ho) = pair[k % 2], pair[(k + 1) % 2]
+            if k % 2 == 0:
+                st = capi.ln_fwd_residual_variant(variant, xi.data_ptr(), ri.data_ptr(),
+                                                  g.data_ptr(), b.data_ptr(), ho.data_ptr(),
+                                                  yo.data_ptr(), mean.data_ptr(),
+                                                  rstd.data_ptr(), rows, d, EPS, s)
+            else:
+                st = capi.rms_fwd_residual_variant(variant, xi.data_ptr(), ri.data_ptr(),
+                                                   g.data_ptr(), ho.data_ptr(), yo.data_ptr(),
+                                                   rows, d, EPS, s)
+            capi.check(st)
+            if sync:
+                torch.cuda.synchronize()
+
+    assert _race(torch, reset, chain, pair[RACE_STEPS % 2]) == 0
