@@ -67,7 +67,10 @@ constexpr int reg_min_ctas(int threads, int op, int vec, int slots, bool pf, boo
         // as the held row (two with prefetch) and a fixed allowance let fit,
         // so that without prefetch every row of a call up to that size is in
         // flight at once (LayerNorm FP32 d = 768: 72 registers, 7 CTAs of 128)
-        const int per = ((48 + slots * vec * (pf ? 2 : 1) + 7) / 8) * 8;
+        // (FP32 rows of 8 vectors a lane need 8 more: at 80 registers they
+        // spilled 4 bytes)
+        const int per = ((48 + slots * vec * (pf ? 2 : 1) + (vec == 4 && slots == 8 ? 8 : 0) + 7) /
+                         8) * 8;
         const int n = 65536 / (per * threads);
         return n < 1 ? 1 : (n > 16 ? 16 : n);
     }
