@@ -277,6 +277,16 @@ class SymbolAddressCache {
 // Compiled configuration space of the register-held kernels.
 constexpr int kMaxSlots = 8;
 constexpr int kWarpRowsPerCta = 4;  // rows (warps) per CTA in the warp variant
+
+// Row groups per CTA of the register-held kernels: 4 warp rows, and 3 rows
+// of 256 threads for aligned FP32 LayerNorm rows of 8 vectors a thread
+// (d 7169-8192). Those run one 768-thread CTA per SM instead of three of
+// 256, so that the SM stages gamma and beta in shared memory once (64 KB)
+// rather than three times. Everything else: one row per CTA.
+constexpr int reg_rows_per_cta(int op, int vec, int slots, int tpr, bool res, bool al) {
+    return tpr == 32 ? kWarpRowsPerCta
+                     : ((op == 0 && vec == 4 && slots == 8 && tpr == 256 && !res && al) ? 3 : 1);
+}
 constexpr int kStreamThreads = 512;
 constexpr int kStagedThreads = 512;
 constexpr int kMaxStages = 4;

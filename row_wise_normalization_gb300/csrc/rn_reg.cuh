@@ -788,7 +788,7 @@ __global__ void __launch_bounds__(TPR * RPC,
 template <int OP, typename T, int VEC, int SLOTS, int TPR, bool PP, bool AL, bool RES,
           bool NOPF = false, bool PS = false>
 struct RegInst {
-    static constexpr int RPC = (TPR == 32) ? kWarpRowsPerCta : 1;
+    static constexpr int RPC = reg_rows_per_cta(OP, VEC, SLOTS, TPR, RES, AL);
     static constexpr bool PF = NOPF ? false : reg_prefetch(VEC, SLOTS, TPR, RES);
     static constexpr int SMEM = reg_sp_bytes<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES, PS>();
     static cudaError_t launch(const Params& p, int grid, cudaStream_t s) {

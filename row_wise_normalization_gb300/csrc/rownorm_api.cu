@@ -252,8 +252,8 @@ int plan_impl(const Request& q, int variant, rn_plan* pl) {
             if (q.res && tpr == 1024) return RN_ERR_VARIANT;
             pl->slots = slots;
             pl->threads_per_row = tpr;
-            pl->rows_per_cta = 1;
-            pl->threads_per_cta = tpr;
+            pl->rows_per_cta = reg_rows_per_cta(q.op, vec, slots, tpr, q.res, al);
+            pl->threads_per_cta = tpr * pl->rows_per_cta;
             pl->prefetch = reg_prefetch(vec, slots, tpr, q.res);
             pl->aligned = al;
             pl->params_held = al && reg_may_hold_params(vec, slots, tpr);
