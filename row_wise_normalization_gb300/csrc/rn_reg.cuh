@@ -474,54 +474,62 @@ __global__ void __launch_bounds__(TPR * RPC,
     // are copied into dynamic shared memory once, while the rows' loads are
     // in flight, and every row reads them from there -- no registers held
     // for them across rows, and no global load of them after a row's
-    // reduction. Aligned rows (SPB): thread 0 has the bulk-copy engine make
-    // the copy, and the first row waits (bounded) for it before its output;
-    // thread 0's group always has a row (the grid is at most one CTA per row
-    // group), so the CTA outlives the copy. Other rows: every thread copies
-    // its share, then the CTA meets once, before any group leaves.
+    // reduction. Where the arrays are 16-byte aligned (always for aligned
+    // rows, SPB), thread 0 has the bulk-copy engine make the copy and the
+    // first row waits (bounded) for it before its output; thread 0's group
+    // always has a row (the grid is at most one CTA per row group), so the
+    // CTA outlives the copy. Otherwise every thread copies its share, then
+    // the CTA meets once, before any group leaves.
     constexpr bool SP = reg_sp_bytes<OP, T, VEC, SLOTS, TPR, RPC, PF, PP, AL, RES, PS>() > 0;
     constexpr bool SPB = SP && AL;
     extern __shared__ __align__(16) unsigned char reg_dyn_smem[];
     __shared__ __align__(8) unsigned long long sp_bar;
     T* const sp0 = reinterpret_cast<T*>(reg_dyn_smem);
     T* const sp1 = sp0 + reg_sp_elems<VEC, SLOTS, TPR>();
-    if constexpr (SP && !SPB) {
-        pdl_wait();                                  // no global access before this
-        const bool active = row < p.rows;
-        if (active)
-            load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
-                                                         RES ? R + row * p.ldr : nullptr, d, t);
-        constexpr int E16 = 16 / (int)sizeof(T);     // elements in 16 bytes
-        int body = 0;
-        if (aligned16(P0, 0) && (OP != OP_LN || aligned16(P1, 0))) {
-            body = d - d % E16;
-            for (int q = threadIdx.x; q < body / E16; q += TPR * RPC) {
-                st_shared_v4(sp0 + q * E16, ld_p_raw16(P0 + q * E16));
-                if constexpr (OP == OP_LN) st_shared_v4(sp1 + q * E16, ld_p_raw16(P1 + q * E16));
-            }
-        }
-        for (int j = body + threadIdx.x; j < d; j += TPR * RPC) {
-            sp0[j] = P0[j];
-            if constexpr (OP == OP_LN) sp1[j] = P1[j];
-        }
-        __syncthreads();
-        if (!active) return;                         // the whole group leaves together
-    } else if constexpr (SPB) {
+    // bulk: the copy is made by the bulk-copy engine (arrays 16-byte aligned;
+    // always for aligned rows); else by the threads behind one barrier
+    bool bulk = true;
+    if constexpr (SP) {
         if (threadIdx.x == 0) {
             mbar_init(smem_addr(&sp_bar), 1);
             mbar_fence_init();
         }
         __syncthreads();
         pdl_wait();                                  // no global access before this
-        if (row >= p.rows) return;                   // the whole group leaves together
-        load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
-                                                     RES ? R + row * p.ldr : nullptr, d, t);
-        if (threadIdx.x == 0) {
-            const uint32_t bytes = (uint32_t)d * (uint32_t)sizeof(T);   // aligned: 16 | bytes
-            const uint32_t bar = smem_addr(&sp_bar);
-            mbar_arrive_expect_tx(bar, (OP == OP_LN ? 2u : 1u) * bytes);
-            bulk_g2s(smem_addr(sp0), P0, bytes, bar);
-            if constexpr (OP == OP_LN) bulk_g2s(smem_addr(sp1), P1, bytes, bar);
+        constexpr int E16 = 16 / (int)sizeof(T);     // elements in 16 bytes
+        if constexpr (!SPB) bulk = aligned16(P0, 0) && (OP != OP_LN || aligned16(P1, 0));
+        const bool active = row < p.rows;
+        if (!bulk) {
+            // the same decision in every thread of the CTA: copy, meet once
+            if (active)
+                load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(
+                    cur, X + row * p.ldx, RES ? R + row * p.ldr : nullptr, d, t);
+            for (int j = threadIdx.x; j < d; j += TPR * RPC) {
+                sp0[j] = P0[j];
+                if constexpr (OP == OP_LN) sp1[j] = P1[j];
+            }
+            __syncthreads();
+            if (!active) return;                     // the whole group leaves together
+        } else {
+            if (!active) return;                     // the whole group leaves together
+            load_row<T, VEC, SLOTS, TPR, AL, RES, KLOAD>(cur, X + row * p.ldx,
+                                                         RES ? R + row * p.ldr : nullptr, d, t);
+            if (threadIdx.x == 0) {
+                // an unaligned row's last d % E16 elements: written by this
+                // thread before its arrive, which releases them to the waiters
+                const int body = AL ? d : d - d % E16;
+                for (int j = body; j < d; ++j) {
+                    sp0[j] = P0[j];
+                    if constexpr (OP == OP_LN) sp1[j] = P1[j];
+                }
+                const uint32_t bytes = (uint32_t)body * (uint32_t)sizeof(T);   // 16 | bytes
+                const uint32_t bar = smem_addr(&sp_bar);
+                mbar_arrive_expect_tx(bar, (OP == OP_LN ? 2u : 1u) * bytes);
+                if (bytes > 0) {
+                    bulk_g2s(smem_addr(sp0), P0, bytes, bar);
+                    if constexpr (OP == OP_LN) bulk_g2s(smem_addr(sp1), P1, bytes, bar);
+                }
+            }
         }
     } else {
         if (row >= p.rows) return;                   // the whole group leaves together
@@ -689,8 +697,8 @@ __global__ void __launch_bounds__(TPR * RPC,
         }
 
         // ---- normalize and store from the held registers ----------------
-        if constexpr (SPB) {
-            if (it == 0 && !mbar_wait_bounded(smem_addr(&sp_bar), 0) && p.err)
+        if constexpr (SP) {
+            if (it == 0 && bulk && !mbar_wait_bounded(smem_addr(&sp_bar), 0) && p.err)
                 atomicOr(p.err, kErrParamsTimeout);   // the outputs are then not valid
         }
         T* yr = Y + row * p.ldy;

@@ -252,6 +252,8 @@ def _race_buffers(torch, rows, d, dtype, seed):
     ("f32", capi.RN_VARIANT_AUTO, 4096, 768),
     ("f32", capi.RN_VARIANT_AUTO, 8192, 768),
     ("f32", capi.RN_VARIANT_AUTO, 2048, 4096),
+    ("f32", capi.RN_VARIANT_AUTO, 200, 8192),    # three 256-thread rows a CTA
+    ("f32", capi.RN_VARIANT_AUTO, 700, 2001),    # unaligned rows, parameters by bulk copy
     ("bf16", capi.RN_VARIANT_AUTO, 4096, 768),
     ("bf16", capi.RN_VARIANT_AUTO, 1024, 4096),
     ("f16", capi.RN_VARIANT_AUTO, 2048, 2048),
