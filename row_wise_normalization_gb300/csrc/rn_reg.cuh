@@ -29,7 +29,11 @@
 // grid-stride hypothesis of issue #54 taken one step further). With PP the
 // parameter vectors are loaded into registers once per thread and reused for
 // every row, which requires every row to start at the same 16-byte phase
-// (d % 4 == 0; the host checks).
+// (d % 4 == 0; the host checks). Instances that hold neither the parameters
+// nor a slice small enough to load them with the row stage them in shared
+// memory once per CTA instead (SP, reg_sp_bytes). Nothing is loaded through
+// the non-coherent path: the kernel ahead on the stream may still be writing
+// when this one starts (programmatic dependent launch).
 //
 // Vector layout of a row: h scalars up to the first 16-byte boundary of the
 // row (the "head peel", 0..3), nv aligned vectors, tl scalars of tail (0..3).
