@@ -55,9 +55,12 @@
  *   eps         Must be finite and >= 0, else RN_ERR_EPS. eps == 0 is
  *               allowed (an all-zero row then gives Inf/NaN, as it should).
  *   Aliasing    No output may overlap any input or another output
- *               (RN_ERR_ALIAS); x, gamma, beta and w are read through the
- *               read-only data path, which assumes they do not change while
- *               the kernel runs. In-place normalization is not supported.
+ *               (RN_ERR_ALIAS): a row's outputs are written while other
+ *               rows' inputs are still being read, and gamma/beta (w) are
+ *               copied once per CTA. In-place normalization is not
+ *               supported. The inputs may be the outputs of the call just
+ *               before on the same stream: every load is coherent and
+ *               comes after the wait for that call.
  *   Errors      Validation happens on the host before anything is enqueued;
  *               on any non-RN_OK status nothing was launched, except
  *               RN_ERR_CUDA, which reports a launch error from the CUDA
