@@ -55,7 +55,7 @@ __device__ __forceinline__ void batched_row_held(HeldRow<Elem<T>::kVec, SLOTS, f
     // the statistics as the warp-per-row kernel takes them (FP32 vector rows
     // leave centred in place: (x - K) - mu_s)
     constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
-    constexpr bool PK = sizeof(T) == 4 && VEC == 4;
+    constexpr bool PK = VEC % 2 == 0;   // FP32 and 16-bit vector rows
     float mu = 0.f, rs, K = 0.f, mu_s = 0.f;
     warp_row_stats<OP, T, VEC, SLOTS, false>(cur, lane, has_e, fd, eps, K, mu_s, mu, rs);
 
@@ -73,7 +73,7 @@ __device__ __forceinline__ void batched_row_held(HeldRow<Elem<T>::kVec, SLOTS, f
                 if constexpr (OP == OP_LN) ldt_p(b, P1 + j, pa);
             }
             if constexpr (PK) {
-                o = out_pairs<OP, false>(cur.v[s], a, b, 0.f, rs);
+                o = out_pairs<OP, false, VEC>(cur.v[s], a, b, 0.f, rs);
             } else if constexpr (OP == OP_LN) {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)

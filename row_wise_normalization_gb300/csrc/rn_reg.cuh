@@ -18,7 +18,8 @@
 //      RMSNorm needs only the sum of squares;
 //   3. rstd = rsqrtf(var + eps) and the row is written from the registers
 //      with streaming 128-bit stores.
-// FP32 vector rows do their element-wise arithmetic on pairs of elements
+// FP32 vector rows, and the 16-bit rows (widened to FP32) of one warp or of
+// a CTA's LayerNorm, do their element-wise arithmetic on pairs of elements
 // with the packed .f32x2 instructions (shift_sum_pairs and the helpers
 // beside it), which halves the instructions a row takes.
 //
@@ -278,15 +279,16 @@ __device__ __forceinline__ float held_ss_pairs(const HeldRow<VEC, SLOTS, RES>& r
     f2_get(a, x0, x1);
     return x0 + x1;
 }
-// One output vector from held FP32 values x: LayerNorm (x - m) * rs * a + b
-// (SUB) or x * rs * a + b, RMSNorm x * rs * a.
-template <int OP, bool SUB>
-__device__ __forceinline__ Vec<4> out_pairs(const Vec<4>& x, const Vec<4>& a, const Vec<4>& b,
-                                            float m, float rs) {
-    Vec<4> o;
+// One output vector from held values x (FP32, or 16-bit storage widened):
+// LayerNorm (x - m) * rs * a + b (SUB) or x * rs * a + b, RMSNorm x * rs * a.
+template <int OP, bool SUB, int VEC = 4>
+__device__ __forceinline__ Vec<VEC> out_pairs(const Vec<VEC>& x, const Vec<VEC>& a,
+                                              const Vec<VEC>& b, float m, float rs) {
+    static_assert(VEC % 2 == 0, "pairs");
+    Vec<VEC> o;
     const F2 r2 = f2s(rs), m2 = f2s(m);
 #pragma unroll
-    for (int k = 0; k < 4; k += 2) {
+    for (int k = 0; k < VEC; k += 2) {
         F2 c = f2(x.v[k], x.v[k + 1]);
         if constexpr (SUB) c = sub2(c, m2);
         if constexpr (OP == OP_LN)
@@ -323,14 +325,16 @@ __device__ __forceinline__ void load_row_params(Vec<VEC> (&a)[SLOTS],
 // Statistics of a row that one warp holds (lane t): the shift K, the shifted
 // mean mu_s, the mean and rs, as the warp-per-row and batched kernels both
 // take them, so that the two agree bit for bit. FP32 LayerNorm works in the
-// frame shifted by K (see reg_kernel); with PK its held vectors leave
-// centred in place, (x - K) - mu_s.
+// frame shifted by K (see reg_kernel). With PK (vector rows without a
+// residual: FP32 and 16-bit storage) the arithmetic runs on packed pairs and
+// the held vectors of a LayerNorm row leave centred in place: (x - K) - mu_s
+// for FP32, x - mu for 16-bit storage (where mu_s is mu).
 template <int OP, typename T, int VEC, int SLOTS, bool RES>
 __device__ __forceinline__ void warp_row_stats(HeldRow<VEC, SLOTS, RES>& cur, int t, bool has_e,
                                                float fd, float eps, float& K, float& mu_s,
                                                float& mu, float& rs) {
     constexpr bool SHIFT = OP == OP_LN && sizeof(T) == 4;
-    constexpr bool PK = sizeof(T) == 4 && VEC == 4 && !RES;
+    constexpr bool PK = VEC % 2 == 0 && !RES;
     const int h = cur.h, nv = cur.nv;
     if constexpr (OP == OP_LN) {
         float sum;
@@ -351,6 +355,8 @@ __device__ __forceinline__ void warp_row_stats(HeldRow<VEC, SLOTS, RES>& cur, in
                     }
                 }
             }
+        } else if constexpr (PK) {
+            sum = cur.e + held_sum_pairs(cur);   // unused slots hold 0
         } else {
             sum = cur.e;
 #pragma unroll
@@ -470,6 +476,8 @@ __global__ void __launch_bounds__(TPR * RPC,
     // FP32 vector rows without a residual: packed pairs, the LayerNorm shift
     // (and, for warp rows, the centring) applied to the held vectors in place
     constexpr bool PK = sizeof(T) == 4 && VEC == 4 && !RES;
+    // 16-bit warp rows without a residual: the same through warp_row_stats
+    constexpr bool PKW = WPR == 1 && VEC == 8 && !RES;
     const int64_t step = (int64_t)gridDim.x * RPC;
     int64_t row = (int64_t)blockIdx.x * RPC + g;
     pdl_launch_dependents();
@@ -729,9 +737,10 @@ __global__ void __launch_bounds__(TPR * RPC,
                     ldt_p(a, P0 + j, pa);
                     if constexpr (OP == OP_LN) ldt_p(b, P1 + j, pa);
                 }
-                if constexpr (PK) {
-                    // warp rows hold (x - K) - mu_s, CTA rows x - K (LayerNorm)
-                    o = out_pairs<OP, (OP == OP_LN && WPR > 1)>(cur.v[s], a, b, mu_s, rs);
+                if constexpr (PK || PKW) {
+                    // LayerNorm: warp rows hold their centred values, FP32
+                    // CTA rows x - K
+                    o = out_pairs<OP, (OP == OP_LN && WPR > 1), VEC>(cur.v[s], a, b, mu_s, rs);
                 } else if constexpr (PAIRS) {
 #pragma unroll
                     for (int k = 0; k < VEC; k += 2) {
