@@ -236,38 +236,57 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
                 const int rem = nq - k * TPB - 32 * w;
                 nw += 4 * (rem <= 0 ? 0 : (rem >= 32 ? 32 : rem));
             }
+            // element pairs on the packed FP32 pipe; LayerNorm shifts the
+            // held quads by K in place (x -> x - K), once
             if constexpr (OP == OP_LN) {
                 const float K = cur.K;
-                float sum = has_e ? cur.e - K : 0.f;
-#pragma unroll
-                for (int k = 0; k < SLOTS; ++k) {
-                    if (t + k * TPB < nq) {
-                        sum += ((cur.v[k].v[0] - K) + (cur.v[k].v[1] - K)) +
-                               ((cur.v[k].v[2] - K) + (cur.v[k].v[3] - K));
-                    }
-                }
-                const float wsum = warp_sum(sum);
-                const float wmean = nw > 0 ? wsum / (float)nw : 0.f;   // of x - K
-                const float de = (cur.e - K) - wmean;
-                float m2 = has_e ? de * de : 0.f;
+                const F2 k2 = f2s(K);
+                F2 acc = f2s(0.f);
 #pragma unroll
                 for (int k = 0; k < SLOTS; ++k) {
                     if (t + k * TPB < nq) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float dd = (cur.v[k].v[j] - K) - wmean;
-                            m2 = fmaf(dd, dd, m2);
+                        for (int j = 0; j < 4; j += 2) {
+                            const F2 d = sub2(f2(cur.v[k].v[j], cur.v[k].v[j + 1]), k2);
+                            f2_get(d, cur.v[k].v[j], cur.v[k].v[j + 1]);
+                            acc = add2(acc, d);
                         }
                     }
                 }
+                float a0, a1;
+                f2_get(acc, a0, a1);
+                const float sum = (has_e ? cur.e - K : 0.f) + (a0 + a1);
+                const float wsum = warp_sum(sum);
+                const float wmean = nw > 0 ? wsum / (float)nw : 0.f;   // of x - K
+                const float de = (cur.e - K) - wmean;
+                const F2 w2 = f2s(wmean);
+                F2 mm = f2s(0.f);
+#pragma unroll
+                for (int k = 0; k < SLOTS; ++k) {
+                    if (t + k * TPB < nq) {
+#pragma unroll
+                        for (int j = 0; j < 4; j += 2) {
+                            const F2 dd = sub2(f2(cur.v[k].v[j], cur.v[k].v[j + 1]), w2);
+                            mm = fma2(dd, dd, mm);
+                        }
+                    }
+                }
+                float m0, m1;
+                f2_get(mm, m0, m1);
+                const float m2 = (has_e ? de * de : 0.f) + (m0 + m1);
                 part = make_float4((float)nw, wsum, wmean, warp_sum(m2));
             } else {
-                float ss = cur.e * cur.e;
+                F2 sq = f2s(0.f);
 #pragma unroll
                 for (int k = 0; k < SLOTS; ++k)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) ss = fmaf(cur.v[k].v[j], cur.v[k].v[j], ss);
-                part = make_float4(0.f, warp_sum(ss), 0.f, 0.f);
+                    for (int j = 0; j < 4; j += 2) {   // unused slots hold 0
+                        const F2 x2 = f2(cur.v[k].v[j], cur.v[k].v[j + 1]);
+                        sq = fma2(x2, x2, sq);
+                    }
+                float s0, s1;
+                f2_get(sq, s0, s1);
+                part = make_float4(0.f, warp_sum(cur.e * cur.e + (s0 + s1)), 0.f, 0.f);
             }
         }
         // lane r sends this warp's partial into CTA r's slot (c, w) and
@@ -336,14 +355,8 @@ __global__ void __launch_bounds__(TPB, (ClusterCfg<OP, SLOTS, TPB, CL, PF, AL>::
                     ld_p(a, p.p0 + j, pa);
                     if constexpr (OP == OP_LN) ld_p(bb, p.p1 + j, pa);
                 }
-                if constexpr (OP == OP_LN) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        o.v[u] = fmaf(((cur.v[k].v[u] - cur.K) - mus) * rs, a.v[u], bb.v[u]);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) o.v[u] = cur.v[k].v[u] * rs * a.v[u];
-                }
+                // LayerNorm: the held quads are x - K
+                o = out_pairs<OP, (OP == OP_LN)>(cur.v[k], a, bb, mus, rs);
                 st_y(yr + j, o);
             }
         }

@@ -334,6 +334,27 @@ __device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
     return o;
 }
 
+// One output vector from held values x (FP32, or 16-bit storage widened):
+// LayerNorm (x - m) * rs * a + b (SUB) or x * rs * a + b, RMSNorm x * rs * a.
+template <int OP, bool SUB, int VEC = 4>
+__device__ __forceinline__ Vec<VEC> out_pairs(const Vec<VEC>& x, const Vec<VEC>& a,
+                                              const Vec<VEC>& b, float m, float rs) {
+    static_assert(VEC % 2 == 0, "pairs");
+    Vec<VEC> o;
+    const F2 r2 = f2s(rs), m2 = f2s(m);
+#pragma unroll
+    for (int k = 0; k < VEC; k += 2) {
+        F2 c = f2(x.v[k], x.v[k + 1]);
+        if constexpr (SUB) c = sub2(c, m2);
+        if constexpr (OP == OP_LN)
+            f2_get(fma2(mul2(c, r2), f2(a.v[k], a.v[k + 1]), f2(b.v[k], b.v[k + 1])), o.v[k],
+                   o.v[k + 1]);
+        else
+            f2_get(mul2(mul2(c, r2), f2(a.v[k], a.v[k + 1])), o.v[k], o.v[k + 1]);
+    }
+    return o;
+}
+
 // Reductions.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {

@@ -279,27 +279,6 @@ __device__ __forceinline__ float held_ss_pairs(const HeldRow<VEC, SLOTS, RES>& r
     f2_get(a, x0, x1);
     return x0 + x1;
 }
-// One output vector from held values x (FP32, or 16-bit storage widened):
-// LayerNorm (x - m) * rs * a + b (SUB) or x * rs * a + b, RMSNorm x * rs * a.
-template <int OP, bool SUB, int VEC = 4>
-__device__ __forceinline__ Vec<VEC> out_pairs(const Vec<VEC>& x, const Vec<VEC>& a,
-                                              const Vec<VEC>& b, float m, float rs) {
-    static_assert(VEC % 2 == 0, "pairs");
-    Vec<VEC> o;
-    const F2 r2 = f2s(rs), m2 = f2s(m);
-#pragma unroll
-    for (int k = 0; k < VEC; k += 2) {
-        F2 c = f2(x.v[k], x.v[k + 1]);
-        if constexpr (SUB) c = sub2(c, m2);
-        if constexpr (OP == OP_LN)
-            f2_get(fma2(mul2(c, r2), f2(a.v[k], a.v[k + 1]), f2(b.v[k], b.v[k + 1])), o.v[k],
-                   o.v[k + 1]);
-        else
-            f2_get(mul2(mul2(c, r2), f2(a.v[k], a.v[k + 1])), o.v[k], o.v[k + 1]);
-    }
-    return o;
-}
-
 // The parameters (gamma/beta or w) of one held row's vectors and its
 // head/tail scalar, for thread t of a row group of TPR threads.
 template <int OP, typename T, int VEC, int SLOTS, int TPR>
