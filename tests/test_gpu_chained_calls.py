@@ -204,6 +204,7 @@ def _race(torch, reset, chain, outs):
     must be deterministic), then back to back RACE_DIRECT times and from a
     CUDA graph RACE_GRAPH times; returns how many of those results differ
     from the synchronised one in any bit of any tensor of ``outs``."""
+    capi.device_error(clear=True)
     reset()
     chain(True)
     ref = [o.clone() for o in outs]
@@ -232,6 +233,8 @@ def _race(torch, reset, chain, outs):
         graph.replay()
         count()
     torch.cuda.synchronize()
+    # no bounded wait (parameter copy, cluster exchange, staging ring) ran out
+    assert capi.device_error() == 0
     return int(bad.item())
 
 
