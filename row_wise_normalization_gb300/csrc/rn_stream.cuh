@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
     T* Y = reinterpret_cast<T*>(p.y);
     T* H = reinterpret_cast<T*>(p.h);
     constexpr int W = TPB / 32;
+    constexpr int U = VEC == 1 ? 8 : 16 / VEC;   // vectors a thread loads at once (first read)
     __shared__ __align__(16) float xch[2][W][4];
     const int t = threadIdx.x;
     const int w = t >> 5, lane = t & 31;
@@ -94,7 +95,33 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
         if constexpr (OP == OP_LN) {
             K = ld_xr1<T, RES>(xr, rr, 0);   // shift (the same address for every thread)
             float n = 0.f, m = 0.f, M = 0.f;
-            for (int64_t q = t; q < nv; q += TPB) {
+            // chunks of U vectors a thread (their loads in flight together),
+            // one merge per chunk; then the remaining vectors one by one
+            int64_t q = t;
+            for (; q + (U - 1) * TPB < nv; q += U * TPB) {
+                Vec<VEC> v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) ld_xr<T, VEC, RES>(v[u], xr, rr, h + (q + u * TPB) * VEC);
+                float s = 0.f;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) {
+                        v[u].v[k] -= K;
+                        s += v[u].v[k];
+                    }
+                const float mc = s * (1.0f / (U * VEC));
+                float Mc = 0.f;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) {
+                        const float c = v[u].v[k] - mc;
+                        Mc = fmaf(c, c, Mc);
+                    }
+                chan_merge(n, m, M, (float)(U * VEC), mc, Mc);
+            }
+            for (; q < nv; q += TPB) {
                 Vec<VEC> v;
                 ld_xr<T, VEC, RES>(v, xr, rr, h + q * VEC);
 #pragma unroll
@@ -127,6 +154,7 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
             rs = rsqrtf(M2 / fd + p.eps);
         } else {
             float ss = 0.f;
+#pragma unroll 4
             for (int64_t q = t; q < nv; q += TPB) {
                 Vec<VEC> v;
                 ld_xr<T, VEC, RES>(v, xr, rr, h + q * VEC);
@@ -149,6 +177,7 @@ __global__ void __launch_bounds__(TPB, 1024 / TPB) stream_kernel(const Params p)
             pa = aligned16(P0, h);
             if constexpr (OP == OP_LN) pa = pa && aligned16(P1, h);
         }
+#pragma unroll 2
         for (int64_t q = t; q < nv; q += TPB) {
             const int64_t j = h + q * VEC;
             Vec<VEC> v, a, o;
