@@ -388,7 +388,8 @@ constexpr bool reg_early_params() {
 // Bytes of shared memory an instance stages its parameters in (0: none).
 // PS instances always do; otherwise every instance that neither holds its
 // parameters in registers (PP) nor loads them with the row (EP), as long as
-// the copies of its resident CTAs take at most 128 KB of an SM. Those instances would otherwise load the parameters
+// the copies of its resident CTAs take at most 136 KB of an SM (128 KB of
+// parameters plus the padding of reg_sp_elems). Those instances would otherwise load the parameters
 // from global memory after each row's reduction, where the dependent chain
 // waits for them. Measured on GB300: LayerNorm 2048 x 4096 13.2 -> 12.5 us
 // back to back (3 CTAs of 32 KB); but with 192 KB of an SM staged (LayerNorm
@@ -409,7 +410,7 @@ constexpr int reg_sp_bytes() {
     if (PS) return bytes;
     if (PP || reg_early_params<OP, VEC, SLOTS, PP, PS>()) return 0;
     const int ctas = reg_min_ctas(TPR * RPC, OP, VEC, SLOTS, PF, PP, RES, AL, PS);
-    return ctas * bytes <= 128 * 1024 ? bytes : 0;
+    return ctas * bytes <= 136 * 1024 ? bytes : 0;
 }
 
 template <int OP, typename T, int VEC, int SLOTS, int TPR, int RPC, bool PF, bool PP, bool AL,
