@@ -28,7 +28,11 @@
  *               page tables (GB300 over NVLink-C2C), ordinary pageable host
  *               memory. Host-resident x is then read and host-resident y
  *               written by the kernel itself over the host link, with no
- *               staging copies. The caller owns every buffer (the
+ *               staging copies; the forward entry points ask the runtime
+ *               where x and y live (cudaPointerGetAttributes, no
+ *               synchronization) and walk host-resident rows on a smaller,
+ *               persistent grid, so that reads and writes share the link.
+ *               The caller owns every buffer (the
  *               backward's workspace included); no entry point allocates
  *               or synchronizes, except the diagnostics that say so. Rows
  *               are contiguous with row stride d (in elements), except in

@@ -108,3 +108,33 @@ def test_16bit_torch_binding():
         parity.check_rstd(s.cpu().numpy(), sr)
         yqr, _ = reference.rms_norm(xw, gw)
         parity.check_y_storage(yq.view(torch.int16).cpu().numpy().view(np.uint16), yqr, name)
+
+
+# host-resident x and y (pinned; the kernel reads and writes them over the
+# host link on a persistent grid), parameters and statistics on the device
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rows,d", [(4096, 1024), (1000, 4096), (333, 1029)])
+def test_16bit_host_resident(dtype, rows, d):
+    torch = G.torch_cuda()
+    bits, wide = _case(rows, d, seed=77, dtype=dtype)
+    dev = torch.device("cuda", 0)
+    xh = torch.from_numpy(bits[0].view(np.int16)).pin_memory()
+    pd = [torch.from_numpy(p.view(np.int16)).to(dev) for p in bits[1:]]
+    code = G.DTYPE_CODE[dtype]
+    s = torch.cuda.current_stream().cuda_stream
+    for op in (LN, RMS):
+        y = torch.full((rows, d), -1, dtype=torch.int16).pin_memory()
+        m = torch.full((rows,), float("nan"), device=dev)
+        r = torch.full((rows,), float("nan"), device=dev)
+        if op == LN:
+            st = capi.ln_fwd_typed(code, capi.RN_VARIANT_AUTO, xh.data_ptr(), pd[0].data_ptr(),
+                                   pd[1].data_ptr(), y.data_ptr(), m.data_ptr(), r.data_ptr(),
+                                   rows, d, float(np.float32(1e-5)), s)
+        else:
+            st = capi.rms_fwd_typed(code, capi.RN_VARIANT_AUTO, xh.data_ptr(), pd[0].data_ptr(),
+                                    y.data_ptr(), rows, d, float(np.float32(1e-5)), s)
+        capi.check(st)
+        torch.cuda.synchronize()
+        yb = y.numpy().view(np.uint16)
+        out = (yb, m.cpu().numpy(), r.cpu().numpy()) if op == LN else (yb, None, None)
+        _check(op, dtype, wide, out)

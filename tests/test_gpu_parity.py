@@ -261,7 +261,8 @@ def test_torch_binding_and_side_stream():
 # over the host link (no staging copies)
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("where", ["host_in", "host_out", "host_both"])
-@pytest.mark.parametrize("rows,d", [(4096, 768), (333, 1029), (64, 40000)])
+@pytest.mark.parametrize("rows,d", [(4096, 768), (333, 1029), (64, 40000), (2000, 4096),
+                                    (1500, 8192), (20000, 256)])
 def test_host_resident_buffers(where, rows, d):
     torch = G.torch_cuda()
     import row_wise_normalization_gb300 as rn
