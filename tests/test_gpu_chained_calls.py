@@ -12,8 +12,9 @@ global access. These tests give that wait something to protect:
   before it read (a write-after-read across launches), checked at the end
   against the oracle chain;
 * both chains captured once into a CUDA graph and replayed on new inputs;
-* ping-pong chains (FP32, 16-bit, with a residual) run back to back hundreds
-  of times, directly and from a CUDA graph, each result compared bit for bit
+* ping-pong chains (FP32, 16-bit, with a residual, on pinned host buffers)
+  run back to back hundreds of times, directly and from a CUDA graph, each
+  result compared bit for bit
   with the same chain run with a device synchronisation after every call
   (the kernels are deterministic, so any difference is a read that the
   dependency wait did not order).
@@ -199,11 +200,11 @@ RACE_DIRECT = 200    # chains enqueued behind a device sleep, so they run back t
 RACE_GRAPH = 600     # replays of one captured chain
 
 
-def _race(torch, reset, chain, outs):
+def _race(torch, reset, chain, outs, graph=True):
     """Runs reset + chain with a sync after every call (twice: the kernels
-    must be deterministic), then back to back RACE_DIRECT times and from a
-    CUDA graph RACE_GRAPH times; returns how many of those results differ
-    from the synchronised one in any bit of any tensor of ``outs``."""
+    must be deterministic), then back to back RACE_DIRECT times and (graph)
+    from a CUDA graph RACE_GRAPH times; returns how many of those results
+    differ from the synchronised one in any bit of any tensor of ``outs``."""
     capi.device_error(clear=True)
     reset()
     chain(True)
@@ -225,13 +226,14 @@ def _race(torch, reset, chain, outs):
         reset()
         chain(False)
         count()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        reset()
-        chain(False)
-    for _ in range(RACE_GRAPH):
-        graph.replay()
-        count()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            reset()
+            chain(False)
+        for _ in range(RACE_GRAPH):
+            g.replay()
+            count()
     torch.cuda.synchronize()
     # no bounded wait (parameter copy, cluster exchange, staging ring) ran out
     assert capi.device_error() == 0
@@ -334,3 +336,59 @@ def test_back_to_back_residual_chains_match_synchronised_ones(variant, rows, d):
                 torch.cuda.synchronize()
 
     assert _race(torch, reset, chain, pair[RACE_STEPS % 2]) == 0
+
+
+@pytest.mark.parametrize("dtype,rows,d", [
+    ("f32", 4096, 768),    # warp rows
+    ("f32", 2048, 4096),   # a CTA per row
+    ("f32", 200, 8192),    # three 256-thread rows a CTA
+    ("bf16", 1024, 4096),
+    ("f32", 700, 2001),    # unaligned rows
+])
+def test_back_to_back_host_resident_chains_match_synchronised_ones(dtype, rows, d):
+    """The ping-pong chain on pinned host buffers, which the kernels read and
+    write over the host link on their persistent grid: every call reads
+    what the call before it wrote to host memory. The buffers are reset and
+    the result brought back by stream-ordered copies, so that the chain and
+    its checks stay on the stream (not captured into a graph: the copies
+    between pinned and device memory are torch's, outside the library)."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn  # noqa: F401
+
+    code = {"f32": capi.RN_DTYPE_F32, "bf16": capi.RN_DTYPE_BF16}[dtype]
+    x0, g, b, mean, rstd = _race_buffers(torch, rows, d, dtype, seed=961)
+    nan = torch.full_like(x0, float("nan"))
+    bufs = (torch.empty(x0.shape, dtype=x0.dtype).pin_memory(),
+            torch.empty(x0.shape, dtype=x0.dtype).pin_memory())
+    mirror = torch.empty_like(x0)
+
+    def reset():
+        bufs[0].copy_(x0, non_blocking=True)
+        bufs[1].copy_(nan, non_blocking=True)
+
+    def chain(sync):
+        s = torch.cuda.current_stream().cuda_stream
+        for k in range(RACE_STEPS):
+            src, dst = bufs[k % 2], bufs[(k + 1) % 2]
+            if k % 2 == 0:
+                st = capi.ln_fwd_typed(code, capi.RN_VARIANT_AUTO, src.data_ptr(), g.data_ptr(),
+                                       b.data_ptr(), dst.data_ptr(), mean.data_ptr(),
+                                       rstd.data_ptr(), rows, d, EPS, s)
+            else:
+                st = capi.rms_fwd_typed(code, capi.RN_VARIANT_AUTO, src.data_ptr(), g.data_ptr(),
+                                        dst.data_ptr(), rows, d, EPS, s)
+            capi.check(st)
+            if sync:
+                torch.cuda.synchronize()
+        mirror.copy_(bufs[RACE_STEPS % 2], non_blocking=True)
+        if sync:
+            torch.cuda.synchronize()
+
+    assert _race(torch, reset, chain, (mirror,), graph=False) == 0
+    # and the chain's result is the oracle chain's
+    torch.cuda.synchronize()
+    if dtype == "f32":
+        got = mirror.cpu().numpy().reshape(rows, d)
+        want = _oracle_chain(x0.cpu().numpy().reshape(rows, d), g.cpu().numpy(),
+                             b.cpu().numpy(), RACE_STEPS)
+        parity.check_y(got, want, what="host chain")
