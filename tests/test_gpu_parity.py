@@ -293,6 +293,53 @@ def test_host_resident_buffers(where, rows, d):
         parity.check_y(y2.numpy(), reference.layer_norm(x, g, b)[0])
 
 
+def _pageable_access_supported(torch):
+    """cudaDevAttrPageableMemoryAccess (88) of device 0 through the CUDA
+    runtime torch has loaded; None when that library cannot be reached."""
+    import ctypes
+    torch.cuda.init()
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+        except OSError:
+            continue
+        v = ctypes.c_int(0)
+        if rt.cudaDeviceGetAttribute(ctypes.byref(v), 88, 0) != 0:
+            return None
+        return v.value == 1
+    return None
+
+
+@pytest.mark.parametrize("rows,d", [(4096, 768), (333, 1029), (1000, 4096)])
+def test_pageable_host_buffers_through_the_c_entry_point(rows, d):
+    """Ordinary (pageable, unregistered) host memory for x and y, on a GPU
+    that reads host page tables (checked first: on any other GPU such an
+    access is not allowed, and the test does not run it)."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn  # noqa: F401  (loads the library)
+
+    ok = _pageable_access_supported(torch)
+    if not ok:
+        pytest.skip("the GPU does not read pageable host memory" if ok is False
+                    else "CUDA runtime library not reachable through ctypes")
+    wl = workloads.Workload("ln", rows, d, seed=37, x_dist="offset", x_std=2.0)
+    x = np.ascontiguousarray(wl.x(), np.float32)
+    g, b = wl.params()
+    dev = torch.device("cuda", 0)
+    gt, bt = torch.from_numpy(g).to(dev), torch.from_numpy(b).to(dev)
+    y = np.full((rows, d), np.nan, np.float32)
+    yq = np.full((rows, d), np.nan, np.float32)
+    m = torch.full((rows,), float("nan"), device=dev)
+    r = torch.full((rows,), float("nan"), device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    capi.check(capi.ln_fwd(x.ctypes.data, gt.data_ptr(), bt.data_ptr(), y.ctypes.data,
+                           m.data_ptr(), r.data_ptr(), rows, d, 1e-5, s))
+    capi.check(capi.rms_fwd(x.ctypes.data, gt.data_ptr(), yq.ctypes.data, rows, d, 1e-5, s))
+    torch.cuda.synchronize()
+    _check_ln(x, g, b, (y, m.cpu().numpy(), r.cpu().numpy()))
+    _check_rms(x, g, yq)
+
+
 # ---------------------------------------------------------------------------
 # full size, in the launch configuration the benchmark times
 # ---------------------------------------------------------------------------
