@@ -1108,9 +1108,9 @@ def run_ours(args, rank, world, local_rank):
                 "ms_per_step": e2e_ms,
                 "path": f"the C entry point {wl.op}_fwd on pinned host buffers: its kernel "
                         "reads x from host memory and writes the outputs to host memory over "
-                        "NVLink-C2C every step (a persistent grid of 2 warps per SM for "
-                        "host-resident rows); K steps back to back over distinct host "
-                        "copies of the batch, one event pair",
+                        "NVLink-C2C every step (host-resident rows walk a persistent grid "
+                        "holding about 1.25 MB in flight); K steps back to back over "
+                        "distinct host copies of the batch, one event pair",
                 "same_result_as_device_path": e2e_match,
                 "explicit_copies": {"value": gbs(case.bytes * world, copy_ms), "unit": UNIT,
                                     "ms_per_step": copy_ms,

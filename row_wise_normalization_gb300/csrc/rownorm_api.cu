@@ -430,16 +430,20 @@ bool host_resident(const void* p) {
     return a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
 }
 
-// Warps per SM (on average over the SMs, at least one CTA) that walk
-// host-resident rows. With every row in flight in one wave, every read of a
-// call is issued before its first write and the host link carries one
-// direction at a time; a persistent grid that walks the rows, the next one
-// prefetched, keeps both directions busy. Measured on GB300, pinned x and y,
-// calls back to back (one wave -> 1 / 2 / 4 warps per SM): LayerNorm FP32
-// 4096 x 768 121 -> 80.6 / 81.8 / 86.5 us, 1024 x 4096 147 -> 104 / 108 /
-// 117 us, 1024 x 8192 262 -> 214 / 206 / 210 us; BF16 4096 x 1024 78.1 ->
-// 65.3 / 58.4 / 63.0 us, 4096 x 4096 239 -> 288 / 206 / 208 us.
-constexpr int kLinkWarpsPerSm = 2;
+// Bytes of host-resident rows a call keeps in flight. With every row in
+// flight in one wave, every read of a call is issued before its first write
+// and the host link carries one direction at a time; a persistent grid that
+// walks the rows (the next one prefetched where the plan says so) keeps both
+// directions busy, and more requests in flight than the link needs only
+// queue on it. Measured on GB300, pinned x and y, calls back to back, one
+// wave against grids holding about 0.3 / 0.6 / 1.2 / 2.4 MB: LayerNorm FP32
+// 4096 x 768 121 -> 80.6 (0.9 MB) / 81.8 (1.8) / 86.5 (3.6) us, 1024 x
+// 4096 147 -> 104 (1.2) / 108 (2.4) / 117 (4.9) us, 1024 x 8192 262 ->
+// 214 (0.7) / 206 (1.25) / 210 (2.5) us; BF16 4096 x 1024 78.1 -> 65.3
+// (0.6) / 58.4 (1.2) / 63.0 (2.4) us, 4096 x 4096 239 -> 288 (0.3) / 206
+// (0.6) / 208 (1.2) us; and FP32 65536 x 128 241 -> 300 us with only
+// 0.3 MB in flight.
+constexpr int64_t kLinkBytesInFlight = 1280 * 1024;
 
 int run(const Request& q, int variant, void* stream) {
     if (variant < 0 || variant >= RN_VARIANT_COUNT) return RN_ERR_VARIANT;
@@ -502,16 +506,13 @@ int run(const Request& q, int variant, void* stream) {
     const int64_t want = (q.rows + e->rows_per_cta - 1) / e->rows_per_cta;
     // Rows read from or written to host memory: the planned instance (it
     // prefetches the next row where the plan says so) on a persistent grid
-    // of kLinkWarpsPerSm warps per SM, rather than the one-wave instances
-    // below, so that each call's reads and writes share the host link.
+    // that holds about kLinkBytesInFlight of rows, rather than the one-wave
+    // instances below, so that each call's reads and writes share the link.
     if ((pl.variant == RN_VARIANT_WARP || pl.variant == RN_VARIANT_BLOCK) &&
         (host_resident(q.x) || host_resident(q.y))) {
-        int dev = 0, sms = 0;
-        if ((err = cudaGetDevice(&dev)) != cudaSuccess ||
-            (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) !=
-                cudaSuccess)
-            return fail_cuda(err);
-        int64_t cap = ((int64_t)sms * 32 * kLinkWarpsPerSm + e->threads - 1) / e->threads;
+        const int64_t row_bytes = q.d * dtype_size(q.dtype) * (q.res ? 2 : 1);
+        const int64_t cta_bytes = row_bytes * e->rows_per_cta * (pl.prefetch ? 2 : 1);
+        int64_t cap = (kLinkBytesInFlight + cta_bytes - 1) / cta_bytes;
         if (cap > resident) cap = resident;
         const int grid = (int)(want < cap ? want : cap);
         err = e->launch(prm, grid, s);
