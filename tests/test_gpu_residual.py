@@ -90,3 +90,33 @@ def test_residual_torch_binding():
     h2, y2 = rn.rms_fwd_residual(xt, rt, gt, write_h=False)
     assert h2 is None
     _check(RMS, x, r, g, b, (None, y2.cpu().numpy(), None, None), want_h=False)
+
+
+# x, res, h and y in pinned host memory: the kernel reads and writes them over
+# the host link, on the persistent grid host-resident rows get
+@pytest.mark.parametrize("rows,d", [(4096, 768), (1000, 4096), (333, 1029)])
+def test_residual_host_resident(rows, d):
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn  # noqa: F401  (loads the library)
+
+    x, r, g, b = _inputs(rows, d, seed=57)
+    dev = torch.device("cuda", 0)
+    xh = torch.from_numpy(x).pin_memory()
+    rh = torch.from_numpy(r).pin_memory()
+    gt, bt = torch.from_numpy(g).to(dev), torch.from_numpy(b).to(dev)
+    s = torch.cuda.current_stream().cuda_stream
+    for op in (LN, RMS):
+        h = torch.full((rows, d), float("nan")).pin_memory()
+        y = torch.full((rows, d), float("nan")).pin_memory()
+        m = torch.full((rows,), float("nan"), device=dev)
+        sd = torch.full((rows,), float("nan"), device=dev)
+        if op == LN:
+            st = capi.ln_fwd_residual(xh.data_ptr(), rh.data_ptr(), gt.data_ptr(), bt.data_ptr(),
+                                      h.data_ptr(), y.data_ptr(), m.data_ptr(), sd.data_ptr(),
+                                      rows, d, float(np.float32(1e-5)), s)
+        else:
+            st = capi.rms_fwd_residual(xh.data_ptr(), rh.data_ptr(), gt.data_ptr(), h.data_ptr(),
+                                       y.data_ptr(), rows, d, float(np.float32(1e-5)), s)
+        capi.check(st)
+        torch.cuda.synchronize()
+        _check(op, x, r, g, b, (h.numpy(), y.numpy(), m.cpu().numpy(), sd.cpu().numpy()))

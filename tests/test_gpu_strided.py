@@ -163,3 +163,27 @@ def test_strided_views_through_the_torch_binding():
         qr, _ = reference.rms_norm(xv.cpu().numpy(), g.cpu().numpy())
         parity.check_y(q.cpu().numpy(), qr, what=f"rms head {h}")
     assert not torch.isnan(out).any()
+
+
+def test_strided_views_of_pinned_host_matrices():
+    """Column blocks of a wider matrix in pinned host memory, read and
+    written in place by the kernel over the host link (the persistent grid
+    host-resident rows get), each against the oracle; the gaps between the
+    blocks' rows stay untouched."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn
+
+    rows, d, heads = 4000, 256, 3
+    wl = workloads.Workload("ln", rows, heads * d, seed=307, x_dist="offset", x_std=2.0)
+    big = torch.from_numpy(wl.x()).pin_memory()
+    g, b = (torch.from_numpy(p[:d].copy()).to("cuda") for p in wl.params())
+    out = torch.full(big.shape, float("nan")).pin_memory()
+    for h in (0, 2):
+        xv = big[:, h * d:(h + 1) * d]                 # row stride heads*d
+        yv = out[:, h * d:(h + 1) * d]
+        rn.ln_fwd(xv, g, b, y=yv)
+        torch.cuda.synchronize()
+        yr, _, _ = reference.layer_norm(xv.numpy(), g.cpu().numpy(), b.cpu().numpy())
+        parity.check_y(yv.numpy(), yr, what=f"host head {h}")
+    assert torch.isnan(out[:, d:2 * d]).all(), "a gap column was written"
+    assert not torch.isnan(out[:, :d]).any() and not torch.isnan(out[:, 2 * d:]).any()
