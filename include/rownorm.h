@@ -32,6 +32,11 @@
  *               where x and y live (cudaPointerGetAttributes, no
  *               synchronization) and walk host-resident rows on a smaller,
  *               persistent grid, so that reads and writes share the link.
+ *               The exception: the parameter vectors of the forward calls
+ *               (gamma, beta, w), which the kernels copy into shared memory
+ *               with the bulk-copy engine, must be device memory, else
+ *               RN_ERR_HOSTMEM (the backward and batched calls take them
+ *               anywhere, as above).
  *               The caller owns every buffer (the
  *               backward's workspace included); no entry point allocates
  *               or synchronizes, except the diagnostics that say so. Rows
@@ -92,7 +97,8 @@ typedef enum rn_status {
     RN_ERR_ALIGN = 6,   /* a pointer is not 4-byte aligned                     */
     RN_ERR_VARIANT = 7, /* a forced variant cannot run this shape / alignment  */
     RN_ERR_DTYPE = 8,   /* unknown storage type, or one the entry point lacks  */
-    RN_ERR_SCRATCH = 9  /* the request needs more than a static scratch holds  */
+    RN_ERR_SCRATCH = 9, /* the request needs more than a static scratch holds  */
+    RN_ERR_HOSTMEM = 10 /* a forward call's parameter vectors in host memory   */
 } rn_status;
 
 /* Storage types of x, y and the parameter vectors (statistics are FP32). */
@@ -433,6 +439,15 @@ int rn_device_error(unsigned int *flags, int clear);
  * device error word and the kernel returns; the context stays usable. No
  * memory other than that word is touched. */
 int rn_selftest_bounded_wait(unsigned int timeout_us, void *stream);
+
+/* Whether the current GPU reads ordinary (pageable, unregistered) host
+ * memory coherently, through the host's page tables, so that such memory may
+ * be passed wherever the Memory convention above allows host memory (GB300
+ * over NVLink-C2C does): *pageable = 1 if the device attribute
+ * cudaDevAttrPageableMemoryAccess is set, else 0. Pinned memory
+ * (cudaHostAlloc / cudaHostRegister) is accepted either way. Host-only (a
+ * device attribute query). Returns RN_OK, RN_ERR_NULL or RN_ERR_CUDA. */
+int rn_pageable_host_access(int *pageable);
 
 /* Measurement aid: launch an empty kernel with `grid` CTAs of `threads`
  * threads on `stream` (the launch-latency floor small shapes are compared

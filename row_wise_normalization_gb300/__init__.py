@@ -29,7 +29,23 @@ def _empty_like_home(x, shape, dtype=None):
     dtype = torch.float32 if dtype is None else dtype
     if x.is_cuda:
         return torch.empty(shape, dtype=dtype, device=x.device)
-    return torch.empty(shape, dtype=dtype, pin_memory=True)
+    return torch.empty(shape, dtype=dtype, pin_memory=x.is_pinned())
+
+
+_PAGEABLE = {}
+
+
+def _pageable_ok():
+    """Whether the current GPU reads pageable host memory (asked once per
+    device)."""
+    import torch
+
+    if not torch.cuda.is_available():
+        return False
+    dev = torch.cuda.current_device()
+    if dev not in _PAGEABLE:
+        _PAGEABLE[dev] = capi.pageable_host_access()
+    return _PAGEABLE[dev]
 
 
 def _dtype_code(t):
@@ -44,14 +60,16 @@ def _dtype_code(t):
 
 def _check_f32_cuda(name, t, dtype=None, contiguous=True):
     """Contiguous, of the expected dtype (FP32 unless given), and addressable
-    by the GPU: a CUDA tensor or a pinned CPU tensor (which the kernel reads or
-    writes over the host link)."""
+    by the GPU: a CUDA tensor, a pinned CPU tensor, or, on a GPU that reads
+    pageable host memory (GB300), any CPU tensor (the kernel reads or writes
+    host tensors over the host link)."""
     import torch
 
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not (t.is_cuda or t.is_pinned()):
-        raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
+    if not (t.is_cuda or t.is_pinned() or (t.device.type == "cpu" and _pageable_ok())):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned CPU tensor (this GPU "
+                         f"does not read pageable host memory)")
     want = torch.float32 if dtype is None else dtype
     if t.dtype != want:
         raise TypeError(f"{name} must be {want}, got {t.dtype}")
@@ -78,7 +96,8 @@ def ln_fwd(x, gamma, beta, eps: float = 1e-5, *, y=None, mean=None, rstd=None, s
     x, gamma, beta (and y) are float32, bfloat16 or float16 -- all the same
     type; statistics are computed in FP32. Returns ``(y, mean, rstd)``: y like
     x; mean and rstd FP32 of shape x.shape[:-1]. Tensors are CUDA tensors or
-    pinned CPU tensors (read or written by the kernel over the host link);
+    pinned CPU tensors, or any CPU tensors on a GPU that reads pageable host
+    memory (read or written by the kernel over the host link);
     outputs not passed in are allocated where x lives. x and y may also be
     2-D row-strided views (``big[:, a:a + d]``): the kernels then read and
     write the rows in place.
@@ -204,7 +223,7 @@ def ln_fwd_residual(x, res, gamma, beta, eps: float = 1e-5, *, h=None, y=None, m
     """h = x + res, then LayerNorm of h over the last dimension, in one kernel.
 
     Returns ``(h, y, mean, rstd)``; h is None when ``write_h`` is False and no
-    h tensor is passed. Tensors are CUDA tensors or pinned CPU tensors.
+    h tensor is passed. Tensors are CUDA tensors or host tensors as for ln_fwd.
     """
     _check_f32_cuda("x", x)
     d = x.shape[-1]

@@ -25,6 +25,7 @@ RN_ERR_ALIGN = 6
 RN_ERR_VARIANT = 7
 RN_ERR_DTYPE = 8
 RN_ERR_SCRATCH = 9
+RN_ERR_HOSTMEM = 10
 
 # device error word bits
 RN_DEVERR_STAGED_TIMEOUT = 1
@@ -106,6 +107,7 @@ SIGNATURES = {
     "rms_fwd_typed": (_INT, [_INT, _INT, _P, _P, _P, _I64, _I64, _F, _P]),
     "rn_plan_for_typed": (_INT, [_INT, _INT, _INT, _I64, _P, _P, _P, _P, ctypes.POINTER(rn_plan)]),
     "rn_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
+    "rn_pageable_host_access": (_INT, [ctypes.POINTER(_INT)]),
 }
 
 _lib = None
@@ -203,6 +205,13 @@ def rms_fwd_variant(variant, x, w, y, rows, d, eps, stream=0) -> int:
 
 def launch_empty(grid, threads, stream=0) -> int:
     return load().rn_launch_empty(grid, threads, stream)
+
+
+def pageable_host_access() -> bool:
+    """Whether the current GPU reads pageable (unpinned) host memory."""
+    out = ctypes.c_int(0)
+    check(load().rn_pageable_host_access(ctypes.byref(out)))
+    return out.value != 0
 
 
 def device_error(clear: bool = False) -> int:

@@ -450,9 +450,21 @@ int run(const Request& q, int variant, void* stream) {
     int st = validate(q);
     if (st != RN_OK) return st;
     if (q.rows == 0) return RN_OK;
+    // The bulk-copy engine is given device memory only: the parameter
+    // vectors, which the register-held kernels stage in shared memory by bulk
+    // copies, must be in device memory, and rows in host memory do not take
+    // the staged kernel (whose ring is filled by bulk copies; the streaming
+    // kernel reads them with ordinary loads instead).
+    if (host_resident(q.p0) || (q.op == OP_LN && host_resident(q.p1))) return RN_ERR_HOSTMEM;
     rn_plan pl;
     st = plan_impl(q, variant, &pl);
     if (st != RN_OK) return st;
+    const bool x_host = host_resident(q.x);
+    if (pl.variant == RN_VARIANT_STAGED && x_host) {
+        if (variant != RN_VARIANT_AUTO) return RN_ERR_VARIANT;
+        st = plan_impl(q, RN_VARIANT_STREAM, &pl);
+        if (st != RN_OK) return st;
+    }
 
     Params prm;
     prm.x = q.x;
@@ -508,15 +520,17 @@ int run(const Request& q, int variant, void* stream) {
     // prefetches the next row where the plan says so) on a persistent grid
     // that holds about kLinkBytesInFlight of rows, rather than the one-wave
     // instances below, so that each call's reads and writes share the link.
+    const auto launch = [&](const KernelEntry* ke, int grid) {
+        const cudaError_t e2 = ke->launch(prm, grid, s);
+        return e2 == cudaSuccess ? RN_OK : fail_cuda(e2);
+    };
     if ((pl.variant == RN_VARIANT_WARP || pl.variant == RN_VARIANT_BLOCK) &&
-        (host_resident(q.x) || host_resident(q.y))) {
+        (x_host || host_resident(q.y))) {
         const int64_t row_bytes = q.d * dtype_size(q.dtype) * (q.res ? 2 : 1);
         const int64_t cta_bytes = row_bytes * e->rows_per_cta * (pl.prefetch ? 2 : 1);
         int64_t cap = (kLinkBytesInFlight + cta_bytes - 1) / cta_bytes;
         if (cap > resident) cap = resident;
-        const int grid = (int)(want < cap ? want : cap);
-        err = e->launch(prm, grid, s);
-        return err == cudaSuccess ? RN_OK : fail_cuda(err);
+        return launch(e, (int)(want < cap ? want : cap));
     }
     // Aligned FP32 rows that prefetch: when every row fits in one wave of
     // the no-prefetch instance (more CTAs resident, no next row to overlap
@@ -583,9 +597,7 @@ int run(const Request& q, int variant, void* stream) {
             }
         }
     }
-    const int grid = (int)(want < resident ? want : resident);
-    err = e->launch(prm, grid, s);
-    return err == cudaSuccess ? RN_OK : fail_cuda(err);
+    return launch(e, (int)(want < resident ? want : resident));
 }
 
 Request ln_request(const float* x, const float* res, const float* gamma, const float* beta,
@@ -774,6 +786,7 @@ struct BwdRequest {
     void* ws;
     size_t ws_bytes;
     int dtype = DT_F32;  // storage of dy, x, dx and the parameters and their gradients
+    bool rows_on_host = false;   // x or dy in host memory: no bulk-copy ring
 };
 
 struct BwdPlan {
@@ -866,7 +879,7 @@ int bwd_plan(const BwdRequest& q, bool pg, bool size_only, BwdPlan* bp, cudaErro
     int dev = 0, sms = 0, smem_sm = 0;
     if (!device_shape(&dev, &sms, &smem_sm, err)) return RN_ERR_CUDA;
     if (vec > 1 && tpr >= 64 && (tpr >= 256 || q.dtype != DT_F32) &&
-        (tpr <= 512 || (q.op == OP_RMS && q.dtype != DT_F32))) {
+        (tpr <= 512 || (q.op == OP_RMS && q.dtype != DT_F32)) && !q.rows_on_host) {
         const BwdEntry* se = bwd_staged_entry(q.op, q.dtype, slots, tpr, pg);
         if (se) {
             // as many stages (up to kBwdRingStages) as the SM's shared memory
@@ -974,7 +987,10 @@ int run_bwd(const BwdRequest& q, void* stream) {
     }
     BwdPlan bp;
     cudaError_t err;
-    st = bwd_plan(q, pg, false, &bp, &err);
+    // the bulk-copy engine fills the staged ring from device memory only
+    BwdRequest qh = q;
+    qh.rows_on_host = host_resident(q.x) || host_resident(q.dy);
+    st = bwd_plan(qh, pg, false, &bp, &err);
     if (st == RN_ERR_CUDA) return fail_cuda(err);
     if (st != RN_OK) return st;
     BwdParams prm;
@@ -1314,6 +1330,9 @@ const char* rn_status_str(int status) {
         case RN_ERR_ALIGN: return "a pointer is not 4-byte aligned";
         case RN_ERR_VARIANT: return "the requested kernel variant cannot run this request";
         case RN_ERR_DTYPE: return "unsupported storage type for this entry point";
+        case RN_ERR_HOSTMEM:
+            return "the parameter vectors (gamma, beta, w) of a forward call must be in device "
+                   "memory";
         case RN_ERR_SCRATCH:
             return "the request needs more than the static scratch holds (ln_bwd_noalloc: "
                    "d <= 4096)";
@@ -1333,6 +1352,17 @@ int rn_selftest_bounded_wait(unsigned int timeout_us, void* stream) {
     if (timeout_us < 1 || timeout_us > 1000000) return RN_ERR_SIZE;
     const cudaError_t e = bounded_wait_selftest(1000ull * timeout_us, (cudaStream_t)stream);
     return e == cudaSuccess ? RN_OK : fail_cuda(e);
+}
+
+int rn_pageable_host_access(int* pageable) {
+    if (!pageable) return RN_ERR_NULL;
+    int dev = 0, v = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess)
+        err = cudaDeviceGetAttribute(&v, cudaDevAttrPageableMemoryAccess, dev);
+    if (err != cudaSuccess) return fail_cuda(err);
+    *pageable = v ? 1 : 0;
+    return RN_OK;
 }
 
 int rn_launch_empty(int64_t grid, int threads, void* stream) {

@@ -278,3 +278,28 @@ def test_backward_graph_capture_and_replay_with_new_inputs():
             for a, b_ in zip(got, (dx, dg, db, dxq, dw)):
                 assert torch.equal(a, b_)
     assert capi.device_error() == 0
+
+
+@pytest.mark.parametrize("rows,d", [(1024, 4096), (300, 8192), (4096, 768)])
+def test_ln_backward_rows_in_pinned_host_memory(rows, d):
+    """x, dy and dx in pinned host memory (read and written over the host
+    link): the rows that would take the staged ring, which the bulk-copy
+    engine fills from device memory only, run the register form instead."""
+    torch = G.torch_cuda()
+    x, dy, g, _ = _case(rows, d, seed=87)
+    m32, r32 = _stats(x, g)
+    dev = torch.device("cuda", 0)
+    xh = torch.from_numpy(x).pin_memory()
+    dyh = torch.from_numpy(dy).pin_memory()
+    dxh = torch.full((rows, d), float("nan")).pin_memory()
+    gt = torch.from_numpy(g).to(dev)
+    mt, rt = torch.from_numpy(m32).to(dev), torch.from_numpy(r32).to(dev)
+    dg = torch.full((d,), float("nan"), device=dev)
+    db = torch.full((d,), float("nan"), device=dev)
+    need = capi.bwd_workspace_size(capi.RN_OP_LN, rows, d)
+    ws = torch.empty(max(need // 4, 4), dtype=torch.float32, device=dev)
+    capi.check(capi.ln_bwd(dyh.data_ptr(), xh.data_ptr(), gt.data_ptr(), mt.data_ptr(),
+                           rt.data_ptr(), dxh.data_ptr(), dg.data_ptr(), db.data_ptr(), rows, d,
+                           ws.data_ptr(), need, G.stream_handle()))
+    torch.cuda.synchronize()
+    _check_ln(x, dy, g, (dxh.numpy(), dg.cpu().numpy(), db.cpu().numpy()), chain=_chain(rows))

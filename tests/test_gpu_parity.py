@@ -340,6 +340,82 @@ def test_pageable_host_buffers_through_the_c_entry_point(rows, d):
     _check_rms(x, g, yq)
 
 
+def test_forward_parameters_in_host_memory_are_refused():
+    """The forward kernels stage gamma/beta (w) in shared memory with the
+    bulk-copy engine, which is given device memory only: host-resident
+    parameters return RN_ERR_HOSTMEM before anything is launched."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn  # noqa: F401  (loads the library)
+
+    rows, d = 64, 768
+    dev = torch.device("cuda", 0)
+    x = torch.ones(rows, d, device=dev)
+    y = torch.empty_like(x)
+    m = torch.empty(rows, device=dev)
+    r = torch.empty(rows, device=dev)
+    g_dev = torch.ones(d, device=dev)
+    g_pin = torch.ones(d).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    assert capi.ln_fwd(x.data_ptr(), g_pin.data_ptr(), g_dev.data_ptr(), y.data_ptr(),
+                       m.data_ptr(), r.data_ptr(), rows, d, 1e-5, s) == capi.RN_ERR_HOSTMEM
+    assert capi.ln_fwd(x.data_ptr(), g_dev.data_ptr(), g_pin.data_ptr(), y.data_ptr(),
+                       m.data_ptr(), r.data_ptr(), rows, d, 1e-5, s) == capi.RN_ERR_HOSTMEM
+    assert capi.rms_fwd(x.data_ptr(), g_pin.data_ptr(), y.data_ptr(), rows, d, 1e-5,
+                        s) == capi.RN_ERR_HOSTMEM
+    g_np = np.ones(d, np.float32)                       # pageable
+    assert capi.rms_fwd(x.data_ptr(), g_np.ctypes.data, y.data_ptr(), rows, d, 1e-5,
+                        s) == capi.RN_ERR_HOSTMEM
+    torch.cuda.synchronize()
+
+
+def test_staged_kernel_refuses_rows_in_host_memory():
+    """The staged kernel's ring is filled by bulk copies: a call forced onto
+    it with x in host memory returns RN_ERR_VARIANT (AUTO never plans it for
+    such rows)."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn  # noqa: F401
+
+    rows, d = 16, 5000
+    dev = torch.device("cuda", 0)
+    xh = torch.ones(rows, d).pin_memory()
+    y = torch.empty(rows, d, device=dev)
+    g = torch.ones(d, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    assert capi.rms_fwd_variant(capi.RN_VARIANT_STAGED, xh.data_ptr(), g.data_ptr(),
+                                y.data_ptr(), rows, d, 1e-5, s) == capi.RN_ERR_VARIANT
+    xd = xh.to(dev)                                     # the same call on device rows runs
+    assert capi.rms_fwd_variant(capi.RN_VARIANT_STAGED, xd.data_ptr(), g.data_ptr(),
+                                y.data_ptr(), rows, d, 1e-5, s) == capi.RN_OK
+    torch.cuda.synchronize()
+    parity.check_y(y.cpu().numpy(), reference.rms_norm(np.ones((rows, d), np.float32),
+                                                       np.ones(d, np.float32))[0])
+
+
+def test_pageable_cpu_tensors_through_the_torch_binding():
+    """On a GPU that reads pageable host memory the binding takes ordinary
+    CPU tensors for x (and allocates y, mean and rstd beside it); the
+    parameters stay on the device."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn
+
+    if not capi.pageable_host_access():
+        pytest.skip("the GPU does not read pageable host memory")
+    wl = workloads.Workload("ln", 2000, 768, seed=39, x_dist="offset", x_std=2.0)
+    x = wl.x()
+    g, b = wl.params()
+    dev = torch.device("cuda", 0)
+    gt, bt = torch.from_numpy(g).to(dev), torch.from_numpy(b).to(dev)
+    xt = torch.from_numpy(x)
+    y, m, r = rn.ln_fwd(xt, gt, bt)
+    yq = rn.rms_fwd(xt, gt)
+    torch.cuda.synchronize()
+    assert not y.is_cuda and not y.is_pinned() and not m.is_cuda
+    _check_ln(x, g, b, (y.numpy(), m.numpy(), r.numpy()))
+    _check_rms(x, g, yq.numpy())
+    with pytest.raises(capi.RowNormError):
+        rn.ln_fwd(xt, torch.from_numpy(g), bt)          # parameters in host memory
+
+
 # ---------------------------------------------------------------------------
 # full size, in the launch configuration the benchmark times
 # ---------------------------------------------------------------------------
