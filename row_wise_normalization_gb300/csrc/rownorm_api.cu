@@ -419,8 +419,10 @@ int fail_cuda(cudaError_t err) {
 
 // Whether p is host memory the GPU reaches over the host link: pinned or
 // registered (cudaMemoryTypeHost), or pageable memory read through the host
-// page tables (cudaMemoryTypeUnregistered). A failed query counts as device
-// memory: the answer only picks a launch shape, never what is computed.
+// page tables (cudaMemoryTypeUnregistered). The query succeeds for every
+// address, allocated or not, unless the runtime itself is failing (no
+// device, or a sticky error from an earlier fault); that counts as device
+// memory, and the launch that follows reports the error.
 bool host_resident(const void* p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
