@@ -252,3 +252,58 @@ def test_fuzz_backward_staged(case):
         out = H._run(op, dtype, xb, dyb, gb, m32, r32, ws_bytes=ws)
         H._check(op, dtype, xw, dyw, gw, bw, out, chain=chain)
     assert capi.device_error() == 0
+
+
+def _pinned_at(torch, a, off, pad=16):
+    """A pinned FP32 buffer holding ``a`` (flattened) ``off`` elements in,
+    NaN everywhere else; returns (buffer, address of the first element)."""
+    n = a.size
+    buf = torch.full((n + off + pad,), float("nan")).pin_memory()
+    if n:
+        buf[off:off + n] = torch.from_numpy(np.ascontiguousarray(a, np.float32).reshape(-1))
+    return buf, buf.data_ptr() + 4 * off
+
+
+@pytest.mark.parametrize("case", range(96))
+def test_fuzz_forward_host_resident(case):
+    """x and y in pinned host memory (read and written over the host link,
+    on the grid host-resident rows get), at random phases, with any variant
+    that accepts the call except the staged one (which refuses host rows);
+    the parameters and statistics in device memory. Every element of the
+    host buffers outside y's rows must stay NaN."""
+    torch = G.torch_cuda()
+    rng, op, rows, d, dist, x_off, y_off, p_off, eps = _draw(5000 + case)
+    rows = min(rows, max(1, 400_000 // d))     # pinned buffers of a few MB at most
+    wl = workloads.Workload("ln" if op == LN else "rms", rows, d, seed=6000 + case,
+                            x_dist=dist, x_std=_x_std(rng), eps=eps)
+    x = wl.x()
+    params = wl.params()
+    variants = [v for v in G.variants_for(op, d, x_off, y_off) if v != capi.RN_VARIANT_STAGED]
+    v = variants[int(rng.integers(0, len(variants)))]
+    dev = torch.device("cuda", 0)
+    xbuf, xp = _pinned_at(torch, x, x_off)
+    ybuf, yp = _pinned_at(torch, np.full_like(x, np.nan), y_off)
+    pts = [G.dev_copy(p, p_off) for p in params]
+    m = torch.full((rows,), float("nan"), device=dev)
+    r = torch.full((rows,), float("nan"), device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    if op == LN:
+        st = capi.ln_fwd_variant(v, xp, pts[0][1], pts[1][1], yp, m.data_ptr(), r.data_ptr(),
+                                 rows, d, eps, s)
+    else:
+        st = capi.rms_fwd_variant(v, xp, pts[0][1], yp, rows, d, eps, s)
+    capi.check(st)
+    torch.cuda.synchronize()
+    yb = ybuf.numpy()
+    y = yb[y_off:y_off + rows * d].reshape(rows, d)
+    assert np.isnan(yb[:y_off]).all() and np.isnan(yb[y_off + rows * d:]).all(), \
+        f"case {case}: a write outside y"
+    if op == LN:
+        yr, mr, rr = reference.layer_norm(x, *params, eps)
+        parity.check_y(y, yr, what=f"case {case} y")
+        parity.check_mean(m.cpu().numpy(), mr, x, what=f"case {case} mean")
+        parity.check_rstd(r.cpu().numpy(), rr, what=f"case {case} rstd")
+    else:
+        yr, _ = reference.rms_norm(x, *params, eps)
+        parity.check_y(y, yr, what=f"case {case} y")
+    assert capi.device_error() == 0
