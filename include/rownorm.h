@@ -32,11 +32,11 @@
  *               where x and y live (cudaPointerGetAttributes, no
  *               synchronization) and walk host-resident rows on a smaller,
  *               persistent grid, so that reads and writes share the link.
- *               The exception: the parameter vectors of the forward calls
- *               (gamma, beta, w), which the kernels copy into shared memory
- *               with the bulk-copy engine, must be device memory, else
- *               RN_ERR_HOSTMEM (the backward and batched calls take them
- *               anywhere, as above).
+ *               The exception: the parameter vectors of the forward calls,
+ *               single and batched (gamma, beta, w), which the kernels copy
+ *               into shared memory with the bulk-copy engine, must be
+ *               device memory, else RN_ERR_HOSTMEM before anything is
+ *               launched (the backward takes them anywhere, as above).
  *               The caller owns every buffer (the
  *               backward's workspace included); no entry point allocates
  *               or synchronizes, except the diagnostics that say so. Rows

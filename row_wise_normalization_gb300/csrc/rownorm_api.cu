@@ -710,6 +710,22 @@ int run_batched(int op, int dtype, const rn_problem* prs, int count, float eps, 
             if (it != outs.begin() && std::prev(it)->second > in.first) return RN_ERR_ALIAS;
         }
     }
+    {
+        // the parameter vectors must be in device memory, as for one call
+        // (problems that take their own launch stage them by bulk copies):
+        // each distinct vector is asked once, before anything is launched
+        std::vector<const void*> ps;
+        ps.reserve(2 * (size_t)count);
+        for (int i = 0; i < count; ++i) {
+            if (prs[i].rows == 0) continue;
+            ps.push_back(prs[i].p0);
+            if (op == OP_LN) ps.push_back(prs[i].p1);
+        }
+        std::sort(ps.begin(), ps.end());
+        ps.erase(std::unique(ps.begin(), ps.end()), ps.end());
+        for (const void* pp : ps)
+            if (host_resident(pp)) return RN_ERR_HOSTMEM;
+    }
     const cudaStream_t s = (cudaStream_t)stream;
     cudaError_t err = cudaSuccess;
     const int vec = 16 / dtype_size(dtype);

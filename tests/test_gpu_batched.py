@@ -207,3 +207,31 @@ def test_graph_capture_and_replay_with_new_inputs():
         for t, q in zip(tiny, batched_out):
             parity.check_y(q.cpu().numpy(), reference.rms_norm(t[0].cpu().numpy(),
                                                                wt.cpu().numpy())[0])
+
+
+def test_batched_parameters_in_host_memory_are_refused_before_any_launch():
+    """A table whose last problem has its gamma in pinned host memory
+    returns RN_ERR_HOSTMEM, and the earlier problems' outputs stay
+    untouched: the check runs before the first launch."""
+    torch = G.torch_cuda()
+    import row_wise_normalization_gb300 as rn  # noqa: F401  (loads the library)
+
+    dev = torch.device("cuda", 0)
+    items, ys = [], []
+    for i, d in enumerate((128, 700, 5000)):
+        x = torch.ones(16, d, device=dev)
+        g = torch.ones(d, device=dev) if i < 2 else torch.ones(d).pin_memory()
+        b = torch.zeros(d, device=dev)
+        y = torch.full((16, d), float("nan"), device=dev)
+        m = torch.full((16,), float("nan"), device=dev)
+        r = torch.full((16,), float("nan"), device=dev)
+        items.append((x, g, b, y, m, r))
+        ys.append(y)
+    table = capi.problems([(x.data_ptr(), g.data_ptr(), b.data_ptr(), y.data_ptr(),
+                            m.data_ptr(), r.data_ptr(), 16, x.shape[1])
+                           for x, g, b, y, m, r in items])
+    st = capi.ln_fwd_batched(capi.RN_DTYPE_F32, table, len(items), 1e-5,
+                             torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == capi.RN_ERR_HOSTMEM
+    assert all(torch.isnan(y).all() for y in ys), "a problem was launched before the refusal"
